@@ -1,0 +1,382 @@
+"""Benchmark of the CTR sparse-embedding path on GB300.
+
+A step is one pass of the whole hot path over one batch of the full-step
+workload (B = 131072, 26 tables x 8M rows x d = 128 fp32, bag lengths
+uniform 1..50, Zipf(1.05) IDs): dedup -> pooled gather into the interaction
+input -> dot interaction -> interaction backward -> per-unique-row gradient
+reduce + SGD row update.  Inputs are resident in HBM when the timed region
+starts; the tables (106.5 GB) and the ID array (0.7 GB) are far larger than
+L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  With --impl reference the CPU oracle runs the
+same path on a bounded sample of the batch instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "pooled embedding lookups/s and interaction samples/s; HBM GB/s vs GB300 peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="full_step")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller cases for profiling)")
+    ap.add_argument("--rows", type=int, default=0, help="override rows per table (smaller cases for profiling)")
+    ap.add_argument("--cpu-sample", type=int, default=2048, help="samples of the batch the oracle runs")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def workload_cfg(args):
+    from sparse_embeddings_feature_gb300 import workload as W
+    cfg = W.CONFIGS[args.workload]
+    kw = {}
+    if args.batch:
+        kw["batch"] = args.batch
+    if args.rows:
+        kw["rows_per_table"] = tuple([args.rows] * cfg.num_tables)
+    return cfg.shrink(**kw) if kw else cfg
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = max(mx, float(p[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample of the batch
+# ---------------------------------------------------------------------------
+def sample_batch(cfg, w, bs):
+    """The first bs samples of every field: a smaller batch of the same workload."""
+    F, B = cfg.num_fields, cfg.batch
+    bs = min(bs, B)
+    offs = w["offsets"]
+    starts = offs[np.arange(F) * B]
+    lens = np.diff(offs).reshape(F, B)[:, :bs]
+    ids = np.concatenate([w["ids"][starts[f]:starts[f] + lens[f].sum()] for f in range(F)])
+    new_offs = np.concatenate([[0], np.cumsum(lens.reshape(-1))]).astype(np.int64)
+    sub = {"ids": ids, "offsets": new_offs, "bag_to_table": w["bag_to_table"], "row_base": w["row_base"],
+           "dense": w["dense"][:bs]}
+    if "dout" in w:
+        sub["dout"] = w["dout"][:bs]
+    if "grad_pooled" in w:
+        sub["grad_pooled"] = w["grad_pooled"][:bs]
+    return cfg.shrink(batch=bs), sub
+
+
+def oracle_step(cfg, w):
+    """The oracle's pass over the path for one (sampled) batch."""
+    from oracle import oracle as O
+    F, B, d, n = cfg.num_fields, cfg.batch, cfg.d, cfg.n_vectors
+    gen = (cfg.fill_kind, cfg.fill_seed, cfg.fill_scale)
+    dd = O.dedup(w["ids"], w["offsets"], F, B, w["bag_to_table"], w["row_base"])
+    pooled = O.embedding_bag_fwd(w["ids"], w["offsets"], F, B, w["bag_to_table"], w["row_base"], d, pool=cfg.pool,
+                                 dtype=cfg.dtype, gen=gen)
+    if cfg.interaction:
+        X = np.concatenate([w["dense"][:, None, :], pooled], axis=1)
+        O.dot_interaction(X, n, d, dtype=cfg.dtype)
+        if cfg.backward == "full":
+            dX = O.dot_interaction_bwd(w["dout"], X, n, d)
+            O.embedding_bag_bwd_update(dX[:, 1:, :], w["ids"], w["offsets"], F, B, w["bag_to_table"], w["row_base"],
+                                       d, cfg.lr, dd["unique_rows"], gen=gen)
+    return w["ids"].size
+
+
+def cpu_baseline(cfg, w, sample, reps=1):
+    from oracle import oracle as O
+    scfg, sw = sample_batch(cfg, w, sample)
+    O.set_threads(os.cpu_count() or 1)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        lookups = oracle_step(scfg, sw)
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": lookups / dt, "unit": "lookups/s", "cores": O.max_threads(), "kind": "oracle",
+            "sample": f"first {scfg.batch} of {cfg.batch} samples of every field ({lookups} lookups), "
+                      f"whole path, fp64, OpenMP over bags/samples", "seconds": dt}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def fwd_compulsory_bytes(cfg, n_ids, n_unique):
+    row = cfg.d * (4 if cfg.dtype == "f32" else 2)
+    nbags = cfg.num_fields * cfg.batch
+    return n_unique * row + n_ids * 8 + (nbags + 1) * 8 + nbags * row
+
+
+def profile_traffic(kernel_src_hash):
+    """dram bytes per launch of the forward gather from the committed ncu summary, if still current."""
+    p = os.path.join(ROOT, "profiles", "fwd_gather_traffic.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        if j.get("kernel_source_sha256") == kernel_src_hash:
+            return float(j["dram_bytes_per_launch_full_step"])
+    except Exception:
+        pass
+    return None
+
+
+def run_ours(args, rank, world):
+    import torch
+    from sparse_embeddings_feature_gb300 import workload as W
+    from sparse_embeddings_feature_gb300.pipeline import CtrPath
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    cfg = workload_cfg(args)
+    w = W.make_workload(cfg)
+    n_ids = int(w["ids"].size)
+    path = CtrPath(cfg, n_ids)
+    path.upload(w)
+    torch.cuda.synchronize()
+    path.reset_status()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        path.step()
+    torch.cuda.synchronize()
+    status = path.check_status()
+    if any(v != 0 for v in status.values()):
+        raise RuntimeError(f"device error during warm-up: {status}")
+    n_unique = int(path.n_unique.item())
+
+    stages = ["dedup", "forward", "interaction", "interaction_bwd", "bwd_update"]
+    run_stage = {"dedup": path.dedup, "forward": path.forward, "interaction": path.interaction,
+                 "interaction_bwd": path.interaction_bwd, "bwd_update": path.bwd_update}
+    active = [s for s in stages if (s != "dedup" or cfg.backward != "none" or cfg.dedup_gather)
+              and (s != "interaction" or cfg.interaction)
+              and (s != "interaction_bwd" or cfg.backward == "full")
+              and (s != "bwd_update" or cfg.backward != "none")]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(active) + 1)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(args.steps):
+            ev[k][0].record(stream)
+            for i, s in enumerate(active):
+                run_stage[s]()
+                ev[k][i + 1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    stage_ms = {s: sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)) / args.steps
+                for i, s in enumerate(active)}
+    status = path.check_status()
+    if any(v != 0 for v in status.values()):
+        raise RuntimeError(f"device error in the timed region: {status}")
+    ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the C-ABI with host buffers: H2D of the step's inputs
+    # from pinned memory, the step, D2H of its output, all inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        host = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in w.items()
+                if k in ("ids", "offsets", "dense", "dout", "grad_pooled")}
+        if cfg.dtype == "bf16":
+            host["dense"] = host["dense"].view(torch.int16).view(torch.bfloat16)
+        result = path.out if path.out is not None else path.pooled
+        out_host = torch.empty(result.shape, dtype=result.dtype).pin_memory()
+        dense_dev = torch.empty(host["dense"].shape, dtype=host["dense"].dtype, device="cuda")
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def e2e_step():
+            path.ids[:n_ids].copy_(host["ids"], non_blocking=True)
+            path.offsets.copy_(host["offsets"], non_blocking=True)
+            dense_dev.copy_(host["dense"], non_blocking=True)
+            path.X[:, 0, :].copy_(dense_dev, non_blocking=True)
+            if path.dout is not None:
+                path.dout.copy_(host["dout"], non_blocking=True)
+            if path.grad_pooled is not None:
+                path.grad_pooled.copy_(host["grad_pooled"], non_blocking=True)
+            path.step()
+            out_host.copy_(result, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        barrier()
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = a.elapsed_time(b) / args.steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": n_ids * world / (e2e_ms / 1e3), "unit": "lookups/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    hbm, peak_kind = peaks()
+    fwd_bytes = fwd_compulsory_bytes(cfg, n_ids, n_unique)
+    fwd_ms = stage_ms["forward"]
+    achieved = fwd_bytes / (fwd_ms / 1e3) / 1e9
+    with open(os.path.join(ROOT, "sparse_embeddings_feature_gb300", "csrc", "embedding_bag.cu"), "rb") as f:
+        src_hash = hashlib.sha256(f.read()).hexdigest()
+    roofline = {"bound": "hbm", "kernel": "bag_fwd_kernel (pooled gather)", "achieved": achieved, "peak": hbm,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": profile_traffic(src_hash),
+                "algorithmic_bytes_per_launch": fwd_bytes, "launch_ms": fwd_ms,
+                "logical_bytes_per_launch": n_ids * (cfg.d * 4 + 8) + cfg.num_fields * cfg.batch * (cfg.d * 4 + 8)}
+    line = {
+        "metric": METRIC, "value": n_ids * world / (ms / 1e3), "unit": "lookups/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "fields": cfg.num_fields, "tables": cfg.num_tables,
+                   "rows_per_table": cfg.rows_per_table[0], "d": cfg.d, "bag_len": list(cfg.bag_len),
+                   "ids": list(cfg.ids), "n_ids": n_ids, "n_unique": n_unique, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (tables %.1f GB, ids %.2f GB)" % (
+                       cfg.total_rows * cfg.d * 4 / 1e9, n_ids * 8 / 1e9)},
+        "interaction_samples_per_s": cfg.batch * world / (ms / 1e3),
+        "stage_ms": stage_ms,
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": path.launches_per_step() * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, w, args.cpu_sample)
+    return line
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is a bounded sample of the batch."""
+    from sparse_embeddings_feature_gb300 import workload as W
+    from oracle import oracle as O
+    cfg = workload_cfg(args)
+    w = W.make_workload(cfg)
+    scfg, sw = sample_batch(cfg, w, args.cpu_sample)
+    O.set_threads(os.cpu_count() or 1)
+    for _ in range(args.warmup):
+        oracle_step(scfg, sw)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        lookups = oracle_step(scfg, sw)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = lookups / dt
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "lookups/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "batch": cfg.batch, "sampled_batch": scfg.batch},
+            "cpu_baseline": {"value": v, "unit": "lookups/s", "cores": O.max_threads(), "kind": "oracle",
+                             "sample": f"first {scfg.batch} of {cfg.batch} samples of every field per step"},
+            "e2e": {"value": v, "unit": "lookups/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+/*
+ * ctr.h -- C-ABI of libctr, the GB300 (sm_103a) CTR sparse-embedding path.
+ *
+ * The path: batch ID dedup -> pooled embedding-bag gather -> pairwise dot
+ * interaction -> interaction backward -> per-unique-row gradient reduce and
+ * SGD row update.  Every step runs in this library's CUDA kernels.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Memory.   Every pointer is DEVICE memory owned by the caller unless its
+ *           comment says "host".  The library never allocates: scratch space
+ *           comes from the caller's workspace `ws` (size from the matching
+ *           *_workspace_size call, 256-byte aligned).
+ * Streams.  Calls enqueue work on `stream` (a cudaStream_t; NULL = the legacy
+ *           default stream) and return without synchronising, except
+ *           ctr_check_status.
+ * Errors.   Host-side validation returns a negative ctr_status before any
+ *           launch.  Conditions only the device can see (an ID outside its
+ *           table, offsets that are not monotone) set a sticky error word in the
+ *           first 256 bytes of `ws`; ctr_check_status reports and clears it.
+ *           The kernels never trap: a bad ID is skipped (treated as a zero
+ *           row) and flagged.  A CUDA launch error maps to CTR_ERR_CUDA.
+ * Bags.     Bags are CSR and field-major: bag (f, b) holds
+ *           indices[offsets[f*B + b] .. offsets[f*B + b + 1]), f < num_fields,
+ *           b < batch.  Each occurrence counts (a count matrix, not a 0/1 one).
+ * Tables.   Several tables live in one buffer [total_rows, d]; table t owns
+ *           global rows row_base[t] .. row_base[t+1]-1, and field f reads table
+ *           bag_to_table[f].  Rows are contiguous, d elements each.
+ * Determinism.  For a given input every output is bit-identical run to run:
+ *           no float atomics, fixed reduction orders.
+ */
+#ifndef CTR_H
+#define CTR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ctr_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  CTR_OK = 0,
+  CTR_ERR_INVALID_ARG = -1,        /* null pointer, bad size, bad enum */
+  CTR_ERR_UNSUPPORTED = -2,        /* valid but outside what the kernels cover */
+  CTR_ERR_WORKSPACE = -3,          /* ws missing, misaligned or too small */
+  CTR_ERR_INDEX_OUT_OF_RANGE = -4, /* device: an ID outside its table */
+  CTR_ERR_CUDA = -5,               /* a CUDA runtime call or launch failed */
+  CTR_ERR_TIMEOUT = -6,            /* device: a bounded wait ran out */
+  CTR_ERR_NOT_IMPLEMENTED = -7,
+  CTR_ERR_BAD_OFFSETS = -8         /* device: offsets not monotone or not ending at n_ids */
+} ctr_status;
+
+typedef enum { CTR_F32 = 0, CTR_BF16 = 1 } ctr_dtype;
+typedef enum { CTR_POOL_SUM = 0, CTR_POOL_MEAN = 1 } ctr_pool;
+
+/* Limits of the host-side per-field and per-table arrays. */
+#define CTR_MAX_FIELDS 512
+#define CTR_MAX_TABLES 512
+
+/* Human-readable name of a ctr_status value (static string). */
+const char* ctr_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int ctr_version(void);
+
+/* Zero the sticky error word at the head of `ws` (async on `stream`).
+ * Call once on a fresh workspace before its first use. */
+int ctr_status_reset(void* ws, ctr_stream_t stream);
+
+/* Synchronise `stream`, read the sticky error word of `ws`, clear it, and
+ * return CTR_OK or the first device-side error recorded since the last reset. */
+int ctr_check_status(void* ws, ctr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Input generation (not part of the method)                                 */
+/* ------------------------------------------------------------------------ */
+/* Fill rows [row0, row0 + rows) of a table buffer with the counter-based
+ * generator.  `table` points at global row row0; element (r, c) gets the value
+ * of global element index (row0 + r) * d + c:
+ *   gen_kind 0 (uniform, fp32 tables): h = splitmix64(seed ^ idx);
+ *       v = (float)((int)(h >> 40) - 2^23) * scale
+ *   gen_kind 1 (normal4, bf16 tables): Irwin-Hall sum of four 22-bit fields of
+ *       splitmix64(seed ^ 2 idx) and splitmix64(seed ^ (2 idx + 1)), minus
+ *       2^23 - 2, times scale, rounded to bf16 (nearest even).
+ * splitmix64 is the output function of Steele, Lea and Flood (OOPSLA 2014). */
+int ctr_fill_table(void* table, ctr_dtype dtype, int64_t rows, int32_t d, int64_t row0, int gen_kind,
+                   uint64_t seed, float scale, ctr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* a1. Dedup: the virtual sparse feature                                     */
+/* ------------------------------------------------------------------------ */
+/* Source: "How TensorNet Supercharges Sparse Feature Training on TensorFlow",
+ * Core Optimizations, embedding_lookup: collect the batch's IDs, sort them and
+ * assign each distinct ID a continuous index; the batch-sized embedding matrix
+ * has one row per distinct ID (its capacity is the batch's ID count).
+ *
+ * Keys are global rows k_i = row_base[bag_to_table[f]] + ids[i] (so equal IDs
+ * of different tables stay apart, and per-table dedup falls out of one sort).
+ * Requires total_rows = row_base[num_tables] <= 2^32 and n_ids < 2^31.
+ *
+ * Inputs
+ *   ids            int64 [n_ids]        table-local IDs, field-major CSR
+ *   offsets        int64 [F*B + 1]      offsets[0] = 0, offsets[F*B] = n_ids
+ *   bag_to_table   host int32 [F]       table of each field
+ *   row_base       host int64 [T + 1]   first global row of each table
+ *   n_ids          host                 number of IDs (the caller sizes buffers by it)
+ * Outputs (capacity n_ids each; a NULL int32 output is skipped)
+ *   unique_rows    int64 [n_ids]        distinct keys, ascending; first n_unique valid
+ *   n_unique       int64 [1]            number of distinct keys (device scalar)
+ *   inverse        int32 [n_ids]        rank of key i in unique_rows (the virtual sparse feature)
+ *   sorted_pos     int32 [n_ids]        stable sort permutation: position of the s-th key
+ *   sorted_bag     int32 [n_ids]        bag (f*B + b) of sorted_pos[s]
+ *   run_offsets    int32 [n_ids + 1]    run of unique u is sorted slots run_offsets[u] ..
+ *                                       run_offsets[u+1]-1; run_offsets[n_unique] = n_ids
+ *   unique_offsets int64 [T + 1]        uniques of table t are unique_rows[unique_offsets[t] ..
+ *                                       unique_offsets[t+1]); unique_offsets[T] = n_unique
+ * Device errors: CTR_ERR_INDEX_OUT_OF_RANGE (an ID outside its table; its key
+ * is then replaced by the last row of its table), CTR_ERR_BAD_OFFSETS.
+ * Workspace: ctr_dedup_workspace_size(n_ids, F, B, total_rows) bytes. */
+size_t ctr_dedup_workspace_size(int64_t n_ids, int32_t num_fields, int32_t batch, int64_t total_rows);
+int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num_fields, int32_t batch,
+              const int32_t* bag_to_table, const int64_t* row_base, int32_t num_tables, int64_t n_ids,
+              int64_t* unique_rows, int64_t* n_unique, int32_t* inverse, int32_t* sorted_pos, int32_t* sorted_bag,
+              int32_t* run_offsets, int64_t* unique_offsets, void* ws, size_t ws_bytes, ctr_stream_t stream);
+
+/* TensorNet's batch-sized matrix (same passage): U[u] = table[unique_rows[u]]
+ * for u < *n_unique.  capacity (host) bounds n_unique; rows of U at or beyond
+ * n_unique are left untouched.  U is [capacity, d] of the table's dtype. */
+int ctr_gather_rows(const void* table, ctr_dtype dtype, int32_t d, int64_t total_rows, const int64_t* unique_rows,
+                    const int64_t* n_unique, int64_t capacity, void* U, void* ws, size_t ws_bytes,
+                    ctr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* a2. Pooled embedding-bag forward                                          */
+/* ------------------------------------------------------------------------ */
+/* Source: "DHEN" notes, section 2.1 (each categorical term has a trainable
+ * d-vector) and section 3.1, Solution 2 (sum the active embeddings); "Meta
+ * DLRM", section 02 (categorical features go through embeddings).
+ *
+ *   out(b, f) = sum_{i in bag(f,b)} table[row_i]          (CTR_POOL_SUM)
+ *             = that sum / len(bag)   (0 for an empty bag)  (CTR_POOL_MEAN)
+ * accumulated in fp32, rounded once to out_dtype.
+ * Row selection: if bag_to_table != NULL, indices are table-local int64 IDs and
+ * row_i = row_base[bag_to_table[f]] + ids[i] (host arrays as in ctr_dedup);
+ * if bag_to_table == NULL, indices are rows of `table` directly (e.g. the
+ * int32 inverse map into the unique-row matrix U), num_tables ignored.
+ * indices_are_int32 selects int32 or int64 indices; n_indices (host) is the
+ * length of `indices` (a bag reaching past it is skipped and flagged).
+ * out(b, f) is the d-vector at out + b*out_stride_b + f*out_stride_f
+ * (element strides; e.g. the pooled slots of an interaction input [B, F+1, d]
+ * are out = X + d, out_stride_b = (F+1)*d, out_stride_f = d).
+ * table dtype CTR_F32 or CTR_BF16; out_dtype CTR_F32, or CTR_BF16 (bf16 tables).
+ * Device errors: CTR_ERR_INDEX_OUT_OF_RANGE (row skipped), CTR_ERR_BAD_OFFSETS
+ * (bag skipped, written as zeros).
+ * Workspace: ctr_embedding_bag_workspace_size() bytes (the error word). */
+size_t ctr_embedding_bag_workspace_size(void);
+int ctr_embedding_bag_fwd(const void* table, ctr_dtype dtype, int32_t d, int64_t total_rows, const void* indices,
+                          int indices_are_int32, int64_t n_indices, const int64_t* offsets, int32_t num_fields, int32_t batch,
+                          const int32_t* bag_to_table, const int64_t* row_base, int32_t num_tables, ctr_pool pool,
+                          void* out, ctr_dtype out_dtype, int64_t out_stride_b, int64_t out_stride_f, void* ws,
+                          size_t ws_bytes, ctr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* a3. Pairwise dot interaction                                              */
+/* Workspace of both interaction calls: ctr_interaction_workspace_size()     */
+/* bytes (the error word; the tensor-core kernel records CTR_ERR_TIMEOUT    */
+/* there if one of its bounded waits runs out).                              */
+/* ------------------------------------------------------------------------ */
+/* Source: "Meta DLRM", section 02 (the interaction is the dot product between
+ * every pair of embedding vectors and the processed dense features, cross terms
+ * only); "DHEN" notes, section 3.1, Eq. (3) (pairwise inner products
+ * concatenated with the dense features).
+ *
+ * X [batch, n, d], slot 0 = the dense vector, slots 1..n-1 = pooled embeddings.
+ *   out[b] = [ X[b,0,:] | Z ],  Z[i(i-1)/2 + j] = <X[b,i,:], X[b,j,:]>,
+ *            1 <= i < n, 0 <= j < i   (strict lower triangle, row by row)
+ * out is [batch, d + n(n-1)/2] of the input dtype.  fp32: CUDA-core FMA.
+ * bf16: tcgen05 tensor cores (fp32 accumulate in TMEM, bf16 output) when
+ * n <= 32 and d is a multiple of 64 up to 256; other shapes use a CUDA-core
+ * kernel with fp32 accumulation.  The fast kernels need X and out 16-byte
+ * aligned; other pointers take the generic kernel. */
+size_t ctr_interaction_workspace_size(void);
+int ctr_dot_interaction(const void* X, ctr_dtype dtype, int32_t batch, int32_t n, int32_t d, void* out, void* ws,
+                        size_t ws_bytes, ctr_stream_t stream);
+
+/* Derivative of ctr_dot_interaction (fp32), not on the pages:
+ *   dX[b,i,:] = sum_{j != i} dZ(i,j) X[b,j,:]  (+ dout[b, 0:d] for i = 0)
+ * with dZ(i,j) = dout[b, d + hi(hi-1)/2 + lo], hi = max(i,j), lo = min(i,j).
+ * dout [batch, d + n(n-1)/2], X and dX [batch, n, d]. */
+int ctr_dot_interaction_bwd(const float* dout, const float* X, int32_t batch, int32_t n, int32_t d, float* dX,
+                            void* ws, size_t ws_bytes, ctr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* a5. Sparse backward: per-unique-row gradient reduce + SGD row update       */
+/* ------------------------------------------------------------------------ */
+/* Source: "How TensorNet ...", Synchronous Architecture (only the sparse
+ * features present in the batch are synchronised) and Core Optimizations (the
+ * batch-sized matrix of unique rows).  The SGD rule is not on the pages.
+ *
+ * For each unique u < *n_unique, over its run of sorted occurrences s (from
+ * ctr_dedup):
+ *   g_u = sum_s scale(bag_s) * grad_pooled(bag_s),  scale = 1 (SUM) or
+ *         1 / len(bag) (MEAN),   bag_s = sorted_bag[s] = f*B + b,
+ *         grad_pooled(bag) = the fp32 d-vector at grad_pooled + b*g_stride_b + f*g_stride_f
+ *   table[unique_rows[u]] <- table[unique_rows[u]] - lr * g_u
+ * Each row is written exactly once; no float atomics.  The sum runs in a fixed
+ * order (pieces of at most 128 occurrences summed in sorted order, then a fixed
+ * tree over the pieces of a long run), so results are deterministic.
+ * fp32 tables: one fused multiply-add, rounded once.  bf16 tables: the update
+ * is computed in fp32 and rounded to bf16 (nearest even).
+ * grad_unique_out (optional, [n_ids, d] fp32): receives g_u in row u.
+ * n_ids (host) is the capacity used to size grids; *n_unique <= n_ids.
+ * Workspace: ctr_bwd_update_workspace_size(n_ids, d) bytes. */
+size_t ctr_bwd_update_workspace_size(int64_t n_ids, int32_t d);
+int ctr_embedding_bag_bwd_update(const float* grad_pooled, int64_t g_stride_b, int64_t g_stride_f,
+                                 const int64_t* offsets, int32_t num_fields, int32_t batch, ctr_pool pool,
+                                 const int64_t* unique_rows, const int64_t* n_unique, const int32_t* run_offsets,
+                                 const int32_t* sorted_bag, int64_t n_ids, float lr, void* table, ctr_dtype dtype,
+                                 int32_t d, int64_t total_rows, float* grad_unique_out, void* ws, size_t ws_bytes,
+                                 ctr_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CTR_H */

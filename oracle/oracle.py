@@ -183,20 +183,20 @@ def dot_interaction_bwd(dout, X, n, d, sample_list=None, with_mag=False):
 
 
 def embedding_bag_bwd_update(G, ids, offsets, num_fields, batch, bag_to_table, row_base, d, lr, target_rows,
-                             pool="sum", table=None, dtype="f32", gen=None, g_strides=None):
+                             pool="sum", table=None, dtype="f32", gen=None):
     """SGD-updated values, fp64 gradient and magnitude sums of the listed global rows.
 
-    G: fp32 gradient of the pooled outputs, [B, F, d] unless g_strides=(stride_b, stride_f)
-    are given in elements.
+    G: fp32 gradient of the pooled outputs, shape [B, F, d] (any memory layout).
     """
     G = _c(G, np.float32)
+    assert G.shape == (int(batch), int(num_fields), int(d)), G.shape
     ids = _c(ids, np.int64)
     offsets = _c(offsets, np.int64)
     b2t = _c(bag_to_table, np.int32)
     rb = _c(row_base, np.int64)
     tr = _c(target_rows, np.int64)
     F, B = int(num_fields), int(batch)
-    sb, sf = g_strides if g_strides is not None else (F * d, d)
+    sb, sf = F * d, d
     if table is not None:
         table = np.ascontiguousarray(table)
         gk, gs, gsc = 0, 0, 0.0

@@ -1,0 +1,95 @@
+// Shared device/host helpers of libctr (the CUDA path).  Nothing here is
+// shared with the CPU oracle.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ctr.h"
+
+namespace ctr {
+
+constexpr int kWarp = 32;
+constexpr unsigned kFull = 0xffffffffu;
+constexpr size_t kWsHeader = 256;  // sticky error word lives at the head of every workspace
+
+// Device-side error codes recorded in the workspace header (first one wins).
+__device__ __forceinline__ void set_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+__host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
+__host__ __device__ __forceinline__ size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
+
+// Per-field table placement, passed by value as a kernel parameter.
+struct FieldMap {
+  int64_t base[CTR_MAX_FIELDS];  // row_base[bag_to_table[f]]
+  int64_t rows[CTR_MAX_FIELDS];  // rows of that table
+};
+
+// Fill a FieldMap from the host arrays; returns a ctr_status.
+inline int make_field_map(const int32_t* bag_to_table, const int64_t* row_base, int32_t F, int32_t T,
+                          FieldMap* fm) {
+  if (F <= 0 || T <= 0) return CTR_ERR_INVALID_ARG;
+  if (F > CTR_MAX_FIELDS || T > CTR_MAX_TABLES) return CTR_ERR_UNSUPPORTED;
+  if (row_base[0] != 0) return CTR_ERR_INVALID_ARG;
+  for (int t = 0; t < T; ++t)
+    if (row_base[t + 1] < row_base[t]) return CTR_ERR_INVALID_ARG;
+  for (int f = 0; f < F; ++f) {
+    int t = bag_to_table[f];
+    if (t < 0 || t >= T) return CTR_ERR_INVALID_ARG;
+    fm->base[f] = row_base[t];
+    fm->rows[f] = row_base[t + 1] - row_base[t];
+  }
+  return CTR_OK;
+}
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+// Map the last CUDA error to a ctr_status.
+inline int launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? CTR_OK : CTR_ERR_CUDA;
+}
+
+// Carves sub-buffers out of a caller workspace (after the header).
+struct WsCarver {
+  char* base;
+  size_t cap;
+  size_t used;
+  explicit WsCarver(void* ws, size_t bytes) : base((char*)ws), cap(bytes), used(kWsHeader) {}
+  template <typename T>
+  T* take(size_t count) {
+    size_t off = align_up(used, 256);
+    used = off + align_up(count * sizeof(T), 256);
+    return used <= cap ? (T*)(base + off) : nullptr;
+  }
+  bool ok() const { return used <= cap; }
+};
+
+// Same arithmetic without a buffer: used to size workspaces.
+struct WsSizer {
+  size_t used = kWsHeader;
+  template <typename T>
+  void take(size_t count) {
+    size_t off = align_up(used, 256);
+    used = off + align_up(count * sizeof(T), 256);
+  }
+};
+
+inline bool ws_valid(void* ws, size_t ws_bytes, size_t need) {
+  return ws != nullptr && ((uintptr_t)ws % 256) == 0 && ws_bytes >= need;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+__device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
+
+}  // namespace ctr

@@ -1,0 +1,399 @@
+// a1. Batch ID dedup into the "virtual sparse feature" index.
+//
+// Source: "How TensorNet Supercharges Sparse Feature Training on TensorFlow",
+// Core Optimizations, embedding_lookup: collect the batch's IDs, sort them and
+// give each distinct ID a continuous index.
+//
+// GPU design (sm_103a, one GPU):
+//   keygen     warp per bag: key = row_base[table(f)] + id (32-bit global row),
+//              bag id per position; IDs outside their table are flagged.
+//   LSD radix  ceil(bits(total_rows) / 8) passes of <= 8 bits.  Each pass is
+//              reduce-then-scan: per-tile digit histograms (digit-major), one
+//              device-wide exclusive scan over them, then a stable scatter.
+//              Stable ranking inside a tile uses __match_any_sync per 32 keys
+//              and per-warp digit counters; the tile is reordered in shared
+//              memory first so the global writes are coalesced runs.  No
+//              block waits on another block.
+//   unique     head flags, per-tile head counts, exclusive scan, then ranks:
+//              unique_rows, run_offsets, inverse (scatter), sorted_bag
+//              (gather of the bag of each sorted position), unique_offsets.
+#include <algorithm>
+
+#include "common.cuh"
+#include "scan.cuh"
+
+namespace ctr {
+namespace {
+
+constexpr int kRsThreads = 256;
+constexpr int kRsWarps = kRsThreads / 32;
+constexpr int kRsItems = 16;                      // keys per lane per tile
+constexpr int kRsTile = kRsThreads * kRsItems;    // 4096 keys
+constexpr int kRsWarpKeys = 32 * kRsItems;        // 512 keys per warp
+constexpr int kMaxDigits = 256;
+
+struct TableBases {
+  int64_t row_base[CTR_MAX_TABLES + 1];
+  int32_t num_tables;
+};
+
+__global__ void __launch_bounds__(256) keygen_kernel(const int64_t* __restrict__ ids,
+                                                     const int64_t* __restrict__ offsets, int32_t F, int32_t B,
+                                                     int64_t n_ids, const __grid_constant__ FieldMap fm,
+                                                     uint32_t* __restrict__ keys, int32_t* __restrict__ bag_of,
+                                                     int* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nbags = (int64_t)F * B;
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (offsets[0] != 0 || offsets[nbags] != n_ids) set_error(err, CTR_ERR_BAD_OFFSETS);
+  }
+  for (int64_t bag = warp0; bag < nbags; bag += nwarps) {
+    const int f = (int)(bag / B);
+    const int64_t o0 = offsets[bag], o1 = offsets[bag + 1];
+    if (o0 < 0 || o1 < o0 || o1 > n_ids) {
+      if (lane == 0) set_error(err, CTR_ERR_BAD_OFFSETS);
+      continue;
+    }
+    const int64_t base = fm.base[f], rows = fm.rows[f];
+    for (int64_t i = o0 + lane; i < o1; i += 32) {
+      int64_t id = ids[i];
+      if (id < 0 || id >= rows) {
+        set_error(err, CTR_ERR_INDEX_OUT_OF_RANGE);
+        id = rows - 1;
+      }
+      keys[i] = (uint32_t)(base + id);
+      bag_of[i] = (int32_t)bag;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t digit_of(uint32_t k, int shift, uint32_t mask) { return (k >> shift) & mask; }
+
+// Per-tile digit histogram, written digit-major: hist[digit * num_tiles + tile].
+__global__ void __launch_bounds__(kRsThreads) radix_upsweep_kernel(const uint32_t* __restrict__ keys, int64_t n,
+                                                                   int shift, int nbits,
+                                                                   uint32_t* __restrict__ hist, int64_t num_tiles) {
+  __shared__ uint32_t cnt[kRsWarps][kMaxDigits];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ndig = 1 << nbits;
+  const uint32_t mask = (uint32_t)ndig - 1;
+  for (int i = threadIdx.x; i < kRsWarps * kMaxDigits; i += kRsThreads) (&cnt[0][0])[i] = 0;
+  __syncthreads();
+  const int64_t base = (int64_t)blockIdx.x * kRsTile + (int64_t)warp * kRsWarpKeys;
+#pragma unroll 4
+  for (int r = 0; r < kRsItems; ++r) {
+    int64_t idx = base + r * 32 + lane;
+    bool valid = idx < n;
+    uint32_t dg = valid ? digit_of(keys[idx], shift, mask) : 0xffffffffu;
+    unsigned peers = __match_any_sync(kFull, dg);
+    if (valid && lane == __ffs(peers) - 1) cnt[warp][dg] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int dg = threadIdx.x; dg < ndig; dg += kRsThreads) {
+    uint32_t t = 0;
+#pragma unroll
+    for (int w = 0; w < kRsWarps; ++w) t += cnt[w][dg];
+    hist[(int64_t)dg * num_tiles + blockIdx.x] = t;
+  }
+}
+
+// Stable scatter of one tile by the current digit.  vals_in == nullptr means
+// the values are the positions 0..n-1 (first pass).
+__global__ void __launch_bounds__(kRsThreads) radix_downsweep_kernel(
+    const uint32_t* __restrict__ keys_in, const int32_t* __restrict__ vals_in, uint32_t* __restrict__ keys_out,
+    int32_t* __restrict__ vals_out, int64_t n, int shift, int nbits, const uint32_t* __restrict__ hist_scan,
+    int64_t num_tiles) {
+  __shared__ uint32_t wcnt[kRsWarps][kMaxDigits];
+  __shared__ uint32_t tile_start[kMaxDigits];
+  __shared__ uint32_t glob_start[kMaxDigits];
+  __shared__ uint32_t skeys[kRsTile];
+  __shared__ int32_t svals[kRsTile];
+  __shared__ uint32_t warp_tot[kRsWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ndig = 1 << nbits;
+  const uint32_t mask = (uint32_t)ndig - 1;
+  for (int i = threadIdx.x; i < kRsWarps * kMaxDigits; i += kRsThreads) (&wcnt[0][0])[i] = 0;
+  __syncthreads();
+
+  const int64_t tile_base = (int64_t)blockIdx.x * kRsTile;
+  const int64_t base = tile_base + (int64_t)warp * kRsWarpKeys;
+  const unsigned lt = lanemask_lt();
+  uint32_t key[kRsItems];
+  int32_t val[kRsItems];
+  uint32_t rank[kRsItems];
+#pragma unroll
+  for (int r = 0; r < kRsItems; ++r) {
+    int64_t idx = base + r * 32 + lane;
+    bool valid = idx < n;
+    key[r] = valid ? keys_in[idx] : 0u;
+    val[r] = valid ? (vals_in ? vals_in[idx] : (int32_t)idx) : 0;
+    uint32_t dg = valid ? digit_of(key[r], shift, mask) : 0xffffffffu;
+    unsigned peers = __match_any_sync(kFull, dg);
+    uint32_t prior = valid ? wcnt[warp][dg] : 0u;
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) wcnt[warp][dg] = prior + __popc(peers);
+    __syncwarp();
+    rank[r] = valid ? prior + __popc(peers & lt) : 0xffffffffu;
+  }
+  __syncthreads();
+  // per digit: exclusive over warps (in place), then exclusive over digits
+  uint32_t dtot[1] = {0};
+  {
+    const int dg = threadIdx.x;  // kRsThreads == kMaxDigits
+    uint32_t run = 0;
+    if (dg < ndig) {
+#pragma unroll
+      for (int w = 0; w < kRsWarps; ++w) {
+        uint32_t c = wcnt[w][dg];
+        wcnt[w][dg] = run;
+        run += c;
+      }
+      glob_start[dg] = hist_scan[(int64_t)dg * num_tiles + blockIdx.x];
+    }
+    dtot[0] = run;
+  }
+  __syncthreads();
+  block_exclusive_scan<uint32_t, kRsThreads, 1>(dtot, warp_tot);
+  if (threadIdx.x < ndig) tile_start[threadIdx.x] = dtot[0];
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kRsItems; ++r) {
+    if (rank[r] != 0xffffffffu) {
+      uint32_t dg = digit_of(key[r], shift, mask);
+      uint32_t local = tile_start[dg] + wcnt[warp][dg] + rank[r];
+      skeys[local] = key[r];
+      svals[local] = val[r];
+    }
+  }
+  __syncthreads();
+  const int count = (int)imin64(kRsTile, n - tile_base);
+  for (int i = threadIdx.x; i < count; i += kRsThreads) {
+    uint32_t k = skeys[i];
+    uint32_t dg = digit_of(k, shift, mask);
+    int64_t dest = (int64_t)glob_start[dg] + (i - (int64_t)tile_start[dg]);
+    keys_out[dest] = k;
+    vals_out[dest] = svals[i];
+  }
+}
+
+// Heads per tile of the sorted keys.
+__global__ void __launch_bounds__(kRsThreads) unique_count_kernel(const uint32_t* __restrict__ skeys, int64_t n,
+                                                                  uint32_t* __restrict__ tile_heads) {
+  __shared__ uint32_t warp_tot[kRsWarps];
+  const int64_t base = (int64_t)blockIdx.x * kRsTile;
+  uint32_t c = 0;
+#pragma unroll 4
+  for (int i = 0; i < kRsItems; ++i) {
+    int64_t s = base + (int64_t)i * kRsThreads + threadIdx.x;
+    if (s < n) c += (s == 0 || skeys[s] != skeys[s - 1]) ? 1u : 0u;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+  if ((threadIdx.x & 31) == 0) warp_tot[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t t = 0;
+    for (int w = 0; w < kRsWarps; ++w) t += warp_tot[w];
+    tile_heads[blockIdx.x] = t;
+  }
+}
+
+__device__ __forceinline__ int table_of(const int64_t* rb, int T, int64_t k) {
+  // largest t in [0, T) with rb[t] <= k
+  int lo = 0, hi = T - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (rb[mid] <= k) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kRsThreads) unique_write_kernel(
+    const uint32_t* __restrict__ skeys, const int32_t* __restrict__ spos, int64_t n,
+    const uint32_t* __restrict__ tile_base_scan, const __grid_constant__ TableBases tb,
+    const int32_t* __restrict__ bag_of, int64_t* __restrict__ unique_rows, int64_t* __restrict__ n_unique,
+    int32_t* __restrict__ inverse, int32_t* __restrict__ sorted_bag, int32_t* __restrict__ run_offsets,
+    int64_t* __restrict__ unique_offsets) {
+  __shared__ uint32_t warp_tot[kRsWarps];
+  __shared__ int64_t rb[CTR_MAX_TABLES + 1];
+  const int T = tb.num_tables;
+  for (int i = threadIdx.x; i <= T; i += kRsThreads) rb[i] = tb.row_base[i];
+  const int64_t base = (int64_t)blockIdx.x * kRsTile + (int64_t)threadIdx.x * kRsItems;
+  uint32_t k[kRsItems];
+  uint32_t h[kRsItems];
+  uint32_t prev = (base > 0 && base - 1 < n) ? skeys[base - 1] : 0u;
+#pragma unroll
+  for (int i = 0; i < kRsItems; ++i) {
+    int64_t s = base + i;
+    k[i] = s < n ? skeys[s] : 0u;
+    h[i] = (s < n && (s == 0 || k[i] != prev)) ? 1u : 0u;
+    prev = k[i];
+  }
+  uint32_t excl[kRsItems];
+#pragma unroll
+  for (int i = 0; i < kRsItems; ++i) excl[i] = h[i];
+  __syncthreads();  // rb ready
+  uint32_t tile_total = block_exclusive_scan<uint32_t, kRsThreads, kRsItems>(excl, warp_tot);
+  const uint32_t tbase = tile_base_scan[blockIdx.x];
+#pragma unroll
+  for (int i = 0; i < kRsItems; ++i) {
+    int64_t s = base + i;
+    if (s >= n) break;
+    // rank of this key = heads in [0, s] - 1
+    uint32_t rank = tbase + excl[i] + h[i] - 1;
+    if (h[i]) {
+      unique_rows[rank] = (int64_t)k[i];
+      if (run_offsets) run_offsets[rank] = (int32_t)s;
+      if (unique_offsets) {
+        int t = table_of(rb, T, (int64_t)k[i]);
+        int t0 = 0;
+        if (s > 0) t0 = table_of(rb, T, (int64_t)skeys[s - 1]) + 1;
+        for (int tt = t0; tt <= t; ++tt) unique_offsets[tt] = rank;
+      }
+    }
+    int32_t p = spos[s];
+    if (inverse) inverse[p] = (int32_t)rank;
+    if (sorted_bag) sorted_bag[s] = bag_of[p];
+    if (s == n - 1) {
+      uint32_t nu = rank + 1;
+      *n_unique = nu;
+      if (run_offsets) run_offsets[nu] = (int32_t)n;
+      if (unique_offsets) {
+        int t = table_of(rb, T, (int64_t)k[i]);
+        for (int tt = t + 1; tt <= T; ++tt) unique_offsets[tt] = nu;
+      }
+    }
+  }
+  (void)tile_total;
+}
+
+__global__ void dedup_empty_kernel(int64_t* n_unique, int32_t* run_offsets, int64_t* unique_offsets, int T) {
+  *n_unique = 0;
+  if (run_offsets) run_offsets[0] = 0;
+  if (unique_offsets)
+    for (int t = 0; t <= T; ++t) unique_offsets[t] = 0;
+}
+
+int key_bits(int64_t total_rows) {
+  int b = 1;
+  while (b < 32 && ((int64_t)1 << b) < total_rows) ++b;
+  return b;
+}
+
+template <typename WS>
+void dedup_layout(WS& ws, int64_t n_ids, int64_t total_rows) {
+  const int64_t tiles = ceil_div(n_ids, kRsTile);
+  const int bits = key_bits(total_rows);
+  const int passes = (bits + 7) / 8;
+  const int nb = (bits + passes - 1) / passes;
+  ws.template take<uint32_t>((size_t)n_ids);           // keys A
+  ws.template take<uint32_t>((size_t)n_ids);           // keys B
+  ws.template take<int32_t>((size_t)n_ids);            // values scratch
+  ws.template take<int32_t>((size_t)n_ids);            // sorted positions if the caller gives none
+  ws.template take<int32_t>((size_t)n_ids);            // bag of each position
+  ws.template take<uint32_t>((size_t)tiles << nb);     // digit histograms
+  ws.template take<uint32_t>((size_t)tiles);           // heads per tile
+  scan_reserve<uint32_t>(ws, tiles << nb);
+}
+
+}  // namespace
+}  // namespace ctr
+
+using namespace ctr;
+
+extern "C" size_t ctr_dedup_workspace_size(int64_t n_ids, int32_t num_fields, int32_t batch, int64_t total_rows) {
+  (void)num_fields;
+  (void)batch;
+  WsSizer s;
+  dedup_layout(s, n_ids > 0 ? n_ids : 1, total_rows > 1 ? total_rows : 2);
+  return s.used;
+}
+
+extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num_fields, int32_t batch,
+                         const int32_t* bag_to_table, const int64_t* row_base, int32_t num_tables, int64_t n_ids,
+                         int64_t* unique_rows, int64_t* n_unique, int32_t* inverse, int32_t* sorted_pos,
+                         int32_t* sorted_bag, int32_t* run_offsets, int64_t* unique_offsets, void* ws,
+                         size_t ws_bytes, ctr_stream_t stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!offsets || !bag_to_table || !row_base || !unique_rows || !n_unique) return CTR_ERR_INVALID_ARG;
+  if (num_fields <= 0 || batch <= 0 || num_tables <= 0) return CTR_ERR_INVALID_ARG;
+  if (num_fields > CTR_MAX_FIELDS || num_tables > CTR_MAX_TABLES) return CTR_ERR_UNSUPPORTED;
+  if (n_ids < 0 || (n_ids > 0 && !ids)) return CTR_ERR_INVALID_ARG;
+  if (n_ids >= ((int64_t)1 << 31)) return CTR_ERR_UNSUPPORTED;
+  if (row_base[0] != 0) return CTR_ERR_INVALID_ARG;
+  for (int t = 0; t < num_tables; ++t)
+    if (row_base[t + 1] < row_base[t]) return CTR_ERR_INVALID_ARG;
+  const int64_t total_rows = row_base[num_tables];
+  if (total_rows > ((int64_t)1 << 32)) return CTR_ERR_UNSUPPORTED;
+  FieldMap fm;
+  for (int f = 0; f < num_fields; ++f) {
+    int t = bag_to_table[f];
+    if (t < 0 || t >= num_tables) return CTR_ERR_INVALID_ARG;
+    fm.base[f] = row_base[t];
+    fm.rows[f] = row_base[t + 1] - row_base[t];
+  }
+  if (!ws_valid(ws, ws_bytes, ctr_dedup_workspace_size(n_ids, num_fields, batch, total_rows)))
+    return CTR_ERR_WORKSPACE;
+  int* err = (int*)ws;
+  TableBases tb;
+  tb.num_tables = num_tables;
+  for (int t = 0; t <= num_tables; ++t) tb.row_base[t] = row_base[t];
+
+  if (n_ids == 0) {
+    dedup_empty_kernel<<<1, 1, 0, s>>>(n_unique, run_offsets, unique_offsets, num_tables);
+    return launch_status();
+  }
+
+  WsCarver c(ws, ws_bytes);
+  const int64_t tiles = ceil_div(n_ids, kRsTile);
+  const int bits = key_bits(total_rows);
+  const int passes = (bits + 7) / 8;
+  const int nb = (bits + passes - 1) / passes;
+  uint32_t* keys[2] = {c.take<uint32_t>(n_ids), c.take<uint32_t>(n_ids)};
+  int32_t* vscratch = c.take<int32_t>(n_ids);
+  int32_t* vfinal_ws = c.take<int32_t>(n_ids);
+  int32_t* bag_of = c.take<int32_t>(n_ids);
+  uint32_t* hist = c.take<uint32_t>((size_t)tiles << nb);
+  uint32_t* tile_heads = c.take<uint32_t>(tiles);
+  if (!c.ok()) return CTR_ERR_WORKSPACE;
+  int32_t* vfinal = sorted_pos ? sorted_pos : vfinal_ws;
+
+  const int64_t nbags = (int64_t)num_fields * batch;
+  {
+    int64_t blocks = imin64(ceil_div(nbags, 8), (int64_t)num_sms() * 16);
+    keygen_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, s>>>(ids, offsets, num_fields, batch, n_ids, fm,
+                                                                        keys[0], bag_of, err);
+    if (int st = launch_status()) return st;
+  }
+  const int32_t* vin = nullptr;
+  int shift = 0;
+  for (int p = 0; p < passes; ++p) {
+    const int pb = std::min(nb, bits - shift);
+    const int64_t nh = tiles << pb;
+    radix_upsweep_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(keys[p & 1], n_ids, shift, pb, hist, tiles);
+    if (int st = launch_status()) return st;
+    WsCarver scan_ws = c;  // scan scratch is reused every pass
+    if (int st = scan_exclusive<uint32_t>(hist, hist, nh, nullptr, nullptr, scan_ws, s)) return st;
+    int32_t* vout = ((passes - 1 - p) % 2 == 0) ? vfinal : vscratch;
+    radix_downsweep_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(keys[p & 1], vin, keys[(p + 1) & 1], vout, n_ids,
+                                                                   shift, pb, hist, tiles);
+    if (int st = launch_status()) return st;
+    vin = vout;
+    shift += pb;
+  }
+  const uint32_t* skeys = keys[passes & 1];
+  unique_count_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(skeys, n_ids, tile_heads);
+  if (int st = launch_status()) return st;
+  {
+    WsCarver scan_ws = c;
+    if (int st = scan_exclusive<uint32_t>(tile_heads, tile_heads, tiles, nullptr, nullptr, scan_ws, s)) return st;
+  }
+  unique_write_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(skeys, vfinal, n_ids, tile_heads, tb, bag_of,
+                                                             unique_rows, n_unique, inverse, sorted_bag, run_offsets,
+                                                             unique_offsets);
+  return launch_status();
+}

@@ -1,0 +1,362 @@
+// a2. Pooled embedding-bag forward, and the unique-row gather.
+//
+// Sources: "DHEN" notes, section 2.1 (a trainable d-vector per categorical
+// term) and section 3.1, Solution 2 (sum the active embeddings); "Meta DLRM",
+// section 02; "How TensorNet ...", Core Optimizations (the batch-sized matrix of
+// unique rows).
+//
+// GPU design: one warp per bag (grid-stride over field-major bags, so the
+// warps in flight all read one table and its Zipf-hot rows stay in L2).  A row
+// is read as 16-byte vectors by LPR lanes (LPR = row bytes / 16, rounded up to a
+// power of two); a warp therefore has 32/LPR rows in flight per step, and the
+// loop is unrolled kUnroll steps deep so each lane keeps several independent
+// loads outstanding.  Indices are fetched 32 at a time with one coalesced load
+// and broadcast by shuffle.  Accumulation is fp32 in a fixed order (each lane
+// group sums its rows in index order; groups combine by a fixed butterfly).
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace ctr {
+namespace {
+
+constexpr int kBagThreads = 256;
+constexpr int kUnroll = 4;
+
+template <typename TT>
+struct Vec;
+template <>
+struct Vec<float> {
+  static constexpr int kN = 4;
+};
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int kN = 8;
+};
+
+__device__ __forceinline__ uint4 ldg16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void unpack(const uint4& v, float (&f)[4], float) {
+  f[0] = __uint_as_float(v.x);
+  f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z);
+  f[3] = __uint_as_float(v.w);
+}
+__device__ __forceinline__ void unpack(const uint4& v, float (&f)[8], __nv_bfloat16) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// Store n consecutive fp32 values as fp32 or bf16 (round to nearest even).
+__device__ __forceinline__ void store_out(void* out, int64_t off, const float* v, int n, bool bf16, bool vec_ok) {
+  if (!bf16) {
+    float* o = (float*)out + off;
+    if (vec_ok && n == 4) {
+      *(float4*)o = make_float4(v[0], v[1], v[2], v[3]);
+    } else if (vec_ok && n == 8) {
+      ((float4*)o)[0] = make_float4(v[0], v[1], v[2], v[3]);
+      ((float4*)o)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+      for (int i = 0; i < n; ++i) o[i] = v[i];
+    }
+  } else {
+    __nv_bfloat16* o = (__nv_bfloat16*)out + off;
+    if (vec_ok && n == 8) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *(uint32_t*)&p;
+      }
+      *(uint4*)o = make_uint4(w[0], w[1], w[2], w[3]);
+    } else if (vec_ok && n == 4) {
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(v[2], v[3]);
+      *(uint2*)o = make_uint2(*(uint32_t*)&p0, *(uint32_t*)&p1);
+    } else {
+      for (int i = 0; i < n; ++i) o[i] = __float2bfloat16_rn(v[i]);
+    }
+  }
+}
+
+struct BagArgs {
+  const void* table;
+  int32_t d;
+  int64_t total_rows;
+  const void* idx;
+  int64_t n_idx;
+  const int64_t* offsets;
+  int32_t F, B;
+  int mapped;      // indices are table-local IDs of the field's table
+  int mean;
+  void* out;
+  int out_bf16;
+  int vec_out;     // output vectors are 16-byte aligned
+  int64_t sb, sf;
+  int* err;
+};
+
+// LPR lanes per row, CPL 16-byte chunks per lane (rows wider than 32 chunks).
+template <typename TT, int LPR, int CPL, typename IT>
+__global__ void __launch_bounds__(kBagThreads) bag_fwd_kernel(const BagArgs a, const __grid_constant__ FieldMap fm) {
+  constexpr int V = Vec<TT>::kN;
+  constexpr int R = 32 / LPR;  // rows per warp step
+  const int lane = threadIdx.x & 31;
+  const int grp = lane / LPR, sub = lane % LPR;
+  const int chunks = a.d / V;  // 16-byte chunks per row
+  const int64_t nbags = (int64_t)a.F * a.B;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const TT* table = (const TT*)a.table;
+  const IT* idx = (const IT*)a.idx;
+  for (int64_t bag = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; bag < nbags; bag += nwarps) {
+    const int f = (int)(bag / a.B);
+    const int b = (int)(bag - (int64_t)f * a.B);
+    int64_t o0 = a.offsets[bag], o1 = a.offsets[bag + 1];
+    const int64_t base = a.mapped ? fm.base[f] : 0;
+    const int64_t nrows = a.mapped ? fm.rows[f] : a.total_rows;
+    float acc[CPL][V];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c)
+#pragma unroll
+      for (int v = 0; v < V; ++v) acc[c][v] = 0.f;
+    if (o0 < 0 || o1 < o0 || o1 > a.n_idx) {
+      if (lane == 0) set_error(a.err, CTR_ERR_BAD_OFFSETS);
+      o0 = o1 = 0;
+    }
+    for (int64_t j0 = o0; j0 < o1; j0 += 32) {
+      const int cnt = (int)imin64(32, o1 - j0);
+      int64_t row = -1;
+      if (lane < cnt) {
+        int64_t id = (int64_t)idx[j0 + lane];
+        if (id < 0 || id >= nrows) set_error(a.err, CTR_ERR_INDEX_OUT_OF_RANGE);
+        else row = base + id;
+      }
+      for (int t0 = 0; t0 < cnt; t0 += R * kUnroll) {
+        uint4 buf[kUnroll][CPL];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int t = t0 + u * R + grp;
+          const int64_t r = __shfl_sync(kFull, row, t & 31);
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            const int ch = sub + c * LPR;
+            if (t < cnt && r >= 0 && ch < chunks) buf[u][c] = ldg16(table + r * a.d + (int64_t)ch * V);
+            else buf[u][c] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            float x[V];
+            unpack(buf[u][c], x, TT());
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[c][v] += x[v];
+          }
+      }
+    }
+    // combine the R lane groups (fixed butterfly order)
+#pragma unroll
+    for (int o = LPR; o < 32; o <<= 1)
+#pragma unroll
+      for (int c = 0; c < CPL; ++c)
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[c][v] += __shfl_xor_sync(kFull, acc[c][v], o);
+    if (a.mean) {
+      const int64_t len = o1 - o0;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c)
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[c][v] = len > 0 ? acc[c][v] / (float)len : 0.f;
+    }
+    if (grp == 0) {
+      const int64_t ob = (int64_t)b * a.sb + (int64_t)f * a.sf;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        const int ch = sub + c * LPR;
+        if (ch < chunks) store_out(a.out, ob + (int64_t)ch * V, acc[c], V, a.out_bf16, a.vec_out);
+      }
+    }
+  }
+}
+
+// Rows whose width is not a multiple of 16 bytes: one element per lane.
+template <typename TT, typename IT>
+__global__ void __launch_bounds__(kBagThreads) bag_fwd_scalar_kernel(const BagArgs a,
+                                                                     const __grid_constant__ FieldMap fm) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nbags = (int64_t)a.F * a.B;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const TT* table = (const TT*)a.table;
+  const IT* idx = (const IT*)a.idx;
+  for (int64_t bag = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; bag < nbags; bag += nwarps) {
+    const int f = (int)(bag / a.B);
+    const int b = (int)(bag - (int64_t)f * a.B);
+    int64_t o0 = a.offsets[bag], o1 = a.offsets[bag + 1];
+    const int64_t base = a.mapped ? fm.base[f] : 0;
+    const int64_t nrows = a.mapped ? fm.rows[f] : a.total_rows;
+    if (o0 < 0 || o1 < o0 || o1 > a.n_idx) {
+      if (lane == 0) set_error(a.err, CTR_ERR_BAD_OFFSETS);
+      o0 = o1 = 0;
+    }
+    for (int c0 = 0; c0 < a.d; c0 += 32) {
+      const int c = c0 + lane;
+      float acc = 0.f;
+      for (int64_t i = o0; i < o1; ++i) {
+        int64_t id = (int64_t)idx[i];
+        if (id < 0 || id >= nrows) {
+          if (lane == 0) set_error(a.err, CTR_ERR_INDEX_OUT_OF_RANGE);
+          continue;
+        }
+        if (c < a.d) acc += (float)table[(base + id) * a.d + c];
+      }
+      if (a.mean) acc = (o1 > o0) ? acc / (float)(o1 - o0) : 0.f;
+      if (c < a.d) store_out(a.out, (int64_t)b * a.sb + (int64_t)f * a.sf + c, &acc, 1, a.out_bf16, false);
+    }
+  }
+}
+
+template <typename K>
+int grid_for(K kernel, int64_t nbags) {
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBagThreads, 0);
+  int64_t want = ceil_div(nbags, kBagThreads / 32);
+  int64_t cap = (int64_t)std::max(per_sm, 1) * num_sms();
+  return (int)std::max<int64_t>(1, std::min(want, cap));
+}
+
+template <typename TT, typename IT>
+int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
+  constexpr int V = Vec<TT>::kN;
+  const int64_t nbags = (int64_t)a.F * a.B;
+  if (a.d % V != 0) {
+    auto k = bag_fwd_scalar_kernel<TT, IT>;
+    k<<<grid_for(k, nbags), kBagThreads, 0, s>>>(a, fm);
+    return launch_status();
+  }
+  const int chunks = a.d / V;
+#define CTR_LAUNCH(LPR, CPL)                                 \
+  {                                                          \
+    auto k = bag_fwd_kernel<TT, LPR, CPL, IT>;               \
+    k<<<grid_for(k, nbags), kBagThreads, 0, s>>>(a, fm);     \
+    return launch_status();                                  \
+  }
+  if (chunks <= 1) CTR_LAUNCH(1, 1)
+  if (chunks <= 2) CTR_LAUNCH(2, 1)
+  if (chunks <= 4) CTR_LAUNCH(4, 1)
+  if (chunks <= 8) CTR_LAUNCH(8, 1)
+  if (chunks <= 16) CTR_LAUNCH(16, 1)
+  if (chunks <= 32) CTR_LAUNCH(32, 1)
+  if (chunks <= 64) CTR_LAUNCH(32, 2)
+  if (chunks <= 128) CTR_LAUNCH(32, 4)
+#undef CTR_LAUNCH
+  return CTR_ERR_UNSUPPORTED;
+}
+
+// U[u] = table[unique_rows[u]]: one warp per row, 16-byte lanes.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const char* __restrict__ table, int64_t row_bytes,
+                                                          int64_t total_rows, const int64_t* __restrict__ unique_rows,
+                                                          const int64_t* __restrict__ n_unique, int64_t capacity,
+                                                          char* __restrict__ U, int* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n = imin64(*n_unique, capacity);
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const bool vec = (row_bytes % 16) == 0;
+  for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < n; u += nwarps) {
+    const int64_t r = unique_rows[u];
+    if (r < 0 || r >= total_rows) {
+      if (lane == 0) set_error(err, CTR_ERR_INDEX_OUT_OF_RANGE);
+      continue;
+    }
+    const char* src = table + r * row_bytes;
+    char* dst = U + u * row_bytes;
+    if (vec) {
+      for (int64_t o = (int64_t)lane * 16; o < row_bytes; o += 32 * 16) *(uint4*)(dst + o) = ldg16(src + o);
+    } else {
+      for (int64_t o = lane; o < row_bytes; o += 32) dst[o] = src[o];
+    }
+  }
+}
+
+}  // namespace
+}  // namespace ctr
+
+using namespace ctr;
+
+extern "C" size_t ctr_embedding_bag_workspace_size(void) { return kWsHeader; }
+
+extern "C" int ctr_embedding_bag_fwd(const void* table, ctr_dtype dtype, int32_t d, int64_t total_rows,
+                                     const void* indices, int indices_are_int32, int64_t n_indices,
+                                     const int64_t* offsets,
+                                     int32_t num_fields, int32_t batch, const int32_t* bag_to_table,
+                                     const int64_t* row_base, int32_t num_tables, ctr_pool pool, void* out,
+                                     ctr_dtype out_dtype, int64_t out_stride_b, int64_t out_stride_f, void* ws,
+                                     size_t ws_bytes, ctr_stream_t stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!table || !offsets || !out || d <= 0 || total_rows <= 0) return CTR_ERR_INVALID_ARG;
+  if (num_fields <= 0 || batch <= 0) return CTR_ERR_INVALID_ARG;
+  if ((dtype != CTR_F32 && dtype != CTR_BF16) || (out_dtype != CTR_F32 && out_dtype != CTR_BF16))
+    return CTR_ERR_INVALID_ARG;
+  if (pool != CTR_POOL_SUM && pool != CTR_POOL_MEAN) return CTR_ERR_INVALID_ARG;
+  if (out_stride_b < 0 || out_stride_f < 0) return CTR_ERR_INVALID_ARG;
+  if (!ws_valid(ws, ws_bytes, ctr_embedding_bag_workspace_size())) return CTR_ERR_WORKSPACE;
+  FieldMap fm;
+  int mapped = bag_to_table != nullptr;
+  if (mapped) {
+    if (!row_base) return CTR_ERR_INVALID_ARG;
+    if (int st = make_field_map(bag_to_table, row_base, num_fields, num_tables, &fm)) return st;
+    if (row_base[num_tables] > total_rows) return CTR_ERR_INVALID_ARG;
+  } else if (num_fields > CTR_MAX_FIELDS) {
+    return CTR_ERR_UNSUPPORTED;
+  }
+  if (n_indices < 0 || (n_indices > 0 && !indices)) return CTR_ERR_INVALID_ARG;
+  BagArgs a;
+  a.table = table;
+  a.d = d;
+  a.total_rows = total_rows;
+  a.idx = indices;
+  a.n_idx = n_indices;
+  a.offsets = offsets;
+  a.F = num_fields;
+  a.B = batch;
+  a.mapped = mapped;
+  a.mean = pool == CTR_POOL_MEAN;
+  a.out = out;
+  a.out_bf16 = out_dtype == CTR_BF16;
+  const int vout = out_dtype == CTR_BF16 ? 8 : 4;
+  a.vec_out = ((uintptr_t)out % 16 == 0) && (out_stride_b % vout == 0) && (out_stride_f % vout == 0) && (d % vout == 0);
+  a.sb = out_stride_b;
+  a.sf = out_stride_f;
+  a.err = (int*)ws;
+  if ((uintptr_t)table % 16 != 0) return CTR_ERR_INVALID_ARG;
+  if (dtype == CTR_F32)
+    return indices_are_int32 ? launch_bag_fwd<float, int32_t>(a, fm, s) : launch_bag_fwd<float, int64_t>(a, fm, s);
+  return indices_are_int32 ? launch_bag_fwd<__nv_bfloat16, int32_t>(a, fm, s)
+                           : launch_bag_fwd<__nv_bfloat16, int64_t>(a, fm, s);
+}
+
+extern "C" int ctr_gather_rows(const void* table, ctr_dtype dtype, int32_t d, int64_t total_rows,
+                               const int64_t* unique_rows, const int64_t* n_unique, int64_t capacity, void* U,
+                               void* ws, size_t ws_bytes, ctr_stream_t stream) {
+  if (!table || !unique_rows || !n_unique || !U || d <= 0 || total_rows <= 0 || capacity < 0)
+    return CTR_ERR_INVALID_ARG;
+  if (dtype != CTR_F32 && dtype != CTR_BF16) return CTR_ERR_INVALID_ARG;
+  if (!ws_valid(ws, ws_bytes, kWsHeader)) return CTR_ERR_WORKSPACE;
+  if (capacity == 0) return CTR_OK;
+  const int64_t row_bytes = (int64_t)d * (dtype == CTR_F32 ? 4 : 2);
+  if (row_bytes % 16 == 0 && (((uintptr_t)table | (uintptr_t)U) % 16) != 0) return CTR_ERR_INVALID_ARG;
+  int64_t blocks = imin64(ceil_div(capacity, 8), (int64_t)num_sms() * 16);
+  gather_rows_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
+      (const char*)table, row_bytes, total_rows, unique_rows, n_unique, capacity, (char*)U, (int*)ws);
+  return launch_status();
+}

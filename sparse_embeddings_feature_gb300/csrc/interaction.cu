@@ -1,0 +1,293 @@
+// a3/a4. Pairwise dot interaction (CUDA-core kernels) and its derivative.
+//
+// Sources: "Meta DLRM", section 02 (dot products between all pairs of the
+// embedding vectors and the processed dense features, cross terms only);
+// "DHEN" notes, section 3.1, Eq. (3) (the pairwise products are concatenated
+// with the dense features).  The derivative is not on the pages.
+//
+// Output layout per sample: [ x_0 (dense, d values) | <x_i, x_j> for
+// 1 <= i < n, 0 <= j < i, row by row ].
+//
+// fp32, n = 27, d = 128 (the DLRM shapes): one warp per sample.  Lane l holds
+// columns 4l..4l+3 of all n vectors in registers (one 16-byte load per vector,
+// coalesced across the warp), forms the partial dots of 32 pairs at a time,
+// and a transpose-reduction (five xor-shuffle stages, halving the live values
+// each stage) leaves pair 32g + l fully summed in lane l, so the stores are
+// coalesced too.  Everything is fp32 FMA in a fixed order.
+// The backward keeps the same register layout: dX_i = sum_j dZ_ij x_j, with
+// the 351 upstream pair gradients of the sample staged in shared memory and
+// read as broadcasts.
+// Other shapes (and bf16 shapes the tensor-core kernel does not cover) use a
+// generic kernel: one block per sample, vectors staged in shared memory as
+// fp32, one thread per pair.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace ctr {
+
+int interaction_bf16_tc(const void* X, int32_t batch, int32_t n, int32_t d, void* out, int* err, cudaStream_t s);
+bool interaction_bf16_tc_supported(int32_t n, int32_t d);
+
+namespace {
+
+constexpr int kIntWarps = 4;
+
+struct PairTable {
+  unsigned char i[32 * 32];
+  unsigned char j[32 * 32];
+};
+
+template <int N>
+constexpr PairTable make_pairs() {
+  PairTable t{};
+  int p = 0;
+  for (int i = 1; i < N; ++i)
+    for (int j = 0; j < i; ++j) {
+      t.i[p] = (unsigned char)i;
+      t.j[p] = (unsigned char)j;
+      ++p;
+    }
+  return t;
+}
+
+template <int N, int D>
+__global__ void __launch_bounds__(kIntWarps * 32) interaction_fwd_f32_regs(const float* __restrict__ X, int32_t batch,
+                                                                          float* __restrict__ out) {
+  static_assert(D == 128, "4 columns per lane");
+  constexpr int P = N * (N - 1) / 2;
+  constexpr int G = (P + 31) / 32;
+  constexpr int W = D + P;
+  constexpr PairTable pt = make_pairs<N>();
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < batch; b += nwarps) {
+    const float* xb = X + b * (int64_t)N * D + lane * 4;
+    float x[N][4];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      float4 v = __ldcs((const float4*)(xb + i * D));
+      x[i][0] = v.x;
+      x[i][1] = v.y;
+      x[i][2] = v.z;
+      x[i][3] = v.w;
+    }
+    float* ob = out + b * (int64_t)W;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) __stcs(ob + lane * 4 + c, x[0][c]);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float v[32];
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        const int p = g * 32 + t;
+        if (p < P) {
+          const int i = pt.i[p], j = pt.j[p];
+          float s = x[i][0] * x[j][0];
+          s = fmaf(x[i][1], x[j][1], s);
+          s = fmaf(x[i][2], x[j][2], s);
+          s = fmaf(x[i][3], x[j][3], s);
+          v[t] = s;
+        } else {
+          v[t] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int st = 16; st >= 1; st >>= 1) {
+        const bool up = lane & st;
+#pragma unroll
+        for (int k = 0; k < st; ++k) {
+          const float keep = up ? v[k + st] : v[k];
+          const float send = up ? v[k] : v[k + st];
+          v[k] = keep + __shfl_xor_sync(kFull, send, st);
+        }
+      }
+      const int p = g * 32 + lane;
+      if (p < P) __stcs(ob + D + p, v[0]);
+    }
+  }
+}
+
+template <int N, int D>
+__global__ void __launch_bounds__(kIntWarps * 32) interaction_bwd_f32_regs(const float* __restrict__ dout,
+                                                                          const float* __restrict__ X, int32_t batch,
+                                                                          float* __restrict__ dX) {
+  static_assert(D == 128, "4 columns per lane");
+  constexpr int P = N * (N - 1) / 2;
+  constexpr int W = D + P;
+  __shared__ float sdz[kIntWarps][P + 1];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  float* dz = sdz[warp];
+  for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < batch; b += nwarps) {
+    const float* xb = X + b * (int64_t)N * D + lane * 4;
+    const float* gb = dout + b * (int64_t)W;
+    float x[N][4];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      float4 v = __ldcs((const float4*)(xb + i * D));
+      x[i][0] = v.x;
+      x[i][1] = v.y;
+      x[i][2] = v.z;
+      x[i][3] = v.w;
+    }
+    __syncwarp();
+    for (int p = lane; p < P; p += 32) dz[p] = __ldcs(gb + D + p);
+    float dense[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) dense[c] = __ldcs(gb + lane * 4 + c);
+    __syncwarp();
+    float* ob = dX + b * (int64_t)N * D + lane * 4;
+#pragma unroll 1
+    for (int i = 0; i < N; ++i) {
+      float acc[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[c] = (i == 0) ? dense[c] : 0.f;
+#pragma unroll
+      for (int j = 0; j < N; ++j) {
+        if (j == i) continue;
+        const int hi = i > j ? i : j, lo = i > j ? j : i;
+        const float g = dz[hi * (hi - 1) / 2 + lo];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[c] = fmaf(g, x[j][c], acc[c]);
+      }
+      __stcs((float4*)(ob + i * D), make_float4(acc[0], acc[1], acc[2], acc[3]));
+    }
+  }
+}
+
+template <typename TT>
+__device__ __forceinline__ float to_f(TT v);
+template <>
+__device__ __forceinline__ float to_f<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+__device__ __forceinline__ void put(float* o, float v) { *o = v; }
+__device__ __forceinline__ void put(__nv_bfloat16* o, float v) { *o = __float2bfloat16_rn(v); }
+
+constexpr int kGenThreads = 128;
+
+// Generic: one block per sample (grid-stride), vectors in shared memory.
+template <typename TT>
+__global__ void __launch_bounds__(kGenThreads) interaction_fwd_generic(const TT* __restrict__ X, int32_t batch,
+                                                                      int32_t n, int32_t d, TT* __restrict__ out) {
+  extern __shared__ float xs[];  // [n][d]
+  const int64_t P = (int64_t)n * (n - 1) / 2;
+  const int64_t W = d + P;
+  for (int64_t b = blockIdx.x; b < batch; b += gridDim.x) {
+    const TT* xb = X + b * (int64_t)n * d;
+    for (int e = threadIdx.x; e < n * d; e += blockDim.x) xs[e] = to_f(xb[e]);
+    __syncthreads();
+    TT* ob = out + b * W;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) ob[c] = xb[c];
+    for (int64_t p = threadIdx.x; p < P; p += blockDim.x) {
+      // row i of pair p: largest i with i(i-1)/2 <= p
+      int i = (int)((1.0 + sqrt(1.0 + 8.0 * (double)p)) * 0.5);
+      while ((int64_t)i * (i - 1) / 2 > p) --i;
+      while ((int64_t)(i + 1) * i / 2 <= p) ++i;
+      const int j = (int)(p - (int64_t)i * (i - 1) / 2);
+      const float* a = xs + i * d;
+      const float* c = xs + j * d;
+      float s = 0.f;
+      for (int k = 0; k < d; ++k) s = fmaf(a[k], c[k], s);
+      put(ob + d + p, s);
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kGenThreads) interaction_bwd_generic(const float* __restrict__ dout,
+                                                                      const float* __restrict__ X, int32_t batch,
+                                                                      int32_t n, int32_t d, float* __restrict__ dX) {
+  extern __shared__ float sm[];  // xs [n][d], dz [P]
+  const int64_t P = (int64_t)n * (n - 1) / 2;
+  const int64_t W = d + P;
+  float* xs = sm;
+  float* dz = sm + (int64_t)n * d;
+  for (int64_t b = blockIdx.x; b < batch; b += gridDim.x) {
+    const float* xb = X + b * (int64_t)n * d;
+    const float* gb = dout + b * W;
+    for (int e = threadIdx.x; e < n * d; e += blockDim.x) xs[e] = xb[e];
+    for (int64_t p = threadIdx.x; p < P; p += blockDim.x) dz[p] = gb[d + p];
+    __syncthreads();
+    for (int e = threadIdx.x; e < n * d; e += blockDim.x) {
+      const int i = e / d, c = e % d;
+      float acc = i == 0 ? gb[c] : 0.f;
+      for (int j = 0; j < n; ++j) {
+        if (j == i) continue;
+        const int hi = i > j ? i : j, lo = i > j ? j : i;
+        acc = fmaf(dz[(int64_t)hi * (hi - 1) / 2 + lo], xs[j * d + c], acc);
+      }
+      dX[b * (int64_t)n * d + e] = acc;
+    }
+    __syncthreads();
+  }
+}
+
+template <typename K>
+int grid_blocks(K kernel, int threads, size_t smem, int64_t work_units) {
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+  int64_t cap = (int64_t)std::max(per_sm, 1) * num_sms();
+  return (int)std::max<int64_t>(1, std::min(work_units, cap));
+}
+
+}  // namespace
+}  // namespace ctr
+
+using namespace ctr;
+
+extern "C" size_t ctr_interaction_workspace_size(void) { return kWsHeader; }
+
+extern "C" int ctr_dot_interaction(const void* X, ctr_dtype dtype, int32_t batch, int32_t n, int32_t d, void* out,
+                                   void* ws, size_t ws_bytes, ctr_stream_t stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!X || !out || batch < 0 || n < 1 || d < 1) return CTR_ERR_INVALID_ARG;
+  if (dtype != CTR_F32 && dtype != CTR_BF16) return CTR_ERR_INVALID_ARG;
+  if (!ws_valid(ws, ws_bytes, kWsHeader)) return CTR_ERR_WORKSPACE;
+  if (batch == 0) return CTR_OK;
+  if (dtype == CTR_F32 && n == 27 && d == 128 && (uintptr_t)X % 16 == 0) {
+    auto k = interaction_fwd_f32_regs<27, 128>;
+    k<<<grid_blocks(k, kIntWarps * 32, 0, ceil_div(batch, kIntWarps)), kIntWarps * 32, 0, s>>>(
+        (const float*)X, batch, (float*)out);
+    return launch_status();
+  }
+  if (dtype == CTR_BF16 && interaction_bf16_tc_supported(n, d) && (uintptr_t)X % 16 == 0 &&
+      (uintptr_t)out % 16 == 0)
+    return interaction_bf16_tc(X, batch, n, d, out, (int*)ws, s);
+  const size_t smem = (size_t)n * d * sizeof(float);
+  if (smem > 48 * 1024) return CTR_ERR_UNSUPPORTED;
+  if (dtype == CTR_F32) {
+    auto k = interaction_fwd_generic<float>;
+    k<<<grid_blocks(k, kGenThreads, smem, batch), kGenThreads, smem, s>>>((const float*)X, batch, n, d, (float*)out);
+  } else {
+    auto k = interaction_fwd_generic<__nv_bfloat16>;
+    k<<<grid_blocks(k, kGenThreads, smem, batch), kGenThreads, smem, s>>>((const __nv_bfloat16*)X, batch, n, d,
+                                                                           (__nv_bfloat16*)out);
+  }
+  return launch_status();
+}
+
+extern "C" int ctr_dot_interaction_bwd(const float* dout, const float* X, int32_t batch, int32_t n, int32_t d,
+                                       float* dX, void* ws, size_t ws_bytes, ctr_stream_t stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!dout || !X || !dX || batch < 0 || n < 1 || d < 1) return CTR_ERR_INVALID_ARG;
+  if (!ws_valid(ws, ws_bytes, kWsHeader)) return CTR_ERR_WORKSPACE;
+  if (batch == 0) return CTR_OK;
+  if (n == 27 && d == 128 && (uintptr_t)X % 16 == 0 && (uintptr_t)dX % 16 == 0) {
+    auto k = interaction_bwd_f32_regs<27, 128>;
+    k<<<grid_blocks(k, kIntWarps * 32, 0, ceil_div(batch, kIntWarps)), kIntWarps * 32, 0, s>>>(dout, X, batch, dX);
+    return launch_status();
+  }
+  const size_t smem = ((size_t)n * d + (size_t)n * (n - 1) / 2) * sizeof(float);
+  if (smem > 48 * 1024) return CTR_ERR_UNSUPPORTED;
+  auto k = interaction_bwd_generic;
+  k<<<grid_blocks(k, kGenThreads, smem, batch), kGenThreads, smem, s>>>(dout, X, batch, n, d, dX);
+  return launch_status();
+}

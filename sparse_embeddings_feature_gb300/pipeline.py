@@ -1,0 +1,181 @@
+"""Device buffers and call sequence of one step of the CTR path.
+
+``CtrPath`` owns the device memory of one workload (tables, index buffers,
+dedup outputs, interaction tensors, workspaces) through torch, and runs the
+step as a sequence of libctr calls on one CUDA stream:
+
+    dedup -> pooled gather (into the interaction input X) -> dot interaction
+          -> interaction backward -> per-unique-row gradient reduce + SGD update
+
+Which steps a workload runs follows its configuration (forward-only
+workloads stop after the interaction; the TensorNet-style workload pools from
+the batch-sized unique-row matrix).  No arithmetic of the method happens here.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+
+from . import ctr
+from .workload import Config
+
+TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+class CtrPath:
+    def __init__(self, cfg: Config, n_ids: int, device="cuda", fill: bool = True, table_chunk_rows: int = 1 << 24):
+        self.cfg = cfg
+        self.dev = torch.device(device)
+        self.n_ids = int(n_ids)
+        F, B, d, n = cfg.num_fields, cfg.batch, cfg.d, cfg.n_vectors
+        tdt = TORCH_DT[cfg.dtype]
+        self.table = torch.empty((cfg.total_rows, d), dtype=tdt, device=self.dev)
+        if fill:
+            self.fill_table(table_chunk_rows)
+        cap = max(self.n_ids, 1)
+        i64, i32 = torch.int64, torch.int32
+        self.ids = torch.empty(cap, dtype=i64, device=self.dev)
+        self.offsets = torch.empty(F * B + 1, dtype=i64, device=self.dev)
+        self.unique_rows = torch.empty(cap, dtype=i64, device=self.dev)
+        self.n_unique = torch.zeros(1, dtype=i64, device=self.dev)
+        self.inverse = torch.empty(cap, dtype=i32, device=self.dev)
+        self.sorted_pos = torch.empty(cap, dtype=i32, device=self.dev)
+        self.sorted_bag = torch.empty(cap, dtype=i32, device=self.dev)
+        self.run_offsets = torch.empty(cap + 1, dtype=i32, device=self.dev)
+        self.unique_offsets = torch.empty(cfg.num_tables + 1, dtype=i64, device=self.dev)
+        self.U = torch.empty((cap, d), dtype=tdt, device=self.dev) if cfg.dedup_gather else None
+        # interaction input: slot 0 = dense, slots 1..F = pooled
+        self.X = torch.zeros((B, n, d), dtype=tdt, device=self.dev)
+        self.out = torch.empty((B, cfg.out_width), dtype=tdt, device=self.dev) if cfg.interaction else None
+        self.pooled = None if cfg.interaction else torch.empty((B, F, d), dtype=tdt, device=self.dev)
+        self.dout = torch.empty((B, cfg.out_width), dtype=torch.float32, device=self.dev) \
+            if cfg.backward == "full" else None
+        self.dX = torch.empty((B, n, d), dtype=torch.float32, device=self.dev) if cfg.backward == "full" else None
+        self.grad_pooled = torch.empty((B, F, d), dtype=torch.float32, device=self.dev) \
+            if cfg.backward == "pooled_grad" else None
+        self.grad_unique = None
+        total_rows = cfg.total_rows
+        self.ws_dedup = ctr.workspace(ctr.ctr_dedup_workspace_size(cap, F, B, total_rows), self.dev)
+        self.ws_bag = ctr.workspace(ctr.ctr_embedding_bag_workspace_size(), self.dev)
+        self.ws_int = ctr.workspace(ctr.ctr_interaction_workspace_size(), self.dev)
+        self.ws_bwd = ctr.workspace(ctr.ctr_bwd_update_workspace_size(cap, d), self.dev)
+        self.b2t = np.asarray(cfg.field_to_table, dtype=np.int32)
+        self.row_base = cfg.row_base
+
+    # -- inputs -----------------------------------------------------------
+    def fill_table(self, chunk_rows: int = 1 << 24) -> None:
+        cfg = self.cfg
+        flat = self.table.view(-1)
+        for r0 in range(0, cfg.total_rows, chunk_rows):
+            r1 = min(cfg.total_rows, r0 + chunk_rows)
+            ctr.ctr_fill_table(flat[r0 * cfg.d:r1 * cfg.d], cfg.d, r0, cfg.fill_kind, cfg.fill_seed, cfg.fill_scale)
+
+    def upload(self, w: Dict[str, np.ndarray], non_blocking: bool = False) -> None:
+        """Copy a workload's host arrays into the device buffers."""
+        n = w["ids"].size
+        assert n == self.n_ids, (n, self.n_ids)
+        if n:
+            self.ids[:n].copy_(torch.from_numpy(w["ids"]), non_blocking=non_blocking)
+        self.offsets.copy_(torch.from_numpy(w["offsets"]), non_blocking=non_blocking)
+        dense = w["dense"]
+        dt = torch.from_numpy(dense.view(np.int16)).view(torch.bfloat16) if self.cfg.dtype == "bf16" \
+            else torch.from_numpy(dense)
+        self.X[:, 0, :].copy_(dt, non_blocking=non_blocking)
+        if self.grad_pooled is not None and "grad_pooled" in w:
+            self.grad_pooled.copy_(torch.from_numpy(w["grad_pooled"]), non_blocking=non_blocking)
+        if self.dout is not None and "dout" in w:
+            self.dout.copy_(torch.from_numpy(w["dout"]), non_blocking=non_blocking)
+
+    def reset_status(self) -> None:
+        for ws in (self.ws_dedup, self.ws_bag, self.ws_int, self.ws_bwd):
+            ctr.ctr_status_reset(ws)
+
+    def check_status(self) -> Dict[str, int]:
+        return {k: ctr.ctr_check_status(ws) for k, ws in
+                (("dedup", self.ws_dedup), ("bag", self.ws_bag), ("interaction", self.ws_int), ("bwd", self.ws_bwd))}
+
+    # -- steps ------------------------------------------------------------
+    def dedup(self) -> None:
+        cfg = self.cfg
+        ctr.ctr_dedup(self.ids, self.offsets, cfg.num_fields, cfg.batch, self.b2t, self.row_base, self.unique_rows,
+                      self.n_unique, self.inverse, self.sorted_pos, self.sorted_bag, self.run_offsets,
+                      self.unique_offsets, self.ws_dedup, n_ids=self.n_ids)
+
+    def forward(self) -> None:
+        cfg = self.cfg
+        F, B, d, n = cfg.num_fields, cfg.batch, cfg.d, cfg.n_vectors
+        pool = ctr.POOL_MEAN if cfg.pool == "mean" else ctr.POOL_SUM
+        if self.pooled is not None:
+            out, sb, sf = self.pooled, F * d, d
+        else:
+            out, sb, sf = self.X[:, 1:, :], n * d, d
+        if cfg.dedup_gather:
+            ctr.ctr_gather_rows(self.table, d, self.unique_rows, self.n_unique, self.U, self.ws_bag)
+            ctr.ctr_embedding_bag_fwd(self.U, d, self.inverse, self.offsets, F, B, None, None, pool, out, sb, sf,
+                                      self.ws_bag, n_indices=self.n_ids)
+        else:
+            ctr.ctr_embedding_bag_fwd(self.table, d, self.ids, self.offsets, F, B, self.b2t, self.row_base, pool,
+                                      out, sb, sf, self.ws_bag, n_indices=self.n_ids)
+
+    def interaction(self) -> None:
+        cfg = self.cfg
+        ctr.ctr_dot_interaction(self.X, cfg.n_vectors, cfg.d, self.out, self.ws_int)
+
+    def interaction_bwd(self) -> None:
+        cfg = self.cfg
+        ctr.ctr_dot_interaction_bwd(self.dout, self.X, cfg.n_vectors, cfg.d, self.dX, self.ws_int)
+
+    def bwd_update(self, grad_unique_out: Optional[torch.Tensor] = None) -> None:
+        cfg = self.cfg
+        F, B, d, n = cfg.num_fields, cfg.batch, cfg.d, cfg.n_vectors
+        pool = ctr.POOL_MEAN if cfg.pool == "mean" else ctr.POOL_SUM
+        if self.dX is not None:
+            G, sb, sf = self.dX[:, 1:, :], n * d, d
+        else:
+            G, sb, sf = self.grad_pooled, F * d, d
+        ctr.ctr_embedding_bag_bwd_update(G, sb, sf, self.offsets, F, B, pool, self.unique_rows, self.n_unique,
+                                         self.run_offsets, self.sorted_bag, max(self.n_ids, 1), cfg.lr, self.table, d,
+                                         grad_unique_out, self.ws_bwd)
+
+    def step(self) -> None:
+        """One pass of the workload's hot path."""
+        cfg = self.cfg
+        if cfg.backward != "none" or cfg.dedup_gather:
+            self.dedup()
+        self.forward()
+        if cfg.interaction:
+            self.interaction()
+        if cfg.backward == "full":
+            self.interaction_bwd()
+        if cfg.backward != "none":
+            self.bwd_update()
+
+    def launches_per_step(self) -> int:
+        """Number of libctr kernel launches one step() makes (for the benchmark's launch count)."""
+        cfg = self.cfg
+        k = 0
+        n = max(self.n_ids, 1)
+        if cfg.backward != "none" or cfg.dedup_gather:
+            bits = 1
+            while bits < 32 and (1 << bits) < cfg.total_rows:
+                bits += 1
+            passes = (bits + 7) // 8
+            nb = (bits + passes - 1) // passes
+            tiles = -(-n // 4096)
+            k += 1 + passes * (2 + _scan_launches(tiles << nb, 4096)) + 1 + _scan_launches(tiles, 4096) + 1
+        k += 2 if cfg.dedup_gather else 1
+        if cfg.interaction:
+            k += 1
+        if cfg.backward == "full":
+            k += 1
+        if cfg.backward != "none":
+            k += 1 + _scan_launches(n, 2048) + _scan_launches(n, 4096) + 1 + 1 + 1
+        return k
+
+
+def _scan_launches(n: int, tile: int) -> int:
+    if n <= tile:
+        return 1
+    return 2 + _scan_launches(-(-n // tile), tile)

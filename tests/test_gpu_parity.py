@@ -1,0 +1,498 @@
+"""GPU parity: every libctr call against the CPU oracle on the same seeded inputs.
+
+Indexing outputs (dedup) must match bit for bit; floating-point outputs within
+the tolerances of tests/_tol.py.  Sizes span several tiles of every kernel and
+end in ragged tails; edge cases cover empty bags and batches, repeated IDs,
+IDs at the ends of their tables, long runs and the degenerate shapes.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from sparse_embeddings_feature_gb300 import ctr
+from sparse_embeddings_feature_gb300 import workload as W
+from sparse_embeddings_feature_gb300.pipeline import CtrPath
+
+from _tol import bf16_close, f32_close
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _t(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.to(DEV)
+
+
+def _np(t):
+    torch.cuda.synchronize()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def _gen(cfg):
+    return (cfg.fill_kind, cfg.fill_seed, cfg.fill_scale)
+
+
+def _csr(lens, rng, rows_of_field, B):
+    offsets = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    ids = np.empty(int(offsets[-1]), dtype=np.int64)
+    for bag in range(lens.size):
+        f = bag // B
+        ids[offsets[bag]:offsets[bag + 1]] = rng.integers(0, rows_of_field[f], size=lens[bag])
+    return ids, offsets
+
+
+def gpu_dedup(ids, offsets, F, B, b2t, row_base):
+    n = int(offsets[-1])
+    cap = max(n, 1)
+    T = len(row_base) - 1
+    dev = {k: torch.full((cap,), -7, dtype=torch.int32, device=DEV)
+           for k in ("inverse", "sorted_pos", "sorted_bag")}
+    uq = torch.full((cap,), -7, dtype=torch.int64, device=DEV)
+    nu = torch.full((1,), -7, dtype=torch.int64, device=DEV)
+    ro = torch.full((cap + 1,), -7, dtype=torch.int32, device=DEV)
+    uo = torch.full((T + 1,), -7, dtype=torch.int64, device=DEV)
+    ws = ctr.workspace(ctr.ctr_dedup_workspace_size(cap, F, B, int(row_base[-1])))
+    ids_d = _t(ids if n else np.zeros(1, np.int64))
+    ctr.ctr_dedup(ids_d, _t(offsets), F, B, b2t, row_base, uq, nu, dev["inverse"], dev["sorted_pos"],
+                  dev["sorted_bag"], ro, uo, ws, n_ids=n)
+    st = ctr.ctr_check_status(ws)
+    k = int(_np(nu)[0])
+    return st, {"unique_rows": _np(uq)[:k], "n_unique": k, "inverse": _np(dev["inverse"])[:n],
+                "sorted_pos": _np(dev["sorted_pos"])[:n], "sorted_bag": _np(dev["sorted_bag"])[:n],
+                "run_offsets": _np(ro)[:k + 1], "unique_offsets": _np(uo)}
+
+
+def assert_dedup_equal(got, ref):
+    assert got["n_unique"] == ref["n_unique"]
+    for k in ("unique_rows", "inverse", "sorted_pos", "sorted_bag", "run_offsets", "unique_offsets"):
+        np.testing.assert_array_equal(got[k], ref[k], err_msg=k)
+
+
+# ---------------------------------------------------------------------------
+# input generator: device fill == oracle fill, bit for bit
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["dlrm_fp32", "bf16_large"])
+def test_fill_table_bit_exact(name):
+    cfg = W.CONFIGS[name]
+    d = cfg.d
+    rows = 5000
+    row0 = 3_999_000
+    tdt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
+    t = torch.empty((rows, d), dtype=tdt, device=DEV)
+    ctr.ctr_fill_table(t, d, row0, cfg.fill_kind, cfg.fill_seed, cfg.fill_scale)
+    ref = O.table_rows(cfg.fill_kind, cfg.fill_seed, cfg.fill_scale, d, np.arange(row0, row0 + rows))
+    np.testing.assert_array_equal(_np(t), ref)
+
+
+# ---------------------------------------------------------------------------
+# a1 dedup
+# ---------------------------------------------------------------------------
+DEDUP_CASES = {
+    "tiny": W.CONFIGS["tiny"],
+    "dlrm_fp32": W.CONFIGS["dlrm_fp32"],
+    "tensornet_b512": W.CONFIGS["tensornet"].shrink(batch=512),
+    "full_step_b256": W.CONFIGS["full_step"].shrink(batch=256),
+    "bf16_b128": W.CONFIGS["bf16_large"].shrink(batch=128),
+}
+
+
+@pytest.mark.parametrize("name", list(DEDUP_CASES))
+def test_dedup_configs(name):
+    cfg = DEDUP_CASES[name]
+    w = W.make_workload(cfg, with_grads=False)
+    args = (w["ids"], w["offsets"], cfg.num_fields, cfg.batch, w["bag_to_table"], w["row_base"])
+    st, got = gpu_dedup(*args)
+    assert st == 0, ctr.status_string(st)
+    assert_dedup_equal(got, O.dedup(*args))
+
+
+def test_dedup_edge_cases():
+    rng = np.random.default_rng(0)
+    # (F, B, rows per table, bag lengths builder)
+    cases = []
+    F, B = 3, 50
+    rows = [7, 1, 100_000]
+    lens = rng.integers(0, 4, size=F * B)
+    lens[:20] = 0                                     # empty bags interleaved
+    cases.append((F, B, rows, lens, None))
+    cases.append((2, 10, [5, 5], np.zeros(20, np.int64), None))   # every bag empty: n_ids = 0
+    lens = np.full(4, 3000)                           # one ID repeated: long runs, ragged tail
+    cases.append((1, 4, [9], lens, "same"))
+    lens = rng.integers(4090, 4100, size=6)           # n_ids just around tile multiples
+    cases.append((2, 3, [2 ** 20, 2 ** 20], lens, "ends"))
+    for F, B, rows, lens, mode in cases:
+        b2t = np.arange(F, dtype=np.int32)
+        rb = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+        ids, offsets = _csr(np.asarray(lens), rng, rows, B)
+        if mode == "same":
+            ids[:] = 4
+        if mode == "ends":
+            ids[::2] = np.array(rows)[np.repeat(np.arange(F), [offsets[(f + 1) * B] - offsets[f * B]
+                                                                for f in range(F)])][::2] - 1
+            ids[1::3] = 0
+        st, got = gpu_dedup(ids, offsets, F, B, b2t, rb)
+        assert st == 0
+        ref = O.dedup(ids, offsets, F, B, b2t, rb)
+        assert_dedup_equal(got, ref)
+
+
+def test_dedup_tables_sharing_and_empty_tables():
+    rng = np.random.default_rng(5)
+    F, B = 4, 64
+    rows = [300, 0, 50]                               # table 1 is empty; fields 0 and 3 share table 0
+    b2t = np.array([0, 2, 2, 0], dtype=np.int32)
+    rb = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    lens = rng.integers(0, 9, size=F * B)
+    ids, offsets = _csr(lens, rng, [rows[t] for t in b2t], B)
+    st, got = gpu_dedup(ids, offsets, F, B, b2t, rb)
+    assert st == 0
+    assert_dedup_equal(got, O.dedup(ids, offsets, F, B, b2t, rb))
+
+
+def test_dedup_flags_out_of_range_id():
+    ids = np.array([0, 3, 5, 1], dtype=np.int64)      # 5 is outside a 5-row table
+    offsets = np.array([0, 2, 4], dtype=np.int64)
+    st, _ = gpu_dedup(ids, offsets, 1, 2, np.array([0], np.int32), np.array([0, 5], np.int64))
+    assert st == -4, ctr.status_string(st)
+
+
+def test_dedup_flags_bad_offsets():
+    ids = np.zeros(4, dtype=np.int64)
+    offsets = np.array([0, 3, 2, 4], dtype=np.int64)  # not monotone
+    st, _ = gpu_dedup(ids, offsets, 1, 3, np.array([0], np.int32), np.array([0, 5], np.int64))
+    assert st == -8
+
+
+def test_dedup_is_deterministic():
+    cfg = DEDUP_CASES["full_step_b256"]
+    w = W.make_workload(cfg, with_grads=False)
+    args = (w["ids"], w["offsets"], cfg.num_fields, cfg.batch, w["bag_to_table"], w["row_base"])
+    _, a = gpu_dedup(*args)
+    _, b = gpu_dedup(*args)
+    assert_dedup_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# a2 pooled embedding bag
+# ---------------------------------------------------------------------------
+def _fwd_case(cfg, w, table=None, out_dtype=None):
+    """GPU pooled output [B, F, d] (fp32 array or bf16 bits) for cfg's tables."""
+    F, B, d = cfg.num_fields, cfg.batch, cfg.d
+    tdt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
+    odt = tdt if out_dtype is None else out_dtype
+    if table is None:
+        tab = torch.empty((cfg.total_rows, d), dtype=tdt, device=DEV)
+        ctr.ctr_fill_table(tab, d, 0, cfg.fill_kind, cfg.fill_seed, cfg.fill_scale)
+    else:
+        tab = _t(table)
+    out = torch.full((B, F, d), float("nan"), dtype=odt, device=DEV)
+    ws = ctr.workspace(ctr.ctr_embedding_bag_workspace_size())
+    pool = ctr.POOL_MEAN if cfg.pool == "mean" else ctr.POOL_SUM
+    ctr.ctr_embedding_bag_fwd(tab, d, _t(w["ids"]), _t(w["offsets"]), F, B, w["bag_to_table"], w["row_base"], pool,
+                              out, F * d, d, ws)
+    assert ctr.ctr_check_status(ws) == 0
+    return _np(out)
+
+
+FWD_CASES = {
+    "tiny": W.CONFIGS["tiny"],
+    "dlrm_fp32": W.CONFIGS["dlrm_fp32"],
+    "bf16_mean_b256": W.CONFIGS["bf16_large"].shrink(batch=256, rows_per_table=tuple([200_000] * 26)),
+    "full_step_b128": W.CONFIGS["full_step"].shrink(batch=128, rows_per_table=tuple([100_000] * 26)),
+}
+
+
+@pytest.mark.parametrize("name", list(FWD_CASES))
+def test_embedding_bag_fwd_configs(name):
+    cfg = FWD_CASES[name]
+    w = W.make_workload(cfg, with_grads=False)
+    got = _fwd_case(cfg, w)
+    ref, mag = O.embedding_bag_fwd(w["ids"], w["offsets"], cfg.num_fields, cfg.batch, w["bag_to_table"],
+                                   w["row_base"], cfg.d, pool=cfg.pool, dtype=cfg.dtype, gen=_gen(cfg),
+                                   with_mag=True)
+    depth = int(np.diff(w["offsets"]).max()) + 1
+    if cfg.dtype == "f32":
+        f32_close(got, ref, mag, depth, what=name)
+    else:
+        bf16_close(got, ref, mag, depth, atol=1e-5, what=name)
+
+
+@pytest.mark.parametrize("d,dtype,pool", [(12, "f32", "sum"), (20, "f32", "mean"), (32, "f32", "sum"),
+                                          (64, "f32", "mean"), (256, "f32", "sum"), (512, "f32", "sum"),
+                                          (8, "bf16", "sum"), (16, "bf16", "mean"), (128, "bf16", "sum"),
+                                          (36, "bf16", "mean")])
+def test_embedding_bag_fwd_shapes(d, dtype, pool):
+    cfg = W.CONFIGS["dlrm_fp32"].shrink(batch=97, num_fields=5, field_to_table=(0, 1, 2, 3, 4),
+                                        rows_per_table=(1000, 1, 50, 70_000, 9), d=d, dtype=dtype, pool=pool,
+                                        table_init=("uniform", 0.5) if dtype == "f32" else ("normal4", 0.1),
+                                        bag_len=("uniform", 0, 40))
+    w = W.make_workload(cfg, with_grads=False)
+    got = _fwd_case(cfg, w)
+    ref, mag = O.embedding_bag_fwd(w["ids"], w["offsets"], cfg.num_fields, cfg.batch, w["bag_to_table"],
+                                   w["row_base"], d, pool=pool, dtype=dtype, gen=_gen(cfg), with_mag=True)
+    if dtype == "f32":
+        f32_close(got, ref, mag, 41, what=f"d={d}")
+    else:
+        bf16_close(got, ref, mag, 41, atol=1e-5, what=f"d={d}")
+
+
+def test_embedding_bag_fwd_exact_and_int32_unique_path():
+    # dyadic table: sums are exact, so GPU == oracle bit for bit; pooling from the
+    # unique-row matrix through the int32 inverse map gives the same bits
+    cfg = W.CONFIGS["tensornet"].shrink(batch=300, rows_per_table=(5000,),
+                                        ids=("zipf_hashed", 1.1, 10 ** 6, 12))
+    w = W.make_workload(cfg, with_grads=False)
+    F, B, d = cfg.num_fields, cfg.batch, cfg.d
+    rng = np.random.default_rng(3)
+    table = (rng.integers(-512, 512, size=(cfg.total_rows, d)) / 1024).astype(np.float32)
+    direct = _fwd_case(cfg, w, table=table)
+    ref = O.embedding_bag_fwd(w["ids"], w["offsets"], F, B, w["bag_to_table"], w["row_base"], d, table=table)
+    np.testing.assert_array_equal(direct, ref)
+    st, dd = gpu_dedup(w["ids"], w["offsets"], F, B, w["bag_to_table"], w["row_base"])
+    assert st == 0
+    tab = _t(table)
+    nu = torch.tensor([dd["n_unique"]], dtype=torch.int64, device=DEV)
+    U = torch.full((w["ids"].size, d), float("nan"), device=DEV)
+    ws = ctr.workspace(256)
+    ctr.ctr_gather_rows(tab, d, _t(dd["unique_rows"]), nu, U, ws)
+    np.testing.assert_array_equal(_np(U)[:dd["n_unique"]], table[dd["unique_rows"]])
+    out = torch.empty((B, F, d), device=DEV)
+    ctr.ctr_embedding_bag_fwd(U, d, _t(dd["inverse"], torch.int32), _t(w["offsets"]), F, B, None, None,
+                              ctr.POOL_SUM, out, F * d, d, ws)
+    assert ctr.ctr_check_status(ws) == 0
+    np.testing.assert_array_equal(_np(out), ref)
+
+
+def test_embedding_bag_fwd_strided_into_interaction_slots():
+    cfg = FWD_CASES["full_step_b128"]
+    w = W.make_workload(cfg, with_grads=False)
+    path = CtrPath(cfg, w["ids"].size)
+    path.upload(w)
+    path.forward()
+    X = _np(path.X)
+    ref = O.embedding_bag_fwd(w["ids"], w["offsets"], cfg.num_fields, cfg.batch, w["bag_to_table"], w["row_base"],
+                              cfg.d, gen=_gen(cfg))
+    f32_close(X[:, 1:, :], ref, None, 0, rtol=1e-5, atol=2e-6, what="X slots")
+    np.testing.assert_array_equal(X[:, 0, :], w["dense"])
+
+
+def test_embedding_bag_fwd_flags_out_of_range():
+    cfg = W.CONFIGS["tiny"]
+    w = W.make_workload(cfg, with_grads=False)
+    w["ids"][17] = 1000                                # rows are 0..999
+    F, B, d = cfg.num_fields, cfg.batch, cfg.d
+    tab = torch.zeros((cfg.total_rows, d), device=DEV)
+    out = torch.empty((B, F, d), device=DEV)
+    ws = ctr.workspace(256)
+    ctr.ctr_embedding_bag_fwd(tab, d, _t(w["ids"]), _t(w["offsets"]), F, B, w["bag_to_table"], w["row_base"],
+                              ctr.POOL_SUM, out, F * d, d, ws)
+    assert ctr.ctr_check_status(ws) == -4
+
+
+# ---------------------------------------------------------------------------
+# a3 dot interaction
+# ---------------------------------------------------------------------------
+def _rand_X(B, n, d, dtype, seed):
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((B, n, d)).astype(np.float32)
+    X[:, 1:, :] *= 0.03
+    if dtype == "bf16":
+        return W.f32_to_bf16_bits(X)
+    return X
+
+
+@pytest.mark.parametrize("B,n,d,dtype", [(1001, 27, 128, "f32"), (64, 5, 16, "f32"), (33, 9, 40, "f32"),
+                                         (1001, 27, 64, "bf16"), (257, 5, 64, "bf16"), (130, 32, 128, "bf16"),
+                                         (77, 2, 256, "bf16"), (40, 16, 192, "bf16"), (50, 27, 48, "bf16"),
+                                         (3, 27, 64, "bf16")])
+def test_dot_interaction(B, n, d, dtype):
+    X = _rand_X(B, n, d, dtype, seed=B + n + d)
+    Xd = _t(X.view(np.int16) if dtype == "bf16" else X)
+    if dtype == "bf16":
+        Xd = Xd.view(torch.bfloat16)
+    width = d + n * (n - 1) // 2
+    out = torch.full((B, width), float("nan"), dtype=Xd.dtype, device=DEV)
+    ws = ctr.workspace(ctr.ctr_interaction_workspace_size())
+    ctr.ctr_dot_interaction(Xd, n, d, out, ws)
+    assert ctr.ctr_check_status(ws) == 0
+    got = _np(out)
+    ref, mag = O.dot_interaction(X, n, d, dtype=dtype, with_mag=True)
+    if dtype == "f32":
+        f32_close(got, ref, mag, d, what="interaction")
+    else:
+        bf16_close(got, ref, mag, d, what="interaction")
+        np.testing.assert_array_equal(got[:, :d], ref[:, :d])
+
+
+def test_dot_interaction_fm_identity_on_gpu_output():
+    # sum of the GPU's pair outputs = 1/2 (|sum x|^2 - sum |x|^2) computed independently
+    B, n, d = 256, 27, 128
+    X = _rand_X(B, n, d, "f32", seed=1)
+    out = torch.empty((B, d + n * (n - 1) // 2), device=DEV)
+    ctr.ctr_dot_interaction(_t(X), n, d, out, ctr.workspace(256))
+    got = _np(out)[:, d:].astype(np.float64).sum(axis=1)
+    X64 = X.astype(np.float64)
+    s = X64.sum(axis=1)
+    rhs = 0.5 * ((s * s).sum(axis=1) - (X64 * X64).sum(axis=(1, 2)))
+    mag = 0.5 * ((np.abs(X64).sum(axis=1) ** 2).sum(axis=1))
+    assert np.all(np.abs(got - rhs) <= 1e-5 * np.abs(rhs) + 200 * 2.0 ** -24 * mag)
+
+
+# ---------------------------------------------------------------------------
+# a4 interaction backward
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("B,n,d", [(1001, 27, 128), (64, 5, 16), (17, 27, 64)])
+def test_dot_interaction_bwd(B, n, d):
+    X = _rand_X(B, n, d, "f32", seed=7)
+    rng = np.random.default_rng(8)
+    dout = rng.standard_normal((B, d + n * (n - 1) // 2)).astype(np.float32)
+    dX = torch.full((B, n, d), float("nan"), device=DEV)
+    ws = ctr.workspace(256)
+    ctr.ctr_dot_interaction_bwd(_t(dout), _t(X), n, d, dX, ws)
+    ref, mag = O.dot_interaction_bwd(dout, X, n, d, with_mag=True)
+    f32_close(_np(dX), ref, mag, n + 1, what="interaction bwd")
+
+
+# ---------------------------------------------------------------------------
+# a5 sparse backward + SGD row update
+# ---------------------------------------------------------------------------
+def gpu_bwd(cfg, w, table_np=None, G=None, with_grad=True):
+    """Runs dedup + bwd_update on the GPU; returns (new table, grad per unique, dedup)."""
+    F, B, d = cfg.num_fields, cfg.batch, cfg.d
+    st, dd = gpu_dedup(w["ids"], w["offsets"], F, B, w["bag_to_table"], w["row_base"])
+    assert st == 0
+    tdt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
+    if table_np is None:
+        tab = torch.empty((cfg.total_rows, d), dtype=tdt, device=DEV)
+        ctr.ctr_fill_table(tab, d, 0, cfg.fill_kind, cfg.fill_seed, cfg.fill_scale)
+    else:
+        tab = _t(table_np.view(np.int16) if table_np.dtype == np.uint16 else table_np)
+        if table_np.dtype == np.uint16:
+            tab = tab.view(torch.bfloat16)
+    n = w["ids"].size
+    Gd = _t(w["grad_pooled"] if G is None else G)
+    gu = torch.full((max(n, 1), d), float("nan"), device=DEV) if with_grad else None
+    ws = ctr.workspace(ctr.ctr_bwd_update_workspace_size(max(n, 1), d))
+    pool = ctr.POOL_MEAN if cfg.pool == "mean" else ctr.POOL_SUM
+    nu = torch.tensor([dd["n_unique"]], dtype=torch.int64, device=DEV)
+    ro = torch.from_numpy(np.concatenate([dd["run_offsets"], np.zeros(max(n, 1) - dd["n_unique"], np.int32)])).to(DEV)
+    ctr.ctr_embedding_bag_bwd_update(Gd, F * d, d, _t(w["offsets"]), F, B, pool, _t(dd["unique_rows"]), nu, ro,
+                                     _t(dd["sorted_bag"]) if n else torch.zeros(1, dtype=torch.int32, device=DEV),
+                                     max(n, 1), cfg.lr, tab, d, gu, ws)
+    assert ctr.ctr_check_status(ws) == 0
+    gnp = _np(gu)[:dd["n_unique"]] if with_grad else None
+    return _np(tab), gnp, dd
+
+
+def _bwd_depth(runs_max):
+    return 128 + (runs_max // 128) // 8 + 8
+
+
+def test_bwd_update_exact_arithmetic_with_long_runs():
+    # dyadic gradients and table, lr a power of two: every sum is exact, so
+    # the GPU must equal the oracle bit for bit, whatever its summation order
+    rng = np.random.default_rng(11)
+    F, B, d = 3, 700, 32
+    rows = [40, 3, 5000]
+    lens = rng.integers(0, 12, size=F * B)
+    lens[B:B + 40] = 400                               # long runs in field 1 (3 rows)
+    ids, offsets = _csr(lens, rng, rows, B)
+    cfg = W.CONFIGS["tiny"].shrink(batch=B, num_fields=F, field_to_table=(0, 1, 2), rows_per_table=tuple(rows),
+                                   d=d, lr=2.0 ** -6)
+    table = (rng.integers(-256, 256, size=(sum(rows), d)) / 256).astype(np.float32)
+    G = (rng.integers(-16, 17, size=(B, F, d)) / 16).astype(np.float32)
+    w = {"ids": ids, "offsets": offsets, "bag_to_table": np.arange(F, dtype=np.int32),
+         "row_base": cfg.row_base, "grad_pooled": G}
+    new_tab, g, dd = gpu_bwd(cfg, w, table_np=table)
+    assert int(np.diff(dd["run_offsets"]).max()) > 128 * 8   # several pieces, several warps per combine
+    rows_t = dd["unique_rows"]
+    ref_new, ref_g, _ = O.embedding_bag_bwd_update(G, ids, offsets, F, B, w["bag_to_table"], cfg.row_base, d,
+                                                   cfg.lr, rows_t, table=table)
+    np.testing.assert_array_equal(g, ref_g.astype(np.float32))
+    np.testing.assert_array_equal(new_tab[rows_t], ref_new)
+    untouched = np.setdiff1d(np.arange(sum(rows)), rows_t)
+    np.testing.assert_array_equal(new_tab[untouched], table[untouched])
+
+
+BWD_CASES = {
+    "tiny": W.CONFIGS["tiny"],
+    "tensornet_b512": W.CONFIGS["tensornet"].shrink(batch=512),
+    "tensornet_mean_b256": W.CONFIGS["tensornet"].shrink(batch=256, pool="mean"),
+    "bf16_b64": W.CONFIGS["bf16_large"].shrink(batch=64, rows_per_table=tuple([30_000] * 26),
+                                               backward="pooled_grad"),
+    "d128_b300": W.CONFIGS["full_step"].shrink(batch=300, rows_per_table=tuple([20_000] * 26),
+                                              backward="pooled_grad"),
+}
+
+
+@pytest.mark.parametrize("name", list(BWD_CASES))
+def test_bwd_update_configs(name):
+    cfg = BWD_CASES[name]
+    w = W.make_workload(cfg)
+    F, B, d = cfg.num_fields, cfg.batch, cfg.d
+    new_tab, g, dd = gpu_bwd(cfg, w)
+    rows_t = dd["unique_rows"]
+    ref_new, ref_g, mag = O.embedding_bag_bwd_update(w["grad_pooled"], w["ids"], w["offsets"], F, B,
+                                                     w["bag_to_table"], w["row_base"], d, cfg.lr, rows_t,
+                                                     pool=cfg.pool, dtype=cfg.dtype, gen=_gen(cfg))
+    depth = _bwd_depth(int(np.diff(dd["run_offsets"]).max()))
+    f32_close(g, ref_g, mag, depth, what=f"{name} grad")
+    old = O.table_rows(cfg.fill_kind, cfg.fill_seed, cfg.fill_scale, d, rows_t)
+    if cfg.dtype == "f32":
+        f32_close(new_tab[rows_t], ref_new, cfg.lr * mag + np.abs(old), depth + 1, what=f"{name} rows")
+    else:
+        bf16_close(new_tab[rows_t], ref_new, cfg.lr * mag, depth + 1, atol=1e-5, what=f"{name} rows")
+    # rows the batch does not touch keep their bits
+    probe = np.setdiff1d(np.arange(0, cfg.total_rows, max(1, cfg.total_rows // 5000)), rows_t)
+    np.testing.assert_array_equal(new_tab[probe], O.table_rows(cfg.fill_kind, cfg.fill_seed, cfg.fill_scale, d, probe))
+
+
+def test_bwd_update_is_deterministic():
+    cfg = BWD_CASES["tensornet_b512"]
+    w = W.make_workload(cfg)
+    a, ga, _ = gpu_bwd(cfg, w)
+    b, gb, _ = gpu_bwd(cfg, w)
+    np.testing.assert_array_equal(ga, gb)
+    np.testing.assert_array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# the whole step, composed, against the oracle composed the same way
+# ---------------------------------------------------------------------------
+def test_full_step_composed_small():
+    cfg = W.CONFIGS["full_step"].shrink(batch=192, rows_per_table=tuple([60_000] * 26))
+    w = W.make_workload(cfg)
+    F, B, d, n = cfg.num_fields, cfg.batch, cfg.d, cfg.n_vectors
+    path = CtrPath(cfg, w["ids"].size)
+    path.upload(w)
+    path.reset_status()
+    path.step()
+    assert all(v == 0 for v in path.check_status().values())
+    gen = _gen(cfg)
+    # oracle chain
+    dd = O.dedup(w["ids"], w["offsets"], F, B, w["bag_to_table"], w["row_base"])
+    pooled = O.embedding_bag_fwd(w["ids"], w["offsets"], F, B, w["bag_to_table"], w["row_base"], d, gen=gen)
+    X = np.concatenate([w["dense"][:, None, :], pooled], axis=1)
+    out_ref, out_mag = O.dot_interaction(X, n, d, with_mag=True)
+    dX_ref, dX_mag = O.dot_interaction_bwd(w["dout"], X, n, d, with_mag=True)
+    rows_t = dd["unique_rows"]
+    new_ref, _, mag = O.embedding_bag_bwd_update(dX_ref[:, 1:, :], w["ids"], w["offsets"], F, B,
+                                                 w["bag_to_table"], w["row_base"], d, cfg.lr, rows_t, gen=gen)
+    got_dd = {"unique_rows": _np(path.unique_rows)[:dd["n_unique"]], "n_unique": int(_np(path.n_unique)[0]),
+              "inverse": _np(path.inverse), "sorted_pos": _np(path.sorted_pos), "sorted_bag": _np(path.sorted_bag),
+              "run_offsets": _np(path.run_offsets)[:dd["n_unique"] + 1], "unique_offsets": _np(path.unique_offsets)}
+    assert_dedup_equal(got_dd, dd)
+    f32_close(_np(path.X)[:, 1:, :], pooled, None, 0, atol=2e-6, what="pooled")
+    # X differs from the oracle's by pooled rounding only: propagate it into the bounds
+    f32_close(_np(path.out), out_ref, out_mag, d + 64, what="interaction")
+    f32_close(_np(path.dX), dX_ref, dX_mag, n + 64, what="interaction bwd")
+    old = O.table_rows(gen[0], gen[1], gen[2], d, rows_t)
+    depth = _bwd_depth(int(np.diff(dd["run_offsets"]).max())) + 64
+    f32_close(_np(path.table)[rows_t], new_ref, cfg.lr * mag + np.abs(old), depth, what="updated rows")
