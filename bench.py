@@ -34,7 +34,7 @@ METRIC = "pooled embedding lookups/s and interaction samples/s; HBM GB/s vs GB30
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="full_step")
@@ -102,10 +102,14 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def mark(self):
+        return len(self.lines)
+
+    def summary(self, lo=0, hi=None):
         sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        sel = self.lines[lo:hi] if self.lines[lo:hi] else self.lines[-3:]
+        for ln in sel:
             p = [x.strip() for x in ln.split(",")]
             if len(p) < 9:
                 continue
@@ -234,6 +238,8 @@ def run_ours(args, rank, world):
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
+        time.sleep(1.0)  # let the sampler start before the timed region
+        mark0 = clk.mark()
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
@@ -244,6 +250,8 @@ def run_ours(args, rank, world):
                 ev[k][i + 1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+        time.sleep(0.25)
+        mark1 = clk.mark()
     barrier()
     total_ms = t_start.elapsed_time(t_end)
     stage_ms = {s: sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)) / args.steps
@@ -328,7 +336,7 @@ def run_ours(args, rank, world):
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": path.launches_per_step() * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clk.summary(mark0, mark1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, w, args.cpu_sample)

@@ -4,24 +4,29 @@
 // Synchronous Architecture (only the sparse features present in the batch are
 // synchronised) and Core Optimizations (the batch-sized matrix of unique rows).
 //
-// GPU design.  The occurrences of unique u are the sorted slots
-// run_offsets[u] .. run_offsets[u+1]-1 (from the dedup); sorted_bag gives the
-// bag whose pooled gradient each one contributes.  Runs are cut into pieces of
-// at most kPiece occurrences:
-//   1. count    pieces per run (and whether the run is long: > 1 piece)
-//   2. scan     exclusive scans give each piece a slot and each long run a
-//               slot in the list of long runs
-//   3. expand   piece -> unique map, list of long runs
-//   4. reduce   one warp per piece sums its rows in sorted order (fp32, fixed
-//               order); a one-piece run is finished here (row update); a piece
-//               of a long run stores a partial sum
-//   5. combine  one CTA per long run sums its partials: each warp a fixed
-//               contiguous segment, then a fixed tree over the warps, then the
-//               row update.
+// The occurrences of unique u are the sorted slots run_offsets[u] ..
+// run_offsets[u+1]-1 (from the dedup); sorted_bag names the bag whose pooled
+// gradient each one contributes.  Under Zipf IDs most runs are 1-5 long and a
+// few are very long, so the work is split by run length:
+//
+//   tiles     one warp per tile of TU consecutive uniques.  The tile's short
+//             runs (<= kShort occurrences) are contiguous in sorted order; the
+//             warp walks their occurrences with kU pooled-gradient rows in
+//             flight, summing each run in sorted order into a shared-memory
+//             accumulator (fp32).  Then it updates the tile's rows with
+//             independent loads (8 rows in flight): the row read-modify-writes
+//             do not wait on one another.  Long runs are appended to a list.
+//   pieces    a long run is cut into pieces of kPiece occurrences; one warp
+//             per piece sums it (same pipelined walk) into a partial row.
+//   combine   one CTA per long run: each warp sums a fixed contiguous segment
+//             of the run's partials, then a fixed tree over the warps, then
+//             the row update.
 // Every row is written by exactly one warp or CTA; there are no float atomics,
-// and the summation order depends only on the run lengths, so the result is
-// deterministic.  Because the unique rows are sorted table-major, the warps in
-// flight all read pooled gradients of one field, whose slice stays in L2.
+// and every summation order depends only on the run lengths, so the results
+// are deterministic (the long-run list order may vary, but a run's result does
+// not depend on where it sits in the list).  The unique rows are sorted
+// table-major, so the warps in flight read pooled gradients of one field,
+// whose slice stays in L2.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -32,10 +37,13 @@
 namespace ctr {
 namespace {
 
-constexpr int kPiece = 128;        // occurrences per piece
-constexpr int kRedThreads = 256;
+constexpr int kShort = 128;        // runs up to this length are summed by the tile kernel
+constexpr int kPiece = 128;        // long runs are cut into pieces of this many occurrences
+constexpr int kTileThreads = 256;
+constexpr int kTileWarps = kTileThreads / 32;
+constexpr int kAccFloats = 2048;   // shared accumulator floats per warp (TU * d)
+constexpr int kU = 8;              // pooled-gradient rows in flight per warp (for d <= 128)
 constexpr int kCombThreads = 256;
-constexpr int kUnrollB = 4;
 
 struct BwdArgs {
   const float* G;
@@ -54,90 +62,32 @@ struct BwdArgs {
   int64_t total_rows;
   float* grad_out;
   int* err;
-  int64_t n_cap;         // occurrences (sorted_bag length)
-  int64_t nbags;         // F * B
+  int64_t n_cap;       // occurrences (sorted_bag length)
+  int64_t nbags;       // F * B
+  int TU;              // uniques per tile
   // scratch
-  uint64_t* pstart;      // [n] lo: first piece, hi: first long piece (exclusive scan)
-  uint32_t* lstart;      // [n] slot in the long-run list (exclusive scan)
-  uint64_t* ptotal;      // lo: pieces, hi: long pieces
-  uint32_t* ltotal;      // long runs
-  int32_t* piece_u;      // [pieces] unique of each piece
-  int32_t* long_list;    // [long runs]
-  float* partial;        // [long pieces, d]
+  int64_t* long_count;
+  int64_t max_long;
+  int32_t* long_list;    // [max_long] unique of each long run
+  uint32_t* long_pstart; // [max_long] pieces of each long run, then (scanned) its first piece
+  uint32_t* pieces_total;
+  int32_t* piece_owner;  // [pieces] long-run slot of each piece
+  float* partial;        // [pieces, d]
 };
 
-__device__ __forceinline__ int64_t n_uniques(const BwdArgs& a, int64_t cap) {
-  int64_t n = *a.n_unique;
-  return n < cap ? n : cap;
+__device__ __forceinline__ int64_t n_uniques(const BwdArgs& a) {
+  const int64_t n = *a.n_unique;
+  return n < a.n_cap ? n : a.n_cap;
 }
 
-// Run bounds of unique u; an inconsistent run is treated as empty (and flagged
-// by piece_count_kernel), so no kernel indexes outside its buffers.
+// Run bounds of unique u; an inconsistent run is flagged and treated as empty,
+// so no kernel indexes outside its buffers.
 __device__ __forceinline__ void run_bounds(const BwdArgs& a, int64_t u, int64_t& r0, int64_t& r1) {
   r0 = a.run_offsets[u];
   r1 = a.run_offsets[u + 1];
-  if (r0 < 0 || r1 < r0 || r1 > a.n_cap) r0 = r1 = 0;
-}
-
-__global__ void piece_count_kernel(const BwdArgs a, int64_t cap, uint64_t* __restrict__ cnt2,
-                                   uint32_t* __restrict__ cnt1) {
-  const int64_t n = n_uniques(a, cap);
-  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n; u += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t q0 = a.run_offsets[u], q1 = a.run_offsets[u + 1];
-    if (q0 < 0 || q1 < q0 || q1 > a.n_cap) set_error(a.err, CTR_ERR_BAD_OFFSETS);
-    int64_t r0, r1;
-    run_bounds(a, u, r0, r1);
-    int64_t len = r1 - r0;
-    uint64_t pcs = len > 0 ? (uint64_t)ceil_div(len, kPiece) : 1u;
-    bool lng = pcs > 1;
-    cnt2[u] = pcs | ((lng ? pcs : 0ull) << 32);
-    cnt1[u] = lng ? 1u : 0u;
-  }
-}
-
-__global__ void expand_kernel(const BwdArgs a, int64_t cap) {
-  const int64_t n = n_uniques(a, cap);
-  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n; u += (int64_t)gridDim.x * blockDim.x) {
-    int64_t r0, r1;
-    run_bounds(a, u, r0, r1);
-    int64_t len = r1 - r0;
-    int64_t pcs = len > 0 ? ceil_div(len, kPiece) : 1;
-    uint64_t p0 = a.pstart[u] & 0xffffffffull;
-    for (int64_t k = 0; k < pcs; ++k) a.piece_u[p0 + k] = (int32_t)u;
-    if (pcs > 1) a.long_list[a.lstart[u]] = (int32_t)u;
-  }
-}
-
-// Row update for unique u with its gradient chunk g (V floats at column c0).
-template <int V>
-__device__ __forceinline__ void finish_chunk(const BwdArgs& a, int64_t u, int c0, const float (&g)[V]) {
-  const int64_t row = a.unique_rows[u];
-  if (row < 0 || row >= a.total_rows) {
-    set_error(a.err, CTR_ERR_INDEX_OUT_OF_RANGE);
-    return;
-  }
-  if (a.grad_out) {
-    float* go = a.grad_out + u * a.d + c0;
-#pragma unroll
-    for (int v = 0; v < V; ++v) go[v] = g[v];
-  }
-  if (!a.bf16) {
-    float* w = (float*)a.table + row * a.d + c0;
-    if (V == 4) {
-      float4 x = *(float4*)w;
-      x.x = fmaf(-a.lr, g[0], x.x);
-      x.y = fmaf(-a.lr, g[1], x.y);
-      x.z = fmaf(-a.lr, g[2], x.z);
-      x.w = fmaf(-a.lr, g[3], x.w);
-      *(float4*)w = x;
-    } else {
-#pragma unroll
-      for (int v = 0; v < V; ++v) w[v] = fmaf(-a.lr, g[v], w[v]);
-    }
-  } else {
-    __nv_bfloat16* w = (__nv_bfloat16*)a.table + row * a.d + c0;
-#pragma unroll
-    for (int v = 0; v < V; ++v) w[v] = __float2bfloat16_rn(fmaf(-a.lr, g[v], __bfloat162float(w[v])));
+  if (r0 < 0 || r1 < r0 || r1 > a.n_cap) {
+    set_error(a.err, CTR_ERR_BAD_OFFSETS);
+    r0 = r1 = 0;
   }
 }
 
@@ -147,170 +97,375 @@ __device__ __forceinline__ float4 ldg_f4(const float* p) {
   return r;
 }
 
-// One warp per piece.  LPR lanes cover a row (4 floats each, CPL chunks per
-// lane); 32/LPR occurrences are summed side by side and combined at the end.
-template <int LPR, int CPL>
-__global__ void __launch_bounds__(kRedThreads) reduce_pieces_kernel(const BwdArgs a) {
-  constexpr int R = 32 / LPR;
+__device__ __forceinline__ float4 fma4(float4 x, float s, float4 acc) {
+  return make_float4(fmaf(x.x, s, acc.x), fmaf(x.y, s, acc.y), fmaf(x.z, s, acc.z), fmaf(x.w, s, acc.w));
+}
+
+// Pooled-gradient offset and scale of sorted occurrence s (-1: contributes nothing).
+__device__ __forceinline__ void occ_info(const BwdArgs& a, int64_t s, int64_t& goff, float& scale) {
+  const int32_t bag = a.sorted_bag[s];
+  if (bag < 0 || bag >= a.nbags) {
+    set_error(a.err, CTR_ERR_BAD_OFFSETS);
+    goff = -1;
+    scale = 0.f;
+    return;
+  }
+  const int32_t f = bag / a.B, b = bag - f * a.B;
+  goff = (int64_t)b * a.sb + (int64_t)f * a.sf;
+  scale = 1.f;
+  if (a.mean) {
+    const int64_t len = a.offsets[bag + 1] - a.offsets[bag];
+    scale = len > 0 ? 1.f / (float)len : 0.f;
+  }
+}
+
+// Row update of unique u with gradient chunk g at column 4*ch (w already loaded).
+__device__ __forceinline__ void store_row_chunk(const BwdArgs& a, int64_t row, int64_t u, int ch, float4 g,
+                                                float4 w, uint2 wb) {
+  if (a.grad_out) *(float4*)(a.grad_out + u * a.d + ch * 4) = g;
+  if (!a.bf16) {
+    float4 x = make_float4(fmaf(-a.lr, g.x, w.x), fmaf(-a.lr, g.y, w.y), fmaf(-a.lr, g.z, w.z),
+                           fmaf(-a.lr, g.w, w.w));
+    *(float4*)((float*)a.table + row * a.d + ch * 4) = x;
+  } else {
+    const float w0 = __uint_as_float(wb.x << 16), w1 = __uint_as_float(wb.x & 0xffff0000u);
+    const float w2 = __uint_as_float(wb.y << 16), w3 = __uint_as_float(wb.y & 0xffff0000u);
+    __nv_bfloat162 p0 = __floats2bfloat162_rn(fmaf(-a.lr, g.x, w0), fmaf(-a.lr, g.y, w1));
+    __nv_bfloat162 p1 = __floats2bfloat162_rn(fmaf(-a.lr, g.z, w2), fmaf(-a.lr, g.w, w3));
+    *(uint2*)((__nv_bfloat16*)a.table + row * a.d + ch * 4) = make_uint2(*(uint32_t*)&p0, *(uint32_t*)&p1);
+  }
+}
+
+__device__ __forceinline__ void load_row_chunk(const BwdArgs& a, int64_t row, int ch, float4& w, uint2& wb) {
+  if (!a.bf16) w = *(const float4*)((const float*)a.table + row * a.d + ch * 4);
+  else wb = *(const uint2*)((const __nv_bfloat16*)a.table + row * a.d + ch * 4);
+}
+
+// Walk occurrences [s0, s1) of one run, kU rows in flight, summing in order.
+template <int CPL>
+__device__ __forceinline__ void sum_run(const BwdArgs& a, int64_t s0, int64_t s1, float4 (&acc)[CPL]) {
+  constexpr int kU = ::ctr::kU / CPL;
   const int lane = threadIdx.x & 31;
-  const int grp = lane / LPR, sub = lane % LPR;
   const int chunks = a.d / 4;
-  const int64_t npieces = (int64_t)(*a.ptotal & 0xffffffffull);
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t p = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < npieces; p += nwarps) {
-    const int64_t u = a.piece_u[p];
-    const uint64_t ps = a.pstart[u];
-    const int64_t k = p - (int64_t)(ps & 0xffffffffull);
-    int64_t r0, r1;
-    run_bounds(a, u, r0, r1);
-    const int64_t s0 = r0 + k * kPiece;
-    const int64_t s1 = imin64(r1, s0 + kPiece);
-    float acc[CPL][4];
+  for (int64_t j0 = s0; j0 < s1; j0 += 32) {
+    const int cnt = (int)imin64(32, s1 - j0);
+    int64_t goff = -1;
+    float scale = 0.f;
+    if (lane < cnt) occ_info(a, j0 + lane, goff, scale);
+    for (int t0 = 0; t0 < cnt; t0 += kU) {
+      float4 buf[kU][CPL];
 #pragma unroll
-    for (int c = 0; c < CPL; ++c)
+      for (int u = 0; u < kU; ++u) {
+        const int t = t0 + u;
+        const int64_t go = __shfl_sync(kFull, goff, t & 31);
 #pragma unroll
-      for (int v = 0; v < 4; ++v) acc[c][v] = 0.f;
-    for (int64_t j0 = s0; j0 < s1; j0 += 32) {
-      const int cnt = (int)imin64(32, s1 - j0);
-      int64_t goff = -1;  // -1: this occurrence contributes nothing
-      float scale = 1.f;
-      if (lane < cnt) {
-        const int32_t bag = a.sorted_bag[j0 + lane];
-        if (bag < 0 || bag >= a.nbags) {
-          set_error(a.err, CTR_ERR_BAD_OFFSETS);
-        } else {
-          const int32_t f = bag / a.B, b = bag - f * a.B;
-          goff = (int64_t)b * a.sb + (int64_t)f * a.sf;
-          if (a.mean) {
-            int64_t len = a.offsets[bag + 1] - a.offsets[bag];
-            scale = len > 0 ? 1.f / (float)len : 0.f;
-          }
+        for (int c = 0; c < CPL; ++c) {
+          const int ch = lane + c * 32;
+          buf[u][c] = (t < cnt && go >= 0 && ch < chunks) ? ldg_f4(a.G + go + ch * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      for (int t0 = 0; t0 < cnt; t0 += R * kUnrollB) {
-        float4 buf[kUnrollB][CPL];
-        float sc[kUnrollB];
 #pragma unroll
-        for (int uu = 0; uu < kUnrollB; ++uu) {
-          const int t = t0 + uu * R + grp;
-          const int64_t go = __shfl_sync(kFull, goff, t & 31);
-          sc[uu] = __shfl_sync(kFull, scale, t & 31);
+      for (int u = 0; u < kU; ++u) {
+        const float sc = __shfl_sync(kFull, scale, (t0 + u) & 31);
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            const int ch = sub + c * LPR;
-            buf[uu][c] = (t < cnt && go >= 0 && ch < chunks) ? ldg_f4(a.G + go + ch * 4)
-                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-          if (t >= cnt) sc[uu] = 0.f;
-        }
-#pragma unroll
-        for (int uu = 0; uu < kUnrollB; ++uu)
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            if (a.mean) {
-              acc[c][0] = fmaf(buf[uu][c].x, sc[uu], acc[c][0]);
-              acc[c][1] = fmaf(buf[uu][c].y, sc[uu], acc[c][1]);
-              acc[c][2] = fmaf(buf[uu][c].z, sc[uu], acc[c][2]);
-              acc[c][3] = fmaf(buf[uu][c].w, sc[uu], acc[c][3]);
-            } else {
-              acc[c][0] += buf[uu][c].x;
-              acc[c][1] += buf[uu][c].y;
-              acc[c][2] += buf[uu][c].z;
-              acc[c][3] += buf[uu][c].w;
-            }
-          }
-      }
-    }
-#pragma unroll
-    for (int o = LPR; o < 32; o <<= 1)
-#pragma unroll
-      for (int c = 0; c < CPL; ++c)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) acc[c][v] += __shfl_xor_sync(kFull, acc[c][v], o);
-    if (grp != 0) continue;
-    const bool single = (r1 - r0) <= kPiece;
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-      const int ch = sub + c * LPR;
-      if (ch >= chunks) continue;
-      if (single) {
-        finish_chunk<4>(a, u, ch * 4, acc[c]);
-      } else {
-        const int64_t lp = (int64_t)(ps >> 32) + k;
-        *(float4*)(a.partial + lp * a.d + ch * 4) = make_float4(acc[c][0], acc[c][1], acc[c][2], acc[c][3]);
+        for (int c = 0; c < CPL; ++c)
+          if (t0 + u < cnt) acc[c] = fma4(buf[u][c], sc, acc[c]);
       }
     }
   }
 }
 
-// One CTA per long run: warps sum fixed contiguous segments of the run's
-// partials, then a fixed tree over the warps.  Threads own 4-float chunks.
+template <int CPL>
+__global__ void __launch_bounds__(kTileThreads, 2) bwd_tiles_kernel(const BwdArgs a) {
+  constexpr int kU = ::ctr::kU / CPL;   // rows in flight in phase 1
+  constexpr int kR = 8 / CPL;           // rows in flight in phase 2
+  extern __shared__ float4 sacc[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int chunks = a.d / 4;
+  const int TU = a.TU;
+  float4* my = sacc + (size_t)warp * TU * chunks;
+  const int64_t nu = n_uniques(a);
+  const int64_t ntiles = ceil_div(nu, TU);
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t tile = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; tile < ntiles; tile += nwarps) {
+    const int64_t u = tile * TU + lane;
+    const bool valid = lane < TU && u < nu;
+    int64_t r0 = 0, r1 = 0;
+    if (valid) run_bounds(a, u, r0, r1);
+    const int64_t len = r1 - r0;
+    const bool is_long = valid && len > kShort;
+    const bool is_short = valid && !is_long && len > 0;
+    int64_t row = -1;
+    if (is_short) {
+      row = a.unique_rows[u];
+      if (row < 0 || row >= a.total_rows) {
+        set_error(a.err, CTR_ERR_INDEX_OUT_OF_RANGE);
+        row = -1;
+      }
+    }
+    if (is_long) {
+      const int64_t slot = (int64_t)atomicAdd((unsigned long long*)a.long_count, 1ull);
+      if (slot < a.max_long) {
+        a.long_list[slot] = (int32_t)u;
+        a.long_pstart[slot] = (uint32_t)ceil_div(len, kPiece);
+      }
+    }
+    // exclusive scan of the short runs' lengths over the tile's lanes
+    const int slen = is_short ? (int)len : 0;
+    int inc = slen;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const int e = inc - slen;
+    const int E = __shfl_sync(kFull, inc, 31);
+
+    // phase 1: per-run sums of the tile's short runs into shared memory
+    float4 acc[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < E; c0 += 32) {
+      const int k = c0 + lane;
+      int seg = 0;
+#pragma unroll
+      for (int step = 16; step > 0; step >>= 1) {  // largest lane i with e_i <= k
+        const int cand = seg + step;
+        const int ec = __shfl_sync(kFull, e, cand);
+        if (ec <= k) seg = cand;
+      }
+      const int64_t r0s = __shfl_sync(kFull, r0, seg);
+      const int es = __shfl_sync(kFull, e, seg);
+      const int ls = __shfl_sync(kFull, slen, seg);
+      int64_t goff = -1;
+      float scale = 0.f;
+      bool last = false;
+      if (k < E) {
+        occ_info(a, r0s + (k - es), goff, scale);
+        last = (k + 1 == es + ls);
+      }
+      const int cnt = min(32, E - c0);
+      for (int t0 = 0; t0 < cnt; t0 += kU) {
+        float4 buf[kU][CPL];
+#pragma unroll
+        for (int uu = 0; uu < kU; ++uu) {
+          const int t = t0 + uu;
+          const int64_t go = __shfl_sync(kFull, goff, t & 31);
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            const int ch = lane + c * 32;
+            buf[uu][c] = (t < cnt && go >= 0 && ch < chunks) ? ldg_f4(a.G + go + ch * 4)
+                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int uu = 0; uu < kU; ++uu) {
+          const int t = (t0 + uu) & 31;
+          const float sc = __shfl_sync(kFull, scale, t);
+          const bool lf = __shfl_sync(kFull, (int)last, t) != 0;
+          const int sg = __shfl_sync(kFull, seg, t);
+          if (t0 + uu < cnt) {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) acc[c] = fma4(buf[uu][c], sc, acc[c]);
+            if (lf) {
+#pragma unroll
+              for (int c = 0; c < CPL; ++c) {
+                const int ch = lane + c * 32;
+                if (ch < chunks) my[sg * chunks + ch] = acc[c];
+                acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    // phase 2: row updates, eight independent rows in flight
+    for (int j0 = 0; j0 < TU; j0 += kR) {
+      float4 w[kR][CPL];
+      uint2 wb[kR][CPL];
+      int64_t rj[kR];
+#pragma unroll
+      for (int jj = 0; jj < kR; ++jj) {
+        const int j = (j0 + jj) & 31;
+        rj[jj] = __shfl_sync(kFull, row, j);
+        const int lj = __shfl_sync(kFull, slen, j);
+        if (j0 + jj >= TU || lj == 0) rj[jj] = -1;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          const int ch = lane + c * 32;
+          if (rj[jj] >= 0 && ch < chunks) load_row_chunk(a, rj[jj], ch, w[jj][c], wb[jj][c]);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < kR; ++jj) {
+        if (rj[jj] < 0) continue;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          const int ch = lane + c * 32;
+          if (ch < chunks) store_row_chunk(a, rj[jj], tile * TU + j0 + jj, ch, my[(j0 + jj) * chunks + ch], w[jj][c],
+                                           wb[jj][c]);
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
+__global__ void clear_i64(int64_t* p) { *p = 0; }
+
+__global__ void expand_long_kernel(const BwdArgs a) {
+  const int64_t nl = imin64(*a.long_count, a.max_long);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nl; i += (int64_t)gridDim.x * blockDim.x) {
+    int64_t r0, r1;
+    run_bounds(a, a.long_list[i], r0, r1);
+    const int64_t pcs = ceil_div(r1 - r0, kPiece);
+    const int64_t p0 = a.long_pstart[i];
+    for (int64_t k = 0; k < pcs; ++k) a.piece_owner[p0 + k] = (int32_t)i;
+  }
+}
+
+// One warp per piece of a long run: its sum goes to partial[piece].
+template <int CPL>
+__global__ void __launch_bounds__(256) long_pieces_kernel(const BwdArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int chunks = a.d / 4;
+  const int64_t np = *a.pieces_total;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t p = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < np; p += nwarps) {
+    const int64_t i = a.piece_owner[p];
+    int64_t r0, r1;
+    run_bounds(a, a.long_list[i], r0, r1);
+    const int64_t k = p - (int64_t)a.long_pstart[i];
+    const int64_t s0 = r0 + k * kPiece;
+    const int64_t s1 = imin64(r1, s0 + kPiece);
+    float4 acc[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    sum_run<CPL>(a, s0, s1, acc);
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      const int ch = lane + c * 32;
+      if (ch < chunks) *(float4*)(a.partial + p * a.d + ch * 4) = acc[c];
+    }
+  }
+}
+
+// One CTA per long run: warps sum fixed contiguous segments of its partials,
+// then a fixed pairwise tree over the warps, then the row update.
 __global__ void __launch_bounds__(kCombThreads) combine_long_kernel(const BwdArgs a) {
   constexpr int W = kCombThreads / 32;
   extern __shared__ float sm[];  // [W][d]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int chunks = a.d / 4;
-  const int64_t nlong = *a.ltotal;
-  for (int64_t i = blockIdx.x; i < nlong; i += gridDim.x) {
+  const int64_t nl = imin64(*a.long_count, a.max_long);
+  for (int64_t i = blockIdx.x; i < nl; i += gridDim.x) {
     const int64_t u = a.long_list[i];
     int64_t r0, r1;
     run_bounds(a, u, r0, r1);
     const int64_t pcs = ceil_div(r1 - r0, kPiece);
-    const int64_t lp0 = (int64_t)(a.pstart[u] >> 32);
+    const int64_t p0 = a.long_pstart[i];
     const int64_t seg = ceil_div(pcs, W);
     const int64_t q0 = imin64(pcs, warp * seg), q1 = imin64(pcs, q0 + seg);
     for (int ch = lane; ch < chunks; ch += 32) {
       float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
       int64_t q = q0;
       for (; q + 4 <= q1; q += 4) {  // four loads in flight, summed in order
-        float4 x0 = ldg_f4(a.partial + (lp0 + q) * a.d + ch * 4);
-        float4 x1 = ldg_f4(a.partial + (lp0 + q + 1) * a.d + ch * 4);
-        float4 x2 = ldg_f4(a.partial + (lp0 + q + 2) * a.d + ch * 4);
-        float4 x3 = ldg_f4(a.partial + (lp0 + q + 3) * a.d + ch * 4);
-        s.x += x0.x; s.y += x0.y; s.z += x0.z; s.w += x0.w;
-        s.x += x1.x; s.y += x1.y; s.z += x1.z; s.w += x1.w;
-        s.x += x2.x; s.y += x2.y; s.z += x2.z; s.w += x2.w;
-        s.x += x3.x; s.y += x3.y; s.z += x3.z; s.w += x3.w;
+        const float4 x0 = ldg_f4(a.partial + (p0 + q) * a.d + ch * 4);
+        const float4 x1 = ldg_f4(a.partial + (p0 + q + 1) * a.d + ch * 4);
+        const float4 x2 = ldg_f4(a.partial + (p0 + q + 2) * a.d + ch * 4);
+        const float4 x3 = ldg_f4(a.partial + (p0 + q + 3) * a.d + ch * 4);
+        s = fma4(x0, 1.f, s);
+        s = fma4(x1, 1.f, s);
+        s = fma4(x2, 1.f, s);
+        s = fma4(x3, 1.f, s);
       }
-      for (; q < q1; ++q) {
-        float4 x = ldg_f4(a.partial + (lp0 + q) * a.d + ch * 4);
-        s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
-      }
+      for (; q < q1; ++q) s = fma4(ldg_f4(a.partial + (p0 + q) * a.d + ch * 4), 1.f, s);
       *(float4*)(sm + warp * a.d + ch * 4) = s;
     }
     __syncthreads();
-    for (int w = W / 2; w > 0; w >>= 1) {  // fixed pairwise tree over the warps
+    for (int w = W / 2; w > 0; w >>= 1) {
       if (warp < w)
         for (int ch = lane; ch < chunks; ch += 32) {
-          float4 x = *(float4*)(sm + warp * a.d + ch * 4);
-          float4 y = *(float4*)(sm + (warp + w) * a.d + ch * 4);
+          const float4 x = *(float4*)(sm + warp * a.d + ch * 4);
+          const float4 y = *(float4*)(sm + (warp + w) * a.d + ch * 4);
           *(float4*)(sm + warp * a.d + ch * 4) = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
         }
       __syncthreads();
     }
-    if (warp == 0)
-      for (int ch = lane; ch < chunks; ch += 32) {
-        float4 x = *(float4*)(sm + ch * 4);
-        float g[4] = {x.x, x.y, x.z, x.w};
-        finish_chunk<4>(a, u, ch * 4, g);
+    if (warp == 0) {
+      const int64_t row = a.unique_rows[u];
+      if (row < 0 || row >= a.total_rows) {
+        if (lane == 0) set_error(a.err, CTR_ERR_INDEX_OUT_OF_RANGE);
+      } else {
+        for (int ch = lane; ch < chunks; ch += 32) {
+          float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+          uint2 wb = make_uint2(0u, 0u);
+          load_row_chunk(a, row, ch, w, wb);
+          store_row_chunk(a, row, u, ch, *(float4*)(sm + ch * 4), w, wb);
+        }
       }
+    }
     __syncthreads();
   }
 }
 
+struct Sizes {
+  int64_t max_long, max_pieces;
+};
+
+Sizes sizes(int64_t n) {
+  Sizes z;
+  z.max_long = n / (kShort + 1) + 1;
+  z.max_pieces = n / kPiece + z.max_long + 1;
+  return z;
+}
+
 template <typename WS>
 void bwd_layout(WS& ws, int64_t n, int32_t d) {
-  const int64_t max_pieces = n + ceil_div(n, kPiece) + 1;
-  const int64_t max_long_pieces = 2 * ceil_div(n, kPiece) + 1;
-  const int64_t max_long = ceil_div(n, kPiece) + 1;
-  ws.template take<uint64_t>((size_t)n);                     // pstart
-  ws.template take<uint32_t>((size_t)n);                     // lstart
-  ws.template take<uint64_t>(1);                             // ptotal
-  ws.template take<uint32_t>(1);                             // ltotal
-  ws.template take<int32_t>((size_t)max_pieces);             // piece_u
-  ws.template take<int32_t>((size_t)max_long);               // long_list
-  ws.template take<float>((size_t)max_long_pieces * d);      // partial sums
-  scan_reserve<uint64_t>(ws, n);
+  const Sizes z = sizes(n);
+  ws.template take<int64_t>(1);                            // long_count
+  ws.template take<uint32_t>(1);                           // pieces_total
+  ws.template take<int32_t>((size_t)z.max_long);           // long_list
+  ws.template take<uint32_t>((size_t)z.max_long);          // long_pstart
+  ws.template take<int32_t>((size_t)z.max_pieces);         // piece_owner
+  ws.template take<float>((size_t)z.max_pieces * d);       // partial sums
+  scan_reserve<uint32_t>(ws, z.max_long);
+}
+
+template <typename K>
+int grid_of(K kernel, int threads, size_t smem, int64_t want) {
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+  return (int)std::max<int64_t>(1, imin64(want, (int64_t)std::max(per_sm, 1) * num_sms()));
+}
+
+template <int CPL>
+int launch_bwd(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
+  const int chunks = a.d / 4;
+  const size_t tile_smem = (size_t)kTileWarps * a.TU * chunks * sizeof(float4);
+  auto tk = bwd_tiles_kernel<CPL>;
+  if (tile_smem > 48 * 1024 &&
+      cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tile_smem) != cudaSuccess)
+    return CTR_ERR_CUDA;
+  clear_i64<<<1, 1, 0, s>>>(a.long_count);
+  if (int st = launch_status()) return st;
+  tk<<<grid_of(tk, kTileThreads, tile_smem, ceil_div(n, (int64_t)a.TU * kTileWarps)), kTileThreads, tile_smem, s>>>(a);
+  if (int st = launch_status()) return st;
+  {
+    WsCarver sc = c;
+    if (int st = scan_exclusive<uint32_t>(a.long_pstart, a.long_pstart, a.max_long, a.long_count, a.pieces_total,
+                                          sc, s))
+      return st;
+  }
+  expand_long_kernel<<<std::max(1, num_sms() * 2), 256, 0, s>>>(a);
+  if (int st = launch_status()) return st;
+  auto pk = long_pieces_kernel<CPL>;
+  pk<<<grid_of(pk, 256, 0, ceil_div(sizes(n).max_pieces, 8)), 256, 0, s>>>(a);
+  if (int st = launch_status()) return st;
+  const size_t csmem = (size_t)(kCombThreads / 32) * a.d * sizeof(float);
+  combine_long_kernel<<<std::max(num_sms() * 2, 1), kCombThreads, csmem, s>>>(a);
+  return launch_status();
 }
 
 }  // namespace
@@ -341,16 +496,13 @@ extern "C" int ctr_embedding_bag_bwd_update(const float* grad_pooled, int64_t g_
   if (n_ids >= ((int64_t)1 << 31)) return CTR_ERR_UNSUPPORTED;
   if (d % 4 != 0 || d > 512) return CTR_ERR_UNSUPPORTED;
   if (g_stride_b % 4 != 0 || g_stride_f % 4 != 0 || (uintptr_t)grad_pooled % 16 != 0) return CTR_ERR_UNSUPPORTED;
-  if (dtype == CTR_F32 && (uintptr_t)table % 16 != 0) return CTR_ERR_UNSUPPORTED;
+  if ((uintptr_t)table % (dtype == CTR_F32 ? 16 : 8) != 0) return CTR_ERR_UNSUPPORTED;
   if (grad_unique_out && (uintptr_t)grad_unique_out % 16 != 0) return CTR_ERR_UNSUPPORTED;
   if (!ws_valid(ws, ws_bytes, ctr_bwd_update_workspace_size(n_ids, d))) return CTR_ERR_WORKSPACE;
   if (n_ids == 0) return CTR_OK;
 
   WsCarver c(ws, ws_bytes);
-  const int64_t n = n_ids;
-  const int64_t max_pieces = n + ceil_div(n, kPiece) + 1;
-  const int64_t max_long_pieces = 2 * ceil_div(n, kPiece) + 1;
-  const int64_t max_long = ceil_div(n, kPiece) + 1;
+  const Sizes z = sizes(n_ids);
   BwdArgs a;
   a.G = grad_pooled;
   a.sb = g_stride_b;
@@ -371,52 +523,17 @@ extern "C" int ctr_embedding_bag_bwd_update(const float* grad_pooled, int64_t g_
   a.err = (int*)ws;
   a.n_cap = n_ids;
   a.nbags = (int64_t)num_fields * batch;
-  a.pstart = c.take<uint64_t>(n);
-  a.lstart = c.take<uint32_t>(n);
-  a.ptotal = c.take<uint64_t>(1);
-  a.ltotal = c.take<uint32_t>(1);
-  a.piece_u = c.take<int32_t>(max_pieces);
-  a.long_list = c.take<int32_t>(max_long);
-  a.partial = c.take<float>((size_t)max_long_pieces * d);
+  a.TU = std::max(1, std::min(32, kAccFloats / d));
+  a.long_count = c.take<int64_t>(1);
+  a.pieces_total = c.take<uint32_t>(1);
+  a.max_long = z.max_long;
+  a.long_list = c.take<int32_t>(z.max_long);
+  a.long_pstart = c.take<uint32_t>(z.max_long);
+  a.piece_owner = c.take<int32_t>(z.max_pieces);
+  a.partial = c.take<float>((size_t)z.max_pieces * d);
   if (!c.ok()) return CTR_ERR_WORKSPACE;
-  (void)max_long_pieces;
-
-  const int sms = num_sms();
-  const int64_t tb = imin64(ceil_div(n, 256), (int64_t)sms * 8);
-  piece_count_kernel<<<(unsigned)tb, 256, 0, s>>>(a, n, a.pstart, a.lstart);
-  if (int st = launch_status()) return st;
-  {
-    WsCarver sc = c;
-    if (int st = scan_exclusive<uint64_t>(a.pstart, a.pstart, n, n_unique, a.ptotal, sc, s)) return st;
-    WsCarver sc2 = c;
-    if (int st = scan_exclusive<uint32_t>(a.lstart, a.lstart, n, n_unique, a.ltotal, sc2, s)) return st;
-  }
-  expand_kernel<<<(unsigned)tb, 256, 0, s>>>(a, n);
-  if (int st = launch_status()) return st;
-
-  const int chunks = d / 4;
-  {
-    int per_sm = 0;
-#define CTR_RED(LPR, CPL)                                                                   \
-  {                                                                                         \
-    auto k = reduce_pieces_kernel<LPR, CPL>;                                                \
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kRedThreads, 0);              \
-    int64_t want = ceil_div(max_pieces, kRedThreads / 32);                                  \
-    int64_t g = std::max<int64_t>(1, imin64(want, (int64_t)std::max(per_sm, 1) * sms)); \
-    k<<<(unsigned)g, kRedThreads, 0, s>>>(a);                                               \
-  }
-    if (chunks <= 1) CTR_RED(1, 1)
-    else if (chunks <= 2) CTR_RED(2, 1)
-    else if (chunks <= 4) CTR_RED(4, 1)
-    else if (chunks <= 8) CTR_RED(8, 1)
-    else if (chunks <= 16) CTR_RED(16, 1)
-    else if (chunks <= 32) CTR_RED(32, 1)
-    else if (chunks <= 64) CTR_RED(32, 2)
-    else CTR_RED(32, 4)
-#undef CTR_RED
-    if (int st = launch_status()) return st;
-  }
-  const size_t smem = (size_t)(kCombThreads / 32) * d * sizeof(float);
-  combine_long_kernel<<<(unsigned)std::max(sms * 2, 1), kCombThreads, smem, s>>>(a);
-  return launch_status();
+  const int cpl = (int)ceil_div(d / 4, 32);
+  if (cpl <= 1) return launch_bwd<1>(a, c, s, n_ids);
+  if (cpl <= 2) return launch_bwd<2>(a, c, s, n_ids);
+  return launch_bwd<4>(a, c, s, n_ids);
 }

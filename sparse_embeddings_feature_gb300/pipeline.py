@@ -171,7 +171,8 @@ class CtrPath:
         if cfg.backward == "full":
             k += 1
         if cfg.backward != "none":
-            k += 1 + _scan_launches(n, 2048) + _scan_launches(n, 4096) + 1 + 1 + 1
+            max_long = n // 129 + 1
+            k += 2 + _scan_launches(max_long, 4096) + 3
         return k
 
 
