@@ -35,24 +35,25 @@ def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _fingerprint() -> str:
+def _fingerprint(extra=()) -> str:
     h = hashlib.sha256()
     for p in sorted(glob.glob(os.path.join(CSRC, "*")) + [os.path.join(INCLUDE, "ctr.h"), __file__]):
         with open(p, "rb") as f:
             h.update(p.encode())
             h.update(f.read())
-    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    h.update(" ".join(ARCH + NVCC_FLAGS + list(extra)).encode())
     return h.hexdigest()
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     stamp = os.path.join(OUT_DIR, "fingerprint")
-    fp = _fingerprint()
+    extra_flags = list(extra_flags or []) + os.environ.get("CTR_NVCC_EXTRA", "").split()
+    fp = _fingerprint(extra_flags)
     if not force and os.path.exists(LIB) and os.path.exists(stamp) and open(stamp).read() == fp:
         return LIB
     cc = nvcc()
-    flags = ARCH + NVCC_FLAGS + list(extra_flags or [])
+    flags = ARCH + NVCC_FLAGS + extra_flags
 
     def compile_one(src):
         obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")

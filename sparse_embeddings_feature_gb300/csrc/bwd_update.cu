@@ -65,6 +65,7 @@ struct BwdArgs {
   int64_t n_cap;       // occurrences (sorted_bag length)
   int64_t nbags;       // F * B
   int TU;              // uniques per tile
+  int g4_ok;           // every pooled-gradient offset / 4 fits 32 bits
   // scratch
   int64_t* long_count;
   int64_t max_long;
@@ -325,7 +326,19 @@ __global__ void expand_long_kernel(const BwdArgs a) {
   }
 }
 
-// One warp per piece of a long run: its sum goes to partial[piece].
+// One warp per piece of a long run: its sum goes to partial[piece].  For rows
+// of at most 512 bytes the walk streams: sorted_bag is read two chunks ahead
+// and the pooled-gradient rows run in a sliding window of kWin loads that
+// continues across chunks.
+constexpr int kWin = 8;
+#ifndef CTR_TILE_MINB
+#define CTR_TILE_MINB 2
+#endif
+#ifndef CTR_BWD_MINB
+#define CTR_BWD_MINB 3  // resident blocks per SM the register budget is sized for
+#endif
+
+// Rows wider than 512 bytes: one warp per piece, kU / CPL rows in flight.
 template <int CPL>
 __global__ void __launch_bounds__(256) long_pieces_kernel(const BwdArgs a) {
   const int lane = threadIdx.x & 31;
@@ -348,6 +361,212 @@ __global__ void __launch_bounds__(256) long_pieces_kernel(const BwdArgs a) {
       const int ch = lane + c * 32;
       if (ch < chunks) *(float4*)(a.partial + p * a.d + ch * 4) = acc[c];
     }
+  }
+}
+
+// Pooled-gradient row of a bag in 16-byte units (kNoG: contributes nothing),
+// and its MEAN scale.
+constexpr uint32_t kNoG = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t bag_g4(const BwdArgs& a, int32_t bag, float& scale) {
+  scale = 0.f;
+  if (bag < 0) return kNoG;
+  if (bag >= a.nbags) {
+    set_error(a.err, CTR_ERR_BAD_OFFSETS);
+    return kNoG;
+  }
+  const int32_t f = bag / a.B, b = bag - f * a.B;
+  scale = 1.f;
+  if (a.mean) {
+    const int64_t len = a.offsets[bag + 1] - a.offsets[bag];
+    scale = len > 0 ? 1.f / (float)len : 0.f;
+  }
+  return (uint32_t)(((int64_t)b * a.sb + (int64_t)f * a.sf) >> 2);
+}
+
+__global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(const BwdArgs a) {
+  const int lane = threadIdx.x & 31;
+  const bool col = lane * 4 < a.d;  // this lane's 16-byte column exists
+  const float* Gl = a.G + lane * 4;
+  const int64_t np = *a.pieces_total;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t p = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < np; p += nwarps) {
+    const int64_t i = a.piece_owner[p];
+    int64_t r0, r1;
+    run_bounds(a, a.long_list[i], r0, r1);
+    const int64_t k = p - (int64_t)a.long_pstart[i];
+    const int32_t* sb = a.sorted_bag + r0 + k * kPiece;
+    const int n = (int)imin64(kPiece, r1 - (r0 + k * kPiece));
+    int32_t bag_b = (32 + lane < n) ? sb[32 + lane] : -1;
+    float sc_cur;
+    uint32_t cur = bag_g4(a, (lane < n) ? sb[lane] : -1, sc_cur);
+    float4 buf[kWin];
+#pragma unroll
+    for (int u = 0; u < kWin; ++u) {
+      const uint32_t r = __shfl_sync(kFull, cur, u);
+      buf[u] = (r != kNoG && col) ? ldg_f4(Gl + (uint64_t)r * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < n; c0 += 32) {
+      const int32_t bag_c = (c0 + 64 + lane < n) ? sb[c0 + 64 + lane] : -1;
+      float sc_nxt;
+      const uint32_t nxt = bag_g4(a, bag_b, sc_nxt);
+      for (int g = 0; g < 32; g += kWin) {
+#pragma unroll
+        for (int j = 0; j < kWin; ++j) {
+          const int t = g + j;
+          const float4 x = buf[j];
+          const int tn = t + kWin;
+          const uint32_t r = __shfl_sync(kFull, tn < 32 ? cur : nxt, tn & 31);
+          buf[j] = (r != kNoG && col) ? ldg_f4(Gl + (uint64_t)r * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (a.mean) acc = fma4(x, __shfl_sync(kFull, sc_cur, t), acc);
+          else acc = make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
+        }
+      }
+      cur = nxt;
+      sc_cur = sc_nxt;
+      bag_b = bag_c;
+    }
+    if (col) *(float4*)(a.partial + p * a.d + lane * 4) = acc;
+  }
+}
+
+// Tile kernel for rows of at most 512 bytes: the same work as bwd_tiles_kernel
+// with a streaming phase 1.  The flattened occurrences of the tile's short
+// runs are resolved 32 at a time (run by shuffle search, sorted_bag fetched one
+// chunk ahead, one ballot for run ends), and the pooled-gradient rows run in a
+// sliding window kWin deep.  The rows the tile will update are prefetched into
+// L2 when the tile starts.
+struct TileChunk {
+  int32_t bag;     // bag of this lane's occurrence (-1: none)
+  int seg;         // run (lane) of the occurrence within the tile
+  uint32_t lastm;  // ballot: occurrence t closes its run
+};
+
+__device__ __forceinline__ TileChunk tile_chunk(const BwdArgs& a, int kk, int E, int e, int r0, int slen) {
+  TileChunk c;
+  c.seg = 0;
+#pragma unroll
+  for (int step = 16; step > 0; step >>= 1) {  // largest lane i with e_i <= kk
+    const int cand = c.seg + step;
+    if (__shfl_sync(kFull, e, cand) <= kk) c.seg = cand;
+  }
+  const int es = __shfl_sync(kFull, e, c.seg);
+  const int rs = __shfl_sync(kFull, r0, c.seg);
+  const int ls = __shfl_sync(kFull, slen, c.seg);
+  c.bag = kk < E ? a.sorted_bag[rs + (kk - es)] : -1;
+  c.lastm = __ballot_sync(kFull, kk < E && kk + 1 == es + ls);
+  return c;
+}
+
+__global__ void __launch_bounds__(kTileThreads, CTR_TILE_MINB) bwd_tiles_stream_kernel(const BwdArgs a) {
+  extern __shared__ float4 sacc[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool col = lane * 4 < a.d;
+  const int chunks = a.d / 4;
+  const int TU = a.TU;
+  float4* my = sacc + (size_t)warp * TU * chunks;
+  const float* Gl = a.G + lane * 4;
+  const int row_bytes = a.d * (a.bf16 ? 2 : 4);
+  const int64_t nu = n_uniques(a);
+  const int64_t ntiles = ceil_div(nu, TU);
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t tile = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; tile < ntiles; tile += nwarps) {
+    const int64_t u = tile * TU + lane;
+    const bool valid = lane < TU && u < nu;
+    int64_t r0 = 0, r1 = 0;
+    if (valid) run_bounds(a, u, r0, r1);
+    const int64_t len = r1 - r0;
+    const bool is_long = valid && len > kShort;
+    const bool is_short = valid && !is_long && len > 0;
+    int64_t row = -1;
+    if (is_short) {
+      row = a.unique_rows[u];
+      if (row < 0 || row >= a.total_rows) {
+        set_error(a.err, CTR_ERR_INDEX_OUT_OF_RANGE);
+        row = -1;
+      } else if ((row_bytes & 15) == 0) {
+        const char* wr = (const char*)a.table + row * row_bytes;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(wr), "r"(row_bytes) : "memory");
+      }
+    }
+    if (is_long) {
+      const int64_t slot = (int64_t)atomicAdd((unsigned long long*)a.long_count, 1ull);
+      if (slot < a.max_long) {
+        a.long_list[slot] = (int32_t)u;
+        a.long_pstart[slot] = (uint32_t)ceil_div(len, kPiece);
+      }
+    }
+    const int slen = is_short ? (int)len : 0;
+    int inc = slen;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const int e = inc - slen;
+    const int E = __shfl_sync(kFull, inc, 31);
+    const int r0i = (int)r0;
+
+    // phase 1: stream the short runs' rows, one accumulator per run into shared memory
+    TileChunk cur = tile_chunk(a, lane, E, e, r0i, slen);
+    TileChunk pend = tile_chunk(a, 32 + lane, E, e, r0i, slen);
+    float sc_cur;
+    uint32_t gcur = bag_g4(a, cur.bag, sc_cur);
+    float4 buf[kWin];
+#pragma unroll
+    for (int q = 0; q < kWin; ++q) {
+      const uint32_t r = __shfl_sync(kFull, gcur, q);
+      buf[q] = (r != kNoG && col) ? ldg_f4(Gl + (uint64_t)r * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < E; c0 += 32) {
+      const TileChunk ahead = tile_chunk(a, c0 + 64 + lane, E, e, r0i, slen);
+      float sc_nxt;
+      const uint32_t gnxt = bag_g4(a, pend.bag, sc_nxt);
+      for (int g = 0; g < 32; g += kWin) {
+#pragma unroll
+        for (int j = 0; j < kWin; ++j) {
+          const int t = g + j;
+          const float4 x = buf[j];
+          const int tn = t + kWin;
+          const uint32_t r = __shfl_sync(kFull, tn < 32 ? gcur : gnxt, tn & 31);
+          buf[j] = (r != kNoG && col) ? ldg_f4(Gl + (uint64_t)r * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (a.mean) acc = fma4(x, __shfl_sync(kFull, sc_cur, t), acc);
+          else acc = make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
+          if ((cur.lastm >> t) & 1u) {
+            const int sg = __shfl_sync(kFull, cur.seg, t);
+            if (col) my[sg * chunks + lane] = acc;
+            acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+      }
+      cur = pend;
+      pend = ahead;
+      gcur = gnxt;
+      sc_cur = sc_nxt;
+    }
+    __syncwarp();
+    // phase 2: row updates, kRow independent rows in flight
+    constexpr int kRow = 8;
+    for (int j0 = 0; j0 < TU; j0 += kRow) {
+      float4 w[kRow];
+      uint2 wb[kRow];
+      int64_t rj[kRow];
+#pragma unroll
+      for (int jj = 0; jj < kRow; ++jj) {
+        const int j = (j0 + jj) & 31;
+        rj[jj] = __shfl_sync(kFull, row, j);
+        const int lj = __shfl_sync(kFull, slen, j);
+        if (j0 + jj >= TU || lj == 0) rj[jj] = -1;
+        if (rj[jj] >= 0 && col) load_row_chunk(a, rj[jj], lane, w[jj], wb[jj]);
+      }
+#pragma unroll
+      for (int jj = 0; jj < kRow; ++jj)
+        if (rj[jj] >= 0 && col)
+          store_row_chunk(a, rj[jj], tile * TU + j0 + jj, lane, my[(j0 + jj) * chunks + lane], w[jj], wb[jj]);
+    }
+    __syncwarp();
   }
 }
 
@@ -444,7 +663,7 @@ template <int CPL>
 int launch_bwd(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
   const int chunks = a.d / 4;
   const size_t tile_smem = (size_t)kTileWarps * a.TU * chunks * sizeof(float4);
-  auto tk = bwd_tiles_kernel<CPL>;
+  auto tk = (CPL == 1 && a.g4_ok) ? bwd_tiles_stream_kernel : bwd_tiles_kernel<CPL>;
   if (tile_smem > 48 * 1024 &&
       cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tile_smem) != cudaSuccess)
     return CTR_ERR_CUDA;
@@ -460,8 +679,13 @@ int launch_bwd(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
   }
   expand_long_kernel<<<std::max(1, num_sms() * 2), 256, 0, s>>>(a);
   if (int st = launch_status()) return st;
-  auto pk = long_pieces_kernel<CPL>;
-  pk<<<grid_of(pk, 256, 0, ceil_div(sizes(n).max_pieces, 8)), 256, 0, s>>>(a);
+  if (CPL == 1 && a.g4_ok) {
+    auto pk = long_pieces_stream_kernel;
+    pk<<<grid_of(pk, 256, 0, ceil_div(sizes(n).max_pieces, 8)), 256, 0, s>>>(a);
+  } else {
+    auto pk = long_pieces_kernel<CPL>;
+    pk<<<grid_of(pk, 256, 0, ceil_div(sizes(n).max_pieces, 8)), 256, 0, s>>>(a);
+  }
   if (int st = launch_status()) return st;
   const size_t csmem = (size_t)(kCombThreads / 32) * a.d * sizeof(float);
   combine_long_kernel<<<std::max(num_sms() * 2, 1), kCombThreads, csmem, s>>>(a);
@@ -524,6 +748,10 @@ extern "C" int ctr_embedding_bag_bwd_update(const float* grad_pooled, int64_t g_
   a.n_cap = n_ids;
   a.nbags = (int64_t)num_fields * batch;
   a.TU = std::max(1, std::min(32, kAccFloats / d));
+  {
+    const int64_t max_off = (int64_t)(batch - 1) * g_stride_b + (int64_t)(num_fields - 1) * g_stride_f + d;
+    a.g4_ok = (max_off >> 2) < (int64_t)0xffffffffll && n_ids < ((int64_t)1 << 31);
+  }
   a.long_count = c.take<int64_t>(1);
   a.pieces_total = c.take<uint32_t>(1);
   a.max_long = z.max_long;

@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -190,6 +191,140 @@ __global__ void __launch_bounds__(kBagThreads) bag_fwd_kernel(const BagArgs a, c
   }
 }
 
+// 512-byte fp32 rows (d = 128): one warp walks 32 consecutive bags as one
+// flattened list of occurrences (their index ranges are contiguous in CSR).
+// Per chunk of 32 occurrences the lanes resolve, in parallel, the bag of each
+// occurrence (binary search over the bags' first offsets by shuffle) and its
+// 32-bit row; one ballot marks the occurrences that close a bag.  Indices are
+// fetched two chunks ahead, and the row loads run in a sliding window kWinF
+// deep that continues across bag and chunk boundaries, so a bag boundary never
+// drains the pipeline.  Per occurrence the warp spends one shuffle (the row),
+// one 16-byte load per lane and four adds.  Each bag is summed in the order of
+// its indices; at its last occurrence the warp stores the row.
+constexpr int kWinF = 8;
+constexpr uint32_t kNoRow = 0xffffffffu;
+#ifndef CTR_FLAT_MINB
+#define CTR_FLAT_MINB 3  // resident blocks per SM the register budget is sized for
+#endif
+
+struct FlatChunk {
+  uint32_t row;    // global row of this lane's occurrence, kNoRow if none
+  uint32_t lastm;  // ballot: occurrence t closes its bag
+  int seg;         // bag (lane) of this lane's occurrence within the block
+};
+
+template <typename IT>
+__device__ __forceinline__ FlatChunk flat_chunk(const BagArgs& a, int kr, IT id, int rel0, int rel1, uint32_t base,
+                                                uint32_t nrows) {
+  FlatChunk m;
+  m.seg = 0;
+#pragma unroll
+  for (int step = 16; step > 0; step >>= 1) {  // largest lane j with rel0_j <= kr
+    const int cand = m.seg + step;
+    if (__shfl_sync(kFull, rel0, cand) <= kr) m.seg = cand;
+  }
+  const uint32_t bs = __shfl_sync(kFull, base, m.seg);
+  const uint32_t nr = __shfl_sync(kFull, nrows, m.seg);
+  const int r1 = __shfl_sync(kFull, rel1, m.seg);
+  m.row = kNoRow;
+  bool last = false;
+  if (kr < r1) {
+    const int64_t v = (int64_t)id;
+    if (v < 0 || v >= (int64_t)nr) set_error(a.err, CTR_ERR_INDEX_OUT_OF_RANGE);
+    else m.row = bs + (uint32_t)v;
+    last = (kr + 1 == r1);
+  }
+  m.lastm = __ballot_sync(kFull, last);
+  return m;
+}
+
+template <typename IT>
+__global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kernel(const BagArgs a,
+                                                                      const __grid_constant__ FieldMap fm) {
+  static_assert(32 % kWinF == 0, "the load window must divide the chunk");
+  const int lane = threadIdx.x & 31;
+  const int64_t nbags = (int64_t)a.F * a.B;
+  const int64_t nblk = ceil_div(nbags, 32);
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const IT* idx = (const IT*)a.idx;
+  const float* table = (const float*)a.table + lane * 4;
+  const int64_t end_all = a.offsets[nbags];
+  for (int64_t blk = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; blk < nblk; blk += nwarps) {
+    const int64_t bag = blk * 32 + lane;
+    const bool bvalid = bag < nbags;
+    int64_t o0 = bvalid ? a.offsets[bag] : end_all;
+    int64_t o1 = bvalid ? a.offsets[bag + 1] : end_all;
+    const bool bad = o0 < 0 || o1 < o0 || o1 > a.n_idx;
+    const int f = bvalid ? (int)(bag / a.B) : 0;
+    const int b = bvalid ? (int)(bag - (int64_t)f * a.B) : 0;
+    const int64_t ooff = (int64_t)b * a.sb + (int64_t)f * a.sf + lane * 4;
+    const float lenf = (float)(o1 - o0);
+    const int64_t S0 = __shfl_sync(kFull, o0, 0);
+    const int64_t S1 = __shfl_sync(kFull, o1, 31);
+    if (__any_sync(kFull, bad) || S1 - S0 >= ((int64_t)1 << 30)) {
+      if (lane == 0) set_error(a.err, CTR_ERR_BAD_OFFSETS);
+      o0 = o1 = S0;  // write this block as zeros
+    }
+    unsigned empty = __ballot_sync(kFull, bvalid && o1 == o0);  // empty bags produce zero rows
+    while (empty) {
+      const int j = __ffs(empty) - 1;
+      empty &= empty - 1;
+      const float z[4] = {0.f, 0.f, 0.f, 0.f};
+      store_out(a.out, __shfl_sync(kFull, ooff, j) - j * 4 + lane * 4, z, 4, a.out_bf16, a.vec_out);
+    }
+    if (__all_sync(kFull, o1 == o0)) continue;
+    const int rel0 = (int)(o0 - S0), rel1 = (int)(o1 - S0);
+    const uint32_t base = a.mapped ? (uint32_t)fm.base[f] : 0u;
+    const uint32_t nrows = a.mapped ? (uint32_t)fm.rows[f] : (uint32_t)a.total_rows;
+    const int total = (int)(S1 - S0);
+
+    const IT* ib = idx + S0;
+    IT id_b = (32 + lane < total) ? ib[32 + lane] : IT(0);
+    FlatChunk cur = flat_chunk(a, lane, (lane < total) ? ib[lane] : IT(0), rel0, rel1, base, nrows);
+    float4 buf[kWinF];
+#pragma unroll
+    for (int u = 0; u < kWinF; ++u) {
+      const uint32_t r = __shfl_sync(kFull, cur.row, u);
+      buf[u] = (r != kNoRow) ? *(const float4*)(table + (uint64_t)r * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < total; c0 += 32) {
+      const IT id_c = (c0 + 64 + lane < total) ? ib[c0 + 64 + lane] : IT(0);
+      const FlatChunk nxt = flat_chunk(a, c0 + 32 + lane, id_b, rel0, rel1, base, nrows);
+      for (int g = 0; g < 32; g += kWinF) {
+#pragma unroll
+        for (int j = 0; j < kWinF; ++j) {
+          const int t = g + j;
+          const float4 x = buf[j];
+          const int tn = t + kWinF;  // refill the slot with occurrence tn
+          const uint32_t r = __shfl_sync(kFull, tn < 32 ? cur.row : nxt.row, tn & 31);
+          buf[j] = (r != kNoRow) ? *(const float4*)(table + (uint64_t)r * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+          acc.x += x.x;
+          acc.y += x.y;
+          acc.z += x.z;
+          acc.w += x.w;
+          if ((cur.lastm >> t) & 1u) {
+            const int jb = __shfl_sync(kFull, cur.seg, t);
+            const int64_t oj = __shfl_sync(kFull, ooff, jb) - jb * 4 + lane * 4;
+            float v[4] = {acc.x, acc.y, acc.z, acc.w};
+            if (a.mean) {  // a closed bag is never empty
+              const float lj = __shfl_sync(kFull, lenf, jb);
+              v[0] /= lj;
+              v[1] /= lj;
+              v[2] /= lj;
+              v[3] /= lj;
+            }
+            store_out(a.out, oj, v, 4, a.out_bf16, a.vec_out);
+            acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+      }
+      cur = nxt;
+      id_b = id_c;
+    }
+  }
+}
+
 // Rows whose width is not a multiple of 16 bytes: one element per lane.
 template <typename TT, typename IT>
 __global__ void __launch_bounds__(kBagThreads) bag_fwd_scalar_kernel(const BagArgs a,
@@ -245,6 +380,11 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
     return launch_status();
   }
   const int chunks = a.d / V;
+  if (std::is_same<TT, float>::value && a.d == 128 && a.total_rows < 0xffffffffll) {
+    auto k = bag_fwd_flat_kernel<IT>;
+    k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm);
+    return launch_status();
+  }
 #define CTR_LAUNCH(LPR, CPL)                                 \
   {                                                          \
     auto k = bag_fwd_kernel<TT, LPR, CPL, IT>;               \
