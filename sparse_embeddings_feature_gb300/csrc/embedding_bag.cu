@@ -19,6 +19,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace ctr {
 namespace {
@@ -202,6 +203,10 @@ __global__ void __launch_bounds__(kBagThreads) bag_fwd_kernel(const BagArgs a, c
 // one 16-byte load per lane and four adds.  Each bag is summed in the order of
 // its indices; at its last occurrence the warp stores the row.
 constexpr int kWinF = 8;
+#ifndef CTR_TMA_GATHER
+#define CTR_TMA_GATHER 0  // measured slower than the register window on GB300; kept selectable
+#endif
+constexpr bool kUseTmaGather = CTR_TMA_GATHER != 0;
 constexpr uint32_t kNoRow = 0xffffffffu;
 #ifndef CTR_FLAT_MINB
 #define CTR_FLAT_MINB 3  // resident blocks per SM the register budget is sized for
@@ -325,6 +330,177 @@ __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kerne
   }
 }
 
+// The same flattened walk as bag_fwd_flat_kernel, with the rows staged by TMA
+// instead of loaded into registers: for every four occurrences one lane issues
+// a tile::gather4 (four 512-byte rows by row index, one mbarrier) into a ring
+// of kTmaStages shared-memory stages owned by its warp, one chunk (32 rows)
+// ahead of the lanes that sum them.  In flight per warp: 32 rows, held in
+// shared memory, so registers no longer cap the loads in flight.  Each warp is
+// an independent pipeline; every mbarrier wait is bounded and a warp that
+// times out records CTR_ERR_TIMEOUT, waits (bounded) for its own copies and
+// stops.
+constexpr int kTmaWarps = 4;
+constexpr int kTmaStages = 8;                 // 8 stages x 4 rows = one chunk ahead
+constexpr int kTmaStageBytes = 4 * 512;
+
+struct TmaRing {
+  uint32_t data;     // shared address of stage 0 of this warp
+  uint32_t bar;      // shared address of this warp's first mbarrier
+  uint32_t issued;   // groups issued (stage = n % kTmaStages, parity = (n / kTmaStages) & 1)
+  uint32_t consumed;
+};
+
+// Issue the gather of occurrences 4q .. 4q+3 of a chunk whose rows the lanes hold.
+__device__ __forceinline__ void tma_issue(TmaRing& r, const CUtensorMap* map, uint32_t rows, int q) {
+  const int lane = threadIdx.x & 31;
+  int32_t rr[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t v = __shfl_sync(kFull, rows, 4 * q + i);
+    rr[i] = v == kNoRow ? 0 : (int32_t)v;  // an unused slot still needs a valid row
+  }
+  const uint32_t st = r.issued % kTmaStages;
+  if (lane == 0) {
+    const uint32_t bar = r.bar + 8 * st;
+    mbar_expect_tx(bar, kTmaStageBytes);
+    tma_gather4(r.data + st * kTmaStageBytes, map, 0, rr[0], rr[1], rr[2], rr[3], bar);
+  }
+  ++r.issued;
+}
+
+template <typename IT>
+__global__ void __launch_bounds__(kTmaWarps * 32) bag_fwd_tma_kernel(const BagArgs a,
+                                                                     const __grid_constant__ FieldMap fm,
+                                                                     const __grid_constant__ CUtensorMap map) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kTmaWarps][kTmaStages];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t aligned = (raw + 1023u) & ~1023u;
+  const uint8_t* gen_base = smem_raw + (aligned - raw);
+  TmaRing ring;
+  ring.data = aligned + (uint32_t)warp * kTmaStages * kTmaStageBytes;
+  ring.bar = smem_u32(&bars[warp][0]);
+  ring.issued = ring.consumed = 0;
+  const uint8_t* my = gen_base + (size_t)warp * kTmaStages * kTmaStageBytes + lane * 16;
+  if (lane == 0) {
+    for (int st = 0; st < kTmaStages; ++st) mbar_init(ring.bar + 8 * st, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const int64_t nbags = (int64_t)a.F * a.B;
+  const int64_t nblk = ceil_div(nbags, 32);
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const IT* idx = (const IT*)a.idx;
+  const int64_t end_all = a.offsets[nbags];
+  bool ok = true;
+  for (int64_t blk = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; ok && blk < nblk; blk += nwarps) {
+    const int64_t bag = blk * 32 + lane;
+    const bool bvalid = bag < nbags;
+    int64_t o0 = bvalid ? a.offsets[bag] : end_all;
+    int64_t o1 = bvalid ? a.offsets[bag + 1] : end_all;
+    const bool bad = o0 < 0 || o1 < o0 || o1 > a.n_idx;
+    const int f = bvalid ? (int)(bag / a.B) : 0;
+    const int b = bvalid ? (int)(bag - (int64_t)f * a.B) : 0;
+    const int64_t ooff = (int64_t)b * a.sb + (int64_t)f * a.sf + lane * 4;
+    const float lenf = (float)(o1 - o0);
+    const int64_t S0 = __shfl_sync(kFull, o0, 0);
+    const int64_t S1 = __shfl_sync(kFull, o1, 31);
+    if (__any_sync(kFull, bad) || S1 - S0 >= ((int64_t)1 << 30)) {
+      if (lane == 0) set_error(a.err, CTR_ERR_BAD_OFFSETS);
+      o0 = o1 = S0;
+    }
+    unsigned empty = __ballot_sync(kFull, bvalid && o1 == o0);
+    while (empty) {
+      const int j = __ffs(empty) - 1;
+      empty &= empty - 1;
+      const float z[4] = {0.f, 0.f, 0.f, 0.f};
+      store_out(a.out, __shfl_sync(kFull, ooff, j) - j * 4 + lane * 4, z, 4, a.out_bf16, a.vec_out);
+    }
+    if (__all_sync(kFull, o1 == o0)) continue;
+    const int rel0 = (int)(o0 - S0), rel1 = (int)(o1 - S0);
+    const uint32_t base = a.mapped ? (uint32_t)fm.base[f] : 0u;
+    const uint32_t nrows = a.mapped ? (uint32_t)fm.rows[f] : (uint32_t)a.total_rows;
+    const int total = (int)(S1 - S0);
+    const IT* ib = idx + S0;
+
+    IT id_b = (32 + lane < total) ? ib[32 + lane] : IT(0);
+    FlatChunk cur = flat_chunk(a, lane, (lane < total) ? ib[lane] : IT(0), rel0, rel1, base, nrows);
+    uint32_t curv = __ballot_sync(kFull, cur.row != kNoRow);
+    for (int q = 0; q < kTmaStages && 4 * q < total; ++q) tma_issue(ring, &map, cur.row, q);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; ok && c0 < total; c0 += 32) {
+      const IT id_c = (c0 + 64 + lane < total) ? ib[c0 + 64 + lane] : IT(0);
+      const FlatChunk nxt = flat_chunk(a, c0 + 32 + lane, id_b, rel0, rel1, base, nrows);
+      const uint32_t nxtv = __ballot_sync(kFull, nxt.row != kNoRow);
+      for (int q = 0; q < kTmaStages; ++q) {
+        if (c0 + 4 * q >= total) break;
+        const uint32_t st = ring.consumed % kTmaStages;
+        if (!mbar_wait(ring.bar + 8 * st, (ring.consumed / kTmaStages) & 1)) {
+          set_error(a.err, CTR_ERR_TIMEOUT);
+          ok = false;
+        }
+        if (!__all_sync(kFull, ok)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sp = my + st * kTmaStageBytes;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int t = 4 * q + i;
+          const float4 x = *(const float4*)(sp + i * 512);
+          if ((curv >> t) & 1u) {
+            acc.x += x.x;
+            acc.y += x.y;
+            acc.z += x.z;
+            acc.w += x.w;
+          }
+          if ((cur.lastm >> t) & 1u) {
+            const int jb = __shfl_sync(kFull, cur.seg, t);
+            const int64_t oj = __shfl_sync(kFull, ooff, jb) - jb * 4 + lane * 4;
+            float v[4] = {acc.x, acc.y, acc.z, acc.w};
+            if (a.mean) {
+              const float lj = __shfl_sync(kFull, lenf, jb);
+              v[0] /= lj;
+              v[1] /= lj;
+              v[2] /= lj;
+              v[3] /= lj;
+            }
+            store_out(a.out, oj, v, 4, a.out_bf16, a.vec_out);
+            acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+        ++ring.consumed;
+        __syncwarp();  // every lane has read the stage before it is refilled
+        if (c0 + 32 + 4 * q < total) tma_issue(ring, &map, nxt.row, q);
+      }
+      cur = nxt;
+      curv = nxtv;
+      id_b = id_c;
+    }
+  }
+  // copies still in flight (only after a timeout) must land before the warp exits
+  while (ring.consumed != ring.issued) {
+    const uint32_t st = ring.consumed % kTmaStages;
+    mbar_wait(ring.bar + 8 * st, (ring.consumed / kTmaStages) & 1);
+    ++ring.consumed;
+  }
+}
+
+// Tensor map of the table viewed as [total_rows, 128] fp32, one-row boxes.
+bool make_row_map(const BagArgs& a, CUtensorMap* map) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || a.total_rows >= ((int64_t)1 << 31)) return false;
+  cuuint64_t gdim[2] = {128, (cuuint64_t)a.total_rows};
+  cuuint64_t gstride[1] = {512};
+  cuuint32_t box[2] = {128, 1};
+  cuuint32_t estride[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(a.table), gdim, gstride, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Rows whose width is not a multiple of 16 bytes: one element per lane.
 template <typename TT, typename IT>
 __global__ void __launch_bounds__(kBagThreads) bag_fwd_scalar_kernel(const BagArgs a,
@@ -380,6 +556,19 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
     return launch_status();
   }
   const int chunks = a.d / V;
+  CUtensorMap map;
+  if (std::is_same<TT, float>::value && a.d == 128 && kUseTmaGather && make_row_map(a, &map)) {
+    auto k = bag_fwd_tma_kernel<IT>;
+    const size_t smem = 1024 + (size_t)kTmaWarps * kTmaStages * kTmaStageBytes;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return CTR_ERR_CUDA;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kTmaWarps * 32, smem);
+    const int64_t want = ceil_div(ceil_div(nbags, 32), kTmaWarps);
+    const int grid = (int)std::max<int64_t>(1, imin64(want, (int64_t)std::max(per_sm, 1) * num_sms()));
+    k<<<grid, kTmaWarps * 32, smem, s>>>(a, fm, map);
+    return launch_status();
+  }
   if (std::is_same<TT, float>::value && a.d == 128 && a.total_rows < 0xffffffffll) {
     auto k = bag_fwd_flat_kernel<IT>;
     k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm);
