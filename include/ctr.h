@@ -222,6 +222,32 @@ int ctr_embedding_bag_bwd_update(const float* grad_pooled, int64_t g_stride_b, i
                                  int32_t d, int64_t total_rows, float* grad_unique_out, void* ws, size_t ws_bytes,
                                  ctr_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Allocation-free dedup (no counterpart in the paper)                       */
+/* ------------------------------------------------------------------------ */
+/* ctr_dedup for callers that may not allocate device memory on this path: a
+ * plugin inside a runtime that owns every device allocation, a server whose
+ * memory budget is fixed at start-up, or a latency-critical loop where an
+ * allocation could stall the device.  Same inputs and outputs as ctr_dedup,
+ * but the scratch space is a fixed array inside the library (about 24 MB per
+ * GPU that loads the library, held until exit) instead of a caller workspace.
+ *   n_ids            at most 1048576 (2^20); larger calls return
+ *                    CTR_ERR_UNSUPPORTED and launch nothing.
+ *   device_status    optional device int32: receives this call's device-side
+ *                    error code (0, CTR_ERR_INDEX_OUT_OF_RANGE or
+ *                    CTR_ERR_BAD_OFFSETS) once the call's work has run.
+ * All calls share the array and it keeps the previous call's contents; its
+ * error word is cleared at the start of every call.  Calls that overlap on
+ * the GPU race on the array: order them (one stream, or explicit events).
+ * The first call on a device looks up the array's address with that device
+ * current and caches it; make that first call before any stream capture.
+ * Nothing here calls cudaMalloc, cudaFree or any other allocator. */
+int ctr_dedup_static(const int64_t* ids, const int64_t* offsets, int32_t num_fields, int32_t batch,
+                     const int32_t* bag_to_table, const int64_t* row_base, int32_t num_tables, int64_t n_ids,
+                     int64_t* unique_rows, int64_t* n_unique, int32_t* inverse, int32_t* sorted_pos,
+                     int32_t* sorted_bag, int32_t* run_offsets, int64_t* unique_offsets, int32_t* device_status,
+                     ctr_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
