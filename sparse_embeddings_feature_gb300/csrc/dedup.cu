@@ -30,7 +30,9 @@ constexpr int kRsWarps = kRsThreads / 32;
 constexpr int kRsItems = 16;                      // keys per lane per tile
 constexpr int kRsTile = kRsThreads * kRsItems;    // 4096 keys
 constexpr int kRsWarpKeys = 32 * kRsItems;        // 512 keys per warp
-constexpr int kMaxDigits = 256;
+constexpr int kMaxBits = 10;                      // digit width limit: 28-bit keys sort in 3 passes
+constexpr int kMaxDigits = 1 << kMaxBits;
+constexpr int kDigitsPerThread = kMaxDigits / kRsThreads;  // 4
 
 struct TableBases {
   int64_t row_base[CTR_MAX_TABLES + 1];
@@ -75,11 +77,12 @@ __device__ __forceinline__ uint32_t digit_of(uint32_t k, int shift, uint32_t mas
 __global__ void __launch_bounds__(kRsThreads) radix_upsweep_kernel(const uint32_t* __restrict__ keys, int64_t n,
                                                                    int shift, int nbits,
                                                                    uint32_t* __restrict__ hist, int64_t num_tiles) {
-  __shared__ uint32_t cnt[kRsWarps][kMaxDigits];
+  extern __shared__ uint32_t up_smem[];
+  uint32_t(*cnt)[kMaxDigits] = reinterpret_cast<uint32_t(*)[kMaxDigits]>(up_smem);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ndig = 1 << nbits;
   const uint32_t mask = (uint32_t)ndig - 1;
-  for (int i = threadIdx.x; i < kRsWarps * kMaxDigits; i += kRsThreads) (&cnt[0][0])[i] = 0;
+  for (int i = threadIdx.x; i < kRsWarps * ndig; i += kRsThreads) cnt[i / ndig][i % ndig] = 0;
   __syncthreads();
   const int64_t base = (int64_t)blockIdx.x * kRsTile + (int64_t)warp * kRsWarpKeys;
 #pragma unroll 4
@@ -106,16 +109,17 @@ __global__ void __launch_bounds__(kRsThreads) radix_downsweep_kernel(
     const uint32_t* __restrict__ keys_in, const int32_t* __restrict__ vals_in, uint32_t* __restrict__ keys_out,
     int32_t* __restrict__ vals_out, int64_t n, int shift, int nbits, const uint32_t* __restrict__ hist_scan,
     int64_t num_tiles) {
-  __shared__ uint32_t wcnt[kRsWarps][kMaxDigits];
-  __shared__ uint32_t tile_start[kMaxDigits];
-  __shared__ uint32_t glob_start[kMaxDigits];
-  __shared__ uint32_t skeys[kRsTile];
-  __shared__ int32_t svals[kRsTile];
+  extern __shared__ uint32_t ds_smem[];
+  uint32_t(*wcnt)[kMaxDigits] = reinterpret_cast<uint32_t(*)[kMaxDigits]>(ds_smem);  // [warps][digits]
+  uint32_t* tile_start = ds_smem + kRsWarps * kMaxDigits;
+  uint32_t* glob_start = tile_start + kMaxDigits;
+  uint32_t* skeys = glob_start + kMaxDigits;
+  int32_t* svals = (int32_t*)(skeys + kRsTile);
   __shared__ uint32_t warp_tot[kRsWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ndig = 1 << nbits;
   const uint32_t mask = (uint32_t)ndig - 1;
-  for (int i = threadIdx.x; i < kRsWarps * kMaxDigits; i += kRsThreads) (&wcnt[0][0])[i] = 0;
+  for (int i = threadIdx.x; i < kRsWarps * ndig; i += kRsThreads) wcnt[i / ndig][i % ndig] = 0;
   __syncthreads();
 
   const int64_t tile_base = (int64_t)blockIdx.x * kRsTile;
@@ -139,25 +143,31 @@ __global__ void __launch_bounds__(kRsThreads) radix_downsweep_kernel(
     rank[r] = valid ? prior + __popc(peers & lt) : 0xffffffffu;
   }
   __syncthreads();
-  // per digit: exclusive over warps (in place), then exclusive over digits
-  uint32_t dtot[1] = {0};
-  {
-    const int dg = threadIdx.x;  // kRsThreads == kMaxDigits
+  // per digit: exclusive over warps (in place), then exclusive over digits;
+  // thread t owns digits kDigitsPerThread*t .. +kDigitsPerThread-1
+  uint32_t dtot[kDigitsPerThread];
+#pragma unroll
+  for (int q = 0; q < kDigitsPerThread; ++q) {
+    const int dg = threadIdx.x * kDigitsPerThread + q;
     uint32_t run = 0;
     if (dg < ndig) {
 #pragma unroll
       for (int w = 0; w < kRsWarps; ++w) {
-        uint32_t c = wcnt[w][dg];
+        const uint32_t c = wcnt[w][dg];
         wcnt[w][dg] = run;
         run += c;
       }
       glob_start[dg] = hist_scan[(int64_t)dg * num_tiles + blockIdx.x];
     }
-    dtot[0] = run;
+    dtot[q] = run;
   }
   __syncthreads();
-  block_exclusive_scan<uint32_t, kRsThreads, 1>(dtot, warp_tot);
-  if (threadIdx.x < ndig) tile_start[threadIdx.x] = dtot[0];
+  block_exclusive_scan<uint32_t, kRsThreads, kDigitsPerThread>(dtot, warp_tot);
+#pragma unroll
+  for (int q = 0; q < kDigitsPerThread; ++q) {
+    const int dg = threadIdx.x * kDigitsPerThread + q;
+    if (dg < ndig) tile_start[dg] = dtot[q];
+  }
   __syncthreads();
 #pragma unroll
   for (int r = 0; r < kRsItems; ++r) {
@@ -212,63 +222,87 @@ __device__ __forceinline__ int table_of(const int64_t* rb, int T, int64_t k) {
   return lo;
 }
 
+// Ranks and outputs of one tile of sorted keys.  The tile's 4096 slots are read
+// as 16 coalesced rows of 256 (slot = row * 256 + thread): head flags come from
+// one ballot per warp and row, and a scan of the 16 x 8 per-warp head counts
+// gives every slot its rank.
 __global__ void __launch_bounds__(kRsThreads) unique_write_kernel(
     const uint32_t* __restrict__ skeys, const int32_t* __restrict__ spos, int64_t n,
     const uint32_t* __restrict__ tile_base_scan, const __grid_constant__ TableBases tb,
     const int32_t* __restrict__ bag_of, int64_t* __restrict__ unique_rows, int64_t* __restrict__ n_unique,
     int32_t* __restrict__ inverse, int32_t* __restrict__ sorted_bag, int32_t* __restrict__ run_offsets,
     int64_t* __restrict__ unique_offsets) {
-  __shared__ uint32_t warp_tot[kRsWarps];
+  constexpr int kRows = kRsTile / kRsThreads;  // 16
+  __shared__ uint32_t cnt[kRows * kRsWarps];     // heads per (row, warp), then exclusive offsets
   __shared__ int64_t rb[CTR_MAX_TABLES + 1];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int T = tb.num_tables;
   for (int i = threadIdx.x; i <= T; i += kRsThreads) rb[i] = tb.row_base[i];
-  const int64_t base = (int64_t)blockIdx.x * kRsTile + (int64_t)threadIdx.x * kRsItems;
-  uint32_t k[kRsItems];
-  uint32_t h[kRsItems];
-  uint32_t prev = (base > 0 && base - 1 < n) ? skeys[base - 1] : 0u;
+  const int64_t tile0 = (int64_t)blockIdx.x * kRsTile;
+  const unsigned lt = lanemask_lt();
+  uint32_t key[kRows];
+  unsigned mask[kRows];
 #pragma unroll
-  for (int i = 0; i < kRsItems; ++i) {
-    int64_t s = base + i;
-    k[i] = s < n ? skeys[s] : 0u;
-    h[i] = (s < n && (s == 0 || k[i] != prev)) ? 1u : 0u;
-    prev = k[i];
+  for (int r = 0; r < kRows; ++r) {
+    const int64_t sl = tile0 + r * kRsThreads + threadIdx.x;
+    const bool valid = sl < n;
+    key[r] = valid ? skeys[sl] : 0u;
+    const uint32_t prevk = (valid && sl > 0) ? skeys[sl - 1] : ~key[r];
+    mask[r] = __ballot_sync(kFull, valid && (sl == 0 || key[r] != prevk));
+    if (lane == 0) cnt[r * kRsWarps + warp] = __popc(mask[r]);
   }
-  uint32_t excl[kRsItems];
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the 128 counts, 4 per lane, in slot order
+    uint32_t v[4], sum = 0;
 #pragma unroll
-  for (int i = 0; i < kRsItems; ++i) excl[i] = h[i];
-  __syncthreads();  // rb ready
-  uint32_t tile_total = block_exclusive_scan<uint32_t, kRsThreads, kRsItems>(excl, warp_tot);
+    for (int q = 0; q < 4; ++q) {
+      v[q] = cnt[lane * 4 + q];
+      sum += v[q];
+    }
+    uint32_t inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += y;
+    }
+    uint32_t run = inc - sum;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      cnt[lane * 4 + q] = run;
+      run += v[q];
+    }
+  }
+  __syncthreads();
   const uint32_t tbase = tile_base_scan[blockIdx.x];
 #pragma unroll
-  for (int i = 0; i < kRsItems; ++i) {
-    int64_t s = base + i;
-    if (s >= n) break;
-    // rank of this key = heads in [0, s] - 1
-    uint32_t rank = tbase + excl[i] + h[i] - 1;
-    if (h[i]) {
-      unique_rows[rank] = (int64_t)k[i];
-      if (run_offsets) run_offsets[rank] = (int32_t)s;
+  for (int r = 0; r < kRows; ++r) {
+    const int64_t sl = tile0 + r * kRsThreads + threadIdx.x;
+    if (sl >= n) break;
+    const bool head = (mask[r] >> lane) & 1u;
+    // rank of this key = heads in [0, sl] - 1
+    const uint32_t rank = tbase + cnt[r * kRsWarps + warp] + __popc(mask[r] & lt) + (head ? 1u : 0u) - 1u;
+    if (head) {
+      unique_rows[rank] = (int64_t)key[r];
+      if (run_offsets) run_offsets[rank] = (int32_t)sl;
       if (unique_offsets) {
-        int t = table_of(rb, T, (int64_t)k[i]);
-        int t0 = 0;
-        if (s > 0) t0 = table_of(rb, T, (int64_t)skeys[s - 1]) + 1;
+        const int t = table_of(rb, T, (int64_t)key[r]);
+        const int t0 = sl > 0 ? table_of(rb, T, (int64_t)skeys[sl - 1]) + 1 : 0;
         for (int tt = t0; tt <= t; ++tt) unique_offsets[tt] = rank;
       }
     }
-    int32_t p = spos[s];
+    const int32_t p = spos[sl];
     if (inverse) inverse[p] = (int32_t)rank;
-    if (sorted_bag) sorted_bag[s] = bag_of[p];
-    if (s == n - 1) {
-      uint32_t nu = rank + 1;
+    if (sorted_bag) sorted_bag[sl] = bag_of[p];
+    if (sl == n - 1) {
+      const uint32_t nu = rank + 1;
       *n_unique = nu;
       if (run_offsets) run_offsets[nu] = (int32_t)n;
       if (unique_offsets) {
-        int t = table_of(rb, T, (int64_t)k[i]);
+        const int t = table_of(rb, T, (int64_t)key[r]);
         for (int tt = t + 1; tt <= T; ++tt) unique_offsets[tt] = nu;
       }
     }
   }
-  (void)tile_total;
 }
 
 __global__ void dedup_empty_kernel(int64_t* n_unique, int32_t* run_offsets, int64_t* unique_offsets, int T) {
@@ -288,7 +322,7 @@ template <typename WS>
 void dedup_layout(WS& ws, int64_t n_ids, int64_t total_rows) {
   const int64_t tiles = ceil_div(n_ids, kRsTile);
   const int bits = key_bits(total_rows);
-  const int passes = (bits + 7) / 8;
+  const int passes = (bits + kMaxBits - 1) / kMaxBits;
   const int nb = (bits + passes - 1) / passes;
   ws.template take<uint32_t>((size_t)n_ids);           // keys A
   ws.template take<uint32_t>((size_t)n_ids);           // keys B
@@ -351,7 +385,7 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
   WsCarver c(ws, ws_bytes);
   const int64_t tiles = ceil_div(n_ids, kRsTile);
   const int bits = key_bits(total_rows);
-  const int passes = (bits + 7) / 8;
+  const int passes = (bits + kMaxBits - 1) / kMaxBits;
   const int nb = (bits + passes - 1) / passes;
   uint32_t* keys[2] = {c.take<uint32_t>(n_ids), c.take<uint32_t>(n_ids)};
   int32_t* vscratch = c.take<int32_t>(n_ids);
@@ -369,17 +403,24 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
                                                                         keys[0], bag_of, err);
     if (int st = launch_status()) return st;
   }
+  const size_t up_smem = (size_t)kRsWarps * kMaxDigits * sizeof(uint32_t);
+  const size_t ds_smem = ((size_t)kRsWarps * kMaxDigits + 2 * kMaxDigits + 2 * kRsTile) * sizeof(uint32_t);
+  if (cudaFuncSetAttribute(radix_upsweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)up_smem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(radix_downsweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ds_smem) !=
+          cudaSuccess)
+    return CTR_ERR_CUDA;
   const int32_t* vin = nullptr;
   int shift = 0;
   for (int p = 0; p < passes; ++p) {
     const int pb = std::min(nb, bits - shift);
     const int64_t nh = tiles << pb;
-    radix_upsweep_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(keys[p & 1], n_ids, shift, pb, hist, tiles);
+    radix_upsweep_kernel<<<(unsigned)tiles, kRsThreads, up_smem, s>>>(keys[p & 1], n_ids, shift, pb, hist, tiles);
     if (int st = launch_status()) return st;
     WsCarver scan_ws = c;  // scan scratch is reused every pass
     if (int st = scan_exclusive<uint32_t>(hist, hist, nh, nullptr, nullptr, scan_ws, s)) return st;
     int32_t* vout = ((passes - 1 - p) % 2 == 0) ? vfinal : vscratch;
-    radix_downsweep_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(keys[p & 1], vin, keys[(p + 1) & 1], vout, n_ids,
+    radix_downsweep_kernel<<<(unsigned)tiles, kRsThreads, ds_smem, s>>>(keys[p & 1], vin, keys[(p + 1) & 1], vout, n_ids,
                                                                    shift, pb, hist, tiles);
     if (int st = launch_status()) return st;
     vin = vout;

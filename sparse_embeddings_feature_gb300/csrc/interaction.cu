@@ -110,6 +110,12 @@ __global__ void __launch_bounds__(kIntWarps * 32) interaction_fwd_f32_regs(const
   }
 }
 
+// Backward, n = 27, d = 128: one warp per sample.  The sample's upstream pair
+// gradients are expanded into a symmetric matrix S (zero diagonal, rows padded
+// to 28 floats) in the warp's shared memory; lane l holds columns 4l..4l+3 of
+// every vector in registers, and row i of dX is the branch-free sweep
+// dX_i = sum_j S[i][j] x_j: one 16-byte broadcast load of S per four j and
+// sixteen FMAs.
 template <int N, int D>
 __global__ void __launch_bounds__(kIntWarps * 32) interaction_bwd_f32_regs(const float* __restrict__ dout,
                                                                           const float* __restrict__ X, int32_t batch,
@@ -117,27 +123,40 @@ __global__ void __launch_bounds__(kIntWarps * 32) interaction_bwd_f32_regs(const
   static_assert(D == 128, "4 columns per lane");
   constexpr int P = N * (N - 1) / 2;
   constexpr int W = D + P;
-  __shared__ float sdz[kIntWarps][P + 1];
+  constexpr int NP = (N + 3) / 4 * 4;  // padded row length of S
+  __shared__ __align__(16) float sS[kIntWarps][N * NP];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  float* dz = sdz[warp];
+  float* S = sS[warp];
+  for (int e = lane; e < N * NP; e += 32) S[e] = 0.f;  // diagonal and padding stay zero
+  __syncwarp();
   for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < batch; b += nwarps) {
     const float* xb = X + b * (int64_t)N * D + lane * 4;
     const float* gb = dout + b * (int64_t)W;
-    float x[N][4];
+    float x[NP][4];
 #pragma unroll
     for (int i = 0; i < N; ++i) {
-      float4 v = __ldcs((const float4*)(xb + i * D));
+      const float4 v = __ldcs((const float4*)(xb + i * D));
       x[i][0] = v.x;
       x[i][1] = v.y;
       x[i][2] = v.z;
       x[i][3] = v.w;
     }
-    __syncwarp();
-    for (int p = lane; p < P; p += 32) dz[p] = __ldcs(gb + D + p);
+#pragma unroll
+    for (int i = N; i < NP; ++i) x[i][0] = x[i][1] = x[i][2] = x[i][3] = 0.f;
     float dense[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) dense[c] = __ldcs(gb + lane * 4 + c);
+    __syncwarp();  // the previous sample's S is no longer read
+    for (int p = lane; p < P; p += 32) {
+      int i = (int)((1.f + sqrtf(1.f + 8.f * (float)p)) * 0.5f);  // row of pair p: i(i-1)/2 <= p
+      if (i * (i - 1) / 2 > p) --i;
+      if ((i + 1) * i / 2 <= p) ++i;
+      const int j = p - i * (i - 1) / 2;
+      const float g = __ldcs(gb + D + p);
+      S[i * NP + j] = g;
+      S[j * NP + i] = g;
+    }
     __syncwarp();
     float* ob = dX + b * (int64_t)N * D + lane * 4;
 #pragma unroll 1
@@ -145,13 +164,15 @@ __global__ void __launch_bounds__(kIntWarps * 32) interaction_bwd_f32_regs(const
       float acc[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[c] = (i == 0) ? dense[c] : 0.f;
+      const float4* Si = (const float4*)(S + i * NP);
 #pragma unroll
-      for (int j = 0; j < N; ++j) {
-        if (j == i) continue;
-        const int hi = i > j ? i : j, lo = i > j ? j : i;
-        const float g = dz[hi * (hi - 1) / 2 + lo];
+      for (int q = 0; q < NP / 4; ++q) {
+        const float4 s4 = Si[q];
+        const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[c] = fmaf(g, x[j][c], acc[c]);
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[c] = fmaf(sv[r], x[4 * q + r][c], acc[c]);
       }
       __stcs((float4*)(ob + i * D), make_float4(acc[0], acc[1], acc[2], acc[3]));
     }
