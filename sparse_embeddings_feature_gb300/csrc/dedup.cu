@@ -30,20 +30,32 @@ constexpr int kRsWarps = kRsThreads / 32;
 constexpr int kRsItems = 16;                      // keys per lane per tile
 constexpr int kRsTile = kRsThreads * kRsItems;    // 4096 keys
 constexpr int kRsWarpKeys = 32 * kRsItems;        // 512 keys per warp
-constexpr int kMaxBits = 10;                      // digit width limit: 28-bit keys sort in 3 passes
+constexpr int kMaxBits = 8;                       // digit width limit (256 buckets)
 constexpr int kMaxDigits = 1 << kMaxBits;
-constexpr int kDigitsPerThread = kMaxDigits / kRsThreads;  // 4
+constexpr int kMaxPasses = 4;                     // 32-bit keys
+constexpr uint64_t kFlagAggregate = 1ull << 32;   // look-back word: tile's own digit count
+constexpr uint64_t kFlagInclusive = 2ull << 32;   // look-back word: count of this and all earlier tiles
 
 struct TableBases {
   int64_t row_base[CTR_MAX_TABLES + 1];
   int32_t num_tables;
 };
 
+struct PassPlan {
+  int passes;
+  int shift[kMaxPasses];
+  int bits[kMaxPasses];
+};
+
+// Keys, bags, and the digit histograms of every radix pass (one read of the IDs).
 __global__ void __launch_bounds__(256) keygen_kernel(const int64_t* __restrict__ ids,
                                                      const int64_t* __restrict__ offsets, int32_t F, int32_t B,
                                                      int64_t n_ids, const __grid_constant__ FieldMap fm,
                                                      uint32_t* __restrict__ keys, int32_t* __restrict__ bag_of,
-                                                     int* err) {
+                                                     const PassPlan plan, uint32_t* __restrict__ g_hist, int* err) {
+  __shared__ uint32_t sh[kMaxPasses][kMaxDigits];
+  for (int i = threadIdx.x; i < kMaxPasses * kMaxDigits; i += blockDim.x) (&sh[0][0])[i] = 0;
+  __syncthreads();
   const int lane = threadIdx.x & 31;
   const int64_t nbags = (int64_t)F * B;
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -65,64 +77,73 @@ __global__ void __launch_bounds__(256) keygen_kernel(const int64_t* __restrict__
         set_error(err, CTR_ERR_INDEX_OUT_OF_RANGE);
         id = rows - 1;
       }
-      keys[i] = (uint32_t)(base + id);
+      const uint32_t k = (uint32_t)(base + id);
+      keys[i] = k;
       bag_of[i] = (int32_t)bag;
+      for (int p = 0; p < plan.passes; ++p)
+        atomicAdd(&sh[p][(k >> plan.shift[p]) & ((1u << plan.bits[p]) - 1)], 1u);
     }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < plan.passes * kMaxDigits; i += blockDim.x) {
+    const uint32_t c = (&sh[0][0])[i];
+    if (c) atomicAdd(&g_hist[i], c);
   }
 }
 
 __device__ __forceinline__ uint32_t digit_of(uint32_t k, int shift, uint32_t mask) { return (k >> shift) & mask; }
 
-// Per-tile digit histogram, written digit-major: hist[digit * num_tiles + tile].
-__global__ void __launch_bounds__(kRsThreads) radix_upsweep_kernel(const uint32_t* __restrict__ keys, int64_t n,
-                                                                   int shift, int nbits,
-                                                                   uint32_t* __restrict__ hist, int64_t num_tiles) {
-  extern __shared__ uint32_t up_smem[];
-  uint32_t(*cnt)[kMaxDigits] = reinterpret_cast<uint32_t(*)[kMaxDigits]>(up_smem);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int ndig = 1 << nbits;
-  const uint32_t mask = (uint32_t)ndig - 1;
-  for (int i = threadIdx.x; i < kRsWarps * ndig; i += kRsThreads) cnt[i / ndig][i % ndig] = 0;
-  __syncthreads();
-  const int64_t base = (int64_t)blockIdx.x * kRsTile + (int64_t)warp * kRsWarpKeys;
-#pragma unroll 4
-  for (int r = 0; r < kRsItems; ++r) {
-    int64_t idx = base + r * 32 + lane;
-    bool valid = idx < n;
-    uint32_t dg = valid ? digit_of(keys[idx], shift, mask) : 0xffffffffu;
-    unsigned peers = __match_any_sync(kFull, dg);
-    if (valid && lane == __ffs(peers) - 1) cnt[warp][dg] += __popc(peers);
-    __syncwarp();
-  }
-  __syncthreads();
-  for (int dg = threadIdx.x; dg < ndig; dg += kRsThreads) {
-    uint32_t t = 0;
-#pragma unroll
-    for (int w = 0; w < kRsWarps; ++w) t += cnt[w][dg];
-    hist[(int64_t)dg * num_tiles + blockIdx.x] = t;
-  }
+// Look-back words carry their flag and count in one 64-bit access, so relaxed
+// gpu-scope loads and stores suffice (nothing else is published through them).
+static __device__ __forceinline__ void st_relaxed(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+static __device__ __forceinline__ uint64_t ld_relaxed(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+constexpr int kLbWindow = 4;  // predecessors read per look-back round trip
+static __device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+constexpr uint64_t kLookbackLimitNs = 1000000000ull;  // 1 s
 
-// Stable scatter of one tile by the current digit.  vals_in == nullptr means
-// the values are the positions 0..n-1 (first pass).
-__global__ void __launch_bounds__(kRsThreads) radix_downsweep_kernel(
+// One radix pass in one kernel (single-pass, after Adinets and Merrill's
+// Onesweep): a block takes the next tile in launch order, ranks its keys
+// stably (per 32 keys __match_any_sync groups equal digits; per-warp digit
+// counters order the warps), publishes its per-digit counts, and finds the
+// counts of all earlier tiles by decoupled look-back: a predecessor's word
+// holds either its own count or its inclusive prefix, so the walk stops at
+// the first inclusive prefix; each thread reads kLbWindow predecessors per
+// round trip.  Lanes holding equal digits are found with one ballot per digit
+// bit (votes, not the match unit).  Tiles are taken in order, so a block only
+// ever waits on blocks that started before it; each wait is bounded by a
+// wall-clock limit, after which the block records CTR_ERR_TIMEOUT and keeps
+// its writes inside the output.  vals_in == nullptr means the values are
+// the positions 0..n-1 (first pass).
+__global__ void __launch_bounds__(kRsThreads) onesweep_kernel(
     const uint32_t* __restrict__ keys_in, const int32_t* __restrict__ vals_in, uint32_t* __restrict__ keys_out,
-    int32_t* __restrict__ vals_out, int64_t n, int shift, int nbits, const uint32_t* __restrict__ hist_scan,
-    int64_t num_tiles) {
-  extern __shared__ uint32_t ds_smem[];
-  uint32_t(*wcnt)[kMaxDigits] = reinterpret_cast<uint32_t(*)[kMaxDigits]>(ds_smem);  // [warps][digits]
-  uint32_t* tile_start = ds_smem + kRsWarps * kMaxDigits;
-  uint32_t* glob_start = tile_start + kMaxDigits;
-  uint32_t* skeys = glob_start + kMaxDigits;
-  int32_t* svals = (int32_t*)(skeys + kRsTile);
+    int32_t* __restrict__ vals_out, int64_t n, int shift, int nbits, const uint32_t* __restrict__ g_hist,
+    uint64_t* __restrict__ lookback, uint32_t* __restrict__ tile_counter, int* err) {
+  __shared__ uint32_t wcnt[kRsWarps][kMaxDigits];
+  __shared__ uint32_t tile_start[kMaxDigits];
+  __shared__ uint32_t glob_start[kMaxDigits];
+  __shared__ uint32_t skeys[kRsTile];
+  __shared__ int32_t svals[kRsTile];
   __shared__ uint32_t warp_tot[kRsWarps];
+  __shared__ uint32_t tile_sh;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ndig = 1 << nbits;
   const uint32_t mask = (uint32_t)ndig - 1;
-  for (int i = threadIdx.x; i < kRsWarps * ndig; i += kRsThreads) wcnt[i / ndig][i % ndig] = 0;
+  for (int i = threadIdx.x; i < kRsWarps * kMaxDigits; i += kRsThreads) (&wcnt[0][0])[i] = 0;
+  if (threadIdx.x == 0) tile_sh = atomicAdd(tile_counter, 1u);
   __syncthreads();
+  const int64_t tile = tile_sh;
 
-  const int64_t tile_base = (int64_t)blockIdx.x * kRsTile;
+  const int64_t tile_base = tile * kRsTile;
   const int64_t base = tile_base + (int64_t)warp * kRsWarpKeys;
   const unsigned lt = lanemask_lt();
   uint32_t key[kRsItems];
@@ -130,50 +151,95 @@ __global__ void __launch_bounds__(kRsThreads) radix_downsweep_kernel(
   uint32_t rank[kRsItems];
 #pragma unroll
   for (int r = 0; r < kRsItems; ++r) {
-    int64_t idx = base + r * 32 + lane;
-    bool valid = idx < n;
+    const int64_t idx = base + r * 32 + lane;
+    const bool valid = idx < n;
     key[r] = valid ? keys_in[idx] : 0u;
     val[r] = valid ? (vals_in ? vals_in[idx] : (int32_t)idx) : 0;
-    uint32_t dg = valid ? digit_of(key[r], shift, mask) : 0xffffffffu;
-    unsigned peers = __match_any_sync(kFull, dg);
-    uint32_t prior = valid ? wcnt[warp][dg] : 0u;
+    const uint32_t dg = valid ? digit_of(key[r], shift, mask) : 0u;
+    unsigned peers = __ballot_sync(kFull, valid);
+#pragma unroll
+    for (int b = 0; b < kMaxBits; ++b) {
+      if (b < nbits) {
+        const unsigned m = __ballot_sync(kFull, (dg >> b) & 1u);
+        peers &= ((dg >> b) & 1u) ? m : ~m;
+      }
+    }
+    const uint32_t prior = valid ? wcnt[warp][dg] : 0u;
     __syncwarp();
     if (valid && lane == __ffs(peers) - 1) wcnt[warp][dg] = prior + __popc(peers);
     __syncwarp();
     rank[r] = valid ? prior + __popc(peers & lt) : 0xffffffffu;
   }
   __syncthreads();
-  // per digit: exclusive over warps (in place), then exclusive over digits;
-  // thread t owns digits kDigitsPerThread*t .. +kDigitsPerThread-1
-  uint32_t dtot[kDigitsPerThread];
+  // thread t owns digit t: exclusive over warps (in place), tile count, bucket start
+  const int dg = threadIdx.x;  // kRsThreads == kMaxDigits
+  uint32_t cnt = 0;
+  if (dg < ndig) {
 #pragma unroll
-  for (int q = 0; q < kDigitsPerThread; ++q) {
-    const int dg = threadIdx.x * kDigitsPerThread + q;
-    uint32_t run = 0;
-    if (dg < ndig) {
-#pragma unroll
-      for (int w = 0; w < kRsWarps; ++w) {
-        const uint32_t c = wcnt[w][dg];
-        wcnt[w][dg] = run;
-        run += c;
-      }
-      glob_start[dg] = hist_scan[(int64_t)dg * num_tiles + blockIdx.x];
+    for (int w = 0; w < kRsWarps; ++w) {
+      const uint32_t c = wcnt[w][dg];
+      wcnt[w][dg] = cnt;
+      cnt += c;
     }
-    dtot[q] = run;
   }
-  __syncthreads();
-  block_exclusive_scan<uint32_t, kRsThreads, kDigitsPerThread>(dtot, warp_tot);
+  uint64_t* my_word = lookback + tile * kMaxDigits + dg;
+  if (dg < ndig) st_relaxed(my_word, (tile == 0 ? kFlagInclusive : kFlagAggregate) | cnt);
+  uint32_t gh[1] = {dg < ndig ? g_hist[dg] : 0u};
+  uint32_t tc[1] = {cnt};
+  block_exclusive_scan<uint32_t, kRsThreads, 1>(gh, warp_tot);  // bucket start of digit dg
+  block_exclusive_scan<uint32_t, kRsThreads, 1>(tc, warp_tot);  // digit dg's start inside the tile
+  bool timed_out = false;
+  uint32_t excl = 0;
+  if (dg < ndig && tile > 0) {
+    // walk back kLbWindow predecessors per round trip; stop at the first
+    // inclusive prefix, wait (bounded) where a predecessor has not published
+    int64_t j = tile - 1;
+    uint64_t t0 = 0;
+    while (j >= 0) {
+      uint64_t w[kLbWindow];
 #pragma unroll
-  for (int q = 0; q < kDigitsPerThread; ++q) {
-    const int dg = threadIdx.x * kDigitsPerThread + q;
-    if (dg < ndig) tile_start[dg] = dtot[q];
+      for (int q = 0; q < kLbWindow; ++q) w[q] = (j - q >= 0) ? ld_relaxed(lookback + (j - q) * kMaxDigits + dg)
+                                                             : kFlagInclusive;
+      int used = 0;
+      bool done = false, stalled = false;
+#pragma unroll
+      for (int q = 0; q < kLbWindow; ++q) {
+        if (done || stalled) continue;
+        const uint64_t flag = w[q] & ~0xffffffffull;
+        if (flag == 0) {
+          stalled = true;
+        } else {
+          excl += (uint32_t)w[q];
+          ++used;
+          if (flag == kFlagInclusive) done = true;
+        }
+      }
+      if (done) break;
+      j -= used;
+      if (stalled) {
+        const uint64_t t = now_ns();
+        if (t0 == 0) t0 = t;
+        else if (t - t0 > kLookbackLimitNs) {
+          timed_out = true;
+          break;
+        }
+      } else {
+        t0 = 0;
+      }
+    }
+    st_relaxed(my_word, kFlagInclusive | (excl + cnt));
+  }
+  if (timed_out) set_error(err, CTR_ERR_TIMEOUT);
+  if (dg < ndig) {
+    tile_start[dg] = tc[0];
+    glob_start[dg] = gh[0] + excl;
   }
   __syncthreads();
 #pragma unroll
   for (int r = 0; r < kRsItems; ++r) {
     if (rank[r] != 0xffffffffu) {
-      uint32_t dg = digit_of(key[r], shift, mask);
-      uint32_t local = tile_start[dg] + wcnt[warp][dg] + rank[r];
+      const uint32_t d = digit_of(key[r], shift, mask);
+      const uint32_t local = tile_start[d] + wcnt[warp][d] + rank[r];
       skeys[local] = key[r];
       svals[local] = val[r];
     }
@@ -181,12 +247,19 @@ __global__ void __launch_bounds__(kRsThreads) radix_downsweep_kernel(
   __syncthreads();
   const int count = (int)imin64(kRsTile, n - tile_base);
   for (int i = threadIdx.x; i < count; i += kRsThreads) {
-    uint32_t k = skeys[i];
-    uint32_t dg = digit_of(k, shift, mask);
-    int64_t dest = (int64_t)glob_start[dg] + (i - (int64_t)tile_start[dg]);
-    keys_out[dest] = k;
-    vals_out[dest] = svals[i];
+    const uint32_t k = skeys[i];
+    const uint32_t d = digit_of(k, shift, mask);
+    const int64_t dest = (int64_t)glob_start[d] + (i - (int64_t)tile_start[d]);
+    if (dest >= 0 && dest < n) {  // always true unless a look-back timed out
+      keys_out[dest] = k;
+      vals_out[dest] = svals[i];
+    }
   }
+}
+
+__global__ void clear_u64_kernel(uint64_t* __restrict__ p, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = 0;
 }
 
 // Heads per tile of the sorted keys.
@@ -318,6 +391,12 @@ int key_bits(int64_t total_rows) {
   return b;
 }
 
+// Sort state: per pass, one look-back word per (tile, digit); then the
+// per-pass digit histograms and tile counters (uint32, packed two per word).
+int64_t state_words(int64_t tiles) {
+  return (int64_t)kMaxPasses * tiles * kMaxDigits + (kMaxPasses * kMaxDigits) / 2 + kMaxPasses;
+}
+
 template <typename WS>
 void dedup_layout(WS& ws, int64_t n_ids, int64_t total_rows) {
   const int64_t tiles = ceil_div(n_ids, kRsTile);
@@ -329,9 +408,10 @@ void dedup_layout(WS& ws, int64_t n_ids, int64_t total_rows) {
   ws.template take<int32_t>((size_t)n_ids);            // values scratch
   ws.template take<int32_t>((size_t)n_ids);            // sorted positions if the caller gives none
   ws.template take<int32_t>((size_t)n_ids);            // bag of each position
-  ws.template take<uint32_t>((size_t)tiles << nb);     // digit histograms
+  ws.template take<uint64_t>((size_t)state_words(tiles));  // look-back words, histograms, tile counters
   ws.template take<uint32_t>((size_t)tiles);           // heads per tile
-  scan_reserve<uint32_t>(ws, tiles << nb);
+  scan_reserve<uint32_t>(ws, tiles);
+  (void)nb;
 }
 
 }  // namespace
@@ -391,40 +471,42 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
   int32_t* vscratch = c.take<int32_t>(n_ids);
   int32_t* vfinal_ws = c.take<int32_t>(n_ids);
   int32_t* bag_of = c.take<int32_t>(n_ids);
-  uint32_t* hist = c.take<uint32_t>((size_t)tiles << nb);
+  uint64_t* state = c.take<uint64_t>((size_t)state_words(tiles));
   uint32_t* tile_heads = c.take<uint32_t>(tiles);
   if (!c.ok()) return CTR_ERR_WORKSPACE;
   int32_t* vfinal = sorted_pos ? sorted_pos : vfinal_ws;
+  uint64_t* lookback = state;
+  uint32_t* g_hist = (uint32_t*)(state + (int64_t)kMaxPasses * tiles * kMaxDigits);
+  uint32_t* tile_counter = g_hist + kMaxPasses * kMaxDigits;
 
+  PassPlan plan;
+  plan.passes = passes;
+  for (int p = 0, sh = 0; p < kMaxPasses; ++p) {
+    const int pb = p < passes ? std::min(nb, bits - sh) : 0;
+    plan.shift[p] = sh;
+    plan.bits[p] = pb;
+    sh += pb;
+  }
+  const int sms = num_sms();
+  clear_u64_kernel<<<(unsigned)std::max<int64_t>(1, imin64(ceil_div(state_words(tiles), 256), (int64_t)sms * 8)),
+                     256, 0, s>>>(state, state_words(tiles));
+  if (int st = launch_status()) return st;
   const int64_t nbags = (int64_t)num_fields * batch;
   {
-    int64_t blocks = imin64(ceil_div(nbags, 8), (int64_t)num_sms() * 16);
+    int64_t blocks = imin64(ceil_div(nbags, 8), (int64_t)sms * 16);
     keygen_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, s>>>(ids, offsets, num_fields, batch, n_ids, fm,
-                                                                        keys[0], bag_of, err);
+                                                                        keys[0], bag_of, plan, g_hist, err);
     if (int st = launch_status()) return st;
   }
-  const size_t up_smem = (size_t)kRsWarps * kMaxDigits * sizeof(uint32_t);
-  const size_t ds_smem = ((size_t)kRsWarps * kMaxDigits + 2 * kMaxDigits + 2 * kRsTile) * sizeof(uint32_t);
-  if (cudaFuncSetAttribute(radix_upsweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)up_smem) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(radix_downsweep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ds_smem) !=
-          cudaSuccess)
-    return CTR_ERR_CUDA;
   const int32_t* vin = nullptr;
-  int shift = 0;
   for (int p = 0; p < passes; ++p) {
-    const int pb = std::min(nb, bits - shift);
-    const int64_t nh = tiles << pb;
-    radix_upsweep_kernel<<<(unsigned)tiles, kRsThreads, up_smem, s>>>(keys[p & 1], n_ids, shift, pb, hist, tiles);
-    if (int st = launch_status()) return st;
-    WsCarver scan_ws = c;  // scan scratch is reused every pass
-    if (int st = scan_exclusive<uint32_t>(hist, hist, nh, nullptr, nullptr, scan_ws, s)) return st;
     int32_t* vout = ((passes - 1 - p) % 2 == 0) ? vfinal : vscratch;
-    radix_downsweep_kernel<<<(unsigned)tiles, kRsThreads, ds_smem, s>>>(keys[p & 1], vin, keys[(p + 1) & 1], vout, n_ids,
-                                                                   shift, pb, hist, tiles);
+    onesweep_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(keys[p & 1], vin, keys[(p + 1) & 1], vout, n_ids,
+                                                           plan.shift[p], plan.bits[p], g_hist + p * kMaxDigits,
+                                                           lookback + (int64_t)p * tiles * kMaxDigits,
+                                                           tile_counter + p, err);
     if (int st = launch_status()) return st;
     vin = vout;
-    shift += pb;
   }
   const uint32_t* skeys = keys[passes & 1];
   unique_count_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(skeys, n_ids, tile_heads);
