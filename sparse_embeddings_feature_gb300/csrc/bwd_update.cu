@@ -334,6 +334,9 @@ constexpr int kWin = 8;
 #ifndef CTR_TILE_MINB
 #define CTR_TILE_MINB 2
 #endif
+#ifndef CTR_TILE_ASYNC_MINB
+#define CTR_TILE_ASYNC_MINB 3
+#endif
 #ifndef CTR_BWD_MINB
 #define CTR_BWD_MINB 3  // resident blocks per SM the register budget is sized for
 #endif
@@ -570,6 +573,132 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_MINB) bwd_tiles_stream_
   }
 }
 
+// Tile kernel with the table rows staged by cp.async: when a tile starts, each
+// lane issues asynchronous copies of its column of the tile's (at most TU)
+// rows into the warp's shared memory, so the rows' DRAM reads overlap the
+// pooled-gradient stream and hold no registers.  A run is updated at its last
+// occurrence, straight from shared memory, and written back at once; there is
+// no second phase and no accumulator staging.
+__device__ __forceinline__ void cp_async_chunk(uint32_t dst, const void* src, int bytes) {
+  if (bytes == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kTileThreads, CTR_TILE_ASYNC_MINB) bwd_tiles_async_kernel(const BwdArgs a) {
+  extern __shared__ __align__(16) unsigned char wsm_raw[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool col = lane * 4 < a.d;
+  const int TU = a.TU;
+  const int esz = a.bf16 ? 2 : 4;
+  const int row_bytes = a.d * esz;
+  const int chunk = 4 * esz;  // this lane's 4 elements
+  unsigned char* wsm = wsm_raw + (size_t)warp * TU * row_bytes;
+  const uint32_t wsm_s = (uint32_t)__cvta_generic_to_shared(wsm);
+  const float* Gl = a.G + lane * 4;
+  const int64_t nu = n_uniques(a);
+  const int64_t ntiles = ceil_div(nu, TU);
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t tile = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; tile < ntiles; tile += nwarps) {
+    const int64_t u = tile * TU + lane;
+    const bool valid = lane < TU && u < nu;
+    int64_t r0 = 0, r1 = 0;
+    if (valid) run_bounds(a, u, r0, r1);
+    const int64_t len = r1 - r0;
+    const bool is_long = valid && len > kShort;
+    const bool is_short = valid && !is_long && len > 0;
+    int64_t row = -1;
+    if (is_short) {
+      row = a.unique_rows[u];
+      if (row < 0 || row >= a.total_rows) {
+        set_error(a.err, CTR_ERR_INDEX_OUT_OF_RANGE);
+        row = -1;
+      }
+    }
+    if (is_long) {
+      const int64_t slot = (int64_t)atomicAdd((unsigned long long*)a.long_count, 1ull);
+      if (slot < a.max_long) {
+        a.long_list[slot] = (int32_t)u;
+        a.long_pstart[slot] = (uint32_t)ceil_div(len, kPiece);
+      }
+    }
+    // stage this tile's table rows (each lane its own column)
+    for (int j = 0; j < TU; ++j) {
+      const int64_t rj = __shfl_sync(kFull, row, j);
+      if (rj >= 0 && col)
+        cp_async_chunk(wsm_s + j * row_bytes + lane * chunk, (const char*)a.table + rj * row_bytes + lane * chunk,
+                       chunk);
+    }
+    cp_async_commit();
+    const int slen = is_short ? (int)len : 0;
+    int inc = slen;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const int e = inc - slen;
+    const int E = __shfl_sync(kFull, inc, 31);
+    const int r0i = (int)r0;
+
+    TileChunk cur = tile_chunk(a, lane, E, e, r0i, slen);
+    TileChunk pend = tile_chunk(a, 32 + lane, E, e, r0i, slen);
+    float sc_cur;
+    uint32_t gcur = bag_g4(a, cur.bag, sc_cur);
+    float4 buf[kWin];
+#pragma unroll
+    for (int q = 0; q < kWin; ++q) {
+      const uint32_t r = __shfl_sync(kFull, gcur, q);
+      buf[q] = (r != kNoG && col) ? ldg_f4(Gl + (uint64_t)r * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool staged = false;
+    for (int c0 = 0; c0 < E; c0 += 32) {
+      const TileChunk ahead = tile_chunk(a, c0 + 64 + lane, E, e, r0i, slen);
+      float sc_nxt;
+      const uint32_t gnxt = bag_g4(a, pend.bag, sc_nxt);
+      for (int g = 0; g < 32; g += kWin) {
+#pragma unroll
+        for (int j = 0; j < kWin; ++j) {
+          const int t = g + j;
+          const float4 x = buf[j];
+          const int tn = t + kWin;
+          const uint32_t r = __shfl_sync(kFull, tn < 32 ? gcur : gnxt, tn & 31);
+          buf[j] = (r != kNoG && col) ? ldg_f4(Gl + (uint64_t)r * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (a.mean) acc = fma4(x, __shfl_sync(kFull, sc_cur, t), acc);
+          else acc = make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
+          if ((cur.lastm >> t) & 1u) {
+            const int sg = __shfl_sync(kFull, cur.seg, t);
+            const int64_t rs = __shfl_sync(kFull, row, sg);
+            if (rs >= 0 && col) {
+              if (!staged) {
+                cp_async_wait_all();  // this lane's own copies only: no warp barrier needed
+                staged = true;
+              }
+              const unsigned char* wp = wsm + sg * row_bytes + lane * chunk;
+              float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+              uint2 wb = make_uint2(0u, 0u);
+              if (!a.bf16) w = *(const float4*)wp;
+              else wb = *(const uint2*)wp;
+              store_row_chunk(a, rs, tile * TU + sg, lane, acc, w, wb);
+            }
+            acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+      }
+      cur = pend;
+      pend = ahead;
+      gcur = gnxt;
+      sc_cur = sc_nxt;
+    }
+    cp_async_wait_all();  // nothing may land in the buffer after the next tile reuses it
+    __syncwarp();
+  }
+}
+
 // One CTA per long run: warps sum fixed contiguous segments of its partials,
 // then a fixed pairwise tree over the warps, then the row update.
 __global__ void __launch_bounds__(kCombThreads) combine_long_kernel(const BwdArgs a) {
@@ -662,8 +791,10 @@ int grid_of(K kernel, int threads, size_t smem, int64_t want) {
 template <int CPL>
 int launch_bwd(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
   const int chunks = a.d / 4;
-  const size_t tile_smem = (size_t)kTileWarps * a.TU * chunks * sizeof(float4);
-  auto tk = (CPL == 1 && a.g4_ok) ? bwd_tiles_stream_kernel : bwd_tiles_kernel<CPL>;
+  const size_t acc_smem = (size_t)kTileWarps * a.TU * chunks * sizeof(float4);
+  const bool use_async = CPL == 1 && a.g4_ok;
+  auto tk = use_async ? bwd_tiles_async_kernel : bwd_tiles_kernel<CPL>;
+  const size_t tile_smem = use_async ? (size_t)kTileWarps * a.TU * a.d * (a.bf16 ? 2 : 4) : acc_smem;
   if (tile_smem > 48 * 1024 &&
       cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tile_smem) != cudaSuccess)
     return CTR_ERR_CUDA;
