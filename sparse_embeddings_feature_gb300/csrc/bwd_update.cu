@@ -68,6 +68,7 @@ struct BwdArgs {
   int g4_ok;           // every pooled-gradient offset / 4 fits 32 bits
   // scratch
   int64_t* long_count;
+  unsigned long long* work;  // [2] work counters: tiles, pieces
   int64_t max_long;
   int32_t* long_list;    // [max_long] unique of each long run
   uint32_t* long_pstart; // [max_long] pieces of each long run, then (scanned) its first piece
@@ -122,12 +123,14 @@ __device__ __forceinline__ void occ_info(const BwdArgs& a, int64_t s, int64_t& g
 
 // Row update of unique u with gradient chunk g at column 4*ch (w already loaded).
 __device__ __forceinline__ void store_row_chunk(const BwdArgs& a, int64_t row, int64_t u, int ch, float4 g,
-                                                float4 w, uint2 wb) {
+                                                float4 w, uint2 wb, uint64_t pol = 0) {
   if (a.grad_out) *(float4*)(a.grad_out + u * a.d + ch * 4) = g;
   if (!a.bf16) {
     float4 x = make_float4(fmaf(-a.lr, g.x, w.x), fmaf(-a.lr, g.y, w.y), fmaf(-a.lr, g.z, w.z),
                            fmaf(-a.lr, g.w, w.w));
-    *(float4*)((float*)a.table + row * a.d + ch * 4) = x;
+    float* dst = (float*)a.table + row * a.d + ch * 4;
+    if (pol) stg_f4_policy(dst, x, pol);
+    else *(float4*)dst = x;
   } else {
     const float w0 = __uint_as_float(wb.x << 16), w1 = __uint_as_float(wb.x & 0xffff0000u);
     const float w2 = __uint_as_float(wb.y << 16), w3 = __uint_as_float(wb.y & 0xffff0000u);
@@ -313,7 +316,11 @@ __global__ void __launch_bounds__(kTileThreads, 2) bwd_tiles_kernel(const BwdArg
   }
 }
 
-__global__ void clear_i64(int64_t* p) { *p = 0; }
+__global__ void clear_i64(int64_t* p, unsigned long long* w) {
+  *p = 0;
+  w[0] = 0;
+  w[1] = 0;
+}
 
 __global__ void expand_long_kernel(const BwdArgs a) {
   const int64_t nl = imin64(*a.long_count, a.max_long);
@@ -391,9 +398,11 @@ __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(c
   const int lane = threadIdx.x & 31;
   const bool col = lane * 4 < a.d;  // this lane's 16-byte column exists
   const float* Gl = a.G + lane * 4;
+  const uint64_t pol_keep = l2_evict_last();
   const int64_t np = *a.pieces_total;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t p = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < np; p += nwarps) {
+  (void)nwarps;
+  for (int64_t p = next_unit(a.work + 1); p < np; p = next_unit(a.work + 1)) {
     const int64_t i = a.piece_owner[p];
     int64_t r0, r1;
     run_bounds(a, a.long_list[i], r0, r1);
@@ -407,7 +416,7 @@ __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(c
 #pragma unroll
     for (int u = 0; u < kWin; ++u) {
       const uint32_t r = __shfl_sync(kFull, cur, u);
-      buf[u] = (r != kNoG && col) ? ldg_f4(Gl + (uint64_t)r * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      buf[u] = (r != kNoG && col) ? ldg_f4_policy(Gl + (uint64_t)r * 4, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c0 = 0; c0 < n; c0 += 32) {
@@ -421,7 +430,7 @@ __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(c
           const float4 x = buf[j];
           const int tn = t + kWin;
           const uint32_t r = __shfl_sync(kFull, tn < 32 ? cur : nxt, tn & 31);
-          buf[j] = (r != kNoG && col) ? ldg_f4(Gl + (uint64_t)r * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          buf[j] = (r != kNoG && col) ? ldg_f4_policy(Gl + (uint64_t)r * 4, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
           if (a.mean) acc = fma4(x, __shfl_sync(kFull, sc_cur, t), acc);
           else acc = make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
         }
@@ -579,11 +588,13 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_MINB) bwd_tiles_stream_
 // pooled-gradient stream and hold no registers.  A run is updated at its last
 // occurrence, straight from shared memory, and written back at once; there is
 // no second phase and no accumulator staging.
-__device__ __forceinline__ void cp_async_chunk(uint32_t dst, const void* src, int bytes) {
+__device__ __forceinline__ void cp_async_chunk(uint32_t dst, const void* src, int bytes, uint64_t pol) {
   if (bytes == 16)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
+                 : "memory");
   else
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+    asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "l"(pol)
+                 : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
@@ -599,10 +610,14 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_ASYNC_MINB) bwd_tiles_a
   unsigned char* wsm = wsm_raw + (size_t)warp * TU * row_bytes;
   const uint32_t wsm_s = (uint32_t)__cvta_generic_to_shared(wsm);
   const float* Gl = a.G + lane * 4;
+  // pooled-gradient rows are re-read by every unique of their bags: keep them
+  // in L2; the table rows are touched once: stream them
+  const uint64_t pol_keep = l2_evict_last(), pol_stream = l2_evict_first();
   const int64_t nu = n_uniques(a);
   const int64_t ntiles = ceil_div(nu, TU);
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t tile = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; tile < ntiles; tile += nwarps) {
+  (void)nwarps;
+  for (int64_t tile = next_unit(a.work); tile < ntiles; tile = next_unit(a.work)) {
     const int64_t u = tile * TU + lane;
     const bool valid = lane < TU && u < nu;
     int64_t r0 = 0, r1 = 0;
@@ -630,7 +645,7 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_ASYNC_MINB) bwd_tiles_a
       const int64_t rj = __shfl_sync(kFull, row, j);
       if (rj >= 0 && col)
         cp_async_chunk(wsm_s + j * row_bytes + lane * chunk, (const char*)a.table + rj * row_bytes + lane * chunk,
-                       chunk);
+                       chunk, pol_stream);
     }
     cp_async_commit();
     const int slen = is_short ? (int)len : 0;
@@ -652,7 +667,7 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_ASYNC_MINB) bwd_tiles_a
 #pragma unroll
     for (int q = 0; q < kWin; ++q) {
       const uint32_t r = __shfl_sync(kFull, gcur, q);
-      buf[q] = (r != kNoG && col) ? ldg_f4(Gl + (uint64_t)r * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      buf[q] = (r != kNoG && col) ? ldg_f4_policy(Gl + (uint64_t)r * 4, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     bool staged = false;
@@ -667,7 +682,7 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_ASYNC_MINB) bwd_tiles_a
           const float4 x = buf[j];
           const int tn = t + kWin;
           const uint32_t r = __shfl_sync(kFull, tn < 32 ? gcur : gnxt, tn & 31);
-          buf[j] = (r != kNoG && col) ? ldg_f4(Gl + (uint64_t)r * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          buf[j] = (r != kNoG && col) ? ldg_f4_policy(Gl + (uint64_t)r * 4, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
           if (a.mean) acc = fma4(x, __shfl_sync(kFull, sc_cur, t), acc);
           else acc = make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
           if ((cur.lastm >> t) & 1u) {
@@ -683,7 +698,7 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_ASYNC_MINB) bwd_tiles_a
               uint2 wb = make_uint2(0u, 0u);
               if (!a.bf16) w = *(const float4*)wp;
               else wb = *(const uint2*)wp;
-              store_row_chunk(a, rs, tile * TU + sg, lane, acc, w, wb);
+              store_row_chunk(a, rs, tile * TU + sg, lane, acc, w, wb, pol_stream);
             }
             acc = make_float4(0.f, 0.f, 0.f, 0.f);
           }
@@ -773,6 +788,7 @@ template <typename WS>
 void bwd_layout(WS& ws, int64_t n, int32_t d) {
   const Sizes z = sizes(n);
   ws.template take<int64_t>(1);                            // long_count
+  ws.template take<unsigned long long>(2);                 // work counters
   ws.template take<uint32_t>(1);                           // pieces_total
   ws.template take<int32_t>((size_t)z.max_long);           // long_list
   ws.template take<uint32_t>((size_t)z.max_long);          // long_pstart
@@ -798,7 +814,7 @@ int launch_bwd(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
   if (tile_smem > 48 * 1024 &&
       cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tile_smem) != cudaSuccess)
     return CTR_ERR_CUDA;
-  clear_i64<<<1, 1, 0, s>>>(a.long_count);
+  clear_i64<<<1, 1, 0, s>>>(a.long_count, a.work);
   if (int st = launch_status()) return st;
   tk<<<grid_of(tk, kTileThreads, tile_smem, ceil_div(n, (int64_t)a.TU * kTileWarps)), kTileThreads, tile_smem, s>>>(a);
   if (int st = launch_status()) return st;
@@ -884,6 +900,7 @@ extern "C" int ctr_embedding_bag_bwd_update(const float* grad_pooled, int64_t g_
     a.g4_ok = (max_off >> 2) < (int64_t)0xffffffffll && n_ids < ((int64_t)1 << 31);
   }
   a.long_count = c.take<int64_t>(1);
+  a.work = c.take<unsigned long long>(2);
   a.pieces_total = c.take<uint32_t>(1);
   a.max_long = z.max_long;
   a.long_list = c.take<int32_t>(z.max_long);

@@ -12,6 +12,17 @@ namespace ctr {
 constexpr int kWarp = 32;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr size_t kWsHeader = 256;  // sticky error word lives at the head of every workspace
+constexpr size_t kWsCounterOffset = 64;  // a work counter some kernels keep in the header
+
+// Next work unit for the calling warp, handed out in launch order from a
+// global counter, so the warps in flight stay on a narrow window of
+// consecutive units (their data shares L2) instead of drifting apart as a
+// grid-stride loop does.
+__device__ __forceinline__ int64_t next_unit(unsigned long long* counter) {
+  unsigned long long u = 0;
+  if ((threadIdx.x & 31) == 0) u = atomicAdd(counter, 1ull);
+  return (int64_t)__shfl_sync(0xffffffffu, u, 0);
+}
 
 // Device-side error codes recorded in the workspace header (first one wins).
 __device__ __forceinline__ void set_error(int* err, int code) {
@@ -91,5 +102,30 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 }
 
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
+
+// L2 cache policies for data with known reuse: keep (evict_last) rows that are
+// read many times within a kernel, let streamed data go first (evict_first).
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ float4 ldg_f4_policy(const float* p, uint64_t pol) {
+  float4 r;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "l"(p), "l"(pol));
+  return r;
+}
+__device__ __forceinline__ void stg_f4_policy(float* p, float4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w), "l"(pol)
+               : "memory");
+}
 
 }  // namespace ctr

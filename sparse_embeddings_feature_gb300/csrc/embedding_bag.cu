@@ -254,7 +254,10 @@ __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kerne
   const IT* idx = (const IT*)a.idx;
   const float* table = (const float*)a.table + lane * 4;
   const int64_t end_all = a.offsets[nbags];
-  for (int64_t blk = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; blk < nblk; blk += nwarps) {
+  const uint64_t pol_stream = l2_evict_first();  // pooled outputs are written once
+  unsigned long long* counter = (unsigned long long*)((char*)a.err + kWsCounterOffset);
+  (void)nwarps;
+  for (int64_t blk = next_unit(counter); blk < nblk; blk = next_unit(counter)) {
     const int64_t bag = blk * 32 + lane;
     const bool bvalid = bag < nbags;
     int64_t o0 = bvalid ? a.offsets[bag] : end_all;
@@ -319,7 +322,8 @@ __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kerne
               v[2] /= lj;
               v[3] /= lj;
             }
-            store_out(a.out, oj, v, 4, a.out_bf16, a.vec_out);
+            if (!a.out_bf16 && a.vec_out) stg_f4_policy((float*)a.out + oj, make_float4(v[0], v[1], v[2], v[3]), pol_stream);
+            else store_out(a.out, oj, v, 4, a.out_bf16, a.vec_out);
             acc = make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
@@ -570,6 +574,8 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
     return launch_status();
   }
   if (std::is_same<TT, float>::value && a.d == 128 && a.total_rows < 0xffffffffll) {
+    if (cudaMemsetAsync((char*)a.err + kWsCounterOffset, 0, sizeof(unsigned long long), s) != cudaSuccess)
+      return CTR_ERR_CUDA;
     auto k = bag_fwd_flat_kernel<IT>;
     k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm);
     return launch_status();
