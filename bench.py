@@ -181,27 +181,65 @@ def cpu_baseline(cfg, w, sample, reps=1):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-def fwd_compulsory_bytes(cfg, n_ids, n_unique):
+def algorithmic_bytes(cfg, path, n_ids, n_unique):
+    """Compulsory DRAM bytes per launch of each timed kernel (each row, index and output once).
+
+    gather       the distinct table rows, the IDs, the offsets, the pooled outputs
+    sort         four radix passes reading and writing (key, value) pairs
+    interaction  X in, [dense | pairs] out;  interaction_bwd: dout and X in, dX out
+    bwd_tiles    read-modify-write of the rows of runs <= 128 occurrences, their
+                 occurrence list, run bounds and rows, and each pooled-gradient row of
+                 the bags they touch once
+    bwd_pieces   each pooled-gradient row of the bags the long runs touch once, their
+                 occurrence list, one partial row per piece written
+    """
+    import torch
     row = cfg.d * (4 if cfg.dtype == "f32" else 2)
-    nbags = cfg.num_fields * cfg.batch
-    return n_unique * row + n_ids * 8 + (nbags + 1) * 8 + nbags * row
+    F, B, n = cfg.num_fields, cfg.batch, cfg.n_vectors
+    nbags = F * B
+    out = {"gather": n_unique * row + n_ids * 8 + (nbags + 1) * 8 + nbags * row,
+           "sort": 4 * n_ids * 16}
+    if cfg.interaction:
+        width = cfg.out_width
+        out["interaction"] = B * n * row + B * width * (row // cfg.d)
+        if cfg.backward == "full":
+            out["interaction_bwd"] = 2 * B * n * cfg.d * 4 + B * width * 4
+    if cfg.backward != "none" and n_unique > 0:
+        ro = path.run_offsets[:n_unique + 1].long()
+        lens = ro[1:] - ro[:-1]
+        short = lens <= 128
+        occ_short = torch.repeat_interleave(short, lens)
+        sb = path.sorted_bag[:n_ids].long()
+        bags_short = int(torch.unique(sb[occ_short]).numel())
+        bags_long = int(torch.unique(sb[~occ_short]).numel())
+        n_short = int(short.sum().item())
+        long_lens = lens[~short]
+        pieces = int(((long_lens + 127) // 128).sum().item())
+        occ_s = int(occ_short.sum().item())
+        out["bwd_tiles"] = n_short * 2 * row + n_unique * 12 + occ_s * 4 + bags_short * cfg.d * 4
+        out["bwd_pieces"] = bags_long * cfg.d * 4 + (n_ids - occ_s) * 4 + pieces * cfg.d * 4
+    return out
 
 
-def profile_traffic(kernel_src_hash):
-    """dram bytes per launch of the forward gather from the committed ncu summary, if still current."""
-    p = os.path.join(ROOT, "profiles", "fwd_gather_traffic.json")
+def profile_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if its source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "full_step_kernel_traffic.json")
     try:
         with open(p) as f:
             j = json.load(f)
-        if j.get("kernel_source_sha256") == kernel_src_hash:
-            return float(j["dram_bytes_per_launch_full_step"])
+        entry = j["kernels"][kernel]
+        src = os.path.join(ROOT, "sparse_embeddings_feature_gb300", "csrc", entry["source"])
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != entry["source_sha256"]:
+                return None
+        return float(entry["dram_bytes_per_launch"])
     except Exception:
-        pass
-    return None
+        return None
 
 
 def run_ours(args, rank, world):
     import torch
+    from sparse_embeddings_feature_gb300 import ctr
     from sparse_embeddings_feature_gb300 import workload as W
     from sparse_embeddings_feature_gb300.pipeline import CtrPath
 
@@ -234,7 +272,18 @@ def run_ours(args, rank, world):
               and (s != "interaction" or cfg.interaction)
               and (s != "interaction_bwd" or cfg.backward == "full")
               and (s != "bwd_update" or cfg.backward != "none")]
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(active) + 1)] for _ in range(args.steps)]
+    kernels = {"gather": ctr.KERNEL_GATHER, "bwd_tiles": ctr.KERNEL_BWD_TILES, "bwd_pieces": ctr.KERNEL_BWD_PIECES,
+               "sort": ctr.KERNEL_SORT, "interaction": ctr.KERNEL_INTERACTION,
+               "interaction_bwd": ctr.KERNEL_INTERACTION_BWD}
+
+    def new_event():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)  # torch creates the CUDA event on first record
+        return e
+
+    ev = [[new_event() for _ in range(len(active) + 1)] for _ in range(args.steps)]
+    kev = [{k: (new_event(), new_event()) for k in kernels} for _ in range(args.steps)]
+    torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
@@ -244,18 +293,29 @@ def run_ours(args, rank, world):
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for k in range(args.steps):
+            for name, kid in kernels.items():
+                ctr.ctr_set_timing_events(kid, *kev[k][name])
             ev[k][0].record(stream)
-            for i, s in enumerate(active):
-                run_stage[s]()
+            for i, s_ in enumerate(active):
+                run_stage[s_]()
                 ev[k][i + 1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
         time.sleep(0.25)
         mark1 = clk.mark()
+    for kid in kernels.values():
+        ctr.ctr_set_timing_events(kid, None, None)
     barrier()
     total_ms = t_start.elapsed_time(t_end)
-    stage_ms = {s: sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)) / args.steps
-                for i, s in enumerate(active)}
+    stage_ms = {s_: sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)) / args.steps
+                for i, s_ in enumerate(active)}
+    kernel_ms = {}
+    for name in kernels:
+        try:
+            kernel_ms[name] = sum(kev[k][name][0].elapsed_time(kev[k][name][1]) for k in range(args.steps)) / args.steps
+        except RuntimeError:
+            pass
+    kernel_ms = {k: v for k, v in kernel_ms.items() if v > 1e-3}
     status = path.check_status()
     if any(v != 0 for v in status.values()):
         raise RuntimeError(f"device error in the timed region: {status}")
@@ -312,16 +372,17 @@ def run_ours(args, rank, world):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     hbm, peak_kind = peaks()
-    fwd_bytes = fwd_compulsory_bytes(cfg, n_ids, n_unique)
-    fwd_ms = stage_ms["forward"]
-    achieved = fwd_bytes / (fwd_ms / 1e3) / 1e9
-    with open(os.path.join(ROOT, "sparse_embeddings_feature_gb300", "csrc", "embedding_bag.cu"), "rb") as f:
-        src_hash = hashlib.sha256(f.read()).hexdigest()
-    roofline = {"bound": "hbm", "kernel": "bag_fwd_kernel (pooled gather)", "achieved": achieved, "peak": hbm,
-                "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": profile_traffic(src_hash),
-                "algorithmic_bytes_per_launch": fwd_bytes, "launch_ms": fwd_ms,
-                "logical_bytes_per_launch": n_ids * (cfg.d * 4 + 8) + cfg.num_fields * cfg.batch * (cfg.d * 4 + 8)}
+    algo = algorithmic_bytes(cfg, path, n_ids, n_unique)
+    kern = {}
+    for name, ms_k in kernel_ms.items():
+        if name in algo:
+            gbs = algo[name] / (ms_k / 1e3) / 1e9
+            kern[name] = {"ms": ms_k, "algorithmic_bytes": algo[name], "achieved_GBs": gbs, "frac": gbs / hbm}
+    dominant = max(kern, key=lambda k: kern[k]["ms"])
+    traffic = profile_traffic(dominant)
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": kern[dominant]["achieved_GBs"], "peak": hbm,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": kern[dominant]["frac"], "traffic": traffic,
+                "algorithmic_bytes_per_launch": algo[dominant], "launch_ms": kern[dominant]["ms"]}
     line = {
         "metric": METRIC, "value": n_ids * world / (ms / 1e3), "unit": "lookups/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -333,6 +394,7 @@ def run_ours(args, rank, world):
                        cfg.total_rows * cfg.d * 4 / 1e9, n_ids * 8 / 1e9)},
         "interaction_samples_per_s": cfg.batch * world / (ms / 1e3),
         "stage_ms": stage_ms,
+        "kernels": kern,
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": path.launches_per_step() * args.steps,

@@ -74,6 +74,29 @@ int ctr_status_reset(void* ws, ctr_stream_t stream);
  * return CTR_OK or the first device-side error recorded since the last reset. */
 int ctr_check_status(void* ws, ctr_stream_t stream);
 
+/* Per-kernel timing hook (diagnostics).  After this call, every launch of the
+ * named kernel records `before_event` on the launching stream just before the
+ * launch and `after_event` just after it (cudaEvent_t handles owned by the
+ * caller; both NULL turns the hook off).  Kernels:
+ *   CTR_KERNEL_GATHER            the pooled-gather kernel of ctr_embedding_bag_fwd
+ *   CTR_KERNEL_BWD_TILES         the short-run tile kernel of ctr_embedding_bag_bwd_update
+ *   CTR_KERNEL_BWD_PIECES        its long-run piece kernel
+ *   CTR_KERNEL_SORT              all radix passes of ctr_dedup (first to last)
+ *   CTR_KERNEL_INTERACTION       the kernel of ctr_dot_interaction
+ *   CTR_KERNEL_INTERACTION_BWD   the kernel of ctr_dot_interaction_bwd
+ * The setting is process-wide and not synchronised with calls running on
+ * other host threads. */
+typedef enum {
+  CTR_KERNEL_GATHER = 1,
+  CTR_KERNEL_BWD_TILES = 2,
+  CTR_KERNEL_BWD_PIECES = 3,
+  CTR_KERNEL_SORT = 4,
+  CTR_KERNEL_INTERACTION = 5,
+  CTR_KERNEL_INTERACTION_BWD = 6
+} ctr_kernel;
+#define CTR_KERNEL_COUNT 7
+int ctr_set_timing_events(int kernel, void* before_event, void* after_event);
+
 /* ------------------------------------------------------------------------ */
 /* Input generation (not part of the method)                                 */
 /* ------------------------------------------------------------------------ */

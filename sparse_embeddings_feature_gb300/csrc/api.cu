@@ -24,6 +24,21 @@ int num_sms() {
 }
 
 namespace {
+std::mutex g_timing_mu;
+cudaEvent_t g_timing[CTR_KERNEL_COUNT][2] = {};
+}  // namespace
+
+void timing_mark(int kernel, bool before, cudaStream_t s) {
+  if (kernel <= 0 || kernel >= CTR_KERNEL_COUNT) return;
+  cudaEvent_t e;
+  {
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    e = g_timing[kernel][before ? 0 : 1];
+  }
+  if (e) cudaEventRecord(e, s);
+}
+
+namespace {
 
 __device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
   uint64_t z = x + 0x9E3779B97F4A7C15ull;
@@ -76,6 +91,15 @@ extern "C" const char* ctr_status_string(int status) {
 }
 
 extern "C" int ctr_version(void) { return 100; }
+
+extern "C" int ctr_set_timing_events(int kernel, void* before_event, void* after_event) {
+  if (kernel <= 0 || kernel >= CTR_KERNEL_COUNT) return CTR_ERR_INVALID_ARG;
+  if ((before_event == nullptr) != (after_event == nullptr)) return CTR_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  g_timing[kernel][0] = (cudaEvent_t)before_event;
+  g_timing[kernel][1] = (cudaEvent_t)after_event;
+  return CTR_OK;
+}
 
 extern "C" int ctr_status_reset(void* ws, ctr_stream_t stream) {
   if (!ws) return CTR_ERR_WORKSPACE;

@@ -816,7 +816,9 @@ int launch_bwd(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
     return CTR_ERR_CUDA;
   clear_i64<<<1, 1, 0, s>>>(a.long_count, a.work);
   if (int st = launch_status()) return st;
+  timing_mark(CTR_KERNEL_BWD_TILES, true, s);
   tk<<<grid_of(tk, kTileThreads, tile_smem, ceil_div(n, (int64_t)a.TU * kTileWarps)), kTileThreads, tile_smem, s>>>(a);
+  timing_mark(CTR_KERNEL_BWD_TILES, false, s);
   if (int st = launch_status()) return st;
   {
     WsCarver sc = c;
@@ -826,6 +828,7 @@ int launch_bwd(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
   }
   expand_long_kernel<<<std::max(1, num_sms() * 2), 256, 0, s>>>(a);
   if (int st = launch_status()) return st;
+  timing_mark(CTR_KERNEL_BWD_PIECES, true, s);
   if (CPL == 1 && a.g4_ok) {
     auto pk = long_pieces_stream_kernel;
     pk<<<grid_of(pk, 256, 0, ceil_div(sizes(n).max_pieces, 8)), 256, 0, s>>>(a);
@@ -833,6 +836,7 @@ int launch_bwd(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
     auto pk = long_pieces_kernel<CPL>;
     pk<<<grid_of(pk, 256, 0, ceil_div(sizes(n).max_pieces, 8)), 256, 0, s>>>(a);
   }
+  timing_mark(CTR_KERNEL_BWD_PIECES, false, s);
   if (int st = launch_status()) return st;
   const size_t csmem = (size_t)(kCombThreads / 32) * a.d * sizeof(float);
   combine_long_kernel<<<std::max(num_sms() * 2, 1), kCombThreads, csmem, s>>>(a);

@@ -57,6 +57,9 @@ inline int make_field_map(const int32_t* bag_to_table, const int64_t* row_base, 
   return CTR_OK;
 }
 
+// Timing hook (ctr_set_timing_events): record the caller's events around a launch.
+void timing_mark(int kernel, bool before, cudaStream_t s);
+
 // Number of SMs of the current device (cached per device).
 int num_sms();
 

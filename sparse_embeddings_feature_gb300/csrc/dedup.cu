@@ -499,6 +499,7 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
     if (int st = launch_status()) return st;
   }
   const int32_t* vin = nullptr;
+  timing_mark(CTR_KERNEL_SORT, true, s);
   for (int p = 0; p < passes; ++p) {
     int32_t* vout = ((passes - 1 - p) % 2 == 0) ? vfinal : vscratch;
     onesweep_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(keys[p & 1], vin, keys[(p + 1) & 1], vout, n_ids,
@@ -508,6 +509,7 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
     if (int st = launch_status()) return st;
     vin = vout;
   }
+  timing_mark(CTR_KERNEL_SORT, false, s);
   const uint32_t* skeys = keys[passes & 1];
   unique_count_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(skeys, n_ids, tile_heads);
   if (int st = launch_status()) return st;

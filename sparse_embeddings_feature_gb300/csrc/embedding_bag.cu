@@ -577,13 +577,17 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
     if (cudaMemsetAsync((char*)a.err + kWsCounterOffset, 0, sizeof(unsigned long long), s) != cudaSuccess)
       return CTR_ERR_CUDA;
     auto k = bag_fwd_flat_kernel<IT>;
+    timing_mark(CTR_KERNEL_GATHER, true, s);
     k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm);
+    timing_mark(CTR_KERNEL_GATHER, false, s);
     return launch_status();
   }
 #define CTR_LAUNCH(LPR, CPL)                                 \
   {                                                          \
     auto k = bag_fwd_kernel<TT, LPR, CPL, IT>;               \
+    timing_mark(CTR_KERNEL_GATHER, true, s);                 \
     k<<<grid_for(k, nbags), kBagThreads, 0, s>>>(a, fm);     \
+    timing_mark(CTR_KERNEL_GATHER, false, s);                \
     return launch_status();                                  \
   }
   if (chunks <= 1) CTR_LAUNCH(1, 1)

@@ -275,8 +275,10 @@ extern "C" int ctr_dot_interaction(const void* X, ctr_dtype dtype, int32_t batch
   if (batch == 0) return CTR_OK;
   if (dtype == CTR_F32 && n == 27 && d == 128 && (uintptr_t)X % 16 == 0) {
     auto k = interaction_fwd_f32_regs<27, 128>;
+    timing_mark(CTR_KERNEL_INTERACTION, true, s);
     k<<<grid_blocks(k, kIntWarps * 32, 0, ceil_div(batch, kIntWarps)), kIntWarps * 32, 0, s>>>(
         (const float*)X, batch, (float*)out);
+    timing_mark(CTR_KERNEL_INTERACTION, false, s);
     return launch_status();
   }
   if (dtype == CTR_BF16 && interaction_bf16_tc_supported(n, d) && (uintptr_t)X % 16 == 0 &&
@@ -303,7 +305,9 @@ extern "C" int ctr_dot_interaction_bwd(const float* dout, const float* X, int32_
   if (batch == 0) return CTR_OK;
   if (n == 27 && d == 128 && (uintptr_t)X % 16 == 0 && (uintptr_t)dX % 16 == 0) {
     auto k = interaction_bwd_f32_regs<27, 128>;
+    timing_mark(CTR_KERNEL_INTERACTION_BWD, true, s);
     k<<<grid_blocks(k, kIntWarps * 32, 0, ceil_div(batch, kIntWarps)), kIntWarps * 32, 0, s>>>(dout, X, batch, dX);
+    timing_mark(CTR_KERNEL_INTERACTION_BWD, false, s);
     return launch_status();
   }
   const size_t smem = ((size_t)n * d + (size_t)n * (n - 1) / 2) * sizeof(float);

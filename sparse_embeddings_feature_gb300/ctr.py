@@ -31,6 +31,7 @@ _i32, _i64, _u64, _f32, _sz = C.c_int32, C.c_int64, C.c_uint64, C.c_float, C.c_s
 _SIGS = {
     "ctr_status_string": (C.c_char_p, [C.c_int]),
     "ctr_version": (C.c_int, []),
+    "ctr_set_timing_events": (C.c_int, [C.c_int, _p, _p]),
     "ctr_status_reset": (C.c_int, [_p, _p]),
     "ctr_check_status": (C.c_int, [_p, _p]),
     "ctr_fill_table": (C.c_int, [_p, C.c_int, _i64, _i32, _i64, C.c_int, _u64, _f32, _p]),
@@ -108,6 +109,20 @@ def _dev(t: torch.Tensor, what: str) -> torch.Tensor:
     if not t.is_cuda:
         raise ValueError(f"{what} must be a CUDA tensor")
     return t
+
+
+KERNEL_GATHER, KERNEL_BWD_TILES, KERNEL_BWD_PIECES, KERNEL_SORT, KERNEL_INTERACTION, KERNEL_INTERACTION_BWD = \
+    1, 2, 3, 4, 5, 6
+
+
+def ctr_set_timing_events(kernel: int, before=None, after=None) -> None:
+    """Record torch.cuda.Events around every later launch of `kernel` (None, None: off).
+
+    The events must already have been recorded once, so that torch has created them.
+    """
+    b = None if before is None else C.c_void_p(before.cuda_event)
+    e = None if after is None else C.c_void_p(after.cuda_event)
+    _ok("ctr_set_timing_events", lib().ctr_set_timing_events(int(kernel), b, e))
 
 
 # ---------------------------------------------------------------------------
