@@ -40,7 +40,10 @@ def parse():
     ap.add_argument("--workload", default="full_step")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller cases for profiling)")
     ap.add_argument("--rows", type=int, default=0, help="override rows per table (smaller cases for profiling)")
-    ap.add_argument("--cpu-sample", type=int, default=2048, help="samples of the batch the oracle runs")
+    ap.add_argument("--cpu-sample", type=int, default=16384,
+                    help="samples of the batch the oracle runs for cpu_baseline (about 10 s of CPU work)")
+    ap.add_argument("--ref-sample", type=int, default=2048,
+                    help="samples of the batch per step of the reference arm (the oracle)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -175,7 +178,8 @@ def cpu_baseline(cfg, w, sample, reps=1):
     dt = (time.perf_counter() - t0) / reps
     return {"value": lookups / dt, "unit": "lookups/s", "cores": O.max_threads(), "kind": "oracle",
             "sample": f"first {scfg.batch} of {cfg.batch} samples of every field ({lookups} lookups), "
-                      f"whole path, fp64, OpenMP over bags/samples", "seconds": dt}
+                      f"whole path, fp64; dedup, gather and interaction OpenMP over bags/samples, "
+                      f"gradient reduce + update single-threaded", "seconds": dt}
 
 
 # ---------------------------------------------------------------------------
@@ -292,6 +296,7 @@ def run_ours(args, rank, world):
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
+        launches0 = ctr.ctr_launch_count()
         for k in range(args.steps):
             for name, kid in kernels.items():
                 ctr.ctr_set_timing_events(kid, *kev[k][name])
@@ -300,6 +305,7 @@ def run_ours(args, rank, world):
                 run_stage[s_]()
                 ev[k][i + 1].record(stream)
         t_end.record(stream)
+        launches = ctr.ctr_launch_count() - launches0
         torch.cuda.synchronize()
         time.sleep(0.25)
         mark1 = clk.mark()
@@ -397,7 +403,7 @@ def run_ours(args, rank, world):
         "kernels": kern,
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": path.launches_per_step() * args.steps,
+        "gpu_launches": launches,
         "clocks": clk.summary(mark0, mark1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -411,7 +417,7 @@ def run_reference(args):
     from oracle import oracle as O
     cfg = workload_cfg(args)
     w = W.make_workload(cfg)
-    scfg, sw = sample_batch(cfg, w, args.cpu_sample)
+    scfg, sw = sample_batch(cfg, w, args.ref_sample)
     O.set_threads(os.cpu_count() or 1)
     for _ in range(args.warmup):
         oracle_step(scfg, sw)

@@ -97,6 +97,12 @@ typedef enum {
 #define CTR_KERNEL_COUNT 7
 int ctr_set_timing_events(int kernel, void* before_event, void* after_event);
 
+/* Number of kernel launches this library has issued in this process, on all
+ * devices and streams, since it was loaded (diagnostics: the difference across
+ * a region counts the library's launches in it).  Host-side atomic counter;
+ * never fails. */
+uint64_t ctr_launch_count(void);
+
 /* ------------------------------------------------------------------------ */
 /* Input generation (not part of the method)                                 */
 /* ------------------------------------------------------------------------ */

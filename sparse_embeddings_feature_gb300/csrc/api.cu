@@ -3,6 +3,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -25,8 +26,11 @@ int num_sms() {
 
 namespace {
 std::mutex g_timing_mu;
+std::atomic<uint64_t> g_launches{0};
 cudaEvent_t g_timing[CTR_KERNEL_COUNT][2] = {};
 }  // namespace
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 void timing_mark(int kernel, bool before, cudaStream_t s) {
   if (kernel <= 0 || kernel >= CTR_KERNEL_COUNT) return;
@@ -92,6 +96,8 @@ extern "C" const char* ctr_status_string(int status) {
 
 extern "C" int ctr_version(void) { return 100; }
 
+extern "C" uint64_t ctr_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
 extern "C" int ctr_set_timing_events(int kernel, void* before_event, void* after_event) {
   if (kernel <= 0 || kernel >= CTR_KERNEL_COUNT) return CTR_ERR_INVALID_ARG;
   if ((before_event == nullptr) != (after_event == nullptr)) return CTR_ERR_INVALID_ARG;
@@ -103,7 +109,7 @@ extern "C" int ctr_set_timing_events(int kernel, void* before_event, void* after
 
 extern "C" int ctr_status_reset(void* ws, ctr_stream_t stream) {
   if (!ws) return CTR_ERR_WORKSPACE;
-  clear_word<<<1, 1, 0, (cudaStream_t)stream>>>((int*)ws);
+  clear_word<<<1, 1, 0, (cudaStream_t)stream>>>((int*)ws); count_launch();
   return launch_status();
 }
 
@@ -128,9 +134,9 @@ extern "C" int ctr_fill_table(void* table, ctr_dtype dtype, int64_t rows, int32_
   const int64_t blocks = imin64(ceil_div(count, 256), (int64_t)num_sms() * 32);
   cudaStream_t s = (cudaStream_t)stream;
   if (gen_kind == 0 && dtype == CTR_F32) {
-    fill_uniform_f32<<<(unsigned)blocks, 256, 0, s>>>((float*)table, count, idx0, seed, scale);
+    fill_uniform_f32<<<(unsigned)blocks, 256, 0, s>>>((float*)table, count, idx0, seed, scale); count_launch();
   } else if (gen_kind == 1 && dtype == CTR_BF16) {
-    fill_normal4_bf16<<<(unsigned)blocks, 256, 0, s>>>((__nv_bfloat16*)table, count, idx0, seed, scale);
+    fill_normal4_bf16<<<(unsigned)blocks, 256, 0, s>>>((__nv_bfloat16*)table, count, idx0, seed, scale); count_launch();
   } else {
     return CTR_ERR_INVALID_ARG;
   }

@@ -814,10 +814,10 @@ int launch_bwd(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
   if (tile_smem > 48 * 1024 &&
       cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tile_smem) != cudaSuccess)
     return CTR_ERR_CUDA;
-  clear_i64<<<1, 1, 0, s>>>(a.long_count, a.work);
+  clear_i64<<<1, 1, 0, s>>>(a.long_count, a.work); count_launch();
   if (int st = launch_status()) return st;
   timing_mark(CTR_KERNEL_BWD_TILES, true, s);
-  tk<<<grid_of(tk, kTileThreads, tile_smem, ceil_div(n, (int64_t)a.TU * kTileWarps)), kTileThreads, tile_smem, s>>>(a);
+  tk<<<grid_of(tk, kTileThreads, tile_smem, ceil_div(n, (int64_t)a.TU * kTileWarps)), kTileThreads, tile_smem, s>>>(a); count_launch();
   timing_mark(CTR_KERNEL_BWD_TILES, false, s);
   if (int st = launch_status()) return st;
   {
@@ -826,20 +826,20 @@ int launch_bwd(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
                                           sc, s))
       return st;
   }
-  expand_long_kernel<<<std::max(1, num_sms() * 2), 256, 0, s>>>(a);
+  expand_long_kernel<<<std::max(1, num_sms() * 2), 256, 0, s>>>(a); count_launch();
   if (int st = launch_status()) return st;
   timing_mark(CTR_KERNEL_BWD_PIECES, true, s);
   if (CPL == 1 && a.g4_ok) {
     auto pk = long_pieces_stream_kernel;
-    pk<<<grid_of(pk, 256, 0, ceil_div(sizes(n).max_pieces, 8)), 256, 0, s>>>(a);
+    pk<<<grid_of(pk, 256, 0, ceil_div(sizes(n).max_pieces, 8)), 256, 0, s>>>(a); count_launch();
   } else {
     auto pk = long_pieces_kernel<CPL>;
-    pk<<<grid_of(pk, 256, 0, ceil_div(sizes(n).max_pieces, 8)), 256, 0, s>>>(a);
+    pk<<<grid_of(pk, 256, 0, ceil_div(sizes(n).max_pieces, 8)), 256, 0, s>>>(a); count_launch();
   }
   timing_mark(CTR_KERNEL_BWD_PIECES, false, s);
   if (int st = launch_status()) return st;
   const size_t csmem = (size_t)(kCombThreads / 32) * a.d * sizeof(float);
-  combine_long_kernel<<<std::max(num_sms() * 2, 1), kCombThreads, csmem, s>>>(a);
+  combine_long_kernel<<<std::max(num_sms() * 2, 1), kCombThreads, csmem, s>>>(a); count_launch();
   return launch_status();
 }
 

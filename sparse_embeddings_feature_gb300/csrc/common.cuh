@@ -59,6 +59,8 @@ inline int make_field_map(const int32_t* bag_to_table, const int64_t* row_base, 
 
 // Timing hook (ctr_set_timing_events): record the caller's events around a launch.
 void timing_mark(int kernel, bool before, cudaStream_t s);
+// Counts one kernel launch (called right after each launch statement).
+void count_launch();
 
 // Number of SMs of the current device (cached per device).
 int num_sms();

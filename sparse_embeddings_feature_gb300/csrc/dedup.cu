@@ -458,7 +458,7 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
   for (int t = 0; t <= num_tables; ++t) tb.row_base[t] = row_base[t];
 
   if (n_ids == 0) {
-    dedup_empty_kernel<<<1, 1, 0, s>>>(n_unique, run_offsets, unique_offsets, num_tables);
+    dedup_empty_kernel<<<1, 1, 0, s>>>(n_unique, run_offsets, unique_offsets, num_tables); count_launch();
     return launch_status();
   }
 
@@ -489,13 +489,13 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
   }
   const int sms = num_sms();
   clear_u64_kernel<<<(unsigned)std::max<int64_t>(1, imin64(ceil_div(state_words(tiles), 256), (int64_t)sms * 8)),
-                     256, 0, s>>>(state, state_words(tiles));
+                     256, 0, s>>>(state, state_words(tiles)); count_launch();
   if (int st = launch_status()) return st;
   const int64_t nbags = (int64_t)num_fields * batch;
   {
     int64_t blocks = imin64(ceil_div(nbags, 8), (int64_t)sms * 16);
     keygen_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, s>>>(ids, offsets, num_fields, batch, n_ids, fm,
-                                                                        keys[0], bag_of, plan, g_hist, err);
+                                                                        keys[0], bag_of, plan, g_hist, err); count_launch();
     if (int st = launch_status()) return st;
   }
   const int32_t* vin = nullptr;
@@ -505,13 +505,13 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
     onesweep_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(keys[p & 1], vin, keys[(p + 1) & 1], vout, n_ids,
                                                            plan.shift[p], plan.bits[p], g_hist + p * kMaxDigits,
                                                            lookback + (int64_t)p * tiles * kMaxDigits,
-                                                           tile_counter + p, err);
+                                                           tile_counter + p, err); count_launch();
     if (int st = launch_status()) return st;
     vin = vout;
   }
   timing_mark(CTR_KERNEL_SORT, false, s);
   const uint32_t* skeys = keys[passes & 1];
-  unique_count_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(skeys, n_ids, tile_heads);
+  unique_count_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(skeys, n_ids, tile_heads); count_launch();
   if (int st = launch_status()) return st;
   {
     WsCarver scan_ws = c;
@@ -519,6 +519,6 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
   }
   unique_write_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(skeys, vfinal, n_ids, tile_heads, tb, bag_of,
                                                              unique_rows, n_unique, inverse, sorted_bag, run_offsets,
-                                                             unique_offsets);
+                                                             unique_offsets); count_launch();
   return launch_status();
 }

@@ -556,7 +556,7 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
   const int64_t nbags = (int64_t)a.F * a.B;
   if (a.d % V != 0) {
     auto k = bag_fwd_scalar_kernel<TT, IT>;
-    k<<<grid_for(k, nbags), kBagThreads, 0, s>>>(a, fm);
+    k<<<grid_for(k, nbags), kBagThreads, 0, s>>>(a, fm); count_launch();
     return launch_status();
   }
   const int chunks = a.d / V;
@@ -570,7 +570,7 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kTmaWarps * 32, smem);
     const int64_t want = ceil_div(ceil_div(nbags, 32), kTmaWarps);
     const int grid = (int)std::max<int64_t>(1, imin64(want, (int64_t)std::max(per_sm, 1) * num_sms()));
-    k<<<grid, kTmaWarps * 32, smem, s>>>(a, fm, map);
+    k<<<grid, kTmaWarps * 32, smem, s>>>(a, fm, map); count_launch();
     return launch_status();
   }
   if (std::is_same<TT, float>::value && a.d == 128 && a.total_rows < 0xffffffffll) {
@@ -578,7 +578,7 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
       return CTR_ERR_CUDA;
     auto k = bag_fwd_flat_kernel<IT>;
     timing_mark(CTR_KERNEL_GATHER, true, s);
-    k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm);
+    k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm); count_launch();
     timing_mark(CTR_KERNEL_GATHER, false, s);
     return launch_status();
   }
@@ -586,7 +586,7 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
   {                                                          \
     auto k = bag_fwd_kernel<TT, LPR, CPL, IT>;               \
     timing_mark(CTR_KERNEL_GATHER, true, s);                 \
-    k<<<grid_for(k, nbags), kBagThreads, 0, s>>>(a, fm);     \
+    k<<<grid_for(k, nbags), kBagThreads, 0, s>>>(a, fm); count_launch();     \
     timing_mark(CTR_KERNEL_GATHER, false, s);                \
     return launch_status();                                  \
   }
@@ -696,6 +696,6 @@ extern "C" int ctr_gather_rows(const void* table, ctr_dtype dtype, int32_t d, in
   if (row_bytes % 16 == 0 && (((uintptr_t)table | (uintptr_t)U) % 16) != 0) return CTR_ERR_INVALID_ARG;
   int64_t blocks = imin64(ceil_div(capacity, 8), (int64_t)num_sms() * 16);
   gather_rows_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
-      (const char*)table, row_bytes, total_rows, unique_rows, n_unique, capacity, (char*)U, (int*)ws);
+      (const char*)table, row_bytes, total_rows, unique_rows, n_unique, capacity, (char*)U, (int*)ws); count_launch();
   return launch_status();
 }

@@ -277,7 +277,7 @@ extern "C" int ctr_dot_interaction(const void* X, ctr_dtype dtype, int32_t batch
     auto k = interaction_fwd_f32_regs<27, 128>;
     timing_mark(CTR_KERNEL_INTERACTION, true, s);
     k<<<grid_blocks(k, kIntWarps * 32, 0, ceil_div(batch, kIntWarps)), kIntWarps * 32, 0, s>>>(
-        (const float*)X, batch, (float*)out);
+        (const float*)X, batch, (float*)out); count_launch();
     timing_mark(CTR_KERNEL_INTERACTION, false, s);
     return launch_status();
   }
@@ -288,11 +288,11 @@ extern "C" int ctr_dot_interaction(const void* X, ctr_dtype dtype, int32_t batch
   if (smem > 48 * 1024) return CTR_ERR_UNSUPPORTED;
   if (dtype == CTR_F32) {
     auto k = interaction_fwd_generic<float>;
-    k<<<grid_blocks(k, kGenThreads, smem, batch), kGenThreads, smem, s>>>((const float*)X, batch, n, d, (float*)out);
+    k<<<grid_blocks(k, kGenThreads, smem, batch), kGenThreads, smem, s>>>((const float*)X, batch, n, d, (float*)out); count_launch();
   } else {
     auto k = interaction_fwd_generic<__nv_bfloat16>;
     k<<<grid_blocks(k, kGenThreads, smem, batch), kGenThreads, smem, s>>>((const __nv_bfloat16*)X, batch, n, d,
-                                                                           (__nv_bfloat16*)out);
+                                                                           (__nv_bfloat16*)out); count_launch();
   }
   return launch_status();
 }
@@ -306,13 +306,13 @@ extern "C" int ctr_dot_interaction_bwd(const float* dout, const float* X, int32_
   if (n == 27 && d == 128 && (uintptr_t)X % 16 == 0 && (uintptr_t)dX % 16 == 0) {
     auto k = interaction_bwd_f32_regs<27, 128>;
     timing_mark(CTR_KERNEL_INTERACTION_BWD, true, s);
-    k<<<grid_blocks(k, kIntWarps * 32, 0, ceil_div(batch, kIntWarps)), kIntWarps * 32, 0, s>>>(dout, X, batch, dX);
+    k<<<grid_blocks(k, kIntWarps * 32, 0, ceil_div(batch, kIntWarps)), kIntWarps * 32, 0, s>>>(dout, X, batch, dX); count_launch();
     timing_mark(CTR_KERNEL_INTERACTION_BWD, false, s);
     return launch_status();
   }
   const size_t smem = ((size_t)n * d + (size_t)n * (n - 1) / 2) * sizeof(float);
   if (smem > 48 * 1024) return CTR_ERR_UNSUPPORTED;
   auto k = interaction_bwd_generic;
-  k<<<grid_blocks(k, kGenThreads, smem, batch), kGenThreads, smem, s>>>(dout, X, batch, n, d, dX);
+  k<<<grid_blocks(k, kGenThreads, smem, batch), kGenThreads, smem, s>>>(dout, X, batch, n, d, dX); count_launch();
   return launch_status();
 }

@@ -307,7 +307,7 @@ int interaction_bf16_tc(const void* X, int32_t batch, int32_t n, int32_t d, void
     return CTR_ERR_CUDA;
   const int64_t ntiles = ceil_div(batch, p.S);
   const int grid = (int)std::max<int64_t>(1, imin64(ntiles, num_sms()));
-  kern<<<grid, kTcThreads, smem, s>>>(p, map);
+  kern<<<grid, kTcThreads, smem, s>>>(p, map); count_launch();
   return launch_status();
 }
 

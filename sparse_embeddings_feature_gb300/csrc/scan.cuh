@@ -141,18 +141,18 @@ inline int scan_exclusive(const T* in, T* out, int64_t n_host, const int64_t* n_
                           cudaStream_t s) {
   using S = ScanTile<T>;
   if (n_host <= S::kTile) {
-    scan_down_kernel<T><<<1, S::kThreads, 0, s>>>(in, out, n_host, n_dev, nullptr, total_out);
+    scan_down_kernel<T><<<1, S::kThreads, 0, s>>>(in, out, n_host, n_dev, nullptr, total_out); count_launch();
     return launch_status();
   }
   int64_t nb = ceil_div(n_host, S::kTile);
   T* sums = ws.take<T>((size_t)nb);
   if (!sums) return CTR_ERR_WORKSPACE;
-  scan_reduce_kernel<T><<<(unsigned)nb, S::kThreads, 0, s>>>(in, n_host, n_dev, sums);
+  scan_reduce_kernel<T><<<(unsigned)nb, S::kThreads, 0, s>>>(in, n_host, n_dev, sums); count_launch();
   int st = launch_status();
   if (st) return st;
   st = scan_exclusive<T>(sums, sums, nb, nullptr, total_out, ws, s);
   if (st) return st;
-  scan_down_kernel<T><<<(unsigned)nb, S::kThreads, 0, s>>>(in, out, n_host, n_dev, sums, nullptr);
+  scan_down_kernel<T><<<(unsigned)nb, S::kThreads, 0, s>>>(in, out, n_host, n_dev, sums, nullptr); count_launch();
   return launch_status();
 }
 

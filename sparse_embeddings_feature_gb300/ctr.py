@@ -32,6 +32,7 @@ _SIGS = {
     "ctr_status_string": (C.c_char_p, [C.c_int]),
     "ctr_version": (C.c_int, []),
     "ctr_set_timing_events": (C.c_int, [C.c_int, _p, _p]),
+    "ctr_launch_count": (C.c_uint64, []),
     "ctr_status_reset": (C.c_int, [_p, _p]),
     "ctr_check_status": (C.c_int, [_p, _p]),
     "ctr_fill_table": (C.c_int, [_p, C.c_int, _i64, _i32, _i64, C.c_int, _u64, _f32, _p]),
@@ -123,6 +124,11 @@ def ctr_set_timing_events(kernel: int, before=None, after=None) -> None:
     b = None if before is None else C.c_void_p(before.cuda_event)
     e = None if after is None else C.c_void_p(after.cuda_event)
     _ok("ctr_set_timing_events", lib().ctr_set_timing_events(int(kernel), b, e))
+
+
+def ctr_launch_count() -> int:
+    """Kernel launches the library has issued in this process so far."""
+    return int(lib().ctr_launch_count())
 
 
 # ---------------------------------------------------------------------------

@@ -151,32 +151,3 @@ class CtrPath:
             self.interaction_bwd()
         if cfg.backward != "none":
             self.bwd_update()
-
-    def launches_per_step(self) -> int:
-        """Number of libctr kernel launches one step() makes (for the benchmark's launch count)."""
-        cfg = self.cfg
-        k = 0
-        n = max(self.n_ids, 1)
-        if cfg.backward != "none" or cfg.dedup_gather:
-            bits = 1
-            while bits < 32 and (1 << bits) < cfg.total_rows:
-                bits += 1
-            passes = (bits + 7) // 8
-            nb = (bits + passes - 1) // passes
-            tiles = -(-n // 4096)
-            k += 1 + passes * (2 + _scan_launches(tiles << nb, 4096)) + 1 + _scan_launches(tiles, 4096) + 1
-        k += 2 if cfg.dedup_gather else 1
-        if cfg.interaction:
-            k += 1
-        if cfg.backward == "full":
-            k += 1
-        if cfg.backward != "none":
-            max_long = n // 129 + 1
-            k += 2 + _scan_launches(max_long, 4096) + 3
-        return k
-
-
-def _scan_launches(n: int, tile: int) -> int:
-    if n <= tile:
-        return 1
-    return 2 + _scan_launches(-(-n // tile), tile)

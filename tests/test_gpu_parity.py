@@ -496,3 +496,22 @@ def test_full_step_composed_small():
     old = O.table_rows(gen[0], gen[1], gen[2], d, rows_t)
     depth = _bwd_depth(int(np.diff(dd["run_offsets"]).max())) + 64
     f32_close(_np(path.table)[rows_t], new_ref, cfg.lr * mag + np.abs(old), depth, what="updated rows")
+
+
+def test_launch_counter_counts_each_step_alike():
+    cfg = W.CONFIGS["full_step"].shrink(batch=64, rows_per_table=tuple([5_000] * 26))
+    w = W.make_workload(cfg)
+    path = CtrPath(cfg, w["ids"].size)
+    path.upload(w)
+    path.reset_status()
+    c0 = ctr.ctr_launch_count()
+    path.step()
+    c1 = ctr.ctr_launch_count()
+    path.step()
+    c2 = ctr.ctr_launch_count()
+    torch.cuda.synchronize()
+    assert all(v == 0 for v in path.check_status().values())
+    # dedup (clear, keygen, radix passes, unique count, scan, unique write), gather,
+    # interaction, interaction backward, and the backward's clear + tiles + pieces + combine
+    assert c1 - c0 >= 14
+    assert c2 - c1 == c1 - c0
