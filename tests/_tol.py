@@ -15,6 +15,13 @@ the tolerance.
 bf16 outputs: |gpu - ref| <= rtol |ref| + atol + gamma_k sum|terms| with
 rtol = 1e-2 (the benchmark spec), the fp32 accumulation term as above, and atol = 1e-5
 for pooled bf16 values (atol 0 for interaction outputs).
+
+`mrel` adds mrel * sum|terms| to the bound.  It is used where a sum's inputs
+are themselves rounded results that may differ by the pooled tolerance: a
+bf16 pair dot computed from pooled vectors that each carry up to one bf16
+rounding differs by at most about 2 * 2^-8 * sum_c |x_ic x_jc|, so those
+checks take the magnitude-aware bound 1e-2 * <|x_i|, |x_j|> next to the
+relative one.
 """
 import numpy as np
 
@@ -26,12 +33,12 @@ def gamma(k: float) -> float:
     return ku / (1.0 - ku)
 
 
-def f32_close(got, ref, mag=None, depth=0, rtol=1e-5, atol=1e-6, what=""):
+def f32_close(got, ref, mag=None, depth=0, rtol=1e-5, atol=1e-6, what="", mrel=0.0):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     tol = atol + rtol * np.abs(ref)
-    if mag is not None and depth:
-        tol = tol + gamma(depth) * np.asarray(mag, dtype=np.float64)
+    if mag is not None and (depth or mrel):
+        tol = tol + (gamma(depth) + mrel) * np.asarray(mag, dtype=np.float64)
     err = np.abs(got - ref)
     bad = ~(err <= tol)
     if bad.any():
@@ -49,12 +56,12 @@ def bf16_to_f64(bits) -> np.ndarray:
     return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
 
 
-def bf16_close(got_bits, ref_bits, mag=None, depth=0, rtol=1e-2, atol=0.0, what=""):
+def bf16_close(got_bits, ref_bits, mag=None, depth=0, rtol=1e-2, atol=0.0, what="", mrel=0.0):
     got = bf16_to_f64(got_bits)
     ref = bf16_to_f64(ref_bits)
     tol = atol + rtol * np.abs(ref)
-    if mag is not None and depth:
-        tol = tol + gamma(depth) * np.asarray(mag, dtype=np.float64)
+    if mag is not None and (depth or mrel):
+        tol = tol + (gamma(depth) + mrel) * np.asarray(mag, dtype=np.float64)
     err = np.abs(got - ref)
     bad = ~(err <= tol)
     if bad.any():
