@@ -189,6 +189,7 @@ def algorithmic_bytes(cfg, path, n_ids, n_unique):
     """Compulsory DRAM bytes per launch of each timed kernel (each row, index and output once).
 
     gather       the distinct table rows, the IDs, the offsets, the pooled outputs
+    gather_rows  the distinct rows read from the table and written to the unique-row matrix
     sort         four radix passes reading and writing (key, value) pairs
     interaction  X in, [dense | pairs] out;  interaction_bwd: dout and X in, dX out
     bwd_tiles    read-modify-write of the rows of runs <= 128 occurrences, their
@@ -201,8 +202,12 @@ def algorithmic_bytes(cfg, path, n_ids, n_unique):
     row = cfg.d * (4 if cfg.dtype == "f32" else 2)
     F, B, n = cfg.num_fields, cfg.batch, cfg.n_vectors
     nbags = F * B
-    out = {"gather": n_unique * row + n_ids * 8 + (nbags + 1) * 8 + nbags * row,
-           "sort": 4 * n_ids * 16}
+    idx_bytes = 4 if cfg.dedup_gather else 8          # int32 inverse into U, or int64 IDs
+    out = {"gather": n_unique * row + n_ids * idx_bytes + (nbags + 1) * 8 + nbags * row}
+    if cfg.backward != "none" or cfg.dedup_gather:
+        out["sort"] = 4 * n_ids * 16
+    if cfg.dedup_gather:
+        out["gather_rows"] = n_unique * (2 * row + 8)
     if cfg.interaction:
         width = cfg.out_width
         out["interaction"] = B * n * row + B * width * (row // cfg.d)
@@ -241,6 +246,21 @@ def profile_traffic(kernel):
         return None
 
 
+def max_over_ranks(x, world, device):
+    """The largest of the ranks' values (each rank's time; the job is as slow as its slowest replica)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank, world, ms):
+    """Whole-job rate of N independent replicas: all ranks' units over the slowest rank's time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def run_ours(args, rank, world):
     import torch
     from sparse_embeddings_feature_gb300 import ctr
@@ -276,9 +296,26 @@ def run_ours(args, rank, world):
               and (s != "interaction" or cfg.interaction)
               and (s != "interaction_bwd" or cfg.backward == "full")
               and (s != "bwd_update" or cfg.backward != "none")]
-    kernels = {"gather": ctr.KERNEL_GATHER, "bwd_tiles": ctr.KERNEL_BWD_TILES, "bwd_pieces": ctr.KERNEL_BWD_PIECES,
-               "sort": ctr.KERNEL_SORT, "interaction": ctr.KERNEL_INTERACTION,
-               "interaction_bwd": ctr.KERNEL_INTERACTION_BWD}
+    if "dedup" not in active:
+        # distinct rows of the batch, for the gather's compulsory bytes (outside the timed region)
+        lens = torch.from_numpy(np.diff(w["offsets"])).cuda()
+        bag_table = torch.from_numpy(np.asarray(cfg.field_to_table, dtype=np.int64)).cuda().repeat_interleave(cfg.batch)
+        base = torch.from_numpy(np.asarray(cfg.row_base, dtype=np.int64)).cuda()[bag_table]
+        keys = base.repeat_interleave(lens) + path.ids[:n_ids]
+        n_unique = int(torch.unique(keys).numel())
+        del lens, bag_table, base, keys
+    kernels = {"gather": ctr.KERNEL_GATHER}
+    if "dedup" in active:
+        kernels["sort"] = ctr.KERNEL_SORT
+    if cfg.dedup_gather:
+        kernels["gather_rows"] = ctr.KERNEL_GATHER_ROWS
+    if cfg.interaction:
+        kernels["interaction"] = ctr.KERNEL_INTERACTION
+    if cfg.backward == "full":
+        kernels["interaction_bwd"] = ctr.KERNEL_INTERACTION_BWD
+    if cfg.backward != "none":
+        kernels["bwd_tiles"] = ctr.KERNEL_BWD_TILES
+        kernels["bwd_pieces"] = ctr.KERNEL_BWD_PIECES
 
     def new_event():
         e = torch.cuda.Event(enable_timing=True)
@@ -321,15 +358,11 @@ def run_ours(args, rank, world):
             kernel_ms[name] = sum(kev[k][name][0].elapsed_time(kev[k][name][1]) for k in range(args.steps)) / args.steps
         except RuntimeError:
             pass
-    kernel_ms = {k: v for k, v in kernel_ms.items() if v > 1e-3}
     status = path.check_status()
     if any(v != 0 for v in status.values()):
         raise RuntimeError(f"device error in the timed region: {status}")
     ms = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, "cuda")
 
     # end to end through the C-ABI with host buffers: H2D of the step's inputs
     # from pinned memory, the step, D2H of its output, all inside the timed region
@@ -370,11 +403,8 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         barrier()
         e2e_ms = a.elapsed_time(b) / args.steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": n_ids * world / (e2e_ms / 1e3), "unit": "lookups/s", "ms_per_step": e2e_ms,
+        e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
+        e2e = {"value": replica_throughput(n_ids, world, e2e_ms), "unit": "lookups/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     hbm, peak_kind = peaks()
@@ -390,7 +420,7 @@ def run_ours(args, rank, world):
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": kern[dominant]["frac"], "traffic": traffic,
                 "algorithmic_bytes_per_launch": algo[dominant], "launch_ms": kern[dominant]["ms"]}
     line = {
-        "metric": METRIC, "value": n_ids * world / (ms / 1e3), "unit": "lookups/s", "n_gpus": world,
+        "metric": METRIC, "value": replica_throughput(n_ids, world, ms), "unit": "lookups/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
         "config": {"workload": cfg.name, "batch": cfg.batch, "fields": cfg.num_fields, "tables": cfg.num_tables,

@@ -84,6 +84,7 @@ int ctr_check_status(void* ws, ctr_stream_t stream);
  *   CTR_KERNEL_SORT              all radix passes of ctr_dedup (first to last)
  *   CTR_KERNEL_INTERACTION       the kernel of ctr_dot_interaction
  *   CTR_KERNEL_INTERACTION_BWD   the kernel of ctr_dot_interaction_bwd
+ *   CTR_KERNEL_GATHER_ROWS       the kernel of ctr_gather_rows
  * The setting is process-wide and not synchronised with calls running on
  * other host threads. */
 typedef enum {
@@ -92,9 +93,10 @@ typedef enum {
   CTR_KERNEL_BWD_PIECES = 3,
   CTR_KERNEL_SORT = 4,
   CTR_KERNEL_INTERACTION = 5,
-  CTR_KERNEL_INTERACTION_BWD = 6
+  CTR_KERNEL_INTERACTION_BWD = 6,
+  CTR_KERNEL_GATHER_ROWS = 7
 } ctr_kernel;
-#define CTR_KERNEL_COUNT 7
+#define CTR_KERNEL_COUNT 8
 int ctr_set_timing_events(int kernel, void* before_event, void* after_event);
 
 /* Number of kernel launches this library has issued in this process, on all

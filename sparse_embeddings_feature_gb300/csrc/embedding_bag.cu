@@ -577,17 +577,14 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
     if (cudaMemsetAsync((char*)a.err + kWsCounterOffset, 0, sizeof(unsigned long long), s) != cudaSuccess)
       return CTR_ERR_CUDA;
     auto k = bag_fwd_flat_kernel<IT>;
-    timing_mark(CTR_KERNEL_GATHER, true, s);
     k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm); count_launch();
-    timing_mark(CTR_KERNEL_GATHER, false, s);
     return launch_status();
   }
 #define CTR_LAUNCH(LPR, CPL)                                 \
   {                                                          \
     auto k = bag_fwd_kernel<TT, LPR, CPL, IT>;               \
-    timing_mark(CTR_KERNEL_GATHER, true, s);                 \
-    k<<<grid_for(k, nbags), kBagThreads, 0, s>>>(a, fm); count_launch();     \
-    timing_mark(CTR_KERNEL_GATHER, false, s);                \
+    k<<<grid_for(k, nbags), kBagThreads, 0, s>>>(a, fm);     \
+    count_launch();                                          \
     return launch_status();                                  \
   }
   if (chunks <= 1) CTR_LAUNCH(1, 1)
@@ -678,10 +675,15 @@ extern "C" int ctr_embedding_bag_fwd(const void* table, ctr_dtype dtype, int32_t
   a.sf = out_stride_f;
   a.err = (int*)ws;
   if ((uintptr_t)table % 16 != 0) return CTR_ERR_INVALID_ARG;
+  timing_mark(CTR_KERNEL_GATHER, true, s);
+  int st;
   if (dtype == CTR_F32)
-    return indices_are_int32 ? launch_bag_fwd<float, int32_t>(a, fm, s) : launch_bag_fwd<float, int64_t>(a, fm, s);
-  return indices_are_int32 ? launch_bag_fwd<__nv_bfloat16, int32_t>(a, fm, s)
+    st = indices_are_int32 ? launch_bag_fwd<float, int32_t>(a, fm, s) : launch_bag_fwd<float, int64_t>(a, fm, s);
+  else
+    st = indices_are_int32 ? launch_bag_fwd<__nv_bfloat16, int32_t>(a, fm, s)
                            : launch_bag_fwd<__nv_bfloat16, int64_t>(a, fm, s);
+  timing_mark(CTR_KERNEL_GATHER, false, s);
+  return st;
 }
 
 extern "C" int ctr_gather_rows(const void* table, ctr_dtype dtype, int32_t d, int64_t total_rows,
@@ -695,7 +697,9 @@ extern "C" int ctr_gather_rows(const void* table, ctr_dtype dtype, int32_t d, in
   const int64_t row_bytes = (int64_t)d * (dtype == CTR_F32 ? 4 : 2);
   if (row_bytes % 16 == 0 && (((uintptr_t)table | (uintptr_t)U) % 16) != 0) return CTR_ERR_INVALID_ARG;
   int64_t blocks = imin64(ceil_div(capacity, 8), (int64_t)num_sms() * 16);
+  timing_mark(CTR_KERNEL_GATHER_ROWS, true, (cudaStream_t)stream);
   gather_rows_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
       (const char*)table, row_bytes, total_rows, unique_rows, n_unique, capacity, (char*)U, (int*)ws); count_launch();
+  timing_mark(CTR_KERNEL_GATHER_ROWS, false, (cudaStream_t)stream);
   return launch_status();
 }

@@ -266,19 +266,14 @@ using namespace ctr;
 
 extern "C" size_t ctr_interaction_workspace_size(void) { return kWsHeader; }
 
-extern "C" int ctr_dot_interaction(const void* X, ctr_dtype dtype, int32_t batch, int32_t n, int32_t d, void* out,
-                                   void* ws, size_t ws_bytes, ctr_stream_t stream) {
-  cudaStream_t s = (cudaStream_t)stream;
-  if (!X || !out || batch < 0 || n < 1 || d < 1) return CTR_ERR_INVALID_ARG;
-  if (dtype != CTR_F32 && dtype != CTR_BF16) return CTR_ERR_INVALID_ARG;
-  if (!ws_valid(ws, ws_bytes, kWsHeader)) return CTR_ERR_WORKSPACE;
-  if (batch == 0) return CTR_OK;
+namespace {
+
+int dot_interaction_launch(const void* X, ctr_dtype dtype, int32_t batch, int32_t n, int32_t d, void* out, void* ws,
+                           cudaStream_t s) {
   if (dtype == CTR_F32 && n == 27 && d == 128 && (uintptr_t)X % 16 == 0) {
     auto k = interaction_fwd_f32_regs<27, 128>;
-    timing_mark(CTR_KERNEL_INTERACTION, true, s);
     k<<<grid_blocks(k, kIntWarps * 32, 0, ceil_div(batch, kIntWarps)), kIntWarps * 32, 0, s>>>(
         (const float*)X, batch, (float*)out); count_launch();
-    timing_mark(CTR_KERNEL_INTERACTION, false, s);
     return launch_status();
   }
   if (dtype == CTR_BF16 && interaction_bf16_tc_supported(n, d) && (uintptr_t)X % 16 == 0 &&
@@ -297,17 +292,11 @@ extern "C" int ctr_dot_interaction(const void* X, ctr_dtype dtype, int32_t batch
   return launch_status();
 }
 
-extern "C" int ctr_dot_interaction_bwd(const float* dout, const float* X, int32_t batch, int32_t n, int32_t d,
-                                       float* dX, void* ws, size_t ws_bytes, ctr_stream_t stream) {
-  cudaStream_t s = (cudaStream_t)stream;
-  if (!dout || !X || !dX || batch < 0 || n < 1 || d < 1) return CTR_ERR_INVALID_ARG;
-  if (!ws_valid(ws, ws_bytes, kWsHeader)) return CTR_ERR_WORKSPACE;
-  if (batch == 0) return CTR_OK;
+int dot_interaction_bwd_launch(const float* dout, const float* X, int32_t batch, int32_t n, int32_t d, float* dX,
+                               cudaStream_t s) {
   if (n == 27 && d == 128 && (uintptr_t)X % 16 == 0 && (uintptr_t)dX % 16 == 0) {
     auto k = interaction_bwd_f32_regs<27, 128>;
-    timing_mark(CTR_KERNEL_INTERACTION_BWD, true, s);
     k<<<grid_blocks(k, kIntWarps * 32, 0, ceil_div(batch, kIntWarps)), kIntWarps * 32, 0, s>>>(dout, X, batch, dX); count_launch();
-    timing_mark(CTR_KERNEL_INTERACTION_BWD, false, s);
     return launch_status();
   }
   const size_t smem = ((size_t)n * d + (size_t)n * (n - 1) / 2) * sizeof(float);
@@ -315,4 +304,31 @@ extern "C" int ctr_dot_interaction_bwd(const float* dout, const float* X, int32_
   auto k = interaction_bwd_generic;
   k<<<grid_blocks(k, kGenThreads, smem, batch), kGenThreads, smem, s>>>(dout, X, batch, n, d, dX); count_launch();
   return launch_status();
+}
+
+}  // namespace
+
+extern "C" int ctr_dot_interaction(const void* X, ctr_dtype dtype, int32_t batch, int32_t n, int32_t d, void* out,
+                                   void* ws, size_t ws_bytes, ctr_stream_t stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!X || !out || batch < 0 || n < 1 || d < 1) return CTR_ERR_INVALID_ARG;
+  if (dtype != CTR_F32 && dtype != CTR_BF16) return CTR_ERR_INVALID_ARG;
+  if (!ws_valid(ws, ws_bytes, kWsHeader)) return CTR_ERR_WORKSPACE;
+  if (batch == 0) return CTR_OK;
+  timing_mark(CTR_KERNEL_INTERACTION, true, s);
+  const int st = dot_interaction_launch(X, dtype, batch, n, d, out, ws, s);
+  timing_mark(CTR_KERNEL_INTERACTION, false, s);
+  return st;
+}
+
+extern "C" int ctr_dot_interaction_bwd(const float* dout, const float* X, int32_t batch, int32_t n, int32_t d,
+                                       float* dX, void* ws, size_t ws_bytes, ctr_stream_t stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!dout || !X || !dX || batch < 0 || n < 1 || d < 1) return CTR_ERR_INVALID_ARG;
+  if (!ws_valid(ws, ws_bytes, kWsHeader)) return CTR_ERR_WORKSPACE;
+  if (batch == 0) return CTR_OK;
+  timing_mark(CTR_KERNEL_INTERACTION_BWD, true, s);
+  const int st = dot_interaction_bwd_launch(dout, X, batch, n, d, dX, s);
+  timing_mark(CTR_KERNEL_INTERACTION_BWD, false, s);
+  return st;
 }

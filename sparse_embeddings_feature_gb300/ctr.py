@@ -112,8 +112,8 @@ def _dev(t: torch.Tensor, what: str) -> torch.Tensor:
     return t
 
 
-KERNEL_GATHER, KERNEL_BWD_TILES, KERNEL_BWD_PIECES, KERNEL_SORT, KERNEL_INTERACTION, KERNEL_INTERACTION_BWD = \
-    1, 2, 3, 4, 5, 6
+KERNEL_GATHER, KERNEL_BWD_TILES, KERNEL_BWD_PIECES, KERNEL_SORT, KERNEL_INTERACTION, KERNEL_INTERACTION_BWD, \
+    KERNEL_GATHER_ROWS = 1, 2, 3, 4, 5, 6, 7
 
 
 def ctr_set_timing_events(kernel: int, before=None, after=None) -> None:
