@@ -364,41 +364,28 @@ def run_ours(args, rank, world):
     ms = total_ms / args.steps
     ms = max_over_ranks(ms, world, "cuda")
 
-    # end to end through the C-ABI with host buffers: H2D of the step's inputs
-    # from pinned memory, the step, D2H of its output, all inside the timed region
+    # end to end from host buffers through the package's HostPipeline (the same C-ABI
+    # calls, with double-buffered inputs): every step's H2D of its inputs from pinned
+    # memory and D2H of its output are inside the timed region, overlapped with the
+    # neighbouring steps' kernels
     e2e = None
     if not args.no_e2e:
         host = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in w.items()
                 if k in ("ids", "offsets", "dense", "dout", "grad_pooled")}
         if cfg.dtype == "bf16":
             host["dense"] = host["dense"].view(torch.int16).view(torch.bfloat16)
+        from sparse_embeddings_feature_gb300.pipeline import HostPipeline
+        pipe = HostPipeline(path)
         result = path.out if path.out is not None else path.pooled
-        out_host = torch.empty(result.shape, dtype=result.dtype).pin_memory()
-        dense_dev = torch.empty(host["dense"].shape, dtype=host["dense"].dtype, device="cuda")
+        outs = [torch.empty(result.shape, dtype=result.dtype).pin_memory() for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = out_host.numel() * out_host.element_size()
-
-        def e2e_step():
-            path.ids[:n_ids].copy_(host["ids"], non_blocking=True)
-            path.offsets.copy_(host["offsets"], non_blocking=True)
-            dense_dev.copy_(host["dense"], non_blocking=True)
-            path.X[:, 0, :].copy_(dense_dev, non_blocking=True)
-            if path.dout is not None:
-                path.dout.copy_(host["dout"], non_blocking=True)
-            if path.grad_pooled is not None:
-                path.grad_pooled.copy_(host["grad_pooled"], non_blocking=True)
-            path.step()
-            out_host.copy_(result, non_blocking=True)
-
-        for _ in range(2):
-            e2e_step()
+        d2h = outs[0].numel() * outs[0].element_size()
+        pipe.run([host] * 2, outs)
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         barrier()
-        a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        pipe.run([host] * args.steps, [outs[k & 1] for k in range(args.steps)], start_event=a)
         b.record(stream)
         torch.cuda.synchronize()
         barrier()

@@ -151,3 +151,97 @@ class CtrPath:
             self.interaction_bwd()
         if cfg.backward != "none":
             self.bwd_update()
+
+
+class HostPipeline:
+    """Runs CtrPath steps over batches held in pinned host memory, with the copies overlapped.
+
+    Two device buffer sets hold the per-batch inputs (IDs, offsets, dense
+    vectors, upstream gradient) and the step's output.  While step k runs on
+    the compute stream, the inputs of step k+1 are copied in on one copy stream
+    and the output of step k-1 is copied out on another, so the host<->device
+    transfers hide behind the kernels.  Every batch's inputs and every step's
+    output still cross the host boundary, in full, once per step.
+
+    A batch is a dict with pinned CPU tensors "ids" (int64), "offsets" (int64,
+    [F*B+1]), "dense" ([B, d], the table dtype), and "dout" ([B, width] fp32) or
+    "grad_pooled" ([B, F, d] fp32) when the workload has a backward.  Outputs are
+    pinned CPU tensors shaped like the step's result (the interaction output, or
+    the pooled vectors for workloads without one).
+    """
+
+    def __init__(self, path: CtrPath):
+        self.path = path
+        cfg = path.cfg
+        self.result_name = "out" if path.out is not None else "pooled"
+        names = ["ids", "offsets"] + [k for k in ("dout", "grad_pooled") if getattr(path, k) is not None]
+        self.sets = []
+        for s in range(2):
+            bufs = {k: (getattr(path, k) if s == 0 else torch.empty_like(getattr(path, k))) for k in names}
+            bufs["dense"] = torch.empty((cfg.batch, cfg.d), dtype=path.X.dtype, device=path.dev)
+            res = getattr(path, self.result_name)
+            bufs["result"] = res if s == 0 else torch.empty_like(res)
+            self.sets.append(bufs)
+        self.names = names
+        self.compute = torch.cuda.current_stream(path.dev)
+        self.h2d = torch.cuda.Stream(path.dev)
+        self.d2h = torch.cuda.Stream(path.dev)
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_done = [torch.cuda.Event() for _ in range(2)]
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]
+        for s in range(2):   # create the events in a completed state
+            self.ev_done[s].record(self.compute)
+            self.ev_out[s].record(self.compute)
+
+    def _copy_in(self, batch, s):
+        bufs = self.sets[s]
+        with torch.cuda.stream(self.h2d):
+            self.h2d.wait_event(self.ev_done[s])            # the step that last read set s has finished
+            n = batch["ids"].numel()
+            bufs["ids"][:n].copy_(batch["ids"], non_blocking=True)
+            bufs["offsets"].copy_(batch["offsets"], non_blocking=True)
+            bufs["dense"].copy_(batch["dense"], non_blocking=True)
+            for k in ("dout", "grad_pooled"):
+                if k in bufs:
+                    bufs[k].copy_(batch[k], non_blocking=True)
+            self.ev_in[s].record(self.h2d)
+
+    def run(self, batches, outputs, start_event=None) -> None:
+        """Step over `batches`, writing step k's result into `outputs[k]` (both pinned host memory).
+
+        The call returns once everything is queued; the compute stream waits for
+        the last output copy, so an event recorded on it afterwards (or a
+        synchronize) covers the whole run.  `start_event`, if given, is recorded
+        on the compute stream before the first copy.
+        """
+        path = self.path
+        K = len(batches)
+        if K == 0:
+            return
+        if start_event is not None:
+            start_event.record(self.compute)
+        self.h2d.wait_stream(self.compute)
+        self._copy_in(batches[0], 0)
+        for k in range(K):
+            s = k & 1
+            bufs = self.sets[s]
+            n = batches[k]["ids"].numel()
+            if n > path.ids.numel():
+                raise ValueError(f"batch {k} has {n} IDs, more than the path's capacity {path.ids.numel()}")
+            self.compute.wait_event(self.ev_in[s])
+            self.compute.wait_event(self.ev_out[s])         # the previous output in this set has been copied out
+            path.n_ids = n
+            for name in self.names:
+                setattr(path, name, bufs[name])
+            setattr(path, self.result_name, bufs["result"])
+            path.X[:, 0, :].copy_(bufs["dense"], non_blocking=True)
+            path.step()
+            self.ev_done[s].record(self.compute)
+            if k + 1 < K:
+                self._copy_in(batches[k + 1], (k + 1) & 1)
+            with torch.cuda.stream(self.d2h):
+                self.d2h.wait_event(self.ev_done[s])
+                outputs[k].copy_(bufs["result"], non_blocking=True)
+                self.ev_out[s].record(self.d2h)
+        self.compute.wait_event(self.ev_out[(K - 1) & 1])
+        self.compute.wait_event(self.ev_out[K & 1])

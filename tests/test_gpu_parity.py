@@ -515,3 +515,40 @@ def test_launch_counter_counts_each_step_alike():
     # interaction, interaction backward, and the backward's clear + tiles + pieces + combine
     assert c1 - c0 >= 14
     assert c2 - c1 == c1 - c0
+
+
+def test_host_pipeline_matches_sequential_steps():
+    # three different batches through the overlapped host pipeline give the same
+    # outputs and the same updated table, bit for bit, as plain sequential steps
+    from sparse_embeddings_feature_gb300.pipeline import HostPipeline
+    base = W.CONFIGS["full_step"].shrink(batch=96, rows_per_table=tuple([4_000] * 26))
+    ws_ = [W.make_workload(base.shrink(seed=s)) for s in (11, 12, 13)]
+    cap = max(w["ids"].size for w in ws_)
+
+    def pinned(w):
+        return {k: torch.from_numpy(np.ascontiguousarray(w[k])).pin_memory() for k in ("ids", "offsets", "dense", "dout")}
+
+    seq = CtrPath(base, cap)
+    seq_out = []
+    for w in ws_:
+        n = w["ids"].size
+        seq.n_ids = n
+        seq.ids[:n].copy_(torch.from_numpy(w["ids"]))
+        seq.offsets.copy_(torch.from_numpy(w["offsets"]))
+        seq.X[:, 0, :].copy_(torch.from_numpy(w["dense"]))
+        seq.dout.copy_(torch.from_numpy(w["dout"]))
+        seq.reset_status()
+        seq.step()
+        seq_out.append(_np(seq.out).copy())
+        assert all(v == 0 for v in seq.check_status().values())
+
+    pip = CtrPath(base, cap)
+    pipe = HostPipeline(pip)
+    outs = [torch.empty(tuple(pip.out.shape), dtype=torch.float32).pin_memory() for _ in ws_]
+    pip.reset_status()
+    pipe.run([pinned(w) for w in ws_], outs)
+    torch.cuda.synchronize()
+    assert all(v == 0 for v in pip.check_status().values())
+    for k in range(len(ws_)):
+        np.testing.assert_array_equal(outs[k].numpy(), seq_out[k])
+    np.testing.assert_array_equal(_np(pip.table), _np(seq.table))
