@@ -148,9 +148,14 @@ int ctr_fill_table(void* table, ctr_dtype dtype, int64_t rows, int32_t d, int64_
  *                                       run_offsets[u+1]-1; run_offsets[n_unique] = n_ids
  *   unique_offsets int64 [T + 1]        uniques of table t are unique_rows[unique_offsets[t] ..
  *                                       unique_offsets[t+1]); unique_offsets[T] = n_unique
+ * sorted_pos is the costliest output: when it is NULL (and total_rows <= 64 *
+ * n_ids, when the ranks come from a presence bitmap over the table rows) the
+ * sort carries bags instead of positions and writes sorted_bag directly.
  * Device errors: CTR_ERR_INDEX_OUT_OF_RANGE (an ID outside its table; its key
- * is then replaced by the last row of its table), CTR_ERR_BAD_OFFSETS.
- * Workspace: ctr_dedup_workspace_size(n_ids, F, B, total_rows) bytes. */
+ * is then replaced by the last row of its table), CTR_ERR_BAD_OFFSETS,
+ * CTR_ERR_TIMEOUT (a radix pass waited over 1 s on an earlier tile).
+ * Workspace: ctr_dedup_workspace_size(n_ids, F, B, total_rows) bytes; it
+ * grows with total_rows / 8 on the bitmap path. */
 size_t ctr_dedup_workspace_size(int64_t n_ids, int32_t num_fields, int32_t batch, int64_t total_rows);
 int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num_fields, int32_t batch,
               const int32_t* bag_to_table, const int64_t* row_base, int32_t num_tables, int64_t n_ids,

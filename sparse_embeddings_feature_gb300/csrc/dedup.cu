@@ -4,19 +4,29 @@
 // Core Optimizations, embedding_lookup: collect the batch's IDs, sort them and
 // give each distinct ID a continuous index.
 //
-// GPU design (sm_103a, one GPU):
-//   keygen     warp per bag: key = row_base[table(f)] + id (32-bit global row),
-//              bag id per position; IDs outside their table are flagged.
-//   LSD radix  ceil(bits(total_rows) / 8) passes of <= 8 bits.  Each pass is
-//              reduce-then-scan: per-tile digit histograms (digit-major), one
-//              device-wide exclusive scan over them, then a stable scatter.
-//              Stable ranking inside a tile uses __match_any_sync per 32 keys
-//              and per-warp digit counters; the tile is reordered in shared
-//              memory first so the global writes are coalesced runs.  No
-//              block waits on another block.
-//   unique     head flags, per-tile head counts, exclusive scan, then ranks:
+// GPU design (sm_103a, one GPU).  Keys are 32-bit global rows
+// (row_base[table(f)] + id).  Two paths, chosen from the sizes alone:
+//
+// Presence bitmap (total_rows <= 64 * n_ids, the common case):
+//   mark       warp per bag: set bit key of a bitmap over all table rows
+//              (L2-resident: 26 MB for 208M rows).
+//   prefix     set bits per 1024-word block, a scan, then per word its bits
+//              and the count of set bits before it; the unique rows are the
+//              set bits in order, n_unique the total.
+//   rank       warp per bag again: rank(key) = prefix(word) + popc(bits below),
+//              which is the inverse map (written in ID order); sort keys =
+//              ranks, values = bags (or positions when the caller wants the
+//              permutation), digit histograms of every pass.
+//   sort       LSD radix passes over the ranks only: ceil(bits(n_unique) / 8)
+//              passes, planned on the device (24-bit ranks: 3 passes).
+//   runs       ranks are dense, so the first slot holding rank r starts run r.
+// Sorted keys (larger tables than the batch can fill):
+//   keygen     warp per bag: keys, bag of each position, digit histograms.
+//   sort       ceil(bits(total_rows) / 8) passes over the keys.
+//   unique     head flags, per-tile head counts, a scan, then ranks:
 //              unique_rows, run_offsets, inverse (scatter), sorted_bag
 //              (gather of the bag of each sorted position), unique_offsets.
+// Each radix pass is one kernel (Onesweep-style decoupled look-back, below).
 #include <algorithm>
 
 #include "common.cuh"
@@ -126,8 +136,15 @@ constexpr uint64_t kLookbackLimitNs = 1000000000ull;  // 1 s
 // the positions 0..n-1 (first pass).
 __global__ void __launch_bounds__(kRsThreads) onesweep_kernel(
     const uint32_t* __restrict__ keys_in, const int32_t* __restrict__ vals_in, uint32_t* __restrict__ keys_out,
-    int32_t* __restrict__ vals_out, int64_t n, int shift, int nbits, const uint32_t* __restrict__ g_hist,
-    uint64_t* __restrict__ lookback, uint32_t* __restrict__ tile_counter, int* err) {
+    int32_t* __restrict__ vals_out, int64_t n, int shift, int nbits, const PassPlan* __restrict__ dplan, int pass,
+    int32_t* __restrict__ vals_final, const uint32_t* __restrict__ g_hist, uint64_t* __restrict__ lookback,
+    uint32_t* __restrict__ tile_counter, int* err) {
+  if (dplan) {  // digit plan decided on the device (rank keys): passes beyond it do nothing
+    if (pass >= dplan->passes) return;
+    shift = dplan->shift[pass];
+    nbits = dplan->bits[pass];
+    if (pass == dplan->passes - 1 && vals_final) vals_out = vals_final;
+  }
   __shared__ uint32_t wcnt[kRsWarps][kMaxDigits];
   __shared__ uint32_t tile_start[kMaxDigits];
   __shared__ uint32_t glob_start[kMaxDigits];
@@ -378,6 +395,290 @@ __global__ void __launch_bounds__(kRsThreads) unique_write_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// Presence-bitmap path (tables not much larger than the batch): the rank of a
+// key among the batch's distinct keys is the number of set bits below it in a
+// bitmap over all table rows, so the inverse map and the unique rows come from
+// the bitmap directly; the radix sort only groups the occurrences by rank
+// (ceil(bits(n_unique) / 8) passes instead of ceil(bits(total_rows) / 8)) and
+// carries each occurrence's bag, so the grouped bags come out of its last pass.
+// ---------------------------------------------------------------------------
+constexpr int64_t kBitmapRowsPerId = 64;  // bitmap path iff total_rows <= 64 * n_ids
+constexpr int kBmWords = 1024;            // bitmap words per prefix block (4 per thread)
+
+// Flat walk over the IDs: a warp takes 32 consecutive bags and its lanes take
+// their IDs 32 at a time (every lane busy whatever the bag lengths); a lane
+// finds its bag by a shuffle binary search over the lanes' bag starts.  Calls
+// f(i, key, bag) for every ID, with the key generator's validation and
+// clamping.  A block of bags with inconsistent offsets is flagged and skipped.
+template <typename Fn>
+__device__ __forceinline__ void for_each_key_flat(const int64_t* __restrict__ ids,
+                                                  const int64_t* __restrict__ offsets, int32_t F, int32_t B,
+                                                  int64_t n_ids, const FieldMap& fm, int* err, Fn f) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nbags = (int64_t)F * B;
+  const int64_t nblk = ceil_div(nbags, (int64_t)32);
+  const int64_t end_all = offsets[nbags];
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t blk = warp0; blk < nblk; blk += nwarps) {
+    const int64_t bag = blk * 32 + lane;
+    const bool bvalid = bag < nbags;
+    const int64_t o0 = bvalid ? offsets[bag] : end_all;
+    const int64_t o1 = bvalid ? offsets[bag + 1] : end_all;
+    const bool bad = o0 < 0 || o1 < o0 || o1 > n_ids;
+    const int64_t S0 = __shfl_sync(kFull, o0, 0);
+    const int64_t S1 = __shfl_sync(kFull, o1, 31);
+    if (__any_sync(kFull, bad) || S1 < S0 || S1 - S0 >= ((int64_t)1 << 30)) {
+      if (lane == 0) set_error(err, CTR_ERR_BAD_OFFSETS);
+      continue;
+    }
+    const int rel0 = (int)(o0 - S0);
+    const int total = (int)(S1 - S0);
+    const int fld = bvalid ? (int)(bag / B) : 0;  // this lane's bag's field, once per block
+    const uint32_t base_l = (uint32_t)fm.base[fld];
+    const uint32_t rows_l = (uint32_t)fm.rows[fld];
+    for (int c0 = 0; c0 < total; c0 += 32) {
+      const int kr = c0 + lane;
+      int seg = 0;
+#pragma unroll
+      for (int step = 16; step > 0; step >>= 1) {  // largest lane j with rel0_j <= kr
+        const int cand = seg + step;
+        if (__shfl_sync(kFull, rel0, cand) <= kr) seg = cand;
+      }
+      const uint32_t base = __shfl_sync(kFull, base_l, seg);
+      const uint32_t rows = __shfl_sync(kFull, rows_l, seg);
+      if (kr < total) {
+        const int64_t i = S0 + kr;
+        int64_t id = ids[i];
+        bool ok = true;
+        if (id < 0 || id >= (int64_t)rows) {
+          set_error(err, CTR_ERR_INDEX_OUT_OF_RANGE);
+          id = (int64_t)rows - 1;
+          ok = rows > 0;  // an ID of an empty table has no row to stand in for it
+        }
+        if (ok) f(i, base + (uint32_t)id, blk * 32 + seg);
+      }
+    }
+  }
+}
+
+// Keys (32-bit global rows), the sort's first values, and the presence bitmap.
+// A key whose bit is already visible in L2 is not set again, so the hot rows
+// of a skewed batch cost loads, not atomics.
+__global__ void __launch_bounds__(256) bitmap_keys_kernel(const int64_t* __restrict__ ids,
+                                                          const int64_t* __restrict__ offsets, int32_t F, int32_t B,
+                                                          int64_t n_ids, const __grid_constant__ FieldMap fm,
+                                                          uint32_t* __restrict__ keys, int32_t* __restrict__ vals,
+                                                          int vals_are_pos, int32_t* __restrict__ bag_of,
+                                                          uint32_t* __restrict__ bitmap, int* err) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (offsets[0] != 0 || offsets[(int64_t)F * B] != n_ids) set_error(err, CTR_ERR_BAD_OFFSETS);
+  }
+  for_each_key_flat(ids, offsets, F, B, n_ids, fm, err, [&](int64_t i, uint32_t k, int64_t bag) {
+    keys[i] = k;
+    vals[i] = vals_are_pos ? (int32_t)i : (int32_t)bag;
+    if (bag_of) bag_of[i] = (int32_t)bag;
+    uint32_t* wp = bitmap + (k >> 5);
+    const uint32_t bit = 1u << (k & 31);
+    if (!(__ldcg(wp) & bit)) atomicOr(wp, bit);
+  });
+}
+
+// Set bits per block of kBmWords words.
+__global__ void __launch_bounds__(256) bitmap_count_kernel(const uint32_t* __restrict__ bitmap, int64_t W,
+                                                           uint32_t* __restrict__ bsum) {
+  __shared__ uint32_t warp_tot[8];
+  const int64_t w0 = (int64_t)blockIdx.x * kBmWords;
+  uint32_t c = 0;
+#pragma unroll
+  for (int j = 0; j < kBmWords / 256; ++j) {
+    const int64_t w = w0 + j * 256 + threadIdx.x;
+    if (w < W) c += __popc(bitmap[w]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+  if ((threadIdx.x & 31) == 0) warp_tot[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t t = 0;
+    for (int q = 0; q < 8; ++q) t += warp_tot[q];
+    bsum[blockIdx.x] = t;
+  }
+}
+
+// pk[w] = (bits of word w, set bits in all earlier words); the unique rows are
+// the set bits in order.
+__global__ void __launch_bounds__(256) bitmap_pack_kernel(const uint32_t* __restrict__ bitmap, int64_t W,
+                                                          const uint32_t* __restrict__ bscan,
+                                                          uint2* __restrict__ pk, int64_t* __restrict__ unique_rows) {
+  __shared__ uint32_t warp_tot[8];
+  constexpr int kPer = kBmWords / 256;
+  const int64_t w0 = (int64_t)blockIdx.x * kBmWords + threadIdx.x * kPer;
+  uint32_t b[kPer], v[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    b[j] = (w0 + j < W) ? bitmap[w0 + j] : 0u;
+    v[j] = __popc(b[j]);
+  }
+  block_exclusive_scan<uint32_t, 256, kPer>(v, warp_tot);
+  const uint32_t base = bscan[blockIdx.x];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int64_t w = w0 + j;
+    if (w >= W) break;
+    uint32_t r = base + v[j];
+    pk[w] = make_uint2(b[j], r);
+    for (uint32_t bits = b[j]; bits; bits &= bits - 1) unique_rows[r++] = w * 32 + (__ffs(bits) - 1);
+  }
+}
+
+__device__ __forceinline__ uint32_t bitmap_rank(const uint2* __restrict__ pk, uint32_t k) {
+  const uint2 e = pk[k >> 5];
+  return e.y + __popc(e.x & ((1u << (k & 31)) - 1u));
+}
+
+// n_unique, the digit plan of the rank keys, and the per-table unique offsets.
+__global__ void bitmap_plan_kernel(const uint32_t* __restrict__ total, int64_t* __restrict__ n_unique,
+                                   const __grid_constant__ TableBases tb, int64_t total_rows,
+                                   const uint2* __restrict__ pk, int64_t* __restrict__ unique_offsets,
+                                   PassPlan* __restrict__ plan) {
+  const uint32_t nu = *total;
+  if (threadIdx.x == 0) {
+    *n_unique = nu;
+    int bits = 1;
+    while (bits < 32 && (1ull << bits) < (unsigned long long)nu) ++bits;
+    const int passes = (bits + kMaxBits - 1) / kMaxBits;
+    const int nb = (bits + passes - 1) / passes;
+    PassPlan p;
+    p.passes = passes;
+    for (int q = 0, sh = 0; q < kMaxPasses; ++q) {
+      const int pb = q < passes ? (nb < bits - sh ? nb : bits - sh) : 0;
+      p.shift[q] = sh;
+      p.bits[q] = pb;
+      sh += pb;
+    }
+    *plan = p;
+  }
+  if (unique_offsets)
+    for (int t = threadIdx.x; t <= tb.num_tables; t += blockDim.x) {
+      const int64_t k = tb.row_base[t];
+      unique_offsets[t] = k >= total_rows ? (int64_t)nu : (int64_t)bitmap_rank(pk, (uint32_t)k);
+    }
+}
+
+// Rank of every key among the distinct keys (the inverse map, which is also
+// the sort's first keys) and the digit histograms of every pass of the device
+// plan (per-warp shared histograms, then one global add per block and digit).
+// A key outside the tables (a slot an invalid bag left unwritten) is flagged
+// and ranked 0.
+__device__ __forceinline__ void hist_add(uint32_t (*h)[kMaxDigits], const PassPlan& plan, uint32_t r) {
+#pragma unroll
+  for (int p = 0; p < kMaxPasses; ++p)
+    if (p < plan.passes) atomicAdd(&h[p][(r >> plan.shift[p]) & ((1u << plan.bits[p]) - 1)], 1u);
+}
+
+__device__ __forceinline__ uint32_t rank_or_flag(const uint2* __restrict__ pk, uint32_t k, int64_t total_rows,
+                                                 int* err) {
+  if ((int64_t)k < total_rows) return bitmap_rank(pk, k);
+  set_error(err, CTR_ERR_BAD_OFFSETS);
+  return 0u;
+}
+
+// Four consecutive keys per thread (one 16-byte load and store, four bitmap
+// lookups in flight); `vec` says both arrays are 16-byte aligned.
+__global__ void __launch_bounds__(256) bitmap_rank_kernel(const uint32_t* __restrict__ keys, int64_t n,
+                                                          int64_t total_rows, const uint2* __restrict__ pk,
+                                                          const PassPlan* __restrict__ dplan,
+                                                          uint32_t* __restrict__ ranks, int vec,
+                                                          uint32_t* __restrict__ g_hist, int* err) {
+  constexpr int kWarps = 256 / 32;
+  __shared__ uint32_t sh[kWarps][kMaxPasses][kMaxDigits];
+  for (int i = threadIdx.x; i < kWarps * kMaxPasses * kMaxDigits; i += blockDim.x) (&sh[0][0][0])[i] = 0;
+  __syncthreads();
+  const PassPlan plan = *dplan;
+  uint32_t (*h)[kMaxDigits] = sh[threadIdx.x >> 5];
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  int64_t done = 0;
+  if (vec) {
+    const int64_t n4 = n / 4;
+    for (int64_t q = t0; q < n4; q += stride) {
+      const uint4 k = ((const uint4*)keys)[q];
+      uint4 r;
+      r.x = rank_or_flag(pk, k.x, total_rows, err);
+      r.y = rank_or_flag(pk, k.y, total_rows, err);
+      r.z = rank_or_flag(pk, k.z, total_rows, err);
+      r.w = rank_or_flag(pk, k.w, total_rows, err);
+      ((uint4*)ranks)[q] = r;
+      hist_add(h, plan, r.x);
+      hist_add(h, plan, r.y);
+      hist_add(h, plan, r.z);
+      hist_add(h, plan, r.w);
+    }
+    done = n4 * 4;
+  }
+  for (int64_t i = done + t0; i < n; i += stride) {
+    const uint32_t r = rank_or_flag(pk, keys[i], total_rows, err);
+    ranks[i] = r;
+    hist_add(h, plan, r);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < plan.passes * kMaxDigits; i += blockDim.x) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) c += (&sh[w][0][0])[i];
+    if (c) atomicAdd(&g_hist[i], c);
+  }
+}
+
+// Run starts from the sorted ranks (ranks are dense, so the first slot of rank
+// r starts run r), and the bag of each sorted position when the sort carried
+// positions.
+__device__ __forceinline__ void run_slot(const uint32_t* __restrict__ keys, int64_t p, uint32_t k, uint32_t prev,
+                                         int64_t n, int64_t nu, int32_t* __restrict__ run_offsets,
+                                         const int32_t* __restrict__ sorted_pos, const int32_t* __restrict__ bag_of,
+                                         int32_t* __restrict__ sorted_bag, int* err) {
+  if ((int64_t)k >= nu) {  // only after an error that left slots unwritten
+    set_error(err, CTR_ERR_BAD_OFFSETS);
+    return;
+  }
+  if (run_offsets) {
+    if (p == 0 || prev != k) run_offsets[k] = (int32_t)p;
+    if (p == n - 1) run_offsets[nu] = (int32_t)n;
+  }
+  if (sorted_bag) {
+    const int32_t q = sorted_pos[p];
+    sorted_bag[p] = (q >= 0 && q < n) ? bag_of[q] : -1;
+  }
+}
+
+// Four consecutive sorted slots per thread (one 16-byte load of their ranks).
+__global__ void __launch_bounds__(256) runs_kernel(const uint32_t* __restrict__ keys0,
+                                                   const uint32_t* __restrict__ keys1,
+                                                   const PassPlan* __restrict__ dplan, int64_t n,
+                                                   const int64_t* __restrict__ n_unique,
+                                                   int32_t* __restrict__ run_offsets,
+                                                   const int32_t* __restrict__ sorted_pos,
+                                                   const int32_t* __restrict__ bag_of,
+                                                   int32_t* __restrict__ sorted_bag, int* err) {
+  const uint32_t* keys = (dplan->passes & 1) ? keys1 : keys0;  // pass p writes buffer (p + 1) & 1
+  const int64_t nu = *n_unique;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t n4 = n / 4;
+  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n4; q += stride) {
+    const uint4 k = ((const uint4*)keys)[q];
+    const int64_t p = q * 4;
+    const uint32_t prev = p > 0 ? keys[p - 1] : 0u;
+    run_slot(keys, p, k.x, prev, n, nu, run_offsets, sorted_pos, bag_of, sorted_bag, err);
+    run_slot(keys, p + 1, k.y, k.x, n, nu, run_offsets, sorted_pos, bag_of, sorted_bag, err);
+    run_slot(keys, p + 2, k.z, k.y, n, nu, run_offsets, sorted_pos, bag_of, sorted_bag, err);
+    run_slot(keys, p + 3, k.w, k.z, n, nu, run_offsets, sorted_pos, bag_of, sorted_bag, err);
+  }
+  for (int64_t p = n4 * 4 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < n; p += stride)
+    run_slot(keys, p, keys[p], p > 0 ? keys[p - 1] : 0u, n, nu, run_offsets, sorted_pos, bag_of, sorted_bag, err);
+}
+
 __global__ void dedup_empty_kernel(int64_t* n_unique, int32_t* run_offsets, int64_t* unique_offsets, int T) {
   *n_unique = 0;
   if (run_offsets) run_offsets[0] = 0;
@@ -397,12 +698,30 @@ int64_t state_words(int64_t tiles) {
   return (int64_t)kMaxPasses * tiles * kMaxDigits + (kMaxPasses * kMaxDigits) / 2 + kMaxPasses;
 }
 
+bool use_bitmap(int64_t n_ids, int64_t total_rows) { return total_rows <= kBitmapRowsPerId * n_ids; }
+
+int64_t bitmap_words(int64_t total_rows) { return ceil_div(total_rows, (int64_t)32); }
+
+// Workspace of each path (the path follows from the sizes alone).
 template <typename WS>
 void dedup_layout(WS& ws, int64_t n_ids, int64_t total_rows) {
   const int64_t tiles = ceil_div(n_ids, kRsTile);
-  const int bits = key_bits(total_rows);
-  const int passes = (bits + kMaxBits - 1) / kMaxBits;
-  const int nb = (bits + passes - 1) / passes;
+  if (use_bitmap(n_ids, total_rows)) {
+    const int64_t W = bitmap_words(total_rows);
+    const int64_t nblk = ceil_div(W, (int64_t)kBmWords);
+    ws.template take<uint32_t>((size_t)n_ids);  // keys A
+    ws.template take<uint32_t>((size_t)n_ids);  // keys B
+    ws.template take<int32_t>((size_t)n_ids);   // values A
+    ws.template take<int32_t>((size_t)n_ids);   // values B
+    ws.template take<int32_t>((size_t)n_ids);   // bag of each position (when positions are sorted)
+    ws.template take<uint64_t>((size_t)(state_words(tiles) + ceil_div(W, (int64_t)2)));  // sort state + bitmap
+    ws.template take<uint2>((size_t)W);         // bitmap words with their prefix counts
+    ws.template take<uint32_t>((size_t)nblk);   // set bits per block, then their exclusive scan
+    ws.template take<uint32_t>(1);              // n_unique
+    ws.template take<PassPlan>(1);
+    scan_reserve<uint32_t>(ws, nblk);
+    return;
+  }
   ws.template take<uint32_t>((size_t)n_ids);           // keys A
   ws.template take<uint32_t>((size_t)n_ids);           // keys B
   ws.template take<int32_t>((size_t)n_ids);            // values scratch
@@ -411,7 +730,87 @@ void dedup_layout(WS& ws, int64_t n_ids, int64_t total_rows) {
   ws.template take<uint64_t>((size_t)state_words(tiles));  // look-back words, histograms, tile counters
   ws.template take<uint32_t>((size_t)tiles);           // heads per tile
   scan_reserve<uint32_t>(ws, tiles);
-  (void)nb;
+}
+
+void clear_words(uint64_t* p, int64_t words, cudaStream_t s) {
+  const int64_t blocks = std::max<int64_t>(1, imin64(ceil_div(words, 256), (int64_t)num_sms() * 8));
+  clear_u64_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, words); count_launch();
+}
+
+int dedup_bitmap(const int64_t* ids, const int64_t* offsets, int32_t F, int32_t B, const FieldMap& fm,
+                 const TableBases& tb, int64_t total_rows, int64_t n_ids, int64_t* unique_rows, int64_t* n_unique,
+                 int32_t* inverse, int32_t* sorted_pos, int32_t* sorted_bag, int32_t* run_offsets,
+                 int64_t* unique_offsets, void* ws, size_t ws_bytes, cudaStream_t s) {
+  int* err = (int*)ws;
+  WsCarver c(ws, ws_bytes);
+  const int64_t tiles = ceil_div(n_ids, kRsTile);
+  const int64_t W = bitmap_words(total_rows);
+  const int64_t nblk = ceil_div(W, (int64_t)kBmWords);
+  uint32_t* keys[2] = {c.take<uint32_t>(n_ids), c.take<uint32_t>(n_ids)};
+  int32_t* vals[2] = {c.take<int32_t>(n_ids), c.take<int32_t>(n_ids)};
+  int32_t* bag_of = c.take<int32_t>(n_ids);
+  const int64_t sw = state_words(tiles);
+  uint64_t* state = c.take<uint64_t>((size_t)(sw + ceil_div(W, (int64_t)2)));
+  uint2* pk = c.take<uint2>((size_t)W);
+  uint32_t* bsum = c.take<uint32_t>((size_t)nblk);
+  uint32_t* total = c.take<uint32_t>(1);
+  PassPlan* dplan = c.take<PassPlan>(1);
+  if (!c.ok()) return CTR_ERR_WORKSPACE;
+  uint64_t* lookback = state;
+  uint32_t* g_hist = (uint32_t*)(state + (int64_t)kMaxPasses * tiles * kMaxDigits);
+  uint32_t* tile_counter = g_hist + kMaxPasses * kMaxDigits;
+  uint32_t* bitmap = (uint32_t*)(state + sw);
+  const int sms = num_sms();
+  const int64_t nbags = (int64_t)F * B;
+  const int64_t key_blocks = std::max<int64_t>(1, imin64(ceil_div(nbags, 8), (int64_t)sms * 16));
+
+  // the sort carries positions only when the caller asks for them; otherwise
+  // it carries bags, and its last pass writes the grouped bags in place
+  const bool pos = sorted_pos != nullptr;
+  clear_words(state, sw + ceil_div(W, (int64_t)2), s);
+  if (int st = launch_status()) return st;
+  bitmap_keys_kernel<<<(unsigned)key_blocks, 256, 0, s>>>(ids, offsets, F, B, n_ids, fm, keys[1], vals[0],
+                                                          pos ? 1 : 0, (pos && sorted_bag) ? bag_of : nullptr,
+                                                          bitmap, err); count_launch();
+  if (int st = launch_status()) return st;
+  bitmap_count_kernel<<<(unsigned)nblk, 256, 0, s>>>(bitmap, W, bsum); count_launch();
+  if (int st = launch_status()) return st;
+  {
+    WsCarver scan_ws = c;
+    if (int st = scan_exclusive<uint32_t>(bsum, bsum, nblk, nullptr, total, scan_ws, s)) return st;
+  }
+  bitmap_pack_kernel<<<(unsigned)nblk, 256, 0, s>>>(bitmap, W, bsum, pk, unique_rows); count_launch();
+  if (int st = launch_status()) return st;
+  bitmap_plan_kernel<<<1, 256, 0, s>>>(total, n_unique, tb, total_rows, pk, unique_offsets, dplan); count_launch();
+  if (int st = launch_status()) return st;
+  // ranks go straight into the caller's inverse map, which the first pass reads
+  uint32_t* ranks = inverse ? (uint32_t*)inverse : keys[0];
+  {
+    const int64_t blocks = std::max<int64_t>(1, imin64(ceil_div(n_ids, 1024), (int64_t)sms * 8));
+    const int vec = ((uintptr_t)ranks % 16) == 0;
+    bitmap_rank_kernel<<<(unsigned)blocks, 256, 0, s>>>(keys[1], n_ids, total_rows, pk, dplan, ranks, vec, g_hist,
+                                                        err);
+    count_launch();
+    if (int st = launch_status()) return st;
+  }
+  int32_t* vals_final = pos ? sorted_pos : sorted_bag;
+  const int max_passes = (key_bits(imin64(n_ids, total_rows)) + kMaxBits - 1) / kMaxBits;
+  timing_mark(CTR_KERNEL_SORT, true, s);
+  for (int p = 0; p < max_passes; ++p) {
+    onesweep_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(p == 0 ? ranks : keys[p & 1], vals[p & 1], keys[(p + 1) & 1],
+                                                           vals[(p + 1) & 1], n_ids, 0, 0, dplan, p, vals_final,
+                                                           g_hist + p * kMaxDigits,
+                                                           lookback + (int64_t)p * tiles * kMaxDigits,
+                                                           tile_counter + p, err); count_launch();
+    if (int st = launch_status()) return st;
+  }
+  timing_mark(CTR_KERNEL_SORT, false, s);
+  if (run_offsets || (pos && sorted_bag)) {
+    const int64_t blocks = std::max<int64_t>(1, imin64(ceil_div(n_ids, 1024), (int64_t)sms * 8));
+    runs_kernel<<<(unsigned)blocks, 256, 0, s>>>(keys[0], keys[1], dplan, n_ids, n_unique, run_offsets, sorted_pos,
+                                                 bag_of, pos ? sorted_bag : nullptr, err); count_launch();
+  }
+  return launch_status();
 }
 
 }  // namespace
@@ -462,6 +861,10 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
     return launch_status();
   }
 
+  if (use_bitmap(n_ids, total_rows))
+    return dedup_bitmap(ids, offsets, num_fields, batch, fm, tb, total_rows, n_ids, unique_rows, n_unique, inverse,
+                        sorted_pos, sorted_bag, run_offsets, unique_offsets, ws, ws_bytes, s);
+
   WsCarver c(ws, ws_bytes);
   const int64_t tiles = ceil_div(n_ids, kRsTile);
   const int bits = key_bits(total_rows);
@@ -488,8 +891,7 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
     sh += pb;
   }
   const int sms = num_sms();
-  clear_u64_kernel<<<(unsigned)std::max<int64_t>(1, imin64(ceil_div(state_words(tiles), 256), (int64_t)sms * 8)),
-                     256, 0, s>>>(state, state_words(tiles)); count_launch();
+  clear_words(state, state_words(tiles), s);
   if (int st = launch_status()) return st;
   const int64_t nbags = (int64_t)num_fields * batch;
   {
@@ -503,7 +905,8 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
   for (int p = 0; p < passes; ++p) {
     int32_t* vout = ((passes - 1 - p) % 2 == 0) ? vfinal : vscratch;
     onesweep_kernel<<<(unsigned)tiles, kRsThreads, 0, s>>>(keys[p & 1], vin, keys[(p + 1) & 1], vout, n_ids,
-                                                           plan.shift[p], plan.bits[p], g_hist + p * kMaxDigits,
+                                                           plan.shift[p], plan.bits[p], nullptr, p, nullptr,
+                                                           g_hist + p * kMaxDigits,
                                                            lookback + (int64_t)p * tiles * kMaxDigits,
                                                            tile_counter + p, err); count_launch();
     if (int st = launch_status()) return st;

@@ -25,7 +25,8 @@ TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
 class CtrPath:
-    def __init__(self, cfg: Config, n_ids: int, device="cuda", fill: bool = True, table_chunk_rows: int = 1 << 24):
+    def __init__(self, cfg: Config, n_ids: int, device="cuda", fill: bool = True, table_chunk_rows: int = 1 << 24,
+                 keep_sorted_pos: bool = False):
         self.cfg = cfg
         self.dev = torch.device(device)
         self.n_ids = int(n_ids)
@@ -41,7 +42,9 @@ class CtrPath:
         self.unique_rows = torch.empty(cap, dtype=i64, device=self.dev)
         self.n_unique = torch.zeros(1, dtype=i64, device=self.dev)
         self.inverse = torch.empty(cap, dtype=i32, device=self.dev)
-        self.sorted_pos = torch.empty(cap, dtype=i32, device=self.dev)
+        # the stable sort permutation is an optional output: without it the dedup's
+        # sort carries bags instead of positions and skips a gather
+        self.sorted_pos = torch.empty(cap, dtype=i32, device=self.dev) if keep_sorted_pos else None
         self.sorted_bag = torch.empty(cap, dtype=i32, device=self.dev)
         self.run_offsets = torch.empty(cap + 1, dtype=i32, device=self.dev)
         self.unique_offsets = torch.empty(cfg.num_tables + 1, dtype=i64, device=self.dev)

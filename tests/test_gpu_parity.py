@@ -48,12 +48,14 @@ def _csr(lens, rng, rows_of_field, B):
     return ids, offsets
 
 
-def gpu_dedup(ids, offsets, F, B, b2t, row_base):
+def gpu_dedup(ids, offsets, F, B, b2t, row_base, with_pos=True):
     n = int(offsets[-1])
     cap = max(n, 1)
     T = len(row_base) - 1
     dev = {k: torch.full((cap,), -7, dtype=torch.int32, device=DEV)
            for k in ("inverse", "sorted_pos", "sorted_bag")}
+    if not with_pos:
+        dev["sorted_pos"] = None
     uq = torch.full((cap,), -7, dtype=torch.int64, device=DEV)
     nu = torch.full((1,), -7, dtype=torch.int64, device=DEV)
     ro = torch.full((cap + 1,), -7, dtype=torch.int32, device=DEV)
@@ -65,14 +67,16 @@ def gpu_dedup(ids, offsets, F, B, b2t, row_base):
     st = ctr.ctr_check_status(ws)
     k = int(_np(nu)[0])
     return st, {"unique_rows": _np(uq)[:k], "n_unique": k, "inverse": _np(dev["inverse"])[:n],
-                "sorted_pos": _np(dev["sorted_pos"])[:n], "sorted_bag": _np(dev["sorted_bag"])[:n],
+                "sorted_pos": _np(dev["sorted_pos"])[:n] if with_pos else None,
+                "sorted_bag": _np(dev["sorted_bag"])[:n],
                 "run_offsets": _np(ro)[:k + 1], "unique_offsets": _np(uo)}
 
 
 def assert_dedup_equal(got, ref):
     assert got["n_unique"] == ref["n_unique"]
     for k in ("unique_rows", "inverse", "sorted_pos", "sorted_bag", "run_offsets", "unique_offsets"):
-        np.testing.assert_array_equal(got[k], ref[k], err_msg=k)
+        if got[k] is not None:
+            np.testing.assert_array_equal(got[k], ref[k], err_msg=k)
 
 
 # ---------------------------------------------------------------------------
@@ -108,9 +112,37 @@ def test_dedup_configs(name):
     cfg = DEDUP_CASES[name]
     w = W.make_workload(cfg, with_grads=False)
     args = (w["ids"], w["offsets"], cfg.num_fields, cfg.batch, w["bag_to_table"], w["row_base"])
-    st, got = gpu_dedup(*args)
-    assert st == 0, ctr.status_string(st)
-    assert_dedup_equal(got, O.dedup(*args))
+    ref = O.dedup(*args)
+    for with_pos in (True, False):
+        st, got = gpu_dedup(*args, with_pos=with_pos)
+        assert st == 0, ctr.status_string(st)
+        assert_dedup_equal(got, ref)
+
+
+# Tables at most 64x the batch's ID count take the presence-bitmap path (ranks
+# from a bitmap, a sort of the ranks); larger ones sort the keys themselves.
+# These cases put both paths, and rank keys of 24 and 25 bits (3 and 4 radix
+# passes), against the oracle.
+BITMAP_CASES = {
+    "tensornet_b4096": W.CONFIGS["tensornet"].shrink(batch=4096),
+    "uniform_b32768_25bit_ranks": W.CONFIGS["full_step"].shrink(batch=32768, ids=("uniform",)),
+    "full_step_b16384": W.CONFIGS["full_step"].shrink(batch=16384),
+}
+
+
+@pytest.mark.parametrize("name", list(BITMAP_CASES))
+def test_dedup_bitmap_path(name):
+    cfg = BITMAP_CASES[name]
+    w = W.make_workload(cfg, with_grads=False)
+    assert cfg.total_rows <= 64 * w["ids"].size           # the bitmap path
+    args = (w["ids"], w["offsets"], cfg.num_fields, cfg.batch, w["bag_to_table"], w["row_base"])
+    ref = O.dedup(*args)
+    if name.endswith("25bit_ranks"):
+        assert ref["n_unique"] > 1 << 24
+    for with_pos in (True, False):
+        st, got = gpu_dedup(*args, with_pos=with_pos)
+        assert st == 0, ctr.status_string(st)
+        assert_dedup_equal(got, ref)
 
 
 def test_dedup_edge_cases():
@@ -160,6 +192,14 @@ def test_dedup_flags_out_of_range_id():
     ids = np.array([0, 3, 5, 1], dtype=np.int64)      # 5 is outside a 5-row table
     offsets = np.array([0, 2, 4], dtype=np.int64)
     st, _ = gpu_dedup(ids, offsets, 1, 2, np.array([0], np.int32), np.array([0, 5], np.int64))
+    assert st == -4, ctr.status_string(st)
+
+
+def test_dedup_flags_id_of_empty_table():
+    # field 0 reads table 0, which has no rows: every such ID is out of range
+    ids = np.array([0, 1, 7, 3], dtype=np.int64)
+    offsets = np.array([0, 2, 4], dtype=np.int64)
+    st, _ = gpu_dedup(ids, offsets, 2, 1, np.array([0, 1], np.int32), np.array([0, 0, 10], np.int64))
     assert st == -4, ctr.status_string(st)
 
 
@@ -470,7 +510,7 @@ def test_full_step_composed_small():
     cfg = W.CONFIGS["full_step"].shrink(batch=192, rows_per_table=tuple([60_000] * 26))
     w = W.make_workload(cfg)
     F, B, d, n = cfg.num_fields, cfg.batch, cfg.d, cfg.n_vectors
-    path = CtrPath(cfg, w["ids"].size)
+    path = CtrPath(cfg, w["ids"].size, keep_sorted_pos=True)
     path.upload(w)
     path.reset_status()
     path.step()
