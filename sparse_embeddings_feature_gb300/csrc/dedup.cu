@@ -124,12 +124,11 @@ constexpr uint64_t kLookbackLimitNs = 1000000000ull;  // 1 s
 // One radix pass in one kernel (single-pass, after Adinets and Merrill's
 // Onesweep): a block takes the next tile in launch order, ranks its keys
 // stably (per 32 keys __match_any_sync groups equal digits; per-warp digit
-// counters order the warps), publishes its per-digit counts, and finds the
+// counters order the rows and warps), publishes its per-digit counts, and finds the
 // counts of all earlier tiles by decoupled look-back: a predecessor's word
 // holds either its own count or its inclusive prefix, so the walk stops at
 // the first inclusive prefix; each thread reads kLbWindow predecessors per
-// round trip.  Lanes holding equal digits are found with one ballot per digit
-// bit (votes, not the match unit).  Tiles are taken in order, so a block only
+// round trip.  Tiles are taken in order, so a block only
 // ever waits on blocks that started before it; each wait is bounded by a
 // wall-clock limit, after which the block records CTR_ERR_TIMEOUT and keeps
 // its writes inside the output.  vals_in == nullptr means the values are
@@ -158,29 +157,28 @@ __global__ void __launch_bounds__(kRsThreads) onesweep_kernel(
   for (int i = threadIdx.x; i < kRsWarps * kMaxDigits; i += kRsThreads) (&wcnt[0][0])[i] = 0;
   if (threadIdx.x == 0) tile_sh = atomicAdd(tile_counter, 1u);
   __syncthreads();
-  const int64_t tile = tile_sh;
-
-  const int64_t tile_base = tile * kRsTile;
-  const int64_t base = tile_base + (int64_t)warp * kRsWarpKeys;
+  // all offsets fit 32 bits: the entry point admits fewer than 2^31 keys
+  const int n32 = (int)n;
+  const int tile = (int)tile_sh;
+  const int tile_base = tile * kRsTile;
+  const int base = tile_base + warp * kRsWarpKeys;
   const unsigned lt = lanemask_lt();
   uint32_t key[kRsItems];
   int32_t val[kRsItems];
   uint32_t rank[kRsItems];
 #pragma unroll
   for (int r = 0; r < kRsItems; ++r) {
-    const int64_t idx = base + r * 32 + lane;
-    const bool valid = idx < n;
+    const int idx = base + r * 32 + lane;
+    const bool valid = idx < n32;
     key[r] = valid ? keys_in[idx] : 0u;
-    val[r] = valid ? (vals_in ? vals_in[idx] : (int32_t)idx) : 0;
-    const uint32_t dg = valid ? digit_of(key[r], shift, mask) : 0u;
-    unsigned peers = __ballot_sync(kFull, valid);
+    val[r] = valid ? (vals_in ? vals_in[idx] : idx) : 0;
+  }
 #pragma unroll
-    for (int b = 0; b < kMaxBits; ++b) {
-      if (b < nbits) {
-        const unsigned m = __ballot_sync(kFull, (dg >> b) & 1u);
-        peers &= ((dg >> b) & 1u) ? m : ~m;
-      }
-    }
+  for (int r = 0; r < kRsItems; ++r) {
+    const bool valid = base + r * 32 + lane < n32;
+    const uint32_t dg = digit_of(key[r], shift, mask);
+    // lanes of this row holding the same digit (invalid lanes share a value no digit takes)
+    const unsigned peers = __match_any_sync(kFull, valid ? dg : 0xffffffffu);
     const uint32_t prior = valid ? wcnt[warp][dg] : 0u;
     __syncwarp();
     if (valid && lane == __ffs(peers) - 1) wcnt[warp][dg] = prior + __popc(peers);
@@ -199,7 +197,7 @@ __global__ void __launch_bounds__(kRsThreads) onesweep_kernel(
       cnt += c;
     }
   }
-  uint64_t* my_word = lookback + tile * kMaxDigits + dg;
+  uint64_t* my_word = lookback + (int64_t)tile * kMaxDigits + dg;
   if (dg < ndig) st_relaxed(my_word, (tile == 0 ? kFlagInclusive : kFlagAggregate) | cnt);
   uint32_t gh[1] = {dg < ndig ? g_hist[dg] : 0u};
   uint32_t tc[1] = {cnt};
@@ -210,13 +208,13 @@ __global__ void __launch_bounds__(kRsThreads) onesweep_kernel(
   if (dg < ndig && tile > 0) {
     // walk back kLbWindow predecessors per round trip; stop at the first
     // inclusive prefix, wait (bounded) where a predecessor has not published
-    int64_t j = tile - 1;
+    int j = tile - 1;
     uint64_t t0 = 0;
     while (j >= 0) {
       uint64_t w[kLbWindow];
 #pragma unroll
-      for (int q = 0; q < kLbWindow; ++q) w[q] = (j - q >= 0) ? ld_relaxed(lookback + (j - q) * kMaxDigits + dg)
-                                                             : kFlagInclusive;
+      for (int q = 0; q < kLbWindow; ++q)
+        w[q] = (j - q >= 0) ? ld_relaxed(lookback + (int64_t)(j - q) * kMaxDigits + dg) : kFlagInclusive;
       int used = 0;
       bool done = false, stalled = false;
 #pragma unroll
@@ -262,12 +260,12 @@ __global__ void __launch_bounds__(kRsThreads) onesweep_kernel(
     }
   }
   __syncthreads();
-  const int count = (int)imin64(kRsTile, n - tile_base);
+  const int count = min(kRsTile, n32 - tile_base);
   for (int i = threadIdx.x; i < count; i += kRsThreads) {
     const uint32_t k = skeys[i];
     const uint32_t d = digit_of(k, shift, mask);
-    const int64_t dest = (int64_t)glob_start[d] + (i - (int64_t)tile_start[d]);
-    if (dest >= 0 && dest < n) {  // always true unless a look-back timed out
+    const uint32_t dest = glob_start[d] + (uint32_t)i - tile_start[d];
+    if (dest < (uint32_t)n32) {  // always true unless a look-back timed out
       keys_out[dest] = k;
       vals_out[dest] = svals[i];
     }
@@ -406,19 +404,35 @@ __global__ void __launch_bounds__(kRsThreads) unique_write_kernel(
 constexpr int64_t kBitmapRowsPerId = 64;  // bitmap path iff total_rows <= 64 * n_ids
 constexpr int kBmWords = 1024;            // bitmap words per prefix block (4 per thread)
 
-// Flat walk over the IDs: a warp takes 32 consecutive bags and its lanes take
-// their IDs 32 at a time (every lane busy whatever the bag lengths); a lane
-// finds its bag by a shuffle binary search over the lanes' bag starts.  Calls
-// f(i, key, bag) for every ID, with the key generator's validation and
-// clamping.  A block of bags with inconsistent offsets is flagged and skipped.
-template <typename Fn>
-__device__ __forceinline__ void for_each_key_flat(const int64_t* __restrict__ ids,
-                                                  const int64_t* __restrict__ offsets, int32_t F, int32_t B,
-                                                  int64_t n_ids, const FieldMap& fm, int* err, Fn f) {
+__device__ __forceinline__ uint32_t ld_l1(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.ca.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+constexpr int kKeyChunks = 4;  // chunks of 32 IDs a warp has in flight
+
+// Keys (32-bit global rows), the sort's first values, and the presence bitmap,
+// in one flat walk over the IDs: a warp takes 32 consecutive bags and its
+// lanes take their IDs 32 at a time, kKeyChunks chunks at once (every lane
+// busy whatever the bag lengths, several loads in flight); a lane finds its
+// bag by a shuffle binary search over the lanes' bag starts.  IDs get the key
+// generator's validation and clamping; a block of bags with inconsistent
+// offsets is flagged and skipped.  A key whose bit is already set is not set
+// again, so the hot rows of a skewed batch cost L1-cached loads, not atomics
+// (bits only go from 0 to 1, so a stale word only costs a redundant atomic).
+__global__ void __launch_bounds__(256) bitmap_keys_kernel(const int64_t* __restrict__ ids,
+                                                          const int64_t* __restrict__ offsets, int32_t F, int32_t B,
+                                                          int64_t n_ids, const __grid_constant__ FieldMap fm,
+                                                          uint32_t* __restrict__ keys, int32_t* __restrict__ vals,
+                                                          int vals_are_pos, int32_t* __restrict__ bag_of,
+                                                          uint32_t* __restrict__ bitmap, int* err) {
   const int lane = threadIdx.x & 31;
   const int64_t nbags = (int64_t)F * B;
   const int64_t nblk = ceil_div(nbags, (int64_t)32);
   const int64_t end_all = offsets[nbags];
+  if (blockIdx.x == 0 && threadIdx.x == 0 && (offsets[0] != 0 || end_all != n_ids))
+    set_error(err, CTR_ERR_BAD_OFFSETS);
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t blk = warp0; blk < nblk; blk += nwarps) {
@@ -438,51 +452,51 @@ __device__ __forceinline__ void for_each_key_flat(const int64_t* __restrict__ id
     const int fld = bvalid ? (int)(bag / B) : 0;  // this lane's bag's field, once per block
     const uint32_t base_l = (uint32_t)fm.base[fld];
     const uint32_t rows_l = (uint32_t)fm.rows[fld];
-    for (int c0 = 0; c0 < total; c0 += 32) {
-      const int kr = c0 + lane;
-      int seg = 0;
+    for (int c0 = 0; c0 < total; c0 += 32 * kKeyChunks) {
+      int64_t id[kKeyChunks];
 #pragma unroll
-      for (int step = 16; step > 0; step >>= 1) {  // largest lane j with rel0_j <= kr
-        const int cand = seg + step;
-        if (__shfl_sync(kFull, rel0, cand) <= kr) seg = cand;
+      for (int q = 0; q < kKeyChunks; ++q) {
+        const int kr = c0 + q * 32 + lane;
+        id[q] = kr < total ? ids[S0 + kr] : 0;
       }
-      const uint32_t base = __shfl_sync(kFull, base_l, seg);
-      const uint32_t rows = __shfl_sync(kFull, rows_l, seg);
-      if (kr < total) {
-        const int64_t i = S0 + kr;
-        int64_t id = ids[i];
-        bool ok = true;
-        if (id < 0 || id >= (int64_t)rows) {
-          set_error(err, CTR_ERR_INDEX_OUT_OF_RANGE);
-          id = (int64_t)rows - 1;
-          ok = rows > 0;  // an ID of an empty table has no row to stand in for it
+      uint32_t key[kKeyChunks];
+      bool ok[kKeyChunks];
+#pragma unroll
+      for (int q = 0; q < kKeyChunks; ++q) {
+        const int kr = c0 + q * 32 + lane;
+        int seg = 0;
+#pragma unroll
+        for (int step = 16; step > 0; step >>= 1) {  // largest lane j with rel0_j <= kr
+          const int cand = seg + step;
+          if (__shfl_sync(kFull, rel0, cand) <= kr) seg = cand;
         }
-        if (ok) f(i, base + (uint32_t)id, blk * 32 + seg);
+        const uint32_t base = __shfl_sync(kFull, base_l, seg);
+        const uint32_t rows = __shfl_sync(kFull, rows_l, seg);
+        ok[q] = kr < total;
+        if (ok[q] && (id[q] < 0 || id[q] >= (int64_t)rows)) {
+          set_error(err, CTR_ERR_INDEX_OUT_OF_RANGE);
+          id[q] = (int64_t)rows - 1;
+          ok[q] = rows > 0;  // an ID of an empty table has no row to stand in for it
+        }
+        key[q] = base + (uint32_t)id[q];
+        if (ok[q]) {
+          const int64_t i = S0 + kr;
+          const int64_t bg = blk * 32 + seg;
+          keys[i] = key[q];
+          vals[i] = vals_are_pos ? (int32_t)i : (int32_t)bg;
+          if (bag_of) bag_of[i] = (int32_t)bg;
+        }
+      }
+      uint32_t word[kKeyChunks];
+#pragma unroll
+      for (int q = 0; q < kKeyChunks; ++q) word[q] = ok[q] ? ld_l1(bitmap + (key[q] >> 5)) : ~0u;
+#pragma unroll
+      for (int q = 0; q < kKeyChunks; ++q) {
+        const uint32_t bit = 1u << (key[q] & 31);
+        if (ok[q] && !(word[q] & bit)) atomicOr(bitmap + (key[q] >> 5), bit);
       }
     }
   }
-}
-
-// Keys (32-bit global rows), the sort's first values, and the presence bitmap.
-// A key whose bit is already visible in L2 is not set again, so the hot rows
-// of a skewed batch cost loads, not atomics.
-__global__ void __launch_bounds__(256) bitmap_keys_kernel(const int64_t* __restrict__ ids,
-                                                          const int64_t* __restrict__ offsets, int32_t F, int32_t B,
-                                                          int64_t n_ids, const __grid_constant__ FieldMap fm,
-                                                          uint32_t* __restrict__ keys, int32_t* __restrict__ vals,
-                                                          int vals_are_pos, int32_t* __restrict__ bag_of,
-                                                          uint32_t* __restrict__ bitmap, int* err) {
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    if (offsets[0] != 0 || offsets[(int64_t)F * B] != n_ids) set_error(err, CTR_ERR_BAD_OFFSETS);
-  }
-  for_each_key_flat(ids, offsets, F, B, n_ids, fm, err, [&](int64_t i, uint32_t k, int64_t bag) {
-    keys[i] = k;
-    vals[i] = vals_are_pos ? (int32_t)i : (int32_t)bag;
-    if (bag_of) bag_of[i] = (int32_t)bag;
-    uint32_t* wp = bitmap + (k >> 5);
-    const uint32_t bit = 1u << (k & 31);
-    if (!(__ldcg(wp) & bit)) atomicOr(wp, bit);
-  });
 }
 
 // Set bits per block of kBmWords words.
@@ -533,8 +547,10 @@ __global__ void __launch_bounds__(256) bitmap_pack_kernel(const uint32_t* __rest
   }
 }
 
+// Read-only lookups through L1: under skewed IDs thousands of warps look up
+// the same few words at once, which L2 would serve from one slice.
 __device__ __forceinline__ uint32_t bitmap_rank(const uint2* __restrict__ pk, uint32_t k) {
-  const uint2 e = pk[k >> 5];
+  const uint2 e = __ldg(pk + (k >> 5));
   return e.y + __popc(e.x & ((1u << (k & 31)) - 1u));
 }
 
@@ -572,12 +588,6 @@ __global__ void bitmap_plan_kernel(const uint32_t* __restrict__ total, int64_t* 
 // plan (per-warp shared histograms, then one global add per block and digit).
 // A key outside the tables (a slot an invalid bag left unwritten) is flagged
 // and ranked 0.
-__device__ __forceinline__ void hist_add(uint32_t (*h)[kMaxDigits], const PassPlan& plan, uint32_t r) {
-#pragma unroll
-  for (int p = 0; p < kMaxPasses; ++p)
-    if (p < plan.passes) atomicAdd(&h[p][(r >> plan.shift[p]) & ((1u << plan.bits[p]) - 1)], 1u);
-}
-
 __device__ __forceinline__ uint32_t rank_or_flag(const uint2* __restrict__ pk, uint32_t k, int64_t total_rows,
                                                  int* err) {
   if ((int64_t)k < total_rows) return bitmap_rank(pk, k);
@@ -585,8 +595,12 @@ __device__ __forceinline__ uint32_t rank_or_flag(const uint2* __restrict__ pk, u
   return 0u;
 }
 
-// Four consecutive keys per thread (one 16-byte load and store, four bitmap
-// lookups in flight); `vec` says both arrays are 16-byte aligned.
+constexpr int kRankVec = 4;                 // uint4 loads per thread and round
+constexpr int kRankPer = 4 * kRankVec;      // keys per thread and round
+
+// kRankPer consecutive keys per thread and round: their bitmap lookups are
+// independent, so 16 are in flight per thread.  `vec` says both arrays are
+// 16-byte aligned.
 __global__ void __launch_bounds__(256) bitmap_rank_kernel(const uint32_t* __restrict__ keys, int64_t n,
                                                           int64_t total_rows, const uint2* __restrict__ pk,
                                                           const PassPlan* __restrict__ dplan,
@@ -597,31 +611,54 @@ __global__ void __launch_bounds__(256) bitmap_rank_kernel(const uint32_t* __rest
   for (int i = threadIdx.x; i < kWarps * kMaxPasses * kMaxDigits; i += blockDim.x) (&sh[0][0][0])[i] = 0;
   __syncthreads();
   const PassPlan plan = *dplan;
-  uint32_t (*h)[kMaxDigits] = sh[threadIdx.x >> 5];
+  const int warp = threadIdx.x >> 5;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   int64_t done = 0;
   if (vec) {
-    const int64_t n4 = n / 4;
-    for (int64_t q = t0; q < n4; q += stride) {
-      const uint4 k = ((const uint4*)keys)[q];
-      uint4 r;
-      r.x = rank_or_flag(pk, k.x, total_rows, err);
-      r.y = rank_or_flag(pk, k.y, total_rows, err);
-      r.z = rank_or_flag(pk, k.z, total_rows, err);
-      r.w = rank_or_flag(pk, k.w, total_rows, err);
-      ((uint4*)ranks)[q] = r;
-      hist_add(h, plan, r.x);
-      hist_add(h, plan, r.y);
-      hist_add(h, plan, r.z);
-      hist_add(h, plan, r.w);
+    const int64_t nu = n / kRankPer;
+    uint4 nxt[kRankVec];  // the next round's keys, loaded while this round's lookups run
+    if (t0 < nu) {
+#pragma unroll
+      for (int v = 0; v < kRankVec; ++v) nxt[v] = ((const uint4*)keys)[t0 * kRankVec + v];
     }
-    done = n4 * 4;
+    for (int64_t u = t0; u < nu; u += stride) {
+      uint4 k[kRankVec];
+#pragma unroll
+      for (int v = 0; v < kRankVec; ++v) k[v] = nxt[v];
+      if (u + stride < nu) {
+#pragma unroll
+        for (int v = 0; v < kRankVec; ++v) nxt[v] = ((const uint4*)keys)[(u + stride) * kRankVec + v];
+      }
+      uint4 r[kRankVec];
+#pragma unroll
+      for (int v = 0; v < kRankVec; ++v) {
+        r[v].x = rank_or_flag(pk, k[v].x, total_rows, err);
+        r[v].y = rank_or_flag(pk, k[v].y, total_rows, err);
+        r[v].z = rank_or_flag(pk, k[v].z, total_rows, err);
+        r[v].w = rank_or_flag(pk, k[v].w, total_rows, err);
+      }
+      uint4* dst = (uint4*)ranks + u * kRankVec;
+#pragma unroll
+      for (int v = 0; v < kRankVec; ++v) dst[v] = r[v];
+#pragma unroll
+      for (int v = 0; v < kRankVec; ++v) {
+        const uint32_t rr[4] = {r[v].x, r[v].y, r[v].z, r[v].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+          for (int p = 0; p < kMaxPasses; ++p)
+            if (p < plan.passes) atomicAdd(&sh[warp][p][(rr[e] >> plan.shift[p]) & ((1u << plan.bits[p]) - 1)], 1u);
+      }
+    }
+    done = nu * kRankPer;
   }
   for (int64_t i = done + t0; i < n; i += stride) {
     const uint32_t r = rank_or_flag(pk, keys[i], total_rows, err);
     ranks[i] = r;
-    hist_add(h, plan, r);
+#pragma unroll
+    for (int p = 0; p < kMaxPasses; ++p)
+      if (p < plan.passes) atomicAdd(&sh[warp][p][(r >> plan.shift[p]) & ((1u << plan.bits[p]) - 1)], 1u);
   }
   __syncthreads();
   for (int i = threadIdx.x; i < plan.passes * kMaxDigits; i += blockDim.x) {
@@ -786,7 +823,7 @@ int dedup_bitmap(const int64_t* ids, const int64_t* offsets, int32_t F, int32_t 
   // ranks go straight into the caller's inverse map, which the first pass reads
   uint32_t* ranks = inverse ? (uint32_t*)inverse : keys[0];
   {
-    const int64_t blocks = std::max<int64_t>(1, imin64(ceil_div(n_ids, 1024), (int64_t)sms * 8));
+    const int64_t blocks = std::max<int64_t>(1, imin64(ceil_div(n_ids, 256 * kRankPer), (int64_t)sms * 6));
     const int vec = ((uintptr_t)ranks % 16) == 0;
     bitmap_rank_kernel<<<(unsigned)blocks, 256, 0, s>>>(keys[1], n_ids, total_rows, pk, dplan, ranks, vec, g_hist,
                                                         err);
