@@ -289,14 +289,8 @@ def run_ours(args, rank, world):
         raise RuntimeError(f"device error during warm-up: {status}")
     n_unique = int(path.n_unique.item())
 
-    stages = ["dedup", "forward", "interaction", "interaction_bwd", "bwd_update"]
-    run_stage = {"dedup": path.dedup, "forward": path.forward, "interaction": path.interaction,
-                 "interaction_bwd": path.interaction_bwd, "bwd_update": path.bwd_update}
-    active = [s for s in stages if (s != "dedup" or cfg.backward != "none" or cfg.dedup_gather)
-              and (s != "interaction" or cfg.interaction)
-              and (s != "interaction_bwd" or cfg.backward == "full")
-              and (s != "bwd_update" or cfg.backward != "none")]
-    if "dedup" not in active:
+    has_dedup = cfg.backward != "none" or cfg.dedup_gather
+    if not has_dedup:
         # distinct rows of the batch, for the gather's compulsory bytes (outside the timed region)
         lens = torch.from_numpy(np.diff(w["offsets"])).cuda()
         bag_table = torch.from_numpy(np.asarray(cfg.field_to_table, dtype=np.int64)).cuda().repeat_interleave(cfg.batch)
@@ -305,7 +299,7 @@ def run_ours(args, rank, world):
         n_unique = int(torch.unique(keys).numel())
         del lens, bag_table, base, keys
     kernels = {"gather": ctr.KERNEL_GATHER}
-    if "dedup" in active:
+    if has_dedup:
         kernels["sort"] = ctr.KERNEL_SORT
     if cfg.dedup_gather:
         kernels["gather_rows"] = ctr.KERNEL_GATHER_ROWS
@@ -322,7 +316,6 @@ def run_ours(args, rank, world):
         e.record(stream)  # torch creates the CUDA event on first record
         return e
 
-    ev = [[new_event() for _ in range(len(active) + 1)] for _ in range(args.steps)]
     kev = [{k: (new_event(), new_event()) for k in kernels} for _ in range(args.steps)]
     torch.cuda.synchronize()
     barrier()
@@ -337,10 +330,7 @@ def run_ours(args, rank, world):
         for k in range(args.steps):
             for name, kid in kernels.items():
                 ctr.ctr_set_timing_events(kid, *kev[k][name])
-            ev[k][0].record(stream)
-            for i, s_ in enumerate(active):
-                run_stage[s_]()
-                ev[k][i + 1].record(stream)
+            path.step()
         t_end.record(stream)
         launches = ctr.ctr_launch_count() - launches0
         torch.cuda.synchronize()
@@ -350,8 +340,6 @@ def run_ours(args, rank, world):
         ctr.ctr_set_timing_events(kid, None, None)
     barrier()
     total_ms = t_start.elapsed_time(t_end)
-    stage_ms = {s_: sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)) / args.steps
-                for i, s_ in enumerate(active)}
     kernel_ms = {}
     for name in kernels:
         try:
@@ -416,7 +404,6 @@ def run_ours(args, rank, world):
                    "l2": "inputs larger than L2 (tables %.1f GB, ids %.2f GB)" % (
                        cfg.total_rows * cfg.d * 4 / 1e9, n_ids * 8 / 1e9)},
         "interaction_samples_per_s": cfg.batch * world / (ms / 1e3),
-        "stage_ms": stage_ms,
         "kernels": kern,
         "roofline": roofline,
         "e2e": e2e,

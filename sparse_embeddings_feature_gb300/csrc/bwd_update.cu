@@ -344,6 +344,20 @@ constexpr int kWin = 8;
 #ifndef CTR_TILE_ASYNC_MINB
 #define CTR_TILE_ASYNC_MINB 3
 #endif
+// L2 policies of the backward: pooled-gradient rows are re-read by every
+// unique of their bags (kept: evict_last on this fraction of their lines),
+// table rows are read and written once (streamed: evict_first).
+#ifndef CTR_BWD_G_KEEP_FRACTION
+#define CTR_BWD_G_KEEP_FRACTION 1.0f
+#endif
+#ifndef CTR_BWD_ROW_STREAM
+#define CTR_BWD_ROW_STREAM 1
+#endif
+__device__ __forceinline__ uint64_t g_policy() {
+  return CTR_BWD_G_KEEP_FRACTION > 0.f ? l2_evict_last_fraction(CTR_BWD_G_KEEP_FRACTION) : l2_evict_normal();
+}
+__device__ __forceinline__ uint64_t row_policy() { return CTR_BWD_ROW_STREAM ? l2_evict_first() : l2_evict_normal(); }
+
 #ifndef CTR_BWD_MINB
 #define CTR_BWD_MINB 3  // resident blocks per SM the register budget is sized for
 #endif
@@ -398,7 +412,7 @@ __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(c
   const int lane = threadIdx.x & 31;
   const bool col = lane * 4 < a.d;  // this lane's 16-byte column exists
   const float* Gl = a.G + lane * 4;
-  const uint64_t pol_keep = l2_evict_last();
+  const uint64_t pol_keep = g_policy();
   const int64_t np = *a.pieces_total;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   (void)nwarps;
@@ -612,7 +626,7 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_ASYNC_MINB) bwd_tiles_a
   const float* Gl = a.G + lane * 4;
   // pooled-gradient rows are re-read by every unique of their bags: keep them
   // in L2; the table rows are touched once: stream them
-  const uint64_t pol_keep = l2_evict_last(), pol_stream = l2_evict_first();
+  const uint64_t pol_keep = g_policy(), pol_stream = row_policy();
   const int64_t nu = n_uniques(a);
   const int64_t ntiles = ceil_div(nu, TU);
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -839,7 +853,12 @@ int launch_bwd(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
   timing_mark(CTR_KERNEL_BWD_PIECES, false, s);
   if (int st = launch_status()) return st;
   const size_t csmem = (size_t)(kCombThreads / 32) * a.d * sizeof(float);
-  combine_long_kernel<<<std::max(num_sms() * 2, 1), kCombThreads, csmem, s>>>(a); count_launch();
+  // one CTA per long run in flight, as many as fit (each run is a short latency chain)
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_long_kernel, kCombThreads, csmem) != cudaSuccess)
+    per_sm = 2;
+  const int64_t cgrid = imin64(std::max<int64_t>(a.max_long, 1), (int64_t)std::max(per_sm, 1) * num_sms());
+  combine_long_kernel<<<(unsigned)cgrid, kCombThreads, csmem, s>>>(a); count_launch();
   return launch_status();
 }
 

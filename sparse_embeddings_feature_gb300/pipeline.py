@@ -66,6 +66,7 @@ class CtrPath:
         self.ws_bwd = ctr.workspace(ctr.ctr_bwd_update_workspace_size(cap, d), self.dev)
         self.b2t = np.asarray(cfg.field_to_table, dtype=np.int32)
         self.row_base = cfg.row_base
+        self._side = None          # side stream of the overlapped dedup (created on first use)
 
     # -- inputs -----------------------------------------------------------
     def fill_table(self, chunk_rows: int = 1 << 24) -> None:
@@ -143,15 +144,38 @@ class CtrPath:
                                          grad_unique_out, self.ws_bwd)
 
     def step(self) -> None:
-        """One pass of the workload's hot path."""
+        """One pass of the workload's hot path, on the current stream.
+
+        When the forward pools straight from the tables, only the backward needs
+        the dedup: it then runs on a side stream, concurrently with the gather and
+        the interaction (its kernels are mostly latency-bound, theirs bandwidth-
+        bound), and the backward waits for it.  The side stream first waits for
+        everything queued before the step, and the step's end (on the current
+        stream) comes after the dedup, so the step orders like a sequential one.
+        """
         cfg = self.cfg
-        if cfg.backward != "none" or cfg.dedup_gather:
+        needs_dedup = cfg.backward != "none" or cfg.dedup_gather
+        overlap = needs_dedup and not cfg.dedup_gather and cfg.backward != "none"
+        if overlap:
+            main = torch.cuda.current_stream(self.dev)
+            if self._side is None:
+                self._side = torch.cuda.Stream(self.dev)
+                self._ev_start = torch.cuda.Event()
+                self._ev_dedup = torch.cuda.Event()
+            self._ev_start.record(main)
+            self._side.wait_event(self._ev_start)
+            with torch.cuda.stream(self._side):
+                self.dedup()
+            self._ev_dedup.record(self._side)
+        elif needs_dedup:
             self.dedup()
         self.forward()
         if cfg.interaction:
             self.interaction()
         if cfg.backward == "full":
             self.interaction_bwd()
+        if overlap:
+            torch.cuda.current_stream(self.dev).wait_event(self._ev_dedup)
         if cfg.backward != "none":
             self.bwd_update()
 
