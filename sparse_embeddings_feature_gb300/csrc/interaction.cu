@@ -33,7 +33,6 @@ bool interaction_bf16_tc_supported(int32_t n, int32_t d);
 
 namespace {
 
-constexpr int kIntWarps = 4;
 
 struct PairTable {
   unsigned char i[32 * 32];
@@ -53,30 +52,55 @@ constexpr PairTable make_pairs() {
   return t;
 }
 
+// Packed fp32 pairs (sm_100+ f32x2 arithmetic): each half is an ordinary
+// IEEE fp32 operation with round-to-nearest, two per instruction.
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ float lo32(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi32(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
+// Forward, n = 27, d = 128: one warp per sample, lane l holding columns
+// 4l..4l+3 of every vector as two packed pairs.  For 32 pairs at a time each
+// lane forms its 4-column partial dots ((x0 y0 + x2 y2) + (x1 y1 + x3 y3),
+// packed), writes them as a row of a padded 32 x 32 block in shared memory,
+// and sums one column: lane t then holds dot t of the group.  (Staging the
+// next sample in shared memory was measured slower: it costs occupancy, and
+// the kernel is bound by issue, not by DRAM latency.)
+constexpr int kFwdWarps = 4;
+constexpr int kRedStride = 36;  // padded row of the transposition block (16-byte rows, conflict-free columns)
 template <int N, int D>
-__global__ void __launch_bounds__(kIntWarps * 32) interaction_fwd_f32_regs(const float* __restrict__ X, int32_t batch,
+__global__ void __launch_bounds__(kFwdWarps * 32) interaction_fwd_f32_regs(const float* __restrict__ X, int32_t batch,
                                                                           float* __restrict__ out) {
   static_assert(D == 128, "4 columns per lane");
   constexpr int P = N * (N - 1) / 2;
   constexpr int G = (P + 31) / 32;
   constexpr int W = D + P;
   constexpr PairTable pt = make_pairs<N>();
-  const int lane = threadIdx.x & 31;
+  __shared__ __align__(16) float sred[kFwdWarps][32 * kRedStride];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* red = sred[warp];
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < batch; b += nwarps) {
-    const float* xb = X + b * (int64_t)N * D + lane * 4;
-    float x[N][4];
+    uint64_t xl[N], xh[N];  // columns (4l, 4l+1) and (4l+2, 4l+3) of each vector
 #pragma unroll
     for (int i = 0; i < N; ++i) {
-      float4 v = __ldcs((const float4*)(xb + i * D));
-      x[i][0] = v.x;
-      x[i][1] = v.y;
-      x[i][2] = v.z;
-      x[i][3] = v.w;
+      const ulonglong2 v = __ldcs((const ulonglong2*)(X + b * (int64_t)N * D + i * D + lane * 4));
+      xl[i] = v.x;
+      xh[i] = v.y;
     }
     float* ob = out + b * (int64_t)W;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) __stcs(ob + lane * 4 + c, x[0][c]);
+    __stcs(ob + lane * 4 + 0, lo32(xl[0]));
+    __stcs(ob + lane * 4 + 1, hi32(xl[0]));
+    __stcs(ob + lane * 4 + 2, lo32(xh[0]));
+    __stcs(ob + lane * 4 + 3, hi32(xh[0]));
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       float v[32];
@@ -85,30 +109,27 @@ __global__ void __launch_bounds__(kIntWarps * 32) interaction_fwd_f32_regs(const
         const int p = g * 32 + t;
         if (p < P) {
           const int i = pt.i[p], j = pt.j[p];
-          float s = x[i][0] * x[j][0];
-          s = fmaf(x[i][1], x[j][1], s);
-          s = fmaf(x[i][2], x[j][2], s);
-          s = fmaf(x[i][3], x[j][3], s);
-          v[t] = s;
+          const uint64_t m = fma2(xh[i], xh[j], mul2(xl[i], xl[j]));
+          v[t] = lo32(m) + hi32(m);
         } else {
           v[t] = 0.f;
         }
       }
+      __syncwarp();  // the previous group's columns have been read
 #pragma unroll
-      for (int st = 16; st >= 1; st >>= 1) {
-        const bool up = lane & st;
+      for (int q = 0; q < 8; ++q)
+        *(float4*)(red + lane * kRedStride + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      __syncwarp();
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < st; ++k) {
-          const float keep = up ? v[k + st] : v[k];
-          const float send = up ? v[k] : v[k + st];
-          v[k] = keep + __shfl_xor_sync(kFull, send, st);
-        }
-      }
+      for (int r = 0; r < 32; ++r) acc[r & 3] += red[r * kRedStride + lane];
       const int p = g * 32 + lane;
-      if (p < P) __stcs(ob + D + p, v[0]);
+      if (p < P) __stcs(ob + D + p, (acc[0] + acc[1]) + (acc[2] + acc[3]));
     }
   }
 }
+
+constexpr int kBwdWarps = 4;
 
 // Backward, n = 27, d = 128: one warp per sample.  The sample's upstream pair
 // gradients are expanded into a symmetric matrix S (zero diagonal, rows padded
@@ -117,14 +138,14 @@ __global__ void __launch_bounds__(kIntWarps * 32) interaction_fwd_f32_regs(const
 // dX_i = sum_j S[i][j] x_j: one 16-byte broadcast load of S per four j and
 // sixteen FMAs.
 template <int N, int D>
-__global__ void __launch_bounds__(kIntWarps * 32) interaction_bwd_f32_regs(const float* __restrict__ dout,
+__global__ void __launch_bounds__(kBwdWarps * 32) interaction_bwd_f32_regs(const float* __restrict__ dout,
                                                                           const float* __restrict__ X, int32_t batch,
                                                                           float* __restrict__ dX) {
   static_assert(D == 128, "4 columns per lane");
   constexpr int P = N * (N - 1) / 2;
   constexpr int W = D + P;
   constexpr int NP = (N + 3) / 4 * 4;  // padded row length of S
-  __shared__ __align__(16) float sS[kIntWarps][N * NP];
+  __shared__ __align__(16) float sS[kBwdWarps][N * NP];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   float* S = sS[warp];
@@ -272,8 +293,9 @@ int dot_interaction_launch(const void* X, ctr_dtype dtype, int32_t batch, int32_
                            cudaStream_t s) {
   if (dtype == CTR_F32 && n == 27 && d == 128 && (uintptr_t)X % 16 == 0) {
     auto k = interaction_fwd_f32_regs<27, 128>;
-    k<<<grid_blocks(k, kIntWarps * 32, 0, ceil_div(batch, kIntWarps)), kIntWarps * 32, 0, s>>>(
-        (const float*)X, batch, (float*)out); count_launch();
+    k<<<grid_blocks(k, kFwdWarps * 32, 0, ceil_div(batch, kFwdWarps)), kFwdWarps * 32, 0, s>>>((const float*)X, batch,
+                                                                                            (float*)out);
+    count_launch();
     return launch_status();
   }
   if (dtype == CTR_BF16 && interaction_bf16_tc_supported(n, d) && (uintptr_t)X % 16 == 0 &&
@@ -296,7 +318,8 @@ int dot_interaction_bwd_launch(const float* dout, const float* X, int32_t batch,
                                cudaStream_t s) {
   if (n == 27 && d == 128 && (uintptr_t)X % 16 == 0 && (uintptr_t)dX % 16 == 0) {
     auto k = interaction_bwd_f32_regs<27, 128>;
-    k<<<grid_blocks(k, kIntWarps * 32, 0, ceil_div(batch, kIntWarps)), kIntWarps * 32, 0, s>>>(dout, X, batch, dX); count_launch();
+    k<<<grid_blocks(k, kBwdWarps * 32, 0, ceil_div(batch, kBwdWarps)), kBwdWarps * 32, 0, s>>>(dout, X, batch, dX);
+    count_launch();
     return launch_status();
   }
   const size_t smem = ((size_t)n * d + (size_t)n * (n - 1) / 2) * sizeof(float);
