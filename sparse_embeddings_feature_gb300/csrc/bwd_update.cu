@@ -207,13 +207,6 @@ __global__ void __launch_bounds__(kTileThreads, 2) bwd_tiles_kernel(const BwdArg
         row = -1;
       }
     }
-    if (is_long) {
-      const int64_t slot = (int64_t)atomicAdd((unsigned long long*)a.long_count, 1ull);
-      if (slot < a.max_long) {
-        a.long_list[slot] = (int32_t)u;
-        a.long_pstart[slot] = (uint32_t)ceil_div(len, kPiece);
-      }
-    }
     // exclusive scan of the short runs' lengths over the tile's lanes
     const int slen = is_short ? (int)len : 0;
     int inc = slen;
@@ -316,10 +309,29 @@ __global__ void __launch_bounds__(kTileThreads, 2) bwd_tiles_kernel(const BwdArg
   }
 }
 
-__global__ void clear_i64(int64_t* p, unsigned long long* w) {
-  *p = 0;
-  w[0] = 0;
-  w[1] = 0;
+// Clears the long-run count and the piece counter (the tile counter belongs
+// to the short-run phase, which may run concurrently).
+__global__ void clear_long_state(int64_t* long_count, unsigned long long* piece_counter) {
+  *long_count = 0;
+  *piece_counter = 0;
+}
+
+// The long runs (more than kShort occurrences), in any order: each one's
+// unique and its piece count (a run's result does not depend on its slot).
+__global__ void __launch_bounds__(256) long_list_kernel(const BwdArgs a) {
+  const int64_t nu = n_uniques(a);
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < nu; u += (int64_t)gridDim.x * blockDim.x) {
+    int64_t r0, r1;
+    run_bounds(a, u, r0, r1);
+    const int64_t len = r1 - r0;
+    if (len > kShort) {
+      const int64_t slot = (int64_t)atomicAdd((unsigned long long*)a.long_count, 1ull);
+      if (slot < a.max_long) {
+        a.long_list[slot] = (int32_t)u;
+        a.long_pstart[slot] = (uint32_t)ceil_div(len, kPiece);
+      }
+    }
+  }
 }
 
 __global__ void expand_long_kernel(const BwdArgs a) {
@@ -516,13 +528,6 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_MINB) bwd_tiles_stream_
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(wr), "r"(row_bytes) : "memory");
       }
     }
-    if (is_long) {
-      const int64_t slot = (int64_t)atomicAdd((unsigned long long*)a.long_count, 1ull);
-      if (slot < a.max_long) {
-        a.long_list[slot] = (int32_t)u;
-        a.long_pstart[slot] = (uint32_t)ceil_div(len, kPiece);
-      }
-    }
     const int slen = is_short ? (int)len : 0;
     int inc = slen;
 #pragma unroll
@@ -645,13 +650,6 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_ASYNC_MINB) bwd_tiles_a
       if (row < 0 || row >= a.total_rows) {
         set_error(a.err, CTR_ERR_INDEX_OUT_OF_RANGE);
         row = -1;
-      }
-    }
-    if (is_long) {
-      const int64_t slot = (int64_t)atomicAdd((unsigned long long*)a.long_count, 1ull);
-      if (slot < a.max_long) {
-        a.long_list[slot] = (int32_t)u;
-        a.long_pstart[slot] = (uint32_t)ceil_div(len, kPiece);
       }
     }
     // stage this tile's table rows (each lane its own column)
@@ -819,7 +817,7 @@ int grid_of(K kernel, int threads, size_t smem, int64_t want) {
 }
 
 template <int CPL>
-int launch_bwd(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
+int launch_short(const BwdArgs& a, cudaStream_t s, int64_t n) {
   const int chunks = a.d / 4;
   const size_t acc_smem = (size_t)kTileWarps * a.TU * chunks * sizeof(float4);
   const bool use_async = CPL == 1 && a.g4_ok;
@@ -828,12 +826,22 @@ int launch_bwd(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
   if (tile_smem > 48 * 1024 &&
       cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tile_smem) != cudaSuccess)
     return CTR_ERR_CUDA;
-  clear_i64<<<1, 1, 0, s>>>(a.long_count, a.work); count_launch();
-  if (int st = launch_status()) return st;
+  if (cudaMemsetAsync(a.work, 0, sizeof(unsigned long long), s) != cudaSuccess) return CTR_ERR_CUDA;
   timing_mark(CTR_KERNEL_BWD_TILES, true, s);
   tk<<<grid_of(tk, kTileThreads, tile_smem, ceil_div(n, (int64_t)a.TU * kTileWarps)), kTileThreads, tile_smem, s>>>(a); count_launch();
   timing_mark(CTR_KERNEL_BWD_TILES, false, s);
+  return launch_status();
+}
+
+template <int CPL>
+int launch_long(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
+  clear_long_state<<<1, 1, 0, s>>>(a.long_count, a.work + 1); count_launch();
   if (int st = launch_status()) return st;
+  {
+    const int64_t blocks = std::max<int64_t>(1, imin64(ceil_div(n, (int64_t)256), (int64_t)num_sms() * 8));
+    long_list_kernel<<<(unsigned)blocks, 256, 0, s>>>(a); count_launch();
+    if (int st = launch_status()) return st;
+  }
   {
     WsCarver sc = c;
     if (int st = scan_exclusive<uint32_t>(a.long_pstart, a.long_pstart, a.max_long, a.long_count, a.pieces_total,
@@ -851,7 +859,10 @@ int launch_bwd(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
     pk<<<grid_of(pk, 256, 0, ceil_div(sizes(n).max_pieces, 8)), 256, 0, s>>>(a); count_launch();
   }
   timing_mark(CTR_KERNEL_BWD_PIECES, false, s);
-  if (int st = launch_status()) return st;
+  return launch_status();
+}
+
+int launch_finish(const BwdArgs& a, cudaStream_t s) {
   const size_t csmem = (size_t)(kCombThreads / 32) * a.d * sizeof(float);
   // one CTA per long run in flight, as many as fit (each run is a short latency chain)
   int per_sm = 0;
@@ -873,19 +884,21 @@ extern "C" size_t ctr_bwd_update_workspace_size(int64_t n_ids, int32_t d) {
   return s.used;
 }
 
-extern "C" int ctr_embedding_bag_bwd_update(const float* grad_pooled, int64_t g_stride_b, int64_t g_stride_f,
-                                            const int64_t* offsets, int32_t num_fields, int32_t batch,
-                                            ctr_pool pool, const int64_t* unique_rows, const int64_t* n_unique,
-                                            const int32_t* run_offsets, const int32_t* sorted_bag, int64_t n_ids,
-                                            float lr, void* table, ctr_dtype dtype, int32_t d, int64_t total_rows,
-                                            float* grad_unique_out, void* ws, size_t ws_bytes,
-                                            ctr_stream_t stream) {
-  cudaStream_t s = (cudaStream_t)stream;
+namespace {
+
+// Validates the arguments, fills the kernels' arguments and runs the phases
+// in `phases` (CTR_BWD_LONG_RUNS, CTR_BWD_SHORT_RUNS, CTR_BWD_FINISH) on s.
+int bwd_update_phases(const float* grad_pooled, int64_t g_stride_b, int64_t g_stride_f, const int64_t* offsets,
+                      int32_t num_fields, int32_t batch, ctr_pool pool, const int64_t* unique_rows,
+                      const int64_t* n_unique, const int32_t* run_offsets, const int32_t* sorted_bag, int64_t n_ids,
+                      float lr, void* table, ctr_dtype dtype, int32_t d, int64_t total_rows, float* grad_unique_out,
+                      int phases, void* ws, size_t ws_bytes, cudaStream_t s) {
   if (!grad_pooled || !offsets || !unique_rows || !n_unique || !run_offsets || !table) return CTR_ERR_INVALID_ARG;
   if (num_fields <= 0 || batch <= 0 || d <= 0 || total_rows <= 0 || n_ids < 0) return CTR_ERR_INVALID_ARG;
   if (n_ids > 0 && !sorted_bag) return CTR_ERR_INVALID_ARG;
   if (dtype != CTR_F32 && dtype != CTR_BF16) return CTR_ERR_INVALID_ARG;
   if (pool != CTR_POOL_SUM && pool != CTR_POOL_MEAN) return CTR_ERR_INVALID_ARG;
+  if (phases <= 0 || phases > (CTR_BWD_LONG_RUNS | CTR_BWD_SHORT_RUNS | CTR_BWD_FINISH)) return CTR_ERR_INVALID_ARG;
   if (g_stride_b < 0 || g_stride_f < 0) return CTR_ERR_INVALID_ARG;
   if (n_ids >= ((int64_t)1 << 31)) return CTR_ERR_UNSUPPORTED;
   if (d % 4 != 0 || d > 512) return CTR_ERR_UNSUPPORTED;
@@ -932,7 +945,44 @@ extern "C" int ctr_embedding_bag_bwd_update(const float* grad_pooled, int64_t g_
   a.partial = c.take<float>((size_t)z.max_pieces * d);
   if (!c.ok()) return CTR_ERR_WORKSPACE;
   const int cpl = (int)ceil_div(d / 4, 32);
-  if (cpl <= 1) return launch_bwd<1>(a, c, s, n_ids);
-  if (cpl <= 2) return launch_bwd<2>(a, c, s, n_ids);
-  return launch_bwd<4>(a, c, s, n_ids);
+  if (phases & CTR_BWD_LONG_RUNS) {
+    const int st = cpl <= 1 ? launch_long<1>(a, c, s, n_ids)
+                 : cpl <= 2 ? launch_long<2>(a, c, s, n_ids) : launch_long<4>(a, c, s, n_ids);
+    if (st) return st;
+  }
+  if (phases & CTR_BWD_SHORT_RUNS) {
+    const int st = cpl <= 1 ? launch_short<1>(a, s, n_ids)
+                 : cpl <= 2 ? launch_short<2>(a, s, n_ids) : launch_short<4>(a, s, n_ids);
+    if (st) return st;
+  }
+  if (phases & CTR_BWD_FINISH) return launch_finish(a, s);
+  return CTR_OK;
+}
+
+}  // namespace
+
+extern "C" int ctr_embedding_bag_bwd_update(const float* grad_pooled, int64_t g_stride_b, int64_t g_stride_f,
+                                            const int64_t* offsets, int32_t num_fields, int32_t batch,
+                                            ctr_pool pool, const int64_t* unique_rows, const int64_t* n_unique,
+                                            const int32_t* run_offsets, const int32_t* sorted_bag, int64_t n_ids,
+                                            float lr, void* table, ctr_dtype dtype, int32_t d, int64_t total_rows,
+                                            float* grad_unique_out, void* ws, size_t ws_bytes,
+                                            ctr_stream_t stream) {
+  return bwd_update_phases(grad_pooled, g_stride_b, g_stride_f, offsets, num_fields, batch, pool, unique_rows,
+                           n_unique, run_offsets, sorted_bag, n_ids, lr, table, dtype, d, total_rows, grad_unique_out,
+                           CTR_BWD_LONG_RUNS | CTR_BWD_SHORT_RUNS | CTR_BWD_FINISH, ws, ws_bytes,
+                           (cudaStream_t)stream);
+}
+
+extern "C" int ctr_embedding_bag_bwd_update_phases(const float* grad_pooled, int64_t g_stride_b, int64_t g_stride_f,
+                                                   const int64_t* offsets, int32_t num_fields, int32_t batch,
+                                                   ctr_pool pool, const int64_t* unique_rows,
+                                                   const int64_t* n_unique, const int32_t* run_offsets,
+                                                   const int32_t* sorted_bag, int64_t n_ids, float lr, void* table,
+                                                   ctr_dtype dtype, int32_t d, int64_t total_rows,
+                                                   float* grad_unique_out, int phases, void* ws, size_t ws_bytes,
+                                                   ctr_stream_t stream) {
+  return bwd_update_phases(grad_pooled, g_stride_b, g_stride_f, offsets, num_fields, batch, pool, unique_rows,
+                           n_unique, run_offsets, sorted_bag, n_ids, lr, table, dtype, d, total_rows, grad_unique_out,
+                           phases, ws, ws_bytes, (cudaStream_t)stream);
 }

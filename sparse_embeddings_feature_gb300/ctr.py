@@ -48,6 +48,8 @@ _SIGS = {
     "ctr_bwd_update_workspace_size": (_sz, [_i64, _i32]),
     "ctr_embedding_bag_bwd_update": (C.c_int, [_p, _i64, _i64, _p, _i32, _i32, C.c_int, _p, _p, _p, _p, _i64, _f32,
                                                _p, C.c_int, _i32, _i64, _p, _p, _sz, _p]),
+    "ctr_embedding_bag_bwd_update_phases": (C.c_int, [_p, _i64, _i64, _p, _i32, _i32, C.c_int, _p, _p, _p, _p, _i64,
+                                                      _f32, _p, C.c_int, _i32, _i64, _p, C.c_int, _p, _sz, _p]),
 }
 
 
@@ -242,3 +244,21 @@ def ctr_embedding_bag_bwd_update(grad_pooled: torch.Tensor, g_stride_b: int, g_s
                                             _ptr(sorted_bag), n_ids, lr, _ptr(table), DTYPES[table.dtype], d,
                                             total_rows, _ptr(grad_unique_out), _ptr(ws), ws.numel(), _stream(stream))
     _ok("ctr_embedding_bag_bwd_update", st)
+
+
+BWD_LONG_RUNS, BWD_SHORT_RUNS, BWD_FINISH = 1, 2, 4
+
+
+def ctr_embedding_bag_bwd_update_phases(grad_pooled: torch.Tensor, g_stride_b: int, g_stride_f: int,
+                                        offsets: torch.Tensor, num_fields: int, batch: int, pool: int,
+                                        unique_rows: torch.Tensor, n_unique: torch.Tensor, run_offsets: torch.Tensor,
+                                        sorted_bag: torch.Tensor, n_ids: int, lr: float, table: torch.Tensor, d: int,
+                                        grad_unique_out: Optional[torch.Tensor], phases: int, ws: torch.Tensor,
+                                        stream=None) -> None:
+    total_rows = table.numel() // d
+    st = lib().ctr_embedding_bag_bwd_update_phases(_ptr(grad_pooled), g_stride_b, g_stride_f, _ptr(offsets),
+                                                   num_fields, batch, pool, _ptr(unique_rows), _ptr(n_unique),
+                                                   _ptr(run_offsets), _ptr(sorted_bag), n_ids, lr, _ptr(table),
+                                                   DTYPES[table.dtype], d, total_rows, _ptr(grad_unique_out),
+                                                   int(phases), _ptr(ws), ws.numel(), _stream(stream))
+    _ok("ctr_embedding_bag_bwd_update_phases", st)

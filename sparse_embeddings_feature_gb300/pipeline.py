@@ -66,7 +66,10 @@ class CtrPath:
         self.ws_bwd = ctr.workspace(ctr.ctr_bwd_update_workspace_size(cap, d), self.dev)
         self.b2t = np.asarray(cfg.field_to_table, dtype=np.int32)
         self.row_base = cfg.row_base
-        self._side = None          # side stream of the overlapped dedup (created on first use)
+        self._side = None          # side stream of the overlapped dedup and long runs (created on first use)
+        # the long-run and short-run phases of the backward are persistent grids that each
+        # fill the GPU, so overlapping them was measured slower: off by default
+        self.overlap_backward = False
 
     # -- inputs -----------------------------------------------------------
     def fill_table(self, chunk_rows: int = 1 << 24) -> None:
@@ -131,7 +134,13 @@ class CtrPath:
         cfg = self.cfg
         ctr.ctr_dot_interaction_bwd(self.dout, self.X, cfg.n_vectors, cfg.d, self.dX, self.ws_int)
 
-    def bwd_update(self, grad_unique_out: Optional[torch.Tensor] = None) -> None:
+    def bwd_update(self, grad_unique_out: Optional[torch.Tensor] = None, overlap: bool = False) -> None:
+        """Per-unique-row gradient reduce + row update.
+
+        With overlap, the long runs' pieces are summed on a side stream while
+        the short runs are reduced and updated on the current one (the two
+        phases touch disjoint rows), and the long runs are finished after both.
+        """
         cfg = self.cfg
         F, B, d, n = cfg.num_fields, cfg.batch, cfg.d, cfg.n_vectors
         pool = ctr.POOL_MEAN if cfg.pool == "mean" else ctr.POOL_SUM
@@ -139,9 +148,30 @@ class CtrPath:
             G, sb, sf = self.dX[:, 1:, :], n * d, d
         else:
             G, sb, sf = self.grad_pooled, F * d, d
-        ctr.ctr_embedding_bag_bwd_update(G, sb, sf, self.offsets, F, B, pool, self.unique_rows, self.n_unique,
-                                         self.run_offsets, self.sorted_bag, max(self.n_ids, 1), cfg.lr, self.table, d,
-                                         grad_unique_out, self.ws_bwd)
+        args = (G, sb, sf, self.offsets, F, B, pool, self.unique_rows, self.n_unique, self.run_offsets, self.sorted_bag,
+                max(self.n_ids, 1), cfg.lr, self.table, d, grad_unique_out)
+        if not overlap:
+            ctr.ctr_embedding_bag_bwd_update(*args, self.ws_bwd)
+            return
+        main = torch.cuda.current_stream(self.dev)
+        side = self._side_stream()
+        self._ev_bwd.record(main)
+        side.wait_event(self._ev_bwd)
+        with torch.cuda.stream(side):
+            ctr.ctr_embedding_bag_bwd_update_phases(*args, ctr.BWD_LONG_RUNS, self.ws_bwd)
+        self._ev_long.record(side)
+        ctr.ctr_embedding_bag_bwd_update_phases(*args, ctr.BWD_SHORT_RUNS, self.ws_bwd)
+        main.wait_event(self._ev_long)
+        ctr.ctr_embedding_bag_bwd_update_phases(*args, ctr.BWD_FINISH, self.ws_bwd)
+
+    def _side_stream(self) -> torch.cuda.Stream:
+        if self._side is None:
+            self._side = torch.cuda.Stream(self.dev)
+            self._ev_start = torch.cuda.Event()
+            self._ev_dedup = torch.cuda.Event()
+            self._ev_bwd = torch.cuda.Event()
+            self._ev_long = torch.cuda.Event()
+        return self._side
 
     def step(self) -> None:
         """One pass of the workload's hot path, on the current stream.
@@ -158,15 +188,12 @@ class CtrPath:
         overlap = needs_dedup and not cfg.dedup_gather and cfg.backward != "none"
         if overlap:
             main = torch.cuda.current_stream(self.dev)
-            if self._side is None:
-                self._side = torch.cuda.Stream(self.dev)
-                self._ev_start = torch.cuda.Event()
-                self._ev_dedup = torch.cuda.Event()
+            side = self._side_stream()
             self._ev_start.record(main)
-            self._side.wait_event(self._ev_start)
-            with torch.cuda.stream(self._side):
+            side.wait_event(self._ev_start)
+            with torch.cuda.stream(side):
                 self.dedup()
-            self._ev_dedup.record(self._side)
+            self._ev_dedup.record(side)
         elif needs_dedup:
             self.dedup()
         self.forward()
@@ -177,7 +204,7 @@ class CtrPath:
         if overlap:
             torch.cuda.current_stream(self.dev).wait_event(self._ev_dedup)
         if cfg.backward != "none":
-            self.bwd_update()
+            self.bwd_update(overlap=self.overlap_backward)
 
 
 class HostPipeline:

@@ -592,3 +592,49 @@ def test_host_pipeline_matches_sequential_steps():
     for k in range(len(ws_)):
         np.testing.assert_array_equal(outs[k].numpy(), seq_out[k])
     np.testing.assert_array_equal(_np(pip.table), _np(seq.table))
+
+
+@pytest.mark.parametrize("mode", ["sequential", "two_streams"])
+def test_bwd_update_phases_match_single_call(mode):
+    # the phased update (long runs, short runs, finish), in order on one stream or
+    # with the long runs on a second stream, gives the single call's bits
+    cfg = BWD_CASES["tensornet_b512"]
+    w = W.make_workload(cfg)
+    F, B, d = cfg.num_fields, cfg.batch, cfg.d
+    ref_tab, ref_g, dd = gpu_bwd(cfg, w)
+    assert int(np.diff(dd["run_offsets"]).max()) > 128            # there are long runs
+    n = w["ids"].size
+    tab = torch.empty((cfg.total_rows, d), dtype=torch.float32, device=DEV)
+    ctr.ctr_fill_table(tab, d, 0, cfg.fill_kind, cfg.fill_seed, cfg.fill_scale)
+    gu = torch.full((n, d), float("nan"), device=DEV)
+    ws = ctr.workspace(ctr.ctr_bwd_update_workspace_size(n, d))
+    nu = torch.tensor([dd["n_unique"]], dtype=torch.int64, device=DEV)
+    ro = torch.from_numpy(np.concatenate([dd["run_offsets"], np.zeros(n - dd["n_unique"], np.int32)])).to(DEV)
+    args = (_t(w["grad_pooled"]), F * d, d, _t(w["offsets"]), F, B, ctr.POOL_SUM, _t(dd["unique_rows"]), nu, ro,
+            _t(dd["sorted_bag"]), n, cfg.lr, tab, d, gu)
+    torch.cuda.synchronize()
+    if mode == "sequential":
+        for ph in (ctr.BWD_LONG_RUNS, ctr.BWD_SHORT_RUNS, ctr.BWD_FINISH):
+            ctr.ctr_embedding_bag_bwd_update_phases(*args, ph, ws)
+    else:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            ctr.ctr_embedding_bag_bwd_update_phases(*args, ctr.BWD_LONG_RUNS, ws)
+        ctr.ctr_embedding_bag_bwd_update_phases(*args, ctr.BWD_SHORT_RUNS, ws)
+        torch.cuda.current_stream().wait_stream(side)
+        ctr.ctr_embedding_bag_bwd_update_phases(*args, ctr.BWD_FINISH, ws)
+    assert ctr.ctr_check_status(ws) == 0
+    np.testing.assert_array_equal(_np(tab), ref_tab)
+    np.testing.assert_array_equal(_np(gu)[:dd["n_unique"]], ref_g)
+
+
+def test_bwd_update_phases_rejects_empty_mask():
+    n, d = 8, 16
+    ws = ctr.workspace(ctr.ctr_bwd_update_workspace_size(n, d))
+    z = torch.zeros(64, device=DEV)
+    i64 = torch.zeros(8, dtype=torch.int64, device=DEV)
+    i32 = torch.zeros(9, dtype=torch.int32, device=DEV)
+    with pytest.raises(ctr.CtrError):
+        ctr.ctr_embedding_bag_bwd_update_phases(z, d, d, i64, 1, 2, ctr.POOL_SUM, i64, i64, i32, i32, n, 0.1,
+                                                z.view(4, 16), d, None, 0, ws)
