@@ -259,17 +259,19 @@ int ctr_embedding_bag_bwd_update(const float* grad_pooled, int64_t g_stride_b, i
                                  ctr_stream_t stream);
 
 /* The same update in phases, for callers that overlap them on two streams.
- *   CTR_BWD_LONG_RUNS   runs of more than 128 occurrences: listed, cut into
- *                       pieces of 128 and each piece summed into the workspace
- *   CTR_BWD_SHORT_RUNS  every other run: summed and its row updated
+ *   CTR_BWD_SHORT_RUNS  runs of at most 128 occurrences: summed and their rows
+ *                       updated
+ *   CTR_BWD_LONG_RUNS   every longer run: listed, cut into pieces of 128 and
+ *                       each piece summed into the workspace
  *   CTR_BWD_FINISH      the long runs' pieces combined and their rows updated
- * ctr_embedding_bag_bwd_update runs all three in this order.  LONG_RUNS and
+ * ctr_embedding_bag_bwd_update runs all three in this order (short runs first:
+ * the long runs then find many pooled-gradient rows still in L2).  LONG_RUNS and
  * SHORT_RUNS touch disjoint rows and disjoint workspace words, so they may run
  * concurrently on two streams with the same arguments and workspace; FINISH
  * must be ordered after LONG_RUNS (and both after the dedup that produced the
  * runs).  `phases` is a non-empty mask of the three; the phases it names run
  * in the order above on `stream`. */
-typedef enum { CTR_BWD_LONG_RUNS = 1, CTR_BWD_SHORT_RUNS = 2, CTR_BWD_FINISH = 4 } ctr_bwd_phase;
+typedef enum { CTR_BWD_SHORT_RUNS = 2, CTR_BWD_LONG_RUNS = 1, CTR_BWD_FINISH = 4 } ctr_bwd_phase;
 int ctr_embedding_bag_bwd_update_phases(const float* grad_pooled, int64_t g_stride_b, int64_t g_stride_f,
                                         const int64_t* offsets, int32_t num_fields, int32_t batch, ctr_pool pool,
                                         const int64_t* unique_rows, const int64_t* n_unique,

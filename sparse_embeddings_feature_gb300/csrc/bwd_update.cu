@@ -316,19 +316,65 @@ __global__ void clear_long_state(int64_t* long_count, unsigned long long* piece_
   *piece_counter = 0;
 }
 
-// The long runs (more than kShort occurrences), in any order: each one's
-// unique and its piece count (a run's result does not depend on its slot).
-__global__ void __launch_bounds__(256) long_list_kernel(const BwdArgs a) {
+// The long runs (more than kShort occurrences) in ascending unique order (so
+// the pieces of one table's runs are processed together and share its
+// pooled-gradient rows in L2): per block of kLongChunk uniques a count, an
+// exclusive scan of the counts, then each block writes its runs in order.
+constexpr int kLongChunk = 2048;  // uniques per block (8 per thread)
+
+__global__ void __launch_bounds__(256) long_count_kernel(const BwdArgs a, uint32_t* __restrict__ counts) {
+  __shared__ uint32_t warp_tot[8];
   const int64_t nu = n_uniques(a);
-  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < nu; u += (int64_t)gridDim.x * blockDim.x) {
-    int64_t r0, r1;
-    run_bounds(a, u, r0, r1);
-    const int64_t len = r1 - r0;
-    if (len > kShort) {
-      const int64_t slot = (int64_t)atomicAdd((unsigned long long*)a.long_count, 1ull);
+  const int64_t u0 = (int64_t)blockIdx.x * kLongChunk;
+  uint32_t c = 0;
+#pragma unroll
+  for (int q = 0; q < kLongChunk / 256; ++q) {
+    const int64_t u = u0 + q * 256 + threadIdx.x;
+    if (u < nu) {
+      int64_t r0, r1;
+      run_bounds(a, u, r0, r1);
+      c += (r1 - r0 > kShort) ? 1u : 0u;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
+  if ((threadIdx.x & 31) == 0) warp_tot[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t t = 0;
+    for (int w = 0; w < 8; ++w) t += warp_tot[w];
+    counts[blockIdx.x] = t;
+  }
+}
+
+__global__ void __launch_bounds__(256) long_write_kernel(const BwdArgs a, const uint32_t* __restrict__ starts,
+                                                         const uint32_t* __restrict__ total) {
+  __shared__ uint32_t warp_tot[8];
+  const int64_t nu = n_uniques(a);
+  const int64_t u0 = (int64_t)blockIdx.x * kLongChunk + threadIdx.x * (kLongChunk / 256);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.long_count = *total;
+  uint32_t v[kLongChunk / 256];
+  int64_t len[kLongChunk / 256];
+#pragma unroll
+  for (int q = 0; q < kLongChunk / 256; ++q) {  // this thread's consecutive uniques
+    const int64_t u = u0 + q;
+    len[q] = 0;
+    if (u < nu) {
+      int64_t r0, r1;
+      run_bounds(a, u, r0, r1);
+      len[q] = r1 - r0;
+    }
+    v[q] = len[q] > kShort ? 1u : 0u;
+  }
+  block_exclusive_scan<uint32_t, 256, kLongChunk / 256>(v, warp_tot);
+  const uint32_t base = starts[blockIdx.x];
+#pragma unroll
+  for (int q = 0; q < kLongChunk / 256; ++q) {
+    if (len[q] > kShort) {
+      const int64_t slot = (int64_t)base + v[q];
       if (slot < a.max_long) {
-        a.long_list[slot] = (int32_t)u;
-        a.long_pstart[slot] = (uint32_t)ceil_div(len, kPiece);
+        a.long_list[slot] = (int32_t)(u0 + q);
+        a.long_pstart[slot] = (uint32_t)ceil_div(len[q], kPiece);
       }
     }
   }
@@ -806,6 +852,10 @@ void bwd_layout(WS& ws, int64_t n, int32_t d) {
   ws.template take<uint32_t>((size_t)z.max_long);          // long_pstart
   ws.template take<int32_t>((size_t)z.max_pieces);         // piece_owner
   ws.template take<float>((size_t)z.max_pieces * d);       // partial sums
+  const int64_t blocks = std::max<int64_t>(1, ceil_div(n, (int64_t)kLongChunk));
+  ws.template take<uint32_t>((size_t)blocks);              // long runs per block of uniques, then their scan
+  ws.template take<uint32_t>(1);                           // their total
+  scan_reserve<uint32_t>(ws, blocks);
   scan_reserve<uint32_t>(ws, z.max_long);
 }
 
@@ -838,9 +888,19 @@ int launch_long(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
   clear_long_state<<<1, 1, 0, s>>>(a.long_count, a.work + 1); count_launch();
   if (int st = launch_status()) return st;
   {
-    const int64_t blocks = std::max<int64_t>(1, imin64(ceil_div(n, (int64_t)256), (int64_t)num_sms() * 8));
-    long_list_kernel<<<(unsigned)blocks, 256, 0, s>>>(a); count_launch();
+    // blocks cover the host bound on n_unique (the ID count); blocks past the
+    // device count find no uniques
+    const int64_t blocks = std::max<int64_t>(1, ceil_div(n, (int64_t)kLongChunk));
+    WsCarver lc = c;
+    uint32_t* counts = lc.take<uint32_t>((size_t)blocks);
+    uint32_t* total = lc.take<uint32_t>(1);
+    if (!lc.ok()) return CTR_ERR_WORKSPACE;
+    long_count_kernel<<<(unsigned)blocks, 256, 0, s>>>(a, counts); count_launch();
     if (int st = launch_status()) return st;
+    if (int st = scan_exclusive<uint32_t>(counts, counts, blocks, nullptr, total, lc, s)) return st;
+    long_write_kernel<<<(unsigned)blocks, 256, 0, s>>>(a, counts, total); count_launch();
+    if (int st = launch_status()) return st;
+    c = lc;  // the scan below carves after these
   }
   {
     WsCarver sc = c;
@@ -887,7 +947,8 @@ extern "C" size_t ctr_bwd_update_workspace_size(int64_t n_ids, int32_t d) {
 namespace {
 
 // Validates the arguments, fills the kernels' arguments and runs the phases
-// in `phases` (CTR_BWD_LONG_RUNS, CTR_BWD_SHORT_RUNS, CTR_BWD_FINISH) on s.
+// in `phases` (CTR_BWD_SHORT_RUNS, CTR_BWD_LONG_RUNS, CTR_BWD_FINISH, in this
+// order) on s.
 int bwd_update_phases(const float* grad_pooled, int64_t g_stride_b, int64_t g_stride_f, const int64_t* offsets,
                       int32_t num_fields, int32_t batch, ctr_pool pool, const int64_t* unique_rows,
                       const int64_t* n_unique, const int32_t* run_offsets, const int32_t* sorted_bag, int64_t n_ids,
@@ -945,14 +1006,15 @@ int bwd_update_phases(const float* grad_pooled, int64_t g_stride_b, int64_t g_st
   a.partial = c.take<float>((size_t)z.max_pieces * d);
   if (!c.ok()) return CTR_ERR_WORKSPACE;
   const int cpl = (int)ceil_div(d / 4, 32);
-  if (phases & CTR_BWD_LONG_RUNS) {
-    const int st = cpl <= 1 ? launch_long<1>(a, c, s, n_ids)
-                 : cpl <= 2 ? launch_long<2>(a, c, s, n_ids) : launch_long<4>(a, c, s, n_ids);
-    if (st) return st;
-  }
+  // short runs first: the long runs' pieces then find many pooled-gradient rows in L2
   if (phases & CTR_BWD_SHORT_RUNS) {
     const int st = cpl <= 1 ? launch_short<1>(a, s, n_ids)
                  : cpl <= 2 ? launch_short<2>(a, s, n_ids) : launch_short<4>(a, s, n_ids);
+    if (st) return st;
+  }
+  if (phases & CTR_BWD_LONG_RUNS) {
+    const int st = cpl <= 1 ? launch_long<1>(a, c, s, n_ids)
+                 : cpl <= 2 ? launch_long<2>(a, c, s, n_ids) : launch_long<4>(a, c, s, n_ids);
     if (st) return st;
   }
   if (phases & CTR_BWD_FINISH) return launch_finish(a, s);
@@ -970,7 +1032,7 @@ extern "C" int ctr_embedding_bag_bwd_update(const float* grad_pooled, int64_t g_
                                             ctr_stream_t stream) {
   return bwd_update_phases(grad_pooled, g_stride_b, g_stride_f, offsets, num_fields, batch, pool, unique_rows,
                            n_unique, run_offsets, sorted_bag, n_ids, lr, table, dtype, d, total_rows, grad_unique_out,
-                           CTR_BWD_LONG_RUNS | CTR_BWD_SHORT_RUNS | CTR_BWD_FINISH, ws, ws_bytes,
+                           CTR_BWD_SHORT_RUNS | CTR_BWD_LONG_RUNS | CTR_BWD_FINISH, ws, ws_bytes,
                            (cudaStream_t)stream);
 }
 
