@@ -190,7 +190,7 @@ def algorithmic_bytes(cfg, path, n_ids, n_unique):
 
     gather       the distinct table rows, the IDs, the offsets, the pooled outputs
     gather_rows  the distinct rows read from the table and written to the unique-row matrix
-    sort         four radix passes reading and writing (key, value) pairs
+    sort         each radix pass reads and writes (4-byte key, 4-byte value) pairs
     interaction  X in, [dense | pairs] out;  interaction_bwd: dout and X in, dX out
     bwd_tiles    read-modify-write of the rows of runs <= 128 occurrences, their
                  occurrence list, run bounds and rows, and each pooled-gradient row of
@@ -205,7 +205,11 @@ def algorithmic_bytes(cfg, path, n_ids, n_unique):
     idx_bytes = 4 if cfg.dedup_gather else 8          # int32 inverse into U, or int64 IDs
     out = {"gather": n_unique * row + n_ids * idx_bytes + (nbags + 1) * 8 + nbags * row}
     if cfg.backward != "none" or cfg.dedup_gather:
-        out["sort"] = 4 * n_ids * 16
+        # radix passes of 8 bits over the sort keys: ranks of the distinct rows when
+        # the tables are at most 64x the batch (presence bitmap), else the rows
+        span = n_unique if cfg.total_rows <= 64 * n_ids else cfg.total_rows
+        bits = max(1, int(span - 1).bit_length())
+        out["sort"] = -(-bits // 8) * n_ids * 16
     if cfg.dedup_gather:
         out["gather_rows"] = n_unique * (2 * row + 8)
     if cfg.interaction:
