@@ -307,10 +307,7 @@ __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kerne
           const int tn = t + kWinF;  // refill the slot with occurrence tn
           const uint32_t r = __shfl_sync(kFull, tn < 32 ? cur.row : nxt.row, tn & 31);
           buf[j] = (r != kNoRow) ? *(const float4*)(table + (uint64_t)r * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
-          acc.x += x.x;
-          acc.y += x.y;
-          acc.z += x.z;
-          acc.w += x.w;
+          acc = add4_packed(acc, x);
           if ((cur.lastm >> t) & 1u) {
             const int jb = __shfl_sync(kFull, cur.seg, t);
             const int64_t oj = __shfl_sync(kFull, ooff, jb) - jb * 4 + lane * 4;
