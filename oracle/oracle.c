@@ -31,6 +31,16 @@
  *                                features).
  *   oracle_dot_interaction_bwd   derivative of the interaction above (not on
  *                                the pages; follows from the definition).
+ *   oracle_dot_interaction_mode  the interaction's variants: mode 0 as above;
+ *                                mode 1 all <x_i, x_j> for i >= j ("DHEN"
+ *                                notes, section 3.1: inner products for
+ *                                i <= j); mode 2 the full Gram matrix X X^T
+ *                                ("DHEN" notes, section 3.3, Eq. (7), the
+ *                                input of the cross network).
+ *   oracle_dot_interaction_bwd_mode
+ *                                their derivatives, accumulated entry by
+ *                                entry: dZ_ij adds dZ_ij x_j to dX_i and
+ *                                dZ_ij x_i to dX_j.
  *   oracle_embedding_bag_bwd_update
  *                                TensorNet, Synchronous Architecture (only the
  *                                sparse features present in the batch are
@@ -406,6 +416,111 @@ int oracle_dot_interaction_bwd(const float* dout, const float* X, int32_t B, int
         if (mag_out) mag_out[o] = mag;
       }
     }
+  }
+  return OR_OK;
+}
+
+/* Interaction variants.  Output row of a sample:
+ *   mode 0  [dense (d) | <x_i, x_j>, i > j, at i(i-1)/2 + j]      width d + n(n-1)/2
+ *   mode 1  [dense (d) | <x_i, x_j>, i >= j, at i(i+1)/2 + j]     width d + n(n+1)/2
+ *   mode 2  [<x_i, x_j> for all i, j, at i n + j]                  width n n
+ * (the order of the pairs and whether the dense vector leads are layout
+ * choices: the pages fix which products appear, not where). */
+static int64_t mode_width(int mode, int32_t n, int32_t d) {
+  if (mode == 0) return d + (int64_t)n * (n - 1) / 2;
+  if (mode == 1) return d + (int64_t)n * (n + 1) / 2;
+  return (int64_t)n * n;
+}
+
+/* Output slot of product (i, j) under `mode`, or -1 if the mode omits it. */
+static int64_t mode_slot(int mode, int32_t n, int32_t d, int32_t i, int32_t j) {
+  if (mode == 0) return i > j ? d + (int64_t)i * (i - 1) / 2 + j : -1;
+  if (mode == 1) return i >= j ? d + (int64_t)i * (i + 1) / 2 + j : -1;
+  return (int64_t)i * n + j;
+}
+
+int oracle_dot_interaction_mode(const void* X, int dtype, int32_t B, int32_t n, int32_t d, int mode,
+                                const int64_t* sample_list, int64_t n_list, void* out, double* mag_out) {
+  if (!X || !out || n < 1 || d < 1 || mode < 0 || mode > 2) return OR_ERR_ARG;
+  int64_t width = mode_width(mode, n, d);
+  int64_t ns = sample_list ? n_list : B;
+#pragma omp parallel for schedule(static)
+  for (int64_t k = 0; k < ns; ++k) {
+    int64_t b = sample_list ? sample_list[k] : k;
+    int64_t xb = b * (int64_t)n * d;
+    int64_t ob = k * width;
+    if (mode != 2) {
+      for (int32_t c = 0; c < d; ++c) {
+        double v = load_value(X, dtype, xb + c);
+        store_value(out, dtype, ob + c, v);
+        if (mag_out) mag_out[ob + c] = fabs(v);
+      }
+    }
+    for (int32_t i = 0; i < n; ++i) {
+      for (int32_t j = 0; j < n; ++j) {
+        int64_t slot = mode_slot(mode, n, d, i, j);
+        if (slot < 0) continue;
+        double acc = 0.0, mag = 0.0;
+        for (int32_t c = 0; c < d; ++c) {
+          double p = load_value(X, dtype, xb + (int64_t)i * d + c) * load_value(X, dtype, xb + (int64_t)j * d + c);
+          acc += p;
+          mag += fabs(p);
+        }
+        store_value(out, dtype, ob + slot, acc);
+        if (mag_out) mag_out[ob + slot] = mag;
+      }
+    }
+  }
+  return OR_OK;
+}
+
+/* Derivative of a mode's output: every emitted product Z_ij = <x_i, x_j>
+ * with upstream gradient g adds g x_j to dX_i and g x_i to dX_j (so a
+ * diagonal entry adds 2 g x_i); modes 0 and 1 also pass dout[b][0:d] to
+ * dX_0.  fp64 accumulation, fp32 out. */
+int oracle_dot_interaction_bwd_mode(const float* dout, const float* X, int32_t B, int32_t n, int32_t d, int mode,
+                                    const int64_t* sample_list, int64_t n_list, float* dX, double* mag_out) {
+  if (!dout || !X || !dX || n < 1 || d < 1 || mode < 0 || mode > 2) return OR_ERR_ARG;
+  int64_t width = mode_width(mode, n, d);
+  int64_t ns = sample_list ? n_list : B;
+  int64_t nd = (int64_t)n * d;
+#pragma omp parallel
+  {
+    double* acc = (double*)malloc((size_t)nd * sizeof(double));
+    double* mag = (double*)malloc((size_t)nd * sizeof(double));
+#pragma omp for schedule(static)
+    for (int64_t k = 0; k < ns; ++k) {
+      if (!acc || !mag) continue;
+      int64_t b = sample_list ? sample_list[k] : k;
+      const float* xb = X + b * nd;
+      const float* gb = dout + b * width;
+      for (int64_t e = 0; e < nd; ++e) acc[e] = mag[e] = 0.0;
+      if (mode != 2)
+        for (int32_t c = 0; c < d; ++c) {
+          acc[c] += (double)gb[c];
+          mag[c] += fabs((double)gb[c]);
+        }
+      for (int32_t i = 0; i < n; ++i)
+        for (int32_t j = 0; j < n; ++j) {
+          int64_t slot = mode_slot(mode, n, d, i, j);
+          if (slot < 0) continue;
+          double g = gb[slot];
+          for (int32_t c = 0; c < d; ++c) {
+            double pi = g * (double)xb[(int64_t)j * d + c];  /* into dX_i */
+            double pj = g * (double)xb[(int64_t)i * d + c];  /* into dX_j */
+            acc[(int64_t)i * d + c] += pi;
+            mag[(int64_t)i * d + c] += fabs(pi);
+            acc[(int64_t)j * d + c] += pj;
+            mag[(int64_t)j * d + c] += fabs(pj);
+          }
+        }
+      for (int64_t e = 0; e < nd; ++e) {
+        dX[k * nd + e] = (float)acc[e];
+        if (mag_out) mag_out[k * nd + e] = mag[e];
+      }
+    }
+    free(acc);
+    free(mag);
   }
   return OR_OK;
 }

@@ -47,6 +47,12 @@ def lib():
         L.oracle_dot_interaction.argtypes = [_p, C.c_int, C.c_int32, C.c_int32, C.c_int32, _p, C.c_int64, _p, _p]
         L.oracle_dot_interaction_bwd.restype = C.c_int
         L.oracle_dot_interaction_bwd.argtypes = [_p, _p, C.c_int32, C.c_int32, C.c_int32, _p, C.c_int64, _p, _p]
+        L.oracle_dot_interaction_mode.restype = C.c_int
+        L.oracle_dot_interaction_mode.argtypes = [_p, C.c_int, C.c_int32, C.c_int32, C.c_int32, C.c_int, _p, C.c_int64,
+                                                  _p, _p]
+        L.oracle_dot_interaction_bwd_mode.restype = C.c_int
+        L.oracle_dot_interaction_bwd_mode.argtypes = [_p, _p, C.c_int32, C.c_int32, C.c_int32, C.c_int, _p, C.c_int64,
+                                                      _p, _p]
         L.oracle_embedding_bag_bwd_update.restype = C.c_int
         L.oracle_embedding_bag_bwd_update.argtypes = [_p, C.c_int64, C.c_int64, _p, _p, C.c_int32, C.c_int32, _p,
                                                       _p, C.c_int32, C.c_int, C.c_float, C.c_int32, _p, C.c_int64,
@@ -179,6 +185,45 @@ def dot_interaction_bwd(dout, X, n, d, sample_list=None, with_mag=False):
     st = lib().oracle_dot_interaction_bwd(_ptr(dout), _ptr(X), B, int(n), int(d), _ptr(sl),
                                           0 if sl is None else sl.size, _ptr(dX), _ptr(mag))
     _check(st, "oracle_dot_interaction_bwd")
+    return (dX, mag) if with_mag else dX
+
+
+INTERACTION_MODES = {"cross": 0, "with_self": 1, "full": 2}
+
+
+def interaction_width(n, d, mode="cross"):
+    m = INTERACTION_MODES[mode]
+    return d + n * (n - 1) // 2 if m == 0 else (d + n * (n + 1) // 2 if m == 1 else n * n)
+
+
+def dot_interaction_mode(X, n, d, mode="cross", dtype="f32", sample_list=None, with_mag=False):
+    """The interaction variants: "cross" (i > j, after the dense vector), "with_self"
+    (i >= j, after the dense vector) or "full" (the n x n Gram matrix, row-major)."""
+    X = np.ascontiguousarray(X)
+    B = X.shape[0]
+    width = interaction_width(n, d, mode)
+    sl = None if sample_list is None else _c(sample_list, np.int64)
+    ns = B if sl is None else sl.size
+    out = np.zeros((ns, width), dtype=np.float32 if dtype == "f32" else np.uint16)
+    mag = np.zeros((ns, width), dtype=np.float64) if with_mag else None
+    st = lib().oracle_dot_interaction_mode(_ptr(X), _DT[dtype], B, int(n), int(d), INTERACTION_MODES[mode], _ptr(sl),
+                                           0 if sl is None else sl.size, _ptr(out), _ptr(mag))
+    _check(st, "oracle_dot_interaction_mode")
+    return (out, mag) if with_mag else out
+
+
+def dot_interaction_bwd_mode(dout, X, n, d, mode="cross", sample_list=None, with_mag=False):
+    """dX[B, n, d] of an interaction variant for upstream gradient dout[B, width] (fp32)."""
+    dout = _c(dout, np.float32)
+    X = _c(X, np.float32)
+    B = X.shape[0]
+    sl = None if sample_list is None else _c(sample_list, np.int64)
+    ns = B if sl is None else sl.size
+    dX = np.zeros((ns, n, d), dtype=np.float32)
+    mag = np.zeros((ns, n, d), dtype=np.float64) if with_mag else None
+    st = lib().oracle_dot_interaction_bwd_mode(_ptr(dout), _ptr(X), B, int(n), int(d), INTERACTION_MODES[mode],
+                                               _ptr(sl), 0 if sl is None else sl.size, _ptr(dX), _ptr(mag))
+    _check(st, "oracle_dot_interaction_bwd_mode")
     return (dX, mag) if with_mag else dX
 
 

@@ -313,6 +313,94 @@ def test_interaction_bwd_matches_autograd(oracle):
 
 
 # ---------------------------------------------------------------------------
+# interaction variants: products with the diagonal, the full Gram matrix
+# ---------------------------------------------------------------------------
+def test_interaction_cross_mode_is_the_default_interaction(oracle):
+    rng = np.random.default_rng(21)
+    X = rng.standard_normal((9, 27, 64)).astype(np.float32)
+    np.testing.assert_array_equal(oracle.dot_interaction_mode(X, 27, 64, "cross"), oracle.dot_interaction(X, 27, 64))
+    dout = rng.standard_normal((9, 64 + 351)).astype(np.float32)
+    np.testing.assert_allclose(oracle.dot_interaction_bwd_mode(dout, X, 27, 64, "cross"),
+                               oracle.dot_interaction_bwd(dout, X, 27, 64), rtol=1e-6, atol=1e-6)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_interaction_with_self_identity(oracle, seed):
+    # sum over i >= j of <x_i, x_j> = 1/2 (|sum x|^2 + sum |x|^2): the FM identity
+    # with the diagonal terms added once (integer vectors: exact in fp32 and fp64)
+    rng = np.random.default_rng(seed)
+    B, n, d = 5, 27, 16
+    X = rng.integers(-40, 41, size=(B, n, d)).astype(np.float32)
+    out = oracle.dot_interaction_mode(X, n, d, "with_self")
+    assert out.shape == (B, d + n * (n + 1) // 2)
+    Xi = X.astype(np.int64)
+    s = Xi.sum(axis=1)
+    rhs = ((s * s).sum(axis=1) + (Xi * Xi).sum(axis=(1, 2))) // 2
+    np.testing.assert_array_equal(out[:, d:].astype(np.int64).sum(axis=1), rhs)
+    np.testing.assert_array_equal(out[:, :d], X[:, 0, :])
+    # the diagonal entries are the squared norms, at i(i+1)/2 + i
+    diag = np.array([d + i * (i + 1) // 2 + i for i in range(n)])
+    np.testing.assert_array_equal(out[:, diag].astype(np.int64), (Xi * Xi).sum(axis=2))
+
+
+def test_interaction_with_self_bruteforce(oracle):
+    g = _golden("dlrm_interaction_small.json")
+    vecs = [g["dense"]] + g["pooled"]
+    X = np.array(vecs, dtype=np.float32)[None]
+    n, d = X.shape[1], X.shape[2]
+    out = oracle.dot_interaction_mode(X, n, d, "with_self")[0]
+    expect = list(g["dense"])
+    for i in range(n):
+        for j in range(i + 1):
+            expect.append(sum(a * b for a, b in zip(vecs[i], vecs[j])))
+    assert out.tolist() == expect
+
+
+def test_interaction_full_gram_matches_numpy(oracle):
+    rng = np.random.default_rng(22)
+    B, n, d = 7, 27, 128
+    X = rng.standard_normal((B, n, d)).astype(np.float32)
+    out = oracle.dot_interaction_mode(X, n, d, "full")
+    Xd = X.astype(np.float64)
+    gram = np.einsum("bic,bjc->bij", Xd, Xd)
+    np.testing.assert_array_equal(out, gram.reshape(B, n * n).astype(np.float32))
+    G = out.reshape(B, n, n)
+    np.testing.assert_array_equal(G, G.transpose(0, 2, 1))           # symmetric
+    sub = oracle.dot_interaction_mode(X, n, d, "full", sample_list=[6, 1])
+    np.testing.assert_array_equal(sub, out[[6, 1]])
+
+
+def test_interaction_full_gram_bf16_rounds_once(oracle):
+    rng = np.random.default_rng(23)
+    B, n, d = 3, 9, 64
+    X = W.f32_to_bf16_bits(rng.standard_normal((B, n, d)).astype(np.float32))
+    out = W.bf16_bits_to_f32(oracle.dot_interaction_mode(X, n, d, "full", dtype="bf16"))
+    Xf = W.bf16_bits_to_f32(X).astype(np.float64)
+    ref = np.einsum("bic,bjc->bij", Xf, Xf).reshape(B, n * n)
+    assert np.all(np.abs(out - ref) <= np.abs(ref) * 2.0 ** -8)
+
+
+@pytest.mark.parametrize("mode", ["cross", "with_self", "full"])
+def test_interaction_mode_bwd_matches_autograd(oracle, mode):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(24)
+    B, n, d = 4, 27, 32
+    X = rng.standard_normal((B, n, d)).astype(np.float32)
+    width = oracle.interaction_width(n, d, mode)
+    dout = rng.standard_normal((B, width)).astype(np.float32)
+    dX = oracle.dot_interaction_bwd_mode(dout, X, n, d, mode)
+    Xt = torch.tensor(X, dtype=torch.float64, requires_grad=True)
+    gram = torch.bmm(Xt, Xt.transpose(1, 2))
+    if mode == "full":
+        out = gram.reshape(B, n * n)
+    else:
+        ii, jj = np.tril_indices(n, -1 if mode == "cross" else 0)
+        out = torch.cat([Xt[:, 0, :], gram[:, ii, jj]], dim=1)
+    (out * torch.tensor(dout, dtype=torch.float64)).sum().backward()
+    np.testing.assert_allclose(dX, Xt.grad.numpy().astype(np.float32), rtol=1e-6, atol=1e-6)
+
+
+# ---------------------------------------------------------------------------
 # sparse backward + SGD
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("pool", ["sum", "mean"])
