@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--workload", default="full_step")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller cases for profiling)")
     ap.add_argument("--rows", type=int, default=0, help="override rows per table (smaller cases for profiling)")
+    ap.add_argument("--interaction-mode", default="", choices=["", "cross", "with_self", "full"],
+                    help="interaction variant (default: the workload's, i > j)")
     ap.add_argument("--cpu-sample", type=int, default=16384,
                     help="samples of the batch the oracle runs for cpu_baseline (about 10 s of CPU work)")
     ap.add_argument("--ref-sample", type=int, default=2048,
@@ -57,6 +59,8 @@ def workload_cfg(args):
         kw["batch"] = args.batch
     if args.rows:
         kw["rows_per_table"] = tuple([args.rows] * cfg.num_tables)
+    if getattr(args, "interaction_mode", ""):
+        kw["interaction_mode"] = args.interaction_mode
     return cfg.shrink(**kw) if kw else cfg
 
 
@@ -160,9 +164,13 @@ def oracle_step(cfg, w):
                                  dtype=cfg.dtype, gen=gen)
     if cfg.interaction:
         X = np.concatenate([w["dense"][:, None, :], pooled], axis=1)
-        O.dot_interaction(X, n, d, dtype=cfg.dtype)
+        if cfg.interaction_mode == "cross":
+            O.dot_interaction(X, n, d, dtype=cfg.dtype)
+        else:
+            O.dot_interaction_mode(X, n, d, cfg.interaction_mode, dtype=cfg.dtype)
         if cfg.backward == "full":
-            dX = O.dot_interaction_bwd(w["dout"], X, n, d)
+            dX = (O.dot_interaction_bwd(w["dout"], X, n, d) if cfg.interaction_mode == "cross"
+                  else O.dot_interaction_bwd_mode(w["dout"], X, n, d, cfg.interaction_mode))
             O.embedding_bag_bwd_update(dX[:, 1:, :], w["ids"], w["offsets"], F, B, w["bag_to_table"], w["row_base"],
                                        d, cfg.lr, dd["unique_rows"], gen=gen)
     return w["ids"].size
@@ -403,6 +411,7 @@ def run_ours(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
         "config": {"workload": cfg.name, "batch": cfg.batch, "fields": cfg.num_fields, "tables": cfg.num_tables,
+                   "interaction": cfg.interaction_mode if cfg.interaction else None,
                    "rows_per_table": cfg.rows_per_table[0], "d": cfg.d, "bag_len": list(cfg.bag_len),
                    "ids": list(cfg.ids), "n_ids": n_ids, "n_unique": n_unique, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (tables %.1f GB, ids %.2f GB)" % (

@@ -229,6 +229,26 @@ int ctr_dot_interaction(const void* X, ctr_dtype dtype, int32_t batch, int32_t n
 int ctr_dot_interaction_bwd(const float* dout, const float* X, int32_t batch, int32_t n, int32_t d, float* dX,
                             void* ws, size_t ws_bytes, ctr_stream_t stream);
 
+/* Interaction variants.  CTR_INTERACT_CROSS is ctr_dot_interaction above.
+ * CTR_INTERACT_WITH_SELF keeps the diagonal too ("DHEN" notes, section 3.1:
+ * the AdvancedDLRM module takes all inner products <x_i, x_j> for i <= j):
+ *   out[b] = [ X[b,0,:] | Z ],  Z[i(i+1)/2 + j] = <X[b,i,:], X[b,j,:]>, 0 <= j <= i < n
+ * CTR_INTERACT_FULL_GRAM emits the whole Gram matrix ("DHEN" notes, section
+ * 3.3, Eq. (7): the cross network's input X X^T), no dense vector:
+ *   out[b] = Z,  Z[i n + j] = <X[b,i,:], X[b,j,:]>,  0 <= i, j < n
+ * The order of the products and the leading dense vector are layout choices.
+ * ctr_interaction_width(n, d, mode) is the output row length (-1 for bad
+ * arguments).  The kernels, dtypes and alignment rules are those of
+ * ctr_dot_interaction.  The derivative (fp32) is, with G the upstream gradient
+ * of the emitted products (0 for products the mode omits) and S = G + G^T:
+ *   dX[b,i,:] = sum_j S[i][j] X[b,j,:]  (+ dout[b, 0:d] for i = 0, first two modes). */
+typedef enum { CTR_INTERACT_CROSS = 0, CTR_INTERACT_WITH_SELF = 1, CTR_INTERACT_FULL_GRAM = 2 } ctr_interaction_mode;
+int64_t ctr_interaction_width(int32_t n, int32_t d, int mode);
+int ctr_dot_interaction_mode(const void* X, ctr_dtype dtype, int32_t batch, int32_t n, int32_t d, int mode, void* out,
+                             void* ws, size_t ws_bytes, ctr_stream_t stream);
+int ctr_dot_interaction_bwd_mode(const float* dout, const float* X, int32_t batch, int32_t n, int32_t d, int mode,
+                                 float* dX, void* ws, size_t ws_bytes, ctr_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* a5. Sparse backward: per-unique-row gradient reduce + SGD row update       */
 /* ------------------------------------------------------------------------ */

@@ -13,9 +13,11 @@
 // A and B are the same shared-memory tile (both K-major, 128-byte swizzle),
 // loaded by TMA straight from X viewed as [B*n, d].  The accumulator lives in
 // TMEM (fp32, double-buffered); the epilogue reads it with tcgen05.ld, keeps
-// the strict lower triangle of each diagonal block, rounds to bf16, adds the
-// dense pass-through and writes the samples' output rows with coalesced
-// stores through a shared-memory staging buffer.
+// the products its mode emits from each diagonal block (the strict lower
+// triangle; or with the diagonal, "DHEN" notes section 3.1; or the whole
+// block, the Gram matrix of "DHEN" notes section 3.3, Eq. (7)), rounds to
+// bf16, adds the dense pass-through (first two modes) and writes the samples'
+// output rows with coalesced stores through a shared-memory staging buffer.
 //
 // Roles (persistent CTA, one per SM): warp 0 issues TMA loads, warp 1 owns
 // TMEM and issues the MMAs, warps 2..5 run the epilogue.  Every mbarrier wait
@@ -38,7 +40,7 @@ constexpr int kTcEpiWarps = 4;
 constexpr uint32_t kTmemCols = 256;
 
 struct TcParams {
-  int32_t batch, n, d, S, rows, N, kb, stages, W;
+  int32_t batch, n, d, S, rows, N, kb, stages, W, mode;
   uint32_t stage_bytes, tx_bytes, staging_bytes;
   const __nv_bfloat16* X;
   __nv_bfloat16* out;
@@ -208,7 +210,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
     const int row = q * 32 + lane;       // tile row = TMEM lane
     const int k = row / p.n;             // sample within the tile
     const int r = row - k * p.n;         // vector index within the sample
-    const int tri = r * (r - 1) / 2;
+    // this row's products: columns j < jend of its sample's block, written from slot base
+    //   mode 0: j < r at d + r(r-1)/2;  mode 1: j <= r at d + r(r+1)/2;  mode 2: all j at r n
+    const int jend = p.mode == 0 ? r : (p.mode == 1 ? r + 1 : p.n);
+    const int base = p.mode == 0 ? p.d + r * (r - 1) / 2 : (p.mode == 1 ? p.d + r * (r + 1) / 2 : r * p.n);
     int64_t it = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
       const int acc = (int)(it & 1);
@@ -231,13 +236,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int j = c0 + e - k * p.n;
-          if (valid && j >= 0 && j < r) st[p.d + tri + j] = __float2bfloat16_rn(__uint_as_float(v[e]));
+          if (valid && j >= 0 && j < jend) st[base + j] = __float2bfloat16_rn(__uint_as_float(v[e]));
         }
       }
       fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-      if (valid) {
+      if (valid && p.mode != 2) {
         const __nv_bfloat16* xd = p.X + b * (int64_t)p.n * p.d;  // dense vector of sample b
         for (int c = r; c < p.d / 8; c += p.n) {
           uint4 w = *(const uint4*)(xd + c * 8);
@@ -272,7 +277,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
 
 bool interaction_bf16_tc_supported(int32_t n, int32_t d) { return n >= 2 && n <= 32 && d % 64 == 0 && d <= 256; }
 
-int interaction_bf16_tc(const void* X, int32_t batch, int32_t n, int32_t d, void* out, int* err, cudaStream_t s) {
+int interaction_bf16_tc(const void* X, int32_t batch, int32_t n, int32_t d, int mode, void* out, int* err,
+                        cudaStream_t s) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return CTR_ERR_CUDA;
   TcParams p;
@@ -286,7 +292,8 @@ int interaction_bf16_tc(const void* X, int32_t batch, int32_t n, int32_t d, void
   p.stage_bytes = 16384u * p.kb;
   p.tx_bytes = (uint32_t)(128 * p.rows * p.kb);
   p.stages = std::max(2, std::min(4, (int)((160 * 1024) / p.stage_bytes)));
-  p.W = d + n * (n - 1) / 2;
+  p.mode = mode;
+  p.W = mode == 0 ? d + n * (n - 1) / 2 : (mode == 1 ? d + n * (n + 1) / 2 : n * n);
   p.staging_bytes = (uint32_t)align_up((size_t)p.S * p.W * 2, 16);
   p.X = (const __nv_bfloat16*)X;
   p.out = (__nv_bfloat16*)out;

@@ -48,6 +48,9 @@ _SIGS = {
     "ctr_bwd_update_workspace_size": (_sz, [_i64, _i32]),
     "ctr_embedding_bag_bwd_update": (C.c_int, [_p, _i64, _i64, _p, _i32, _i32, C.c_int, _p, _p, _p, _p, _i64, _f32,
                                                _p, C.c_int, _i32, _i64, _p, _p, _sz, _p]),
+    "ctr_interaction_width": (C.c_int64, [_i32, _i32, C.c_int]),
+    "ctr_dot_interaction_mode": (C.c_int, [_p, C.c_int, _i32, _i32, _i32, C.c_int, _p, _p, _sz, _p]),
+    "ctr_dot_interaction_bwd_mode": (C.c_int, [_p, _p, _i32, _i32, _i32, C.c_int, _p, _p, _sz, _p]),
     "ctr_embedding_bag_bwd_update_phases": (C.c_int, [_p, _i64, _i64, _p, _i32, _i32, C.c_int, _p, _p, _p, _p, _i64,
                                                       _f32, _p, C.c_int, _i32, _i64, _p, C.c_int, _p, _sz, _p]),
 }
@@ -231,6 +234,29 @@ def ctr_dot_interaction_bwd(dout: torch.Tensor, X: torch.Tensor, n: int, d: int,
     st = lib().ctr_dot_interaction_bwd(_ptr(dout), _ptr(X), batch, n, d, _ptr(dX), _ptr(ws), ws.numel(),
                                        _stream(stream))
     _ok("ctr_dot_interaction_bwd", st)
+
+
+INTERACT_CROSS, INTERACT_WITH_SELF, INTERACT_FULL_GRAM = 0, 1, 2
+
+
+def ctr_interaction_width(n: int, d: int, mode: int) -> int:
+    return int(lib().ctr_interaction_width(n, d, mode))
+
+
+def ctr_dot_interaction_mode(X: torch.Tensor, n: int, d: int, mode: int, out: torch.Tensor, ws: torch.Tensor,
+                             stream=None) -> None:
+    batch = X.numel() // (n * d)
+    st = lib().ctr_dot_interaction_mode(_ptr(X), DTYPES[X.dtype], batch, n, d, int(mode), _ptr(out), _ptr(ws),
+                                        ws.numel(), _stream(stream))
+    _ok("ctr_dot_interaction_mode", st)
+
+
+def ctr_dot_interaction_bwd_mode(dout: torch.Tensor, X: torch.Tensor, n: int, d: int, mode: int, dX: torch.Tensor,
+                                 ws: torch.Tensor, stream=None) -> None:
+    batch = X.numel() // (n * d)
+    st = lib().ctr_dot_interaction_bwd_mode(_ptr(dout), _ptr(X), batch, n, d, int(mode), _ptr(dX), _ptr(ws),
+                                            ws.numel(), _stream(stream))
+    _ok("ctr_dot_interaction_bwd_mode", st)
 
 
 def ctr_embedding_bag_bwd_update(grad_pooled: torch.Tensor, g_stride_b: int, g_stride_f: int, offsets: torch.Tensor,

@@ -22,6 +22,7 @@ from . import ctr
 from .workload import Config
 
 TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+_MODES = {"cross": ctr.INTERACT_CROSS, "with_self": ctr.INTERACT_WITH_SELF, "full": ctr.INTERACT_FULL_GRAM}
 
 
 class CtrPath:
@@ -128,11 +129,12 @@ class CtrPath:
 
     def interaction(self) -> None:
         cfg = self.cfg
-        ctr.ctr_dot_interaction(self.X, cfg.n_vectors, cfg.d, self.out, self.ws_int)
+        ctr.ctr_dot_interaction_mode(self.X, cfg.n_vectors, cfg.d, _MODES[cfg.interaction_mode], self.out, self.ws_int)
 
     def interaction_bwd(self) -> None:
         cfg = self.cfg
-        ctr.ctr_dot_interaction_bwd(self.dout, self.X, cfg.n_vectors, cfg.d, self.dX, self.ws_int)
+        ctr.ctr_dot_interaction_bwd_mode(self.dout, self.X, cfg.n_vectors, cfg.d, _MODES[cfg.interaction_mode], self.dX,
+                                         self.ws_int)
 
     def bwd_update(self, grad_unique_out: Optional[torch.Tensor] = None, overlap: bool = False) -> None:
         """Per-unique-row gradient reduce + row update.

@@ -143,6 +143,7 @@ class Config:
     backward: str                   # "none" | "pooled_grad" | "full"
     lr: float
     dedup_gather: bool = False      # pool from the batch-sized unique-row matrix via the inverse map
+    interaction_mode: str = "cross"  # "cross" (i > j) | "with_self" (i >= j) | "full" (n x n Gram matrix)
 
     @property
     def num_tables(self) -> int:
@@ -162,8 +163,11 @@ class Config:
 
     @property
     def out_width(self) -> int:
+        """Interaction output row: [dense | products i > j], [dense | products i >= j] or the n x n Gram matrix."""
         n = self.n_vectors
-        return self.d + n * (n - 1) // 2
+        if self.interaction_mode == "full":
+            return n * n
+        return self.d + (n * (n - 1) // 2 if self.interaction_mode == "cross" else n * (n + 1) // 2)
 
     @property
     def fill_seed(self) -> int:

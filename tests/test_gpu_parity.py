@@ -638,3 +638,56 @@ def test_bwd_update_phases_rejects_empty_mask():
     with pytest.raises(ctr.CtrError):
         ctr.ctr_embedding_bag_bwd_update_phases(z, d, d, i64, 1, 2, ctr.POOL_SUM, i64, i64, i32, i32, n, 0.1,
                                                 z.view(4, 16), d, None, 0, ws)
+
+
+# ---------------------------------------------------------------------------
+# interaction variants: with the diagonal, full Gram matrix
+# ---------------------------------------------------------------------------
+MODES = {"cross": ctr.INTERACT_CROSS, "with_self": ctr.INTERACT_WITH_SELF, "full": ctr.INTERACT_FULL_GRAM}
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("B,n,d,dtype", [(1001, 27, 128, "f32"), (33, 9, 40, "f32"), (1001, 27, 64, "bf16"),
+                                         (130, 32, 128, "bf16"), (77, 2, 256, "bf16"), (50, 27, 48, "bf16")])
+def test_dot_interaction_modes(mode, B, n, d, dtype):
+    X = _rand_X(B, n, d, dtype, seed=B + n + d + 7)
+    Xd = _t(X.view(np.int16) if dtype == "bf16" else X)
+    if dtype == "bf16":
+        Xd = Xd.view(torch.bfloat16)
+    width = ctr.ctr_interaction_width(n, d, MODES[mode])
+    assert width == O.interaction_width(n, d, mode)
+    out = torch.full((B, width), float("nan"), dtype=Xd.dtype, device=DEV)
+    ws = ctr.workspace(ctr.ctr_interaction_workspace_size())
+    ctr.ctr_dot_interaction_mode(Xd, n, d, MODES[mode], out, ws)
+    assert ctr.ctr_check_status(ws) == 0
+    got = _np(out)
+    ref, mag = O.dot_interaction_mode(X, n, d, mode, dtype=dtype, with_mag=True)
+    if dtype == "f32":
+        f32_close(got, ref, mag, d, what=f"interaction {mode}")
+    else:
+        bf16_close(got, ref, mag, d, what=f"interaction {mode}")
+    if mode != "full":
+        np.testing.assert_array_equal(got[:, :d], ref[:, :d])
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("B,n,d", [(1001, 27, 128), (64, 5, 16), (17, 27, 64)])
+def test_dot_interaction_bwd_modes(mode, B, n, d):
+    rng = np.random.default_rng(B * n + d)
+    X = rng.standard_normal((B, n, d)).astype(np.float32)
+    width = O.interaction_width(n, d, mode)
+    dout = rng.standard_normal((B, width)).astype(np.float32)
+    dX = torch.full((B, n, d), float("nan"), device=DEV)
+    ws = ctr.workspace(ctr.ctr_interaction_workspace_size())
+    ctr.ctr_dot_interaction_bwd_mode(_t(dout), _t(X), n, d, MODES[mode], dX, ws)
+    assert ctr.ctr_check_status(ws) == 0
+    ref, mag = O.dot_interaction_bwd_mode(dout, X, n, d, mode, with_mag=True)
+    f32_close(_np(dX), ref, mag, 2 * n + 64, what=f"interaction bwd {mode}")
+
+
+def test_dot_interaction_mode_rejects_bad_mode():
+    X = torch.zeros((4, 5, 16), device=DEV)
+    out = torch.zeros((4, 64), device=DEV)
+    with pytest.raises(ctr.CtrError):
+        ctr.ctr_dot_interaction_mode(X, 5, 16, 3, out, ctr.workspace(256))
+    assert ctr.ctr_interaction_width(5, 16, 3) == -1
