@@ -93,11 +93,13 @@ template <int N, int D, int MODE>
 __global__ void __launch_bounds__(kFwdWarps * 32) interaction_fwd_f32_regs(const float* __restrict__ X, int32_t batch,
                                                                           float* __restrict__ out) {
   static_assert(D == 128, "4 columns per lane");
-  constexpr int P = (int)mode_pairs(N, MODE);
+  // the full Gram matrix is symmetric: compute i >= j once, store (i, j) and (j, i)
+  constexpr int CM = MODE == 2 ? 1 : MODE;
+  constexpr int P = (int)mode_pairs(N, CM);
   constexpr int G = (P + 31) / 32;
   constexpr int W = (int)mode_width(N, D, MODE);
   constexpr int OFF = MODE == 2 ? 0 : D;  // where the products start in an output row
-  constexpr PairTable pt = make_pairs<N, MODE>();
+  constexpr PairTable pt = make_pairs<N, CM>();
   __shared__ __align__(16) float sred[kFwdWarps][32 * kRedStride];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float* red = sred[warp];
@@ -140,7 +142,19 @@ __global__ void __launch_bounds__(kFwdWarps * 32) interaction_fwd_f32_regs(const
 #pragma unroll
       for (int r = 0; r < 32; ++r) acc[r & 3] += red[r * kRedStride + lane];
       const int p = g * 32 + lane;
-      if (p < P) __stcs(ob + OFF + p, (acc[0] + acc[1]) + (acc[2] + acc[3]));
+      if (p < P) {
+        const float dot = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        if (MODE == 2) {
+          int i = (int)((1.f + sqrtf(1.f + 8.f * (float)p)) * 0.5f) - 1;  // pair p = i(i+1)/2 + j, j <= i
+          if (i * (i + 1) / 2 > p) --i;
+          if ((i + 1) * (i + 2) / 2 <= p) ++i;
+          const int j = p - i * (i + 1) / 2;
+          __stcs(ob + i * N + j, dot);
+          if (i != j) __stcs(ob + j * N + i, dot);
+        } else {
+          __stcs(ob + OFF + p, dot);
+        }
+      }
     }
   }
 }
