@@ -47,6 +47,11 @@
  *                                synchronised): the table gradient of the
  *                                pooled output restricted to the batch's rows,
  *                                applied as plain SGD (rule not on the pages).
+ *   oracle_bag_fm                the factorization-machine second-order term
+ *                                of each bag's active embeddings, summed over
+ *                                pairs of positions ("DHEN" notes, section
+ *                                3.1, Solution 2; each occurrence is one
+ *                                active feature).
  *   oracle_table_rows            the counter-based table generator
  *                                (splitmix64, Steele/Lea/Flood 2014); input
  *                                generation, not the method.
@@ -338,6 +343,47 @@ int oracle_embedding_bag_fwd(const void* table, int dtype, int gen_kind, uint64_
       store_value(out, out_dtype, base + c, acc);
       if (mag_out) mag_out[base + c] = mag;
     }
+  }
+  return err;
+}
+
+/* FM second-order term of each bag: fm = sum over pairs of positions i < j
+ * of the bag of <v_i, v_j>, v the table rows of the bag's IDs (a repeated ID
+ * is a repeated feature), independent of the pooling mode.  fp64, rounded
+ * once to fp32.  bag_list (or NULL for all F*B bags, bag-major) selects bags;
+ * out is compact over the list.  mag_out (may be NULL) gets the sum over the
+ * same pairs of sum_c |v_i[c] v_j[c]|. */
+int oracle_bag_fm(const void* table, int dtype, int gen_kind, uint64_t gen_seed, float gen_scale, int32_t d,
+                  const int64_t* ids, const int64_t* offsets, int32_t F, int32_t B, const int32_t* bag_to_table,
+                  const int64_t* row_base, int32_t T, const int64_t* bag_list, int64_t n_list, float* out,
+                  double* mag_out) {
+  if (!ids || !out || d <= 0) return OR_ERR_ARG;
+  int st = check_bags(offsets, F, B);
+  if (st) return st;
+  table_src src = {table, dtype, gen_kind, gen_seed, gen_scale, d};
+  int64_t nb = bag_list ? n_list : (int64_t)F * B;
+  int err = OR_OK;
+#pragma omp parallel for schedule(dynamic, 16)
+  for (int64_t k = 0; k < nb; ++k) {
+    int64_t bag = bag_list ? bag_list[k] : k;
+    int32_t f = (int32_t)(bag / B);
+    double acc = 0.0, mag = 0.0;
+    for (int64_t i = offsets[bag]; i < offsets[bag + 1]; ++i) {
+      for (int64_t j = i + 1; j < offsets[bag + 1]; ++j) {
+        int64_t ki, kj;
+        if (key_of(ids, i, f, bag_to_table, row_base, T, &ki) || key_of(ids, j, f, bag_to_table, row_base, T, &kj)) {
+          err = OR_ERR_INDEX;
+          continue;
+        }
+        for (int32_t c = 0; c < d; ++c) {
+          double p = table_value(&src, ki, c) * table_value(&src, kj, c);
+          acc += p;
+          mag += fabs(p);
+        }
+      }
+    }
+    out[k] = (float)acc;
+    if (mag_out) mag_out[k] = mag;
   }
   return err;
 }

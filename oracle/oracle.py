@@ -47,6 +47,9 @@ def lib():
         L.oracle_dot_interaction.argtypes = [_p, C.c_int, C.c_int32, C.c_int32, C.c_int32, _p, C.c_int64, _p, _p]
         L.oracle_dot_interaction_bwd.restype = C.c_int
         L.oracle_dot_interaction_bwd.argtypes = [_p, _p, C.c_int32, C.c_int32, C.c_int32, _p, C.c_int64, _p, _p]
+        L.oracle_bag_fm.restype = C.c_int
+        L.oracle_bag_fm.argtypes = [_p, C.c_int, C.c_int, C.c_uint64, C.c_float, C.c_int32, _p, _p, C.c_int32,
+                                    C.c_int32, _p, _p, C.c_int32, _p, C.c_int64, _p, _p]
         L.oracle_dot_interaction_mode.restype = C.c_int
         L.oracle_dot_interaction_mode.argtypes = [_p, C.c_int, C.c_int32, C.c_int32, C.c_int32, C.c_int, _p, C.c_int64,
                                                   _p, _p]
@@ -155,6 +158,33 @@ def embedding_bag_fwd(ids, offsets, num_fields, batch, bag_to_table, row_base, d
                                         _ptr(ids), _ptr(offsets), F, B, _ptr(b2t), _ptr(rb), rb.size - 1,
                                         _POOL[pool], _ptr(bl), nl, _ptr(out), odt, sb, sf, _ptr(mag))
     _check(st, "oracle_embedding_bag_fwd")
+    return (out, mag) if with_mag else out
+
+
+def bag_fm(ids, offsets, num_fields, batch, bag_to_table, row_base, d, table=None, dtype="f32", gen=None,
+           bag_list=None, with_mag=False):
+    """FM second-order term of each bag: sum over pairs of positions i < j of <v_i, v_j>.
+
+    Returns fm[F * B] (bag-major: bag f * B + b) or fm[len(bag_list)], fp32, and
+    optionally the magnitude sums (double)."""
+    ids = _c(ids, np.int64)
+    offsets = _c(offsets, np.int64)
+    b2t = _c(bag_to_table, np.int32)
+    rb = _c(row_base, np.int64)
+    if table is not None:
+        table = np.ascontiguousarray(table)
+        gk, gs, gsc = 0, 0, 0.0
+    else:
+        gk, gs, gsc = gen
+    F, B = int(num_fields), int(batch)
+    bl = None if bag_list is None else _c(bag_list, np.int64)
+    nb = F * B if bl is None else bl.size
+    out = np.zeros(nb, dtype=np.float32)
+    mag = np.zeros(nb, dtype=np.float64) if with_mag else None
+    st = lib().oracle_bag_fm(_ptr(table), _DT[dtype], int(gk), C.c_uint64(gs), C.c_float(gsc), int(d), _ptr(ids),
+                             _ptr(offsets), F, B, _ptr(b2t), _ptr(rb), rb.size - 1, _ptr(bl),
+                             0 if bl is None else bl.size, _ptr(out), _ptr(mag))
+    _check(st, "oracle_bag_fm")
     return (out, mag) if with_mag else out
 
 

@@ -313,6 +313,62 @@ def test_interaction_bwd_matches_autograd(oracle):
 
 
 # ---------------------------------------------------------------------------
+# FM second-order term of a bag
+# ---------------------------------------------------------------------------
+def test_bag_fm_golden_identity(oracle):
+    # the golden vectors as the rows of a one-bag table: the pairwise sum equals
+    # 1/2 (|sum v|^2 - sum |v|^2), exactly (integers)
+    g = _golden("fm_identity_small.json")
+    v = np.array(g["vectors"], dtype=np.float32)
+    m, d = v.shape
+    ids = np.arange(m, dtype=np.int64)
+    offsets = np.array([0, m], dtype=np.int64)
+    fm = oracle.bag_fm(ids, offsets, 1, 1, [0], [0, m], d, table=v)
+    s = v.astype(np.int64).sum(axis=0)
+    rhs = Fraction(int((s * s).sum()) - int((v.astype(np.int64) ** 2).sum()), 2)
+    assert Fraction(int(fm[0])) == rhs
+
+
+def test_bag_fm_identity_random_bags(oracle):
+    # integer rows, bags with repeated IDs, empty bags and single-ID bags
+    rng = np.random.default_rng(31)
+    F, B, d, rows = 2, 40, 8, 50
+    table = rng.integers(-30, 31, size=(2 * rows, d)).astype(np.float32)
+    lens = rng.integers(0, 9, size=F * B)
+    lens[:3] = [0, 1, 6]
+    offsets = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    ids = rng.integers(0, 6, size=offsets[-1]).astype(np.int64)   # many repeats
+    rb = np.array([0, rows, 2 * rows], dtype=np.int64)
+    fm = oracle.bag_fm(ids, offsets, F, B, [0, 1], rb, d, table=table)
+    for bag in range(F * B):
+        f = bag // B
+        vs = table[rb[f] + ids[offsets[bag]:offsets[bag + 1]]].astype(np.int64)
+        s = vs.sum(axis=0)
+        expect = ((s * s).sum() - (vs * vs).sum()) // 2
+        assert int(fm[bag]) == expect, bag
+    assert fm[0] == 0 and fm[1] == 0                                 # empty and single-ID bags
+
+
+def test_bag_fm_bruteforce_and_list(oracle):
+    rng = np.random.default_rng(32)
+    F, B, d, rows = 3, 7, 5, 9
+    table = (rng.integers(-64, 64, size=(F * rows, d)) / 16).astype(np.float32)
+    lens = rng.integers(0, 5, size=F * B)
+    offsets = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    ids = rng.integers(0, rows, size=offsets[-1]).astype(np.int64)
+    rb = np.arange(F + 1, dtype=np.int64) * rows
+    fm = oracle.bag_fm(ids, offsets, F, B, list(range(F)), rb, d, table=table)
+    for bag in range(F * B):
+        f = bag // B
+        rws = [table[rb[f] + k] for k in ids[offsets[bag]:offsets[bag + 1]]]
+        ref = sum(Fraction(float(a)) * Fraction(float(b)) for i in range(len(rws)) for j in range(i + 1, len(rws))
+                  for a, b in zip(rws[i], rws[j]))
+        assert Fraction(float(fm[bag])) == ref, bag
+    sub = oracle.bag_fm(ids, offsets, F, B, list(range(F)), rb, d, table=table, bag_list=[20, 3])
+    np.testing.assert_array_equal(sub, fm[[20, 3]])
+
+
+# ---------------------------------------------------------------------------
 # interaction variants: products with the diagonal, the full Gram matrix
 # ---------------------------------------------------------------------------
 def test_interaction_cross_mode_is_the_default_interaction(oracle):
