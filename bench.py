@@ -40,6 +40,7 @@ def parse():
     ap.add_argument("--workload", default="full_step")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller cases for profiling)")
     ap.add_argument("--rows", type=int, default=0, help="override rows per table (smaller cases for profiling)")
+    ap.add_argument("--fm", action="store_true", help="the gather also writes each bag's FM second-order term")
     ap.add_argument("--interaction-mode", default="", choices=["", "cross", "with_self", "full"],
                     help="interaction variant (default: the workload's, i > j)")
     ap.add_argument("--cpu-sample", type=int, default=16384,
@@ -211,7 +212,8 @@ def algorithmic_bytes(cfg, path, n_ids, n_unique):
     F, B, n = cfg.num_fields, cfg.batch, cfg.n_vectors
     nbags = F * B
     idx_bytes = 4 if cfg.dedup_gather else 8          # int32 inverse into U, or int64 IDs
-    out = {"gather": n_unique * row + n_ids * idx_bytes + (nbags + 1) * 8 + nbags * row}
+    out = {"gather": n_unique * row + n_ids * idx_bytes + (nbags + 1) * 8 + nbags * row
+           + (nbags * 4 if path.fm is not None else 0)}
     if cfg.backward != "none" or cfg.dedup_gather:
         # radix passes of 8 bits over the sort keys: ranks of the distinct rows when
         # the tables are at most 64x the batch (presence bitmap), else the rows
@@ -283,7 +285,7 @@ def run_ours(args, rank, world):
     cfg = workload_cfg(args)
     w = W.make_workload(cfg)
     n_ids = int(w["ids"].size)
-    path = CtrPath(cfg, n_ids)
+    path = CtrPath(cfg, n_ids, fm=args.fm)
     path.upload(w)
     torch.cuda.synchronize()
     path.reset_status()
@@ -411,7 +413,7 @@ def run_ours(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
         "config": {"workload": cfg.name, "batch": cfg.batch, "fields": cfg.num_fields, "tables": cfg.num_tables,
-                   "interaction": cfg.interaction_mode if cfg.interaction else None,
+                   "interaction": cfg.interaction_mode if cfg.interaction else None, "fm_term": bool(args.fm),
                    "rows_per_table": cfg.rows_per_table[0], "d": cfg.d, "bag_len": list(cfg.bag_len),
                    "ids": list(cfg.ids), "n_ids": n_ids, "n_unique": n_unique, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (tables %.1f GB, ids %.2f GB)" % (

@@ -199,6 +199,23 @@ int ctr_embedding_bag_fwd(const void* table, ctr_dtype dtype, int32_t d, int64_t
                           void* out, ctr_dtype out_dtype, int64_t out_stride_b, int64_t out_stride_f, void* ws,
                           size_t ws_bytes, ctr_stream_t stream);
 
+/* The same pooled gather, also writing the factorization-machine second-order
+ * term of each bag ("DHEN" notes, section 3.1, Solution 2: the sum over pairs
+ * of active features of <v_i, v_j> equals 1/2 (|sum v|^2 - sum |v|^2), one
+ * pass over the rows):
+ *   fm_out[f*B + b] = 1/2 ( |sum_{i in bag} row_i|^2 - sum_{i in bag} |row_i|^2 )
+ * over the bag's occurrences (a repeated ID is a repeated feature), from the
+ * raw sum whatever the pooling mode; 0 for bags with fewer than two IDs.
+ * fp32 accumulation and arithmetic (the difference of the two terms loses
+ * relative accuracy when they nearly cancel, as the identity's own form does).
+ * fm_out: fp32 [F*B] device, required.  Supported for rows that are a whole
+ * number of 16-byte chunks; CTR_ERR_UNSUPPORTED otherwise. */
+int ctr_embedding_bag_fwd_fm(const void* table, ctr_dtype dtype, int32_t d, int64_t total_rows, const void* indices,
+                             int indices_are_int32, int64_t n_indices, const int64_t* offsets, int32_t num_fields,
+                             int32_t batch, const int32_t* bag_to_table, const int64_t* row_base, int32_t num_tables,
+                             ctr_pool pool, void* out, ctr_dtype out_dtype, int64_t out_stride_b,
+                             int64_t out_stride_f, float* fm_out, void* ws, size_t ws_bytes, ctr_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* a3. Pairwise dot interaction                                              */
 /* Workspace of both interaction calls: ctr_interaction_workspace_size()     */

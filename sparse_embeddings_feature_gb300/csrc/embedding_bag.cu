@@ -106,6 +106,7 @@ struct BagArgs {
   int vec_out;     // output vectors are 16-byte aligned
   int64_t sb, sf;
   int* err;
+  float* fm_out;   // optional: FM second-order term per bag (bag-major), or null
 };
 
 // LPR lanes per row, CPL 16-byte chunks per lane (rows wider than 32 chunks).
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(kBagThreads) bag_fwd_kernel(const BagArgs a, c
     const int64_t base = a.mapped ? fm.base[f] : 0;
     const int64_t nrows = a.mapped ? fm.rows[f] : a.total_rows;
     float acc[CPL][V];
+    float sq = 0.f;  // this lane's share of the sum of squared row entries (FM term)
 #pragma unroll
     for (int c = 0; c < CPL; ++c)
 #pragma unroll
@@ -164,6 +166,10 @@ __global__ void __launch_bounds__(kBagThreads) bag_fwd_kernel(const BagArgs a, c
             unpack(buf[u][c], x, TT());
 #pragma unroll
             for (int v = 0; v < V; ++v) acc[c][v] += x[v];
+            if (a.fm_out) {
+#pragma unroll
+              for (int v = 0; v < V; ++v) sq = fmaf(x[v], x[v], sq);
+            }
           }
       }
     }
@@ -174,6 +180,20 @@ __global__ void __launch_bounds__(kBagThreads) bag_fwd_kernel(const BagArgs a, c
       for (int c = 0; c < CPL; ++c)
 #pragma unroll
         for (int v = 0; v < V; ++v) acc[c][v] += __shfl_xor_sync(kFull, acc[c][v], o);
+    if (a.fm_out) {  // 1/2 (|sum v|^2 - sum |v|^2), from the bag's raw sum
+      float s2 = 0.f;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c)
+#pragma unroll
+        for (int v = 0; v < V; ++v) s2 = fmaf(acc[c][v], acc[c][v], s2);
+      if (grp != 0) s2 = 0.f;  // every lane group holds the whole sum: count one
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        s2 += __shfl_xor_sync(kFull, s2, o);
+        sq += __shfl_xor_sync(kFull, sq, o);
+      }
+      if (lane == 0) a.fm_out[bag] = 0.5f * (s2 - sq);
+    }
     if (a.mean) {
       const int64_t len = o1 - o0;
 #pragma unroll
@@ -243,7 +263,10 @@ __device__ __forceinline__ FlatChunk flat_chunk(const BagArgs& a, int kr, IT id,
   return m;
 }
 
-template <typename IT>
+// With FM, each lane also sums the squares of its columns of the rows, and at a
+// bag's last occurrence the warp reduces |sum v|^2 and sum |v|^2 of the bag
+// and stores 1/2 (|sum v|^2 - sum |v|^2).
+template <typename IT, bool FM>
 __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kernel(const BagArgs a,
                                                                       const __grid_constant__ FieldMap fm) {
   static_assert(32 % kWinF == 0, "the load window must divide the chunk");
@@ -280,6 +303,7 @@ __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kerne
       const float z[4] = {0.f, 0.f, 0.f, 0.f};
       store_out(a.out, __shfl_sync(kFull, ooff, j) - j * 4 + lane * 4, z, 4, a.out_bf16, a.vec_out);
     }
+    if (FM && bvalid && o1 == o0) a.fm_out[bag] = 0.f;
     if (__all_sync(kFull, o1 == o0)) continue;
     const int rel0 = (int)(o0 - S0), rel1 = (int)(o1 - S0);
     const uint32_t base = a.mapped ? (uint32_t)fm.base[f] : 0u;
@@ -296,6 +320,7 @@ __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kerne
       buf[u] = (r != kNoRow) ? *(const float4*)(table + (uint64_t)r * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float sq = 0.f;
     for (int c0 = 0; c0 < total; c0 += 32) {
       const IT id_c = (c0 + 64 + lane < total) ? ib[c0 + 64 + lane] : IT(0);
       const FlatChunk nxt = flat_chunk(a, c0 + 32 + lane, id_b, rel0, rel1, base, nrows);
@@ -308,8 +333,20 @@ __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kerne
           const uint32_t r = __shfl_sync(kFull, tn < 32 ? cur.row : nxt.row, tn & 31);
           buf[j] = (r != kNoRow) ? *(const float4*)(table + (uint64_t)r * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
           acc = add4_packed(acc, x);
+          if (FM) sq = fmaf(x.w, x.w, fmaf(x.z, x.z, fmaf(x.y, x.y, fmaf(x.x, x.x, sq))));
           if ((cur.lastm >> t) & 1u) {
             const int jb = __shfl_sync(kFull, cur.seg, t);
+            if (FM) {
+              float s2 = fmaf(acc.w, acc.w, fmaf(acc.z, acc.z, fmaf(acc.y, acc.y, acc.x * acc.x)));
+              float q = sq;
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) {
+                s2 += __shfl_xor_sync(kFull, s2, o);
+                q += __shfl_xor_sync(kFull, q, o);
+              }
+              if (lane == 0) a.fm_out[blk * 32 + jb] = 0.5f * (s2 - q);
+              sq = 0.f;
+            }
             const int64_t oj = __shfl_sync(kFull, ooff, jb) - jb * 4 + lane * 4;
             float v[4] = {acc.x, acc.y, acc.z, acc.w};
             if (a.mean) {  // a closed bag is never empty
@@ -552,13 +589,14 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
   constexpr int V = Vec<TT>::kN;
   const int64_t nbags = (int64_t)a.F * a.B;
   if (a.d % V != 0) {
+    if (a.fm_out) return CTR_ERR_UNSUPPORTED;
     auto k = bag_fwd_scalar_kernel<TT, IT>;
     k<<<grid_for(k, nbags), kBagThreads, 0, s>>>(a, fm); count_launch();
     return launch_status();
   }
   const int chunks = a.d / V;
   CUtensorMap map;
-  if (std::is_same<TT, float>::value && a.d == 128 && kUseTmaGather && make_row_map(a, &map)) {
+  if (std::is_same<TT, float>::value && a.d == 128 && kUseTmaGather && !a.fm_out && make_row_map(a, &map)) {
     auto k = bag_fwd_tma_kernel<IT>;
     const size_t smem = 1024 + (size_t)kTmaWarps * kTmaStages * kTmaStageBytes;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -573,8 +611,13 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
   if (std::is_same<TT, float>::value && a.d == 128 && a.total_rows < 0xffffffffll) {
     if (cudaMemsetAsync((char*)a.err + kWsCounterOffset, 0, sizeof(unsigned long long), s) != cudaSuccess)
       return CTR_ERR_CUDA;
-    auto k = bag_fwd_flat_kernel<IT>;
-    k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm); count_launch();
+    if (a.fm_out) {
+      auto k = bag_fwd_flat_kernel<IT, true>;
+      k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm); count_launch();
+    } else {
+      auto k = bag_fwd_flat_kernel<IT, false>;
+      k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm); count_launch();
+    }
     return launch_status();
   }
 #define CTR_LAUNCH(LPR, CPL)                                 \
@@ -628,14 +671,13 @@ using namespace ctr;
 
 extern "C" size_t ctr_embedding_bag_workspace_size(void) { return kWsHeader; }
 
-extern "C" int ctr_embedding_bag_fwd(const void* table, ctr_dtype dtype, int32_t d, int64_t total_rows,
-                                     const void* indices, int indices_are_int32, int64_t n_indices,
-                                     const int64_t* offsets,
-                                     int32_t num_fields, int32_t batch, const int32_t* bag_to_table,
-                                     const int64_t* row_base, int32_t num_tables, ctr_pool pool, void* out,
-                                     ctr_dtype out_dtype, int64_t out_stride_b, int64_t out_stride_f, void* ws,
-                                     size_t ws_bytes, ctr_stream_t stream) {
-  cudaStream_t s = (cudaStream_t)stream;
+namespace {
+
+int embedding_bag_fwd(const void* table, ctr_dtype dtype, int32_t d, int64_t total_rows, const void* indices,
+                      int indices_are_int32, int64_t n_indices, const int64_t* offsets, int32_t num_fields,
+                      int32_t batch, const int32_t* bag_to_table, const int64_t* row_base, int32_t num_tables,
+                      ctr_pool pool, void* out, ctr_dtype out_dtype, int64_t out_stride_b, int64_t out_stride_f,
+                      float* fm_out, void* ws, size_t ws_bytes, cudaStream_t s) {
   if (!table || !offsets || !out || d <= 0 || total_rows <= 0) return CTR_ERR_INVALID_ARG;
   if (num_fields <= 0 || batch <= 0) return CTR_ERR_INVALID_ARG;
   if ((dtype != CTR_F32 && dtype != CTR_BF16) || (out_dtype != CTR_F32 && out_dtype != CTR_BF16))
@@ -671,6 +713,7 @@ extern "C" int ctr_embedding_bag_fwd(const void* table, ctr_dtype dtype, int32_t
   a.sb = out_stride_b;
   a.sf = out_stride_f;
   a.err = (int*)ws;
+  a.fm_out = fm_out;
   if ((uintptr_t)table % 16 != 0) return CTR_ERR_INVALID_ARG;
   timing_mark(CTR_KERNEL_GATHER, true, s);
   int st;
@@ -681,6 +724,33 @@ extern "C" int ctr_embedding_bag_fwd(const void* table, ctr_dtype dtype, int32_t
                            : launch_bag_fwd<__nv_bfloat16, int64_t>(a, fm, s);
   timing_mark(CTR_KERNEL_GATHER, false, s);
   return st;
+}
+
+}  // namespace
+
+extern "C" int ctr_embedding_bag_fwd(const void* table, ctr_dtype dtype, int32_t d, int64_t total_rows,
+                                     const void* indices, int indices_are_int32, int64_t n_indices,
+                                     const int64_t* offsets,
+                                     int32_t num_fields, int32_t batch, const int32_t* bag_to_table,
+                                     const int64_t* row_base, int32_t num_tables, ctr_pool pool, void* out,
+                                     ctr_dtype out_dtype, int64_t out_stride_b, int64_t out_stride_f, void* ws,
+                                     size_t ws_bytes, ctr_stream_t stream) {
+  return embedding_bag_fwd(table, dtype, d, total_rows, indices, indices_are_int32, n_indices, offsets, num_fields,
+                           batch, bag_to_table, row_base, num_tables, pool, out, out_dtype, out_stride_b,
+                           out_stride_f, nullptr, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" int ctr_embedding_bag_fwd_fm(const void* table, ctr_dtype dtype, int32_t d, int64_t total_rows,
+                                        const void* indices, int indices_are_int32, int64_t n_indices,
+                                        const int64_t* offsets, int32_t num_fields, int32_t batch,
+                                        const int32_t* bag_to_table, const int64_t* row_base, int32_t num_tables,
+                                        ctr_pool pool, void* out, ctr_dtype out_dtype, int64_t out_stride_b,
+                                        int64_t out_stride_f, float* fm_out, void* ws, size_t ws_bytes,
+                                        ctr_stream_t stream) {
+  if (!fm_out) return CTR_ERR_INVALID_ARG;
+  return embedding_bag_fwd(table, dtype, d, total_rows, indices, indices_are_int32, n_indices, offsets, num_fields,
+                           batch, bag_to_table, row_base, num_tables, pool, out, out_dtype, out_stride_b,
+                           out_stride_f, fm_out, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 extern "C" int ctr_gather_rows(const void* table, ctr_dtype dtype, int32_t d, int64_t total_rows,

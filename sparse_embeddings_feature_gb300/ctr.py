@@ -42,6 +42,8 @@ _SIGS = {
     "ctr_embedding_bag_workspace_size": (_sz, []),
     "ctr_embedding_bag_fwd": (C.c_int, [_p, C.c_int, _i32, _i64, _p, C.c_int, _i64, _p, _i32, _i32, _p, _p, _i32, C.c_int,
                                         _p, C.c_int, _i64, _i64, _p, _sz, _p]),
+    "ctr_embedding_bag_fwd_fm": (C.c_int, [_p, C.c_int, _i32, _i64, _p, C.c_int, _i64, _p, _i32, _i32, _p, _p, _i32,
+                                           C.c_int, _p, C.c_int, _i64, _i64, _p, _p, _sz, _p]),
     "ctr_interaction_workspace_size": (_sz, []),
     "ctr_dot_interaction": (C.c_int, [_p, C.c_int, _i32, _i32, _i32, _p, _p, _sz, _p]),
     "ctr_dot_interaction_bwd": (C.c_int, [_p, _p, _i32, _i32, _i32, _p, _p, _sz, _p]),
@@ -206,7 +208,9 @@ def ctr_embedding_bag_fwd(table: torch.Tensor, d: int, indices: torch.Tensor, of
                           num_fields: int, batch: int, bag_to_table: Optional[Sequence[int]],
                           row_base: Optional[Sequence[int]], pool: int, out: torch.Tensor, out_stride_b: int,
                           out_stride_f: int, ws: torch.Tensor, total_rows: Optional[int] = None,
-                          n_indices: Optional[int] = None, stream=None) -> None:
+                          n_indices: Optional[int] = None, stream=None, fm_out: Optional[torch.Tensor] = None) -> None:
+    """Pooled gather; with fm_out (fp32 [F*B]) the ctr_embedding_bag_fwd_fm call, which also
+    writes each bag's FM second-order term."""
     total = int(table.numel() // d) if total_rows is None else int(total_rows)
     if bag_to_table is not None:
         rb = np.asarray(row_base, dtype=np.int64)
@@ -214,11 +218,15 @@ def ctr_embedding_bag_fwd(table: torch.Tensor, d: int, indices: torch.Tensor, of
     else:
         b2t, rbp, T = None, None, 0
     n_idx = int(indices.numel()) if n_indices is None else int(n_indices)
-    st = lib().ctr_embedding_bag_fwd(_ptr(table), DTYPES[table.dtype], d, total, _ptr(indices),
-                                     1 if indices.dtype == torch.int32 else 0, n_idx, _ptr(offsets), num_fields, batch, b2t,
-                                     rbp, T, pool, _ptr(out), DTYPES[out.dtype], out_stride_b, out_stride_f, _ptr(ws),
-                                     ws.numel(), _stream(stream))
-    _ok("ctr_embedding_bag_fwd", st)
+    args = (_ptr(table), DTYPES[table.dtype], d, total, _ptr(indices), 1 if indices.dtype == torch.int32 else 0, n_idx,
+            _ptr(offsets), num_fields, batch, b2t, rbp, T, pool, _ptr(out), DTYPES[out.dtype], out_stride_b,
+            out_stride_f)
+    if fm_out is None:
+        st = lib().ctr_embedding_bag_fwd(*args, _ptr(ws), ws.numel(), _stream(stream))
+        _ok("ctr_embedding_bag_fwd", st)
+    else:
+        st = lib().ctr_embedding_bag_fwd_fm(*args, _ptr(fm_out), _ptr(ws), ws.numel(), _stream(stream))
+        _ok("ctr_embedding_bag_fwd_fm", st)
 
 
 def ctr_dot_interaction(X: torch.Tensor, n: int, d: int, out: torch.Tensor, ws: torch.Tensor, stream=None) -> None:

@@ -27,7 +27,7 @@ _MODES = {"cross": ctr.INTERACT_CROSS, "with_self": ctr.INTERACT_WITH_SELF, "ful
 
 class CtrPath:
     def __init__(self, cfg: Config, n_ids: int, device="cuda", fill: bool = True, table_chunk_rows: int = 1 << 24,
-                 keep_sorted_pos: bool = False):
+                 keep_sorted_pos: bool = False, fm: bool = False):
         self.cfg = cfg
         self.dev = torch.device(device)
         self.n_ids = int(n_ids)
@@ -60,6 +60,8 @@ class CtrPath:
         self.grad_pooled = torch.empty((B, F, d), dtype=torch.float32, device=self.dev) \
             if cfg.backward == "pooled_grad" else None
         self.grad_unique = None
+        # FM second-order term of every bag, written by the gather when requested
+        self.fm = torch.empty(F * B, dtype=torch.float32, device=self.dev) if fm else None
         total_rows = cfg.total_rows
         self.ws_dedup = ctr.workspace(ctr.ctr_dedup_workspace_size(cap, F, B, total_rows), self.dev)
         self.ws_bag = ctr.workspace(ctr.ctr_embedding_bag_workspace_size(), self.dev)
@@ -122,10 +124,10 @@ class CtrPath:
         if cfg.dedup_gather:
             ctr.ctr_gather_rows(self.table, d, self.unique_rows, self.n_unique, self.U, self.ws_bag)
             ctr.ctr_embedding_bag_fwd(self.U, d, self.inverse, self.offsets, F, B, None, None, pool, out, sb, sf,
-                                      self.ws_bag, n_indices=self.n_ids)
+                                      self.ws_bag, n_indices=self.n_ids, fm_out=self.fm)
         else:
             ctr.ctr_embedding_bag_fwd(self.table, d, self.ids, self.offsets, F, B, self.b2t, self.row_base, pool,
-                                      out, sb, sf, self.ws_bag, n_indices=self.n_ids)
+                                      out, sb, sf, self.ws_bag, n_indices=self.n_ids, fm_out=self.fm)
 
     def interaction(self) -> None:
         cfg = self.cfg

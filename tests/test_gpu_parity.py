@@ -691,3 +691,51 @@ def test_dot_interaction_mode_rejects_bad_mode():
     with pytest.raises(ctr.CtrError):
         ctr.ctr_dot_interaction_mode(X, 5, 16, 3, out, ctr.workspace(256))
     assert ctr.ctr_interaction_width(5, 16, 3) == -1
+
+
+# ---------------------------------------------------------------------------
+# FM second-order term of each bag, fused into the pooled gather
+# ---------------------------------------------------------------------------
+FM_CASES = {
+    "tiny": W.CONFIGS["tiny"],
+    "dlrm_fp32": W.CONFIGS["dlrm_fp32"],
+    "bf16_mean_b256": W.CONFIGS["bf16_large"].shrink(batch=256, rows_per_table=tuple([200_000] * 26)),
+    "tensornet_b300": W.CONFIGS["tensornet"].shrink(batch=300),
+    "full_step_b128": W.CONFIGS["full_step"].shrink(batch=128, rows_per_table=tuple([100_000] * 26)),
+}
+
+
+@pytest.mark.parametrize("name", list(FM_CASES))
+def test_embedding_bag_fwd_fm(name):
+    cfg = FM_CASES[name]
+    w = W.make_workload(cfg, with_grads=False)
+    F, B, d = cfg.num_fields, cfg.batch, cfg.d
+    tdt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
+    tab = torch.empty((cfg.total_rows, d), dtype=tdt, device=DEV)
+    ctr.ctr_fill_table(tab, d, 0, cfg.fill_kind, cfg.fill_seed, cfg.fill_scale)
+    out = torch.empty((B, F, d), dtype=tdt, device=DEV)
+    fm = torch.full((F * B,), float("nan"), device=DEV)
+    ws = ctr.workspace(ctr.ctr_embedding_bag_workspace_size())
+    pool = ctr.POOL_MEAN if cfg.pool == "mean" else ctr.POOL_SUM
+    ctr.ctr_embedding_bag_fwd(tab, d, _t(w["ids"]), _t(w["offsets"]), F, B, w["bag_to_table"], w["row_base"], pool,
+                              out, F * d, d, ws, fm_out=fm)
+    assert ctr.ctr_check_status(ws) == 0
+    ref, mag = O.bag_fm(w["ids"], w["offsets"], F, B, w["bag_to_table"], w["row_base"], d, dtype=cfg.dtype,
+                        gen=_gen(cfg), with_mag=True)
+    # the GPU evaluates 1/2 (|sum v|^2 - sum |v|^2) in fp32: its error is bounded by the
+    # accumulation depth times the two terms' magnitudes, 2 (sum |v_i v_j| + sum |v|^2 / 2)
+    lens = np.diff(w["offsets"])
+    rows = cfg.row_base[np.asarray(cfg.field_to_table)[np.repeat(np.arange(F * B) // B, lens)]] + w["ids"]
+    vals = O.table_rows(cfg.fill_kind, cfg.fill_seed, cfg.fill_scale, d, rows)
+    if cfg.dtype == "bf16":
+        vals = W.bf16_bits_to_f32(vals)
+    per_id = np.concatenate([(vals.astype(np.float64) ** 2).sum(axis=1), [0.0]])  # sentinel: empty last bag
+    sq = np.add.reduceat(per_id, w["offsets"][:-1]) * (lens > 0)
+    depth = int(lens.max()) + d + 16
+    f32_close(_np(fm), ref, 2.0 * mag + sq, depth, what=f"FM term {name}")
+    # the pooled output is the plain gather's
+    out2 = torch.empty_like(out)
+    ctr.ctr_embedding_bag_fwd(tab, d, _t(w["ids"]), _t(w["offsets"]), F, B, w["bag_to_table"], w["row_base"], pool,
+                              out2, F * d, d, ws)
+    assert torch.equal(out.view(torch.int16) if cfg.dtype == "bf16" else out,
+                       out2.view(torch.int16) if cfg.dtype == "bf16" else out2)
