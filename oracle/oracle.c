@@ -52,6 +52,14 @@
  *                                pairs of positions ("DHEN" notes, section
  *                                3.1, Solution 2; each occurrence is one
  *                                active feature).
+ *   oracle_optimizer_step        the row update of the listed rows under SGD,
+ *                                Adagrad (state: sum of squared gradients),
+ *                                row-wise Adagrad (one state per row: sum of
+ *                                the mean squared gradient) or Adam (Kingma
+ *                                and Ba 2015, with bias correction), moments
+ *                                kept only for the rows the batch touches
+ *                                (the pages name no rule; the Baidu page's
+ *                                k-step Adam merge is multi-worker).
  *   oracle_table_rows            the counter-based table generator
  *                                (splitmix64, Steele/Lea/Flood 2014); input
  *                                generation, not the method.
@@ -386,6 +394,59 @@ int oracle_bag_fm(const void* table, int dtype, int gen_kind, uint64_t gen_seed,
     if (mag_out) mag_out[k] = mag;
   }
   return err;
+}
+
+/* One optimizer step on n rows of d values.  w_old and g in fp64 (the row's
+ * value and its exact gradient); state in fp32, updated into s0_out/s1_out:
+ *   opt 0 SGD:               w -= lr g
+ *   opt 1 Adagrad:           s += g^2 (per value);          w -= lr g / (sqrt(s) + eps)
+ *   opt 2 row-wise Adagrad:  s += mean over the row of g^2;  w -= lr g / (sqrt(s) + eps)
+ *   opt 3 Adam (step t >= 1): m = b1 m + (1 - b1) g;  v = b2 v + (1 - b2) g^2;
+ *                            w -= lr (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps)
+ * s0 is the Adagrad state or Adam's m ([n][d]; [n] for row-wise), s1 Adam's v.
+ * New values are computed in fp64 and rounded once (w to the table dtype,
+ * state to fp32). */
+int oracle_optimizer_step(int opt, double lr, double eps, double beta1, double beta2, int64_t step, int32_t d,
+                          int64_t n, const double* w_old, const double* g, const float* s0_in, const float* s1_in,
+                          void* w_new, int dtype, float* s0_out, float* s1_out) {
+  if (opt < 0 || opt > 3 || d <= 0 || n < 0 || !w_old || !g || !w_new) return OR_ERR_ARG;
+  if (opt != 0 && (!s0_in || !s0_out)) return OR_ERR_ARG;
+  if (opt == 3 && (!s1_in || !s1_out || step < 1)) return OR_ERR_ARG;
+  double bc1 = 1.0, bc2 = 1.0;
+  if (opt == 3) {
+    bc1 = 1.0 - pow(beta1, (double)step);
+    bc2 = 1.0 - pow(beta2, (double)step);
+  }
+  for (int64_t r = 0; r < n; ++r) {
+    double srow = 0.0;
+    if (opt == 2) {
+      double msq = 0.0;
+      for (int32_t c = 0; c < d; ++c) msq += g[r * d + c] * g[r * d + c];
+      srow = (double)s0_in[r] + msq / (double)d;
+      s0_out[r] = (float)srow;
+    }
+    for (int32_t c = 0; c < d; ++c) {
+      int64_t e = r * d + c;
+      double gv = g[e], upd;
+      if (opt == 0) {
+        upd = lr * gv;
+      } else if (opt == 1) {
+        double sv = (double)s0_in[e] + gv * gv;
+        s0_out[e] = (float)sv;
+        upd = lr * gv / (sqrt(sv) + eps);
+      } else if (opt == 2) {
+        upd = lr * gv / (sqrt(srow) + eps);
+      } else {
+        double m = beta1 * (double)s0_in[e] + (1.0 - beta1) * gv;
+        double v = beta2 * (double)s1_in[e] + (1.0 - beta2) * gv * gv;
+        s0_out[e] = (float)m;
+        s1_out[e] = (float)v;
+        upd = lr * (m / bc1) / (sqrt(v / bc2) + eps);
+      }
+      store_value(w_new, dtype, e, w_old[e] - upd);
+    }
+  }
+  return OR_OK;
 }
 
 /* ---------------------------------------------------------------------- */

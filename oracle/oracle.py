@@ -47,6 +47,9 @@ def lib():
         L.oracle_dot_interaction.argtypes = [_p, C.c_int, C.c_int32, C.c_int32, C.c_int32, _p, C.c_int64, _p, _p]
         L.oracle_dot_interaction_bwd.restype = C.c_int
         L.oracle_dot_interaction_bwd.argtypes = [_p, _p, C.c_int32, C.c_int32, C.c_int32, _p, C.c_int64, _p, _p]
+        L.oracle_optimizer_step.restype = C.c_int
+        L.oracle_optimizer_step.argtypes = [C.c_int, C.c_double, C.c_double, C.c_double, C.c_double, C.c_int64,
+                                            C.c_int32, C.c_int64, _p, _p, _p, _p, _p, C.c_int, _p, _p]
         L.oracle_bag_fm.restype = C.c_int
         L.oracle_bag_fm.argtypes = [_p, C.c_int, C.c_int, C.c_uint64, C.c_float, C.c_int32, _p, _p, C.c_int32,
                                     C.c_int32, _p, _p, C.c_int32, _p, C.c_int64, _p, _p]
@@ -255,6 +258,31 @@ def dot_interaction_bwd_mode(dout, X, n, d, mode="cross", sample_list=None, with
                                                _ptr(sl), 0 if sl is None else sl.size, _ptr(dX), _ptr(mag))
     _check(st, "oracle_dot_interaction_bwd_mode")
     return (dX, mag) if with_mag else dX
+
+
+OPTIMIZERS = {"sgd": 0, "adagrad": 1, "rowwise_adagrad": 2, "adam": 3}
+
+
+def optimizer_step(opt, w_old, g, lr, state0=None, state1=None, eps=1e-8, beta1=0.9, beta2=0.999, step=1,
+                   dtype="f32"):
+    """One optimizer step on rows w_old [n, d] (fp64 values) with exact gradients g [n, d] (fp64).
+
+    Returns (w_new in the table dtype, state0_new, state1_new) with fp32 states:
+    Adagrad's sum of squares [n, d] (row-wise: [n]) or Adam's m [n, d]; Adam's v [n, d]."""
+    o = OPTIMIZERS[opt]
+    w_old = _c(w_old, np.float64)
+    g = _c(g, np.float64)
+    n, d = w_old.shape
+    s0 = None if state0 is None else _c(state0, np.float32)
+    s1 = None if state1 is None else _c(state1, np.float32)
+    w_new = np.zeros((n, d), dtype=np.float32 if dtype == "f32" else np.uint16)
+    s0o = None if s0 is None else np.zeros_like(s0)
+    s1o = None if s1 is None else np.zeros_like(s1)
+    st = lib().oracle_optimizer_step(o, float(lr), float(eps), float(beta1), float(beta2), int(step), int(d), int(n),
+                                     _ptr(w_old), _ptr(g), _ptr(s0), _ptr(s1), _ptr(w_new), _DT[dtype], _ptr(s0o),
+                                     _ptr(s1o))
+    _check(st, "oracle_optimizer_step")
+    return w_new, s0o, s1o
 
 
 def embedding_bag_bwd_update(G, ids, offsets, num_fields, batch, bag_to_table, row_base, d, lr, target_rows,

@@ -369,6 +369,75 @@ def test_bag_fm_bruteforce_and_list(oracle):
 
 
 # ---------------------------------------------------------------------------
+# optimizer step on the batch's rows
+# ---------------------------------------------------------------------------
+def _rows_and_grads(seed, n=6, d=8):
+    rng = np.random.default_rng(seed)
+    w = rng.standard_normal((n, d)) * 0.1
+    g = rng.standard_normal((n, d))
+    return w, g, rng
+
+
+def test_optimizer_sgd_is_the_plain_update(oracle):
+    w, g, _ = _rows_and_grads(40)
+    new, _, _ = oracle.optimizer_step("sgd", w, g, 0.01)
+    np.testing.assert_array_equal(new, (w - 0.01 * g).astype(np.float32))
+
+
+def test_optimizer_adagrad_matches_torch(oracle):
+    torch = pytest.importorskip("torch")
+    w, g, rng = _rows_and_grads(41)
+    s0 = rng.uniform(0, 2, size=w.shape).astype(np.float32)
+    lr, eps = 0.05, 1e-6
+    new, s_new, _ = oracle.optimizer_step("adagrad", w, g, lr, state0=s0, eps=eps)
+    p = torch.nn.Parameter(torch.tensor(w, dtype=torch.float64))
+    opt = torch.optim.Adagrad([p], lr=lr, eps=eps)
+    opt.state[p]["sum"] = torch.tensor(s0, dtype=torch.float64)
+    opt.state[p]["step"] = torch.tensor(0.0)
+    p.grad = torch.tensor(g, dtype=torch.float64)
+    opt.step()
+    np.testing.assert_allclose(new, p.detach().numpy().astype(np.float32), rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(s_new, opt.state[p]["sum"].numpy().astype(np.float32), rtol=1e-6)
+
+
+def test_optimizer_rowwise_adagrad(oracle):
+    # a gradient constant along the row and a uniform state make row-wise and
+    # elementwise Adagrad the same rule; in general the row's state grows by the
+    # mean squared gradient
+    w, _, rng = _rows_and_grads(42)
+    g = np.repeat(rng.standard_normal((w.shape[0], 1)), w.shape[1], axis=1)
+    srow = rng.uniform(0, 1, size=w.shape[0]).astype(np.float32)
+    a, sa, _ = oracle.optimizer_step("rowwise_adagrad", w, g, 0.1, state0=srow, eps=1e-7)
+    b, sb, _ = oracle.optimizer_step("adagrad", w, g, 0.1, state0=np.repeat(srow[:, None], w.shape[1], axis=1),
+                                     eps=1e-7)
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(sa, sb[:, 0])
+    w, g, _ = _rows_and_grads(43)
+    _, s2, _ = oracle.optimizer_step("rowwise_adagrad", w, g, 0.1, state0=srow)
+    np.testing.assert_allclose(s2, srow + (g * g).mean(axis=1), rtol=1e-6)
+
+
+@pytest.mark.parametrize("step", [1, 7])
+def test_optimizer_adam_matches_torch(oracle, step):
+    torch = pytest.importorskip("torch")
+    w, g, rng = _rows_and_grads(44 + step)
+    m0 = (rng.standard_normal(w.shape) * 0.1).astype(np.float32) if step > 1 else np.zeros(w.shape, np.float32)
+    v0 = (rng.uniform(0, 0.5, size=w.shape)).astype(np.float32) if step > 1 else np.zeros(w.shape, np.float32)
+    lr, b1, b2, eps = 0.01, 0.9, 0.99, 1e-6
+    new, m, v = oracle.optimizer_step("adam", w, g, lr, state0=m0, state1=v0, eps=eps, beta1=b1, beta2=b2, step=step)
+    p = torch.nn.Parameter(torch.tensor(w, dtype=torch.float64))
+    opt = torch.optim.Adam([p], lr=lr, betas=(b1, b2), eps=eps)
+    opt.state[p]["exp_avg"] = torch.tensor(m0, dtype=torch.float64)
+    opt.state[p]["exp_avg_sq"] = torch.tensor(v0, dtype=torch.float64)
+    opt.state[p]["step"] = torch.tensor(float(step - 1))
+    p.grad = torch.tensor(g, dtype=torch.float64)
+    opt.step()
+    np.testing.assert_allclose(new, p.detach().numpy().astype(np.float32), rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(m, opt.state[p]["exp_avg"].numpy().astype(np.float32), rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(v, opt.state[p]["exp_avg_sq"].numpy().astype(np.float32), rtol=1e-6, atol=1e-9)
+
+
+# ---------------------------------------------------------------------------
 # interaction variants: products with the diagonal, the full Gram matrix
 # ---------------------------------------------------------------------------
 def test_interaction_cross_mode_is_the_default_interaction(oracle):
