@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller cases for profiling)")
     ap.add_argument("--rows", type=int, default=0, help="override rows per table (smaller cases for profiling)")
     ap.add_argument("--fm", action="store_true", help="the gather also writes each bag's FM second-order term")
+    ap.add_argument("--optimizer", default="sgd", choices=["sgd", "adagrad", "rowwise_adagrad", "adam"],
+                    help="row update rule (state kept for the batch's rows)")
     ap.add_argument("--interaction-mode", default="", choices=["", "cross", "with_self", "full"],
                     help="interaction variant (default: the workload's, i > j)")
     ap.add_argument("--cpu-sample", type=int, default=16384,
@@ -59,7 +61,13 @@ def workload_cfg(args):
     if args.batch:
         kw["batch"] = args.batch
     if args.rows:
-        kw["rows_per_table"] = tuple([args.rows] * cfg.num_tables)
+        rows = args.rows
+        if cfg.ids[0] == "zipf_hashed":
+            # hashed IDs index 2^row_bits rows: shrink the hash with the table
+            bits = max(1, int(rows).bit_length() - 1)
+            rows = 1 << bits
+            kw["ids"] = (cfg.ids[0], cfg.ids[1], cfg.ids[2], bits)
+        kw["rows_per_table"] = tuple([rows] * cfg.num_tables)
     if getattr(args, "interaction_mode", ""):
         kw["interaction_mode"] = args.interaction_mode
     return cfg.shrink(**kw) if kw else cfg
@@ -239,7 +247,9 @@ def algorithmic_bytes(cfg, path, n_ids, n_unique):
         long_lens = lens[~short]
         pieces = int(((long_lens + 127) // 128).sum().item())
         occ_s = int(occ_short.sum().item())
-        out["bwd_tiles"] = n_short * 2 * row + n_unique * 12 + occ_s * 4 + bags_short * cfg.d * 4
+        state = {"sgd": 0, "adagrad": 2 * cfg.d * 4, "rowwise_adagrad": 2 * 4, "adam": 4 * cfg.d * 4}[
+            path.optimizer]                       # optimizer state read and written per updated row
+        out["bwd_tiles"] = n_short * (2 * row + state) + n_unique * 12 + occ_s * 4 + bags_short * cfg.d * 4
         out["bwd_pieces"] = bags_long * cfg.d * 4 + (n_ids - occ_s) * 4 + pieces * cfg.d * 4
     return out
 
@@ -285,7 +295,7 @@ def run_ours(args, rank, world):
     cfg = workload_cfg(args)
     w = W.make_workload(cfg)
     n_ids = int(w["ids"].size)
-    path = CtrPath(cfg, n_ids, fm=args.fm)
+    path = CtrPath(cfg, n_ids, fm=args.fm, optimizer=args.optimizer)
     path.upload(w)
     torch.cuda.synchronize()
     path.reset_status()
@@ -414,6 +424,7 @@ def run_ours(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
         "config": {"workload": cfg.name, "batch": cfg.batch, "fields": cfg.num_fields, "tables": cfg.num_tables,
                    "interaction": cfg.interaction_mode if cfg.interaction else None, "fm_term": bool(args.fm),
+                   "optimizer": args.optimizer if cfg.backward != "none" else None,
                    "rows_per_table": cfg.rows_per_table[0], "d": cfg.d, "bag_len": list(cfg.bag_len),
                    "ids": list(cfg.ids), "n_ids": n_ids, "n_unique": n_unique, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (tables %.1f GB, ids %.2f GB)" % (

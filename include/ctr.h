@@ -317,6 +317,38 @@ int ctr_embedding_bag_bwd_update_phases(const float* grad_pooled, int64_t g_stri
                                         float* grad_unique_out, int phases, void* ws, size_t ws_bytes,
                                         ctr_stream_t stream);
 
+/* The same update under an optimizer with per-row state, kept only for the
+ * rows the batch touches (the pages name no update rule; these are readings):
+ *   CTR_OPT_SGD               w -= lr g                                   (no state)
+ *   CTR_OPT_ADAGRAD           s += g^2;  w -= lr g / (sqrt(s) + eps)      state0 [total_rows, d]
+ *   CTR_OPT_ROWWISE_ADAGRAD   s += mean over the row of g^2;
+ *                             w -= lr g / (sqrt(s) + eps)                state0 [total_rows]
+ *   CTR_OPT_ADAM              m = b1 m + (1 - b1) g;  v = b2 v + (1 - b2) g^2;
+ *                             w -= lr (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps)
+ *                             (Kingma and Ba 2015)          state0 = m, state1 = v [total_rows, d]
+ * g is the row's reduced gradient (as in ctr_embedding_bag_bwd_update); state
+ * arrays are fp32 device memory owned by the caller, indexed by global row,
+ * 16-byte aligned, and only the batch's rows are read and written.  t = step
+ * (>= 1) is this update's step number for Adam's bias correction; eps > 0.
+ * phases as in ctr_embedding_bag_bwd_update_phases.  The optimizer
+ * arithmetic is fp32. */
+typedef enum { CTR_OPT_SGD = 0, CTR_OPT_ADAGRAD = 1, CTR_OPT_ROWWISE_ADAGRAD = 2, CTR_OPT_ADAM = 3 } ctr_opt_kind;
+typedef struct {
+  int kind;       /* ctr_opt_kind */
+  float eps;
+  float beta1;    /* Adam */
+  float beta2;    /* Adam */
+  int64_t step;   /* Adam: t >= 1 */
+  float* state0;  /* Adagrad sum of squares, or Adam m */
+  float* state1;  /* Adam v */
+} ctr_optimizer;
+int ctr_embedding_bag_bwd_update_opt(const float* grad_pooled, int64_t g_stride_b, int64_t g_stride_f,
+                                     const int64_t* offsets, int32_t num_fields, int32_t batch, ctr_pool pool,
+                                     const int64_t* unique_rows, const int64_t* n_unique, const int32_t* run_offsets,
+                                     const int32_t* sorted_bag, int64_t n_ids, float lr, void* table, ctr_dtype dtype,
+                                     int32_t d, int64_t total_rows, float* grad_unique_out, int phases,
+                                     const ctr_optimizer* opt, void* ws, size_t ws_bytes, ctr_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Allocation-free dedup (no counterpart in the paper)                       */
 /* ------------------------------------------------------------------------ */

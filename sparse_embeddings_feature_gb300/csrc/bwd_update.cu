@@ -30,6 +30,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cmath>
 
 #include "common.cuh"
 #include "scan.cuh"
@@ -62,6 +63,12 @@ struct BwdArgs {
   int64_t total_rows;
   float* grad_out;
   int* err;
+  // optimizer (CTR_OPT_*): Adagrad sum of squares or Adam m in s0 ([rows, d];
+  // [rows] row-wise), Adam v in s1; bc1, bc2 = 1 - beta^step
+  int opt;
+  float eps, beta1, beta2, bc1, bc2;
+  float* s0;
+  float* s1;
   int64_t n_cap;       // occurrences (sorted_bag length)
   int64_t nbags;       // F * B
   int TU;              // uniques per tile
@@ -122,21 +129,115 @@ __device__ __forceinline__ void occ_info(const BwdArgs& a, int64_t s, int64_t& g
 }
 
 // Row update of unique u with gradient chunk g at column 4*ch (w already loaded).
-__device__ __forceinline__ void store_row_chunk(const BwdArgs& a, int64_t row, int64_t u, int ch, float4 g,
-                                                float4 w, uint2 wb, uint64_t pol = 0) {
+// The step of one value under optimizer OPT (state read-modify-written here):
+//   Adagrad  s += g^2,                 step = lr g / (sqrt(s) + eps)
+//   row-wise step = lr g * row_inv     (row_inv = 1 / (sqrt(s_row) + eps), from rowwise_inv)
+//   Adam     m = b1 m + (1 - b1) g,  v = b2 v + (1 - b2) g^2,
+//            step = lr (m / bc1) / (sqrt(v / bc2) + eps)
+// The optimizer is a template argument so that the SGD kernels carry none of it.
+template <int OPT>
+__device__ __forceinline__ float opt_step1(const BwdArgs& a, float g, float& s, float& v, float row_inv) {
+  if constexpr (OPT == CTR_OPT_ADAGRAD) {
+    s = fmaf(g, g, s);
+    return a.lr * g / (sqrtf(s) + a.eps);
+  } else if constexpr (OPT == CTR_OPT_ROWWISE_ADAGRAD) {
+    return a.lr * g * row_inv;
+  } else {
+    s = fmaf(1.f - a.beta1, g, a.beta1 * s);
+    v = fmaf(1.f - a.beta2, g * g, a.beta2 * v);
+    return a.lr * (s / a.bc1) / (sqrtf(v / a.bc2) + a.eps);
+  }
+}
+
+template <int OPT>
+__device__ __forceinline__ float4 opt_step(const BwdArgs& a, float4 g, float4& st, float4& sv, float row_inv) {
+  float4 d;
+  d.x = opt_step1<OPT>(a, g.x, st.x, sv.x, row_inv);
+  d.y = opt_step1<OPT>(a, g.y, st.y, sv.y, row_inv);
+  d.z = opt_step1<OPT>(a, g.z, st.z, sv.z, row_inv);
+  d.w = opt_step1<OPT>(a, g.w, st.w, sv.w, row_inv);
+  return d;
+}
+
+template <int OPT>
+constexpr int kElemStates = OPT == CTR_OPT_ADAGRAD ? 1 : (OPT == CTR_OPT_ADAM ? 2 : 0);
+
+// Row-wise Adagrad: s_row = s_prev + (sum over the row of g^2) / d and the
+// row's 1 / (sqrt(s_row) + eps).  Called by all 32 lanes of a warp with their
+// share of the sum of squares and the row's previous state; lane 0 writes it.
+__device__ __forceinline__ float rowwise_inv(const BwdArgs& a, int64_t row, float ssq, float s_prev) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ssq += __shfl_xor_sync(kFull, ssq, o);
+  const float s = s_prev + ssq / (float)a.d;
+  __syncwarp();  // every lane has read the previous state before lane 0 replaces it
+  if ((threadIdx.x & 31) == 0) a.s0[row] = s;
+  return 1.f / (sqrtf(s) + a.eps);
+}
+
+__device__ __forceinline__ float sumsq4(float4 g) { return fmaf(g.w, g.w, fmaf(g.z, g.z, fmaf(g.y, g.y, g.x * g.x))); }
+
+// Update one 4-value chunk of a row: w -= step, the elementwise states given
+// (st, sv: their previous values) written back.
+template <int OPT>
+__device__ __forceinline__ void store_row_chunk_s(const BwdArgs& a, int64_t row, int64_t u, int ch, float4 g,
+                                                  float4 w, uint2 wb, uint64_t pol, float row_inv, float4 st,
+                                                  float4 sv) {
   if (a.grad_out) *(float4*)(a.grad_out + u * a.d + ch * 4) = g;
+  // SGD keeps its single fused multiply-add per value
+  float4 step = g;
+  float k = -a.lr;
+  if constexpr (OPT != CTR_OPT_SGD) {
+    step = opt_step<OPT>(a, g, st, sv, row_inv);
+    k = -1.f;
+    const int64_t e = row * a.d + ch * 4;
+    if constexpr (kElemStates<OPT> >= 1) *(float4*)(a.s0 + e) = st;
+    if constexpr (kElemStates<OPT> >= 2) *(float4*)(a.s1 + e) = sv;
+  }
   if (!a.bf16) {
-    float4 x = make_float4(fmaf(-a.lr, g.x, w.x), fmaf(-a.lr, g.y, w.y), fmaf(-a.lr, g.z, w.z),
-                           fmaf(-a.lr, g.w, w.w));
+    float4 x = make_float4(fmaf(k, step.x, w.x), fmaf(k, step.y, w.y), fmaf(k, step.z, w.z), fmaf(k, step.w, w.w));
     float* dst = (float*)a.table + row * a.d + ch * 4;
     if (pol) stg_f4_policy(dst, x, pol);
     else *(float4*)dst = x;
   } else {
     const float w0 = __uint_as_float(wb.x << 16), w1 = __uint_as_float(wb.x & 0xffff0000u);
     const float w2 = __uint_as_float(wb.y << 16), w3 = __uint_as_float(wb.y & 0xffff0000u);
-    __nv_bfloat162 p0 = __floats2bfloat162_rn(fmaf(-a.lr, g.x, w0), fmaf(-a.lr, g.y, w1));
-    __nv_bfloat162 p1 = __floats2bfloat162_rn(fmaf(-a.lr, g.z, w2), fmaf(-a.lr, g.w, w3));
+    __nv_bfloat162 p0 = __floats2bfloat162_rn(fmaf(k, step.x, w0), fmaf(k, step.y, w1));
+    __nv_bfloat162 p1 = __floats2bfloat162_rn(fmaf(k, step.z, w2), fmaf(k, step.w, w3));
     *(uint2*)((__nv_bfloat16*)a.table + row * a.d + ch * 4) = make_uint2(*(uint32_t*)&p0, *(uint32_t*)&p1);
+  }
+}
+
+// store_row_chunk_s as one out-of-line copy: the tile kernel's occurrence loop
+// is unrolled 32 times, and an inlined optimizer update in each copy overflows
+// the instruction cache.
+template <int OPT>
+__device__ __noinline__ void store_row_chunk_call(const BwdArgs& a, int64_t row, int64_t u, int ch, float4 g,
+                                                  float4 w, uint2 wb, uint64_t pol, float row_inv, float4 st,
+                                                  float4 sv) {
+  store_row_chunk_s<OPT>(a, row, u, ch, g, w, wb, pol, row_inv, st, sv);
+}
+
+// The same, reading the elementwise states from global memory.
+template <int OPT>
+__device__ __forceinline__ void store_row_chunk_t(const BwdArgs& a, int64_t row, int64_t u, int ch, float4 g,
+                                                  float4 w, uint2 wb, uint64_t pol, float row_inv) {
+  float4 st = make_float4(0.f, 0.f, 0.f, 0.f), sv = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t e = row * a.d + ch * 4;
+  if constexpr (kElemStates<OPT> >= 1) st = *(const float4*)(a.s0 + e);
+  if constexpr (kElemStates<OPT> >= 2) sv = *(const float4*)(a.s1 + e);
+  store_row_chunk_s<OPT>(a, row, u, ch, g, w, wb, pol, row_inv, st, sv);
+}
+
+// The same with the optimizer chosen at run time (for the kernels off the hot path).
+__device__ __forceinline__ void store_row_chunk(const BwdArgs& a, int64_t row, int64_t u, int ch, float4 g,
+                                                float4 w, uint2 wb, uint64_t pol = 0, float row_inv = 0.f) {
+  switch (a.opt) {
+    case CTR_OPT_ADAGRAD: store_row_chunk_t<CTR_OPT_ADAGRAD>(a, row, u, ch, g, w, wb, pol, row_inv); break;
+    case CTR_OPT_ROWWISE_ADAGRAD:
+      store_row_chunk_t<CTR_OPT_ROWWISE_ADAGRAD>(a, row, u, ch, g, w, wb, pol, row_inv);
+      break;
+    case CTR_OPT_ADAM: store_row_chunk_t<CTR_OPT_ADAM>(a, row, u, ch, g, w, wb, pol, row_inv); break;
+    default: store_row_chunk_t<CTR_OPT_SGD>(a, row, u, ch, g, w, wb, pol, row_inv); break;
   }
 }
 
@@ -297,11 +398,21 @@ __global__ void __launch_bounds__(kTileThreads, 2) bwd_tiles_kernel(const BwdArg
 #pragma unroll
       for (int jj = 0; jj < kR; ++jj) {
         if (rj[jj] < 0) continue;
+        float rinv = 0.f;
+        if (a.opt == CTR_OPT_ROWWISE_ADAGRAD) {
+          float q = 0.f;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            const int ch = lane + c * 32;
+            if (ch < chunks) q += sumsq4(my[(j0 + jj) * chunks + ch]);
+          }
+          rinv = rowwise_inv(a, rj[jj], q, a.s0[rj[jj]]);
+        }
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
           const int ch = lane + c * 32;
           if (ch < chunks) store_row_chunk(a, rj[jj], tile * TU + j0 + jj, ch, my[(j0 + jj) * chunks + ch], w[jj][c],
-                                           wb[jj][c]);
+                                           wb[jj][c], 0, rinv);
         }
       }
     }
@@ -396,9 +507,6 @@ __global__ void expand_long_kernel(const BwdArgs a) {
 // and the pooled-gradient rows run in a sliding window of kWin loads that
 // continues across chunks.
 constexpr int kWin = 8;
-#ifndef CTR_TILE_MINB
-#define CTR_TILE_MINB 2
-#endif
 #ifndef CTR_TILE_ASYNC_MINB
 #define CTR_TILE_ASYNC_MINB 3
 #endif
@@ -515,12 +623,9 @@ __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(c
   }
 }
 
-// Tile kernel for rows of at most 512 bytes: the same work as bwd_tiles_kernel
-// with a streaming phase 1.  The flattened occurrences of the tile's short
-// runs are resolved 32 at a time (run by shuffle search, sorted_bag fetched one
-// chunk ahead, one ballot for run ends), and the pooled-gradient rows run in a
-// sliding window kWin deep.  The rows the tile will update are prefetched into
-// L2 when the tile starts.
+// Streaming walk over a tile's short runs (rows of at most 512 bytes): the
+// flattened occurrences are resolved 32 at a time (run by shuffle search,
+// sorted_bag fetched ahead, one ballot for run ends).
 struct TileChunk {
   int32_t bag;     // bag of this lane's occurrence (-1: none)
   int seg;         // run (lane) of the occurrence within the tile
@@ -543,110 +648,6 @@ __device__ __forceinline__ TileChunk tile_chunk(const BwdArgs& a, int kk, int E,
   return c;
 }
 
-__global__ void __launch_bounds__(kTileThreads, CTR_TILE_MINB) bwd_tiles_stream_kernel(const BwdArgs a) {
-  extern __shared__ float4 sacc[];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool col = lane * 4 < a.d;
-  const int chunks = a.d / 4;
-  const int TU = a.TU;
-  float4* my = sacc + (size_t)warp * TU * chunks;
-  const float* Gl = a.G + lane * 4;
-  const int row_bytes = a.d * (a.bf16 ? 2 : 4);
-  const int64_t nu = n_uniques(a);
-  const int64_t ntiles = ceil_div(nu, TU);
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t tile = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; tile < ntiles; tile += nwarps) {
-    const int64_t u = tile * TU + lane;
-    const bool valid = lane < TU && u < nu;
-    int64_t r0 = 0, r1 = 0;
-    if (valid) run_bounds(a, u, r0, r1);
-    const int64_t len = r1 - r0;
-    const bool is_long = valid && len > kShort;
-    const bool is_short = valid && !is_long && len > 0;
-    int64_t row = -1;
-    if (is_short) {
-      row = a.unique_rows[u];
-      if (row < 0 || row >= a.total_rows) {
-        set_error(a.err, CTR_ERR_INDEX_OUT_OF_RANGE);
-        row = -1;
-      } else if ((row_bytes & 15) == 0) {
-        const char* wr = (const char*)a.table + row * row_bytes;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(wr), "r"(row_bytes) : "memory");
-      }
-    }
-    const int slen = is_short ? (int)len : 0;
-    int inc = slen;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(kFull, inc, o);
-      if (lane >= o) inc += y;
-    }
-    const int e = inc - slen;
-    const int E = __shfl_sync(kFull, inc, 31);
-    const int r0i = (int)r0;
-
-    // phase 1: stream the short runs' rows, one accumulator per run into shared memory
-    TileChunk cur = tile_chunk(a, lane, E, e, r0i, slen);
-    TileChunk pend = tile_chunk(a, 32 + lane, E, e, r0i, slen);
-    float sc_cur;
-    uint32_t gcur = bag_g4(a, cur.bag, sc_cur);
-    float4 buf[kWin];
-#pragma unroll
-    for (int q = 0; q < kWin; ++q) {
-      const uint32_t r = __shfl_sync(kFull, gcur, q);
-      buf[q] = (r != kNoG && col) ? ldg_f4(Gl + (uint64_t)r * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = 0; c0 < E; c0 += 32) {
-      const TileChunk ahead = tile_chunk(a, c0 + 64 + lane, E, e, r0i, slen);
-      float sc_nxt;
-      const uint32_t gnxt = bag_g4(a, pend.bag, sc_nxt);
-      for (int g = 0; g < 32; g += kWin) {
-#pragma unroll
-        for (int j = 0; j < kWin; ++j) {
-          const int t = g + j;
-          const float4 x = buf[j];
-          const int tn = t + kWin;
-          const uint32_t r = __shfl_sync(kFull, tn < 32 ? gcur : gnxt, tn & 31);
-          buf[j] = (r != kNoG && col) ? ldg_f4(Gl + (uint64_t)r * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-          if (a.mean) acc = fma4(x, __shfl_sync(kFull, sc_cur, t), acc);
-          else acc = make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
-          if ((cur.lastm >> t) & 1u) {
-            const int sg = __shfl_sync(kFull, cur.seg, t);
-            if (col) my[sg * chunks + lane] = acc;
-            acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-      }
-      cur = pend;
-      pend = ahead;
-      gcur = gnxt;
-      sc_cur = sc_nxt;
-    }
-    __syncwarp();
-    // phase 2: row updates, kRow independent rows in flight
-    constexpr int kRow = 8;
-    for (int j0 = 0; j0 < TU; j0 += kRow) {
-      float4 w[kRow];
-      uint2 wb[kRow];
-      int64_t rj[kRow];
-#pragma unroll
-      for (int jj = 0; jj < kRow; ++jj) {
-        const int j = (j0 + jj) & 31;
-        rj[jj] = __shfl_sync(kFull, row, j);
-        const int lj = __shfl_sync(kFull, slen, j);
-        if (j0 + jj >= TU || lj == 0) rj[jj] = -1;
-        if (rj[jj] >= 0 && col) load_row_chunk(a, rj[jj], lane, w[jj], wb[jj]);
-      }
-#pragma unroll
-      for (int jj = 0; jj < kRow; ++jj)
-        if (rj[jj] >= 0 && col)
-          store_row_chunk(a, rj[jj], tile * TU + j0 + jj, lane, my[(j0 + jj) * chunks + lane], w[jj], wb[jj]);
-    }
-    __syncwarp();
-  }
-}
-
 // Tile kernel with the table rows staged by cp.async: when a tile starts, each
 // lane issues asynchronous copies of its column of the tile's (at most TU)
 // rows into the warp's shared memory, so the rows' DRAM reads overlap the
@@ -664,7 +665,15 @@ __device__ __forceinline__ void cp_async_chunk(uint32_t dst, const void* src, in
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kTileThreads, CTR_TILE_ASYNC_MINB) bwd_tiles_async_kernel(const BwdArgs a) {
+// Optimizers with state run at 2 blocks per SM: the state arithmetic needs the
+// registers, and the staged states the shared memory.
+#ifndef CTR_TILE_OPT_MINB
+#define CTR_TILE_OPT_MINB 2
+#endif
+constexpr int kOptStageBytes = 12288;  // staged bytes per warp (rows and states) with an optimizer
+template <int OPT>
+__global__ void __launch_bounds__(kTileThreads, OPT == CTR_OPT_SGD ? CTR_TILE_ASYNC_MINB : CTR_TILE_OPT_MINB)
+    bwd_tiles_async_kernel(const BwdArgs a) {
   extern __shared__ __align__(16) unsigned char wsm_raw[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool col = lane * 4 < a.d;
@@ -672,8 +681,13 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_ASYNC_MINB) bwd_tiles_a
   const int esz = a.bf16 ? 2 : 4;
   const int row_bytes = a.d * esz;
   const int chunk = 4 * esz;  // this lane's 4 elements
-  unsigned char* wsm = wsm_raw + (size_t)warp * TU * row_bytes;
+  // per warp: the tile's table rows, then its elementwise optimizer states (fp32)
+  constexpr int NS = kElemStates<OPT>;
+  const int state_bytes = a.d * 4;
+  unsigned char* wsm = wsm_raw + (size_t)warp * TU * (row_bytes + NS * state_bytes);
   const uint32_t wsm_s = (uint32_t)__cvta_generic_to_shared(wsm);
+  unsigned char* ssm = wsm + (size_t)TU * row_bytes;  // state s of unique j: ssm + (s * TU + j) * state_bytes
+  const uint32_t ssm_s = (uint32_t)__cvta_generic_to_shared(ssm);
   const float* Gl = a.G + lane * 4;
   // pooled-gradient rows are re-read by every unique of their bags: keep them
   // in L2; the table rows are touched once: stream them
@@ -698,14 +712,23 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_ASYNC_MINB) bwd_tiles_a
         row = -1;
       }
     }
-    // stage this tile's table rows (each lane its own column)
+    // stage this tile's table rows and states (each lane its own column)
     for (int j = 0; j < TU; ++j) {
       const int64_t rj = __shfl_sync(kFull, row, j);
-      if (rj >= 0 && col)
+      if (rj >= 0 && col) {
         cp_async_chunk(wsm_s + j * row_bytes + lane * chunk, (const char*)a.table + rj * row_bytes + lane * chunk,
                        chunk, pol_stream);
+        if constexpr (NS >= 1)
+          cp_async_chunk(ssm_s + j * state_bytes + lane * 16, a.s0 + rj * a.d + lane * 4, 16, pol_stream);
+        if constexpr (NS >= 2)
+          cp_async_chunk(ssm_s + (TU + j) * state_bytes + lane * 16, a.s1 + rj * a.d + lane * 4, 16, pol_stream);
+      }
     }
     cp_async_commit();
+    float s_row = 0.f;  // row-wise Adagrad: the state of this lane's unique, fetched while the tile streams
+    if constexpr (OPT == CTR_OPT_ROWWISE_ADAGRAD) {
+      if (row >= 0) s_row = a.s0[row];
+    }
     const int slen = is_short ? (int)len : 0;
     int inc = slen;
 #pragma unroll
@@ -746,6 +769,11 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_ASYNC_MINB) bwd_tiles_a
           if ((cur.lastm >> t) & 1u) {
             const int sg = __shfl_sync(kFull, cur.seg, t);
             const int64_t rs = __shfl_sync(kFull, row, sg);
+            float rinv = 0.f;
+            if constexpr (OPT == CTR_OPT_ROWWISE_ADAGRAD) {
+              const float sp = __shfl_sync(kFull, s_row, sg);
+              if (rs >= 0) rinv = rowwise_inv(a, rs, col ? sumsq4(acc) : 0.f, sp);
+            }
             if (rs >= 0 && col) {
               if (!staged) {
                 cp_async_wait_all();  // this lane's own copies only: no warp barrier needed
@@ -756,7 +784,14 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_ASYNC_MINB) bwd_tiles_a
               uint2 wb = make_uint2(0u, 0u);
               if (!a.bf16) w = *(const float4*)wp;
               else wb = *(const uint2*)wp;
-              store_row_chunk(a, rs, tile * TU + sg, lane, acc, w, wb, pol_stream);
+              float4 st = make_float4(0.f, 0.f, 0.f, 0.f), sv = make_float4(0.f, 0.f, 0.f, 0.f);
+              if constexpr (NS >= 1) st = *(const float4*)(ssm + sg * state_bytes + lane * 16);
+              if constexpr (NS >= 2) sv = *(const float4*)(ssm + (TU + sg) * state_bytes + lane * 16);
+              // the elementwise optimizers' updates (a divide and a square root per value) out of line
+              if constexpr (OPT == CTR_OPT_ADAGRAD || OPT == CTR_OPT_ADAM)
+                store_row_chunk_call<OPT>(a, rs, tile * TU + sg, lane, acc, w, wb, pol_stream, rinv, st, sv);
+              else
+                store_row_chunk_s<OPT>(a, rs, tile * TU + sg, lane, acc, w, wb, pol_stream, rinv, st, sv);
             }
             acc = make_float4(0.f, 0.f, 0.f, 0.f);
           }
@@ -819,11 +854,17 @@ __global__ void __launch_bounds__(kCombThreads) combine_long_kernel(const BwdArg
       if (row < 0 || row >= a.total_rows) {
         if (lane == 0) set_error(a.err, CTR_ERR_INDEX_OUT_OF_RANGE);
       } else {
+        float rinv = 0.f;
+        if (a.opt == CTR_OPT_ROWWISE_ADAGRAD) {
+          float q = 0.f;
+          for (int ch = lane; ch < chunks; ch += 32) q += sumsq4(*(float4*)(sm + ch * 4));
+          rinv = rowwise_inv(a, row, q, a.s0[row]);
+        }
         for (int ch = lane; ch < chunks; ch += 32) {
           float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
           uint2 wb = make_uint2(0u, 0u);
           load_row_chunk(a, row, ch, w, wb);
-          store_row_chunk(a, row, u, ch, *(float4*)(sm + ch * 4), w, wb);
+          store_row_chunk(a, row, u, ch, *(float4*)(sm + ch * 4), w, wb, 0, rinv);
         }
       }
     }
@@ -871,8 +912,14 @@ int launch_short(const BwdArgs& a, cudaStream_t s, int64_t n) {
   const int chunks = a.d / 4;
   const size_t acc_smem = (size_t)kTileWarps * a.TU * chunks * sizeof(float4);
   const bool use_async = CPL == 1 && a.g4_ok;
-  auto tk = use_async ? bwd_tiles_async_kernel : bwd_tiles_kernel<CPL>;
-  const size_t tile_smem = use_async ? (size_t)kTileWarps * a.TU * a.d * (a.bf16 ? 2 : 4) : acc_smem;
+  auto async_k = a.opt == CTR_OPT_ADAGRAD           ? bwd_tiles_async_kernel<CTR_OPT_ADAGRAD>
+                 : a.opt == CTR_OPT_ROWWISE_ADAGRAD ? bwd_tiles_async_kernel<CTR_OPT_ROWWISE_ADAGRAD>
+                 : a.opt == CTR_OPT_ADAM            ? bwd_tiles_async_kernel<CTR_OPT_ADAM>
+                                                    : bwd_tiles_async_kernel<CTR_OPT_SGD>;
+  auto tk = use_async ? async_k : bwd_tiles_kernel<CPL>;
+  const int ns = a.opt == CTR_OPT_ADAGRAD ? 1 : (a.opt == CTR_OPT_ADAM ? 2 : 0);
+  const size_t tile_smem =
+      use_async ? (size_t)kTileWarps * a.TU * ((size_t)a.d * (a.bf16 ? 2 : 4) + (size_t)ns * a.d * 4) : acc_smem;
   if (tile_smem > 48 * 1024 &&
       cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tile_smem) != cudaSuccess)
     return CTR_ERR_CUDA;
@@ -953,7 +1000,15 @@ int bwd_update_phases(const float* grad_pooled, int64_t g_stride_b, int64_t g_st
                       int32_t num_fields, int32_t batch, ctr_pool pool, const int64_t* unique_rows,
                       const int64_t* n_unique, const int32_t* run_offsets, const int32_t* sorted_bag, int64_t n_ids,
                       float lr, void* table, ctr_dtype dtype, int32_t d, int64_t total_rows, float* grad_unique_out,
-                      int phases, void* ws, size_t ws_bytes, cudaStream_t s) {
+                      int phases, const ctr_optimizer* opt, void* ws, size_t ws_bytes, cudaStream_t s) {
+  const int kind = opt ? opt->kind : CTR_OPT_SGD;
+  if (kind < CTR_OPT_SGD || kind > CTR_OPT_ADAM) return CTR_ERR_INVALID_ARG;
+  if (kind != CTR_OPT_SGD && (!opt->state0 || (uintptr_t)opt->state0 % 16 != 0 || !(opt->eps > 0.f)))
+    return CTR_ERR_INVALID_ARG;
+  if (kind == CTR_OPT_ADAM &&
+      (!opt->state1 || (uintptr_t)opt->state1 % 16 != 0 || opt->step < 1 || !(opt->beta1 >= 0.f && opt->beta1 < 1.f) ||
+       !(opt->beta2 >= 0.f && opt->beta2 < 1.f)))
+    return CTR_ERR_INVALID_ARG;
   if (!grad_pooled || !offsets || !unique_rows || !n_unique || !run_offsets || !table) return CTR_ERR_INVALID_ARG;
   if (num_fields <= 0 || batch <= 0 || d <= 0 || total_rows <= 0 || n_ids < 0) return CTR_ERR_INVALID_ARG;
   if (n_ids > 0 && !sorted_bag) return CTR_ERR_INVALID_ARG;
@@ -989,9 +1044,24 @@ int bwd_update_phases(const float* grad_pooled, int64_t g_stride_b, int64_t g_st
   a.total_rows = total_rows;
   a.grad_out = grad_unique_out;
   a.err = (int*)ws;
+  a.opt = kind;
+  a.eps = opt ? opt->eps : 0.f;
+  a.beta1 = opt ? opt->beta1 : 0.f;
+  a.beta2 = opt ? opt->beta2 : 0.f;
+  a.bc1 = kind == CTR_OPT_ADAM ? (float)(1.0 - std::pow((double)opt->beta1, (double)opt->step)) : 1.f;
+  a.bc2 = kind == CTR_OPT_ADAM ? (float)(1.0 - std::pow((double)opt->beta2, (double)opt->step)) : 1.f;
+  a.s0 = kind != CTR_OPT_SGD ? opt->state0 : nullptr;
+  a.s1 = kind == CTR_OPT_ADAM ? opt->state1 : nullptr;
   a.n_cap = n_ids;
   a.nbags = (int64_t)num_fields * batch;
-  a.TU = std::max(1, std::min(32, kAccFloats / d));
+  {
+    // uniques per tile: the tile kernel stages the tile's rows and elementwise
+    // states in kAccFloats * 4 bytes of shared memory per warp
+    const int ns = kind == CTR_OPT_ADAGRAD ? 1 : (kind == CTR_OPT_ADAM ? 2 : 0);
+    const int staged = d * (dtype == CTR_BF16 ? 2 : 4) + ns * d * 4;
+    const int budget = kind == CTR_OPT_SGD ? kAccFloats * 4 : kOptStageBytes;
+    a.TU = std::max(1, std::min({32, kAccFloats / d, budget / staged}));
+  }
   {
     const int64_t max_off = (int64_t)(batch - 1) * g_stride_b + (int64_t)(num_fields - 1) * g_stride_f + d;
     a.g4_ok = (max_off >> 2) < (int64_t)0xffffffffll && n_ids < ((int64_t)1 << 31);
@@ -1032,7 +1102,7 @@ extern "C" int ctr_embedding_bag_bwd_update(const float* grad_pooled, int64_t g_
                                             ctr_stream_t stream) {
   return bwd_update_phases(grad_pooled, g_stride_b, g_stride_f, offsets, num_fields, batch, pool, unique_rows,
                            n_unique, run_offsets, sorted_bag, n_ids, lr, table, dtype, d, total_rows, grad_unique_out,
-                           CTR_BWD_SHORT_RUNS | CTR_BWD_LONG_RUNS | CTR_BWD_FINISH, ws, ws_bytes,
+                           CTR_BWD_SHORT_RUNS | CTR_BWD_LONG_RUNS | CTR_BWD_FINISH, nullptr, ws, ws_bytes,
                            (cudaStream_t)stream);
 }
 
@@ -1046,5 +1116,18 @@ extern "C" int ctr_embedding_bag_bwd_update_phases(const float* grad_pooled, int
                                                    ctr_stream_t stream) {
   return bwd_update_phases(grad_pooled, g_stride_b, g_stride_f, offsets, num_fields, batch, pool, unique_rows,
                            n_unique, run_offsets, sorted_bag, n_ids, lr, table, dtype, d, total_rows, grad_unique_out,
-                           phases, ws, ws_bytes, (cudaStream_t)stream);
+                           phases, nullptr, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" int ctr_embedding_bag_bwd_update_opt(const float* grad_pooled, int64_t g_stride_b, int64_t g_stride_f,
+                                                const int64_t* offsets, int32_t num_fields, int32_t batch,
+                                                ctr_pool pool, const int64_t* unique_rows, const int64_t* n_unique,
+                                                const int32_t* run_offsets, const int32_t* sorted_bag, int64_t n_ids,
+                                                float lr, void* table, ctr_dtype dtype, int32_t d, int64_t total_rows,
+                                                float* grad_unique_out, int phases, const ctr_optimizer* opt, void* ws,
+                                                size_t ws_bytes, ctr_stream_t stream) {
+  if (!opt) return CTR_ERR_INVALID_ARG;
+  return bwd_update_phases(grad_pooled, g_stride_b, g_stride_f, offsets, num_fields, batch, pool, unique_rows,
+                           n_unique, run_offsets, sorted_bag, n_ids, lr, table, dtype, d, total_rows, grad_unique_out,
+                           phases, opt, ws, ws_bytes, (cudaStream_t)stream);
 }

@@ -51,6 +51,8 @@ _SIGS = {
     "ctr_embedding_bag_bwd_update": (C.c_int, [_p, _i64, _i64, _p, _i32, _i32, C.c_int, _p, _p, _p, _p, _i64, _f32,
                                                _p, C.c_int, _i32, _i64, _p, _p, _sz, _p]),
     "ctr_interaction_width": (C.c_int64, [_i32, _i32, C.c_int]),
+    "ctr_embedding_bag_bwd_update_opt": (C.c_int, [_p, _i64, _i64, _p, _i32, _i32, C.c_int, _p, _p, _p, _p, _i64,
+                                                   _f32, _p, C.c_int, _i32, _i64, _p, C.c_int, _p, _p, _sz, _p]),
     "ctr_dot_interaction_mode": (C.c_int, [_p, C.c_int, _i32, _i32, _i32, C.c_int, _p, _p, _sz, _p]),
     "ctr_dot_interaction_bwd_mode": (C.c_int, [_p, _p, _i32, _i32, _i32, C.c_int, _p, _p, _sz, _p]),
     "ctr_embedding_bag_bwd_update_phases": (C.c_int, [_p, _i64, _i64, _p, _i32, _i32, C.c_int, _p, _p, _p, _p, _i64,
@@ -281,6 +283,35 @@ def ctr_embedding_bag_bwd_update(grad_pooled: torch.Tensor, g_stride_b: int, g_s
 
 
 BWD_LONG_RUNS, BWD_SHORT_RUNS, BWD_FINISH = 1, 2, 4
+BWD_ALL = BWD_SHORT_RUNS | BWD_LONG_RUNS | BWD_FINISH
+OPT_SGD, OPT_ADAGRAD, OPT_ROWWISE_ADAGRAD, OPT_ADAM = 0, 1, 2, 3
+
+
+class CtrOptimizer(C.Structure):
+    """ctr_optimizer of ctr.h."""
+    _fields_ = [("kind", C.c_int), ("eps", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float),
+                ("step", C.c_int64), ("state0", C.c_void_p), ("state1", C.c_void_p)]
+
+
+def optimizer(kind: int, eps: float = 1e-8, beta1: float = 0.9, beta2: float = 0.999, step: int = 1,
+              state0: Optional[torch.Tensor] = None, state1: Optional[torch.Tensor] = None) -> CtrOptimizer:
+    return CtrOptimizer(int(kind), float(eps), float(beta1), float(beta2), int(step),
+                        None if state0 is None else _ptr(state0), None if state1 is None else _ptr(state1))
+
+
+def ctr_embedding_bag_bwd_update_opt(grad_pooled: torch.Tensor, g_stride_b: int, g_stride_f: int,
+                                     offsets: torch.Tensor, num_fields: int, batch: int, pool: int,
+                                     unique_rows: torch.Tensor, n_unique: torch.Tensor, run_offsets: torch.Tensor,
+                                     sorted_bag: torch.Tensor, n_ids: int, lr: float, table: torch.Tensor, d: int,
+                                     grad_unique_out: Optional[torch.Tensor], phases: int, opt: CtrOptimizer,
+                                     ws: torch.Tensor, stream=None) -> None:
+    total_rows = table.numel() // d
+    st = lib().ctr_embedding_bag_bwd_update_opt(_ptr(grad_pooled), g_stride_b, g_stride_f, _ptr(offsets), num_fields,
+                                                batch, pool, _ptr(unique_rows), _ptr(n_unique), _ptr(run_offsets),
+                                                _ptr(sorted_bag), n_ids, lr, _ptr(table), DTYPES[table.dtype], d,
+                                                total_rows, _ptr(grad_unique_out), int(phases), C.addressof(opt),
+                                                _ptr(ws), ws.numel(), _stream(stream))
+    _ok("ctr_embedding_bag_bwd_update_opt", st)
 
 
 def ctr_embedding_bag_bwd_update_phases(grad_pooled: torch.Tensor, g_stride_b: int, g_stride_f: int,

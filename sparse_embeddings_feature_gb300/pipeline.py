@@ -27,7 +27,8 @@ _MODES = {"cross": ctr.INTERACT_CROSS, "with_self": ctr.INTERACT_WITH_SELF, "ful
 
 class CtrPath:
     def __init__(self, cfg: Config, n_ids: int, device="cuda", fill: bool = True, table_chunk_rows: int = 1 << 24,
-                 keep_sorted_pos: bool = False, fm: bool = False):
+                 keep_sorted_pos: bool = False, fm: bool = False, optimizer: str = "sgd", eps: float = 1e-8,
+                 betas=(0.9, 0.999)):
         self.cfg = cfg
         self.dev = torch.device(device)
         self.n_ids = int(n_ids)
@@ -62,6 +63,15 @@ class CtrPath:
         self.grad_unique = None
         # FM second-order term of every bag, written by the gather when requested
         self.fm = torch.empty(F * B, dtype=torch.float32, device=self.dev) if fm else None
+        # optimizer state of the row update (zero-initialised, indexed by global row)
+        self.optimizer = optimizer
+        self.opt_kind = {"sgd": ctr.OPT_SGD, "adagrad": ctr.OPT_ADAGRAD, "rowwise_adagrad": ctr.OPT_ROWWISE_ADAGRAD,
+                         "adam": ctr.OPT_ADAM}[optimizer]
+        self.eps, self.betas, self.opt_step = eps, betas, 0
+        R = cfg.total_rows
+        self.state0 = None if optimizer == "sgd" else torch.zeros(
+            (R,) if optimizer == "rowwise_adagrad" else (R, d), dtype=torch.float32, device=self.dev)
+        self.state1 = torch.zeros((R, d), dtype=torch.float32, device=self.dev) if optimizer == "adam" else None
         total_rows = cfg.total_rows
         self.ws_dedup = ctr.workspace(ctr.ctr_dedup_workspace_size(cap, F, B, total_rows), self.dev)
         self.ws_bag = ctr.workspace(ctr.ctr_embedding_bag_workspace_size(), self.dev)
@@ -154,6 +164,12 @@ class CtrPath:
             G, sb, sf = self.grad_pooled, F * d, d
         args = (G, sb, sf, self.offsets, F, B, pool, self.unique_rows, self.n_unique, self.run_offsets, self.sorted_bag,
                 max(self.n_ids, 1), cfg.lr, self.table, d, grad_unique_out)
+        if self.opt_kind != ctr.OPT_SGD:
+            self.opt_step += 1
+            opt = ctr.optimizer(self.opt_kind, eps=self.eps, beta1=self.betas[0], beta2=self.betas[1],
+                                step=self.opt_step, state0=self.state0, state1=self.state1)
+            ctr.ctr_embedding_bag_bwd_update_opt(*args, ctr.BWD_ALL, opt, self.ws_bwd)
+            return
         if not overlap:
             ctr.ctr_embedding_bag_bwd_update(*args, self.ws_bwd)
             return

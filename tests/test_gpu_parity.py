@@ -739,3 +739,100 @@ def test_embedding_bag_fwd_fm(name):
                               out2, F * d, d, ws)
     assert torch.equal(out.view(torch.int16) if cfg.dtype == "bf16" else out,
                        out2.view(torch.int16) if cfg.dtype == "bf16" else out2)
+
+
+# ---------------------------------------------------------------------------
+# optimizer state in the row update (Adagrad, row-wise Adagrad, Adam)
+# ---------------------------------------------------------------------------
+U32 = 2.0 ** -24
+
+
+def _opt_case(seed, d, dtype, opt):
+    """Dyadic table, gradients and states: the reduced gradients are exact on both
+    sides, so only the optimizer's own fp32 arithmetic differs from the oracle."""
+    rng = np.random.default_rng(seed)
+    F, B = 3, 700
+    rows = [40, 3, 5000]
+    lens = rng.integers(0, 12, size=F * B)
+    lens[B:B + 40] = 400                               # long runs (pieces, combine)
+    ids, offsets = _csr(lens, rng, rows, B)
+    T = sum(rows)
+    table = (rng.integers(-256, 256, size=(T, d)) / 256).astype(np.float32)
+    if dtype == "bf16":
+        table = W.bf16_bits_to_f32(W.f32_to_bf16_bits(table))  # bf16-exact values
+    G = (rng.integers(-16, 17, size=(B, F, d)) / 16).astype(np.float32)
+    rb = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    s0 = (rng.integers(0, 64, size=(T,) if opt == "rowwise_adagrad" else (T, d)) / 16).astype(np.float32)
+    s1 = (rng.integers(0, 64, size=(T, d)) / 64).astype(np.float32) if opt == "adam" else None
+    if opt == "adam":
+        s0 = (rng.integers(-32, 33, size=(T, d)) / 64).astype(np.float32)
+    return F, B, rows, ids, offsets, table, G, rb, s0, s1
+
+
+@pytest.mark.parametrize("opt", ["adagrad", "rowwise_adagrad", "adam"])
+@pytest.mark.parametrize("d,dtype", [(32, "f32"), (128, "f32"), (256, "f32"), (64, "bf16")])
+def test_bwd_update_optimizers_exact_gradients(opt, d, dtype):
+    F, B, rows, ids, offsets, table, G, rb, s0, s1 = _opt_case(d + len(opt), d, dtype, opt)
+    b2t = np.arange(F, dtype=np.int32)
+    st, dd = gpu_dedup(ids, offsets, F, B, b2t, rb)
+    assert st == 0
+    n = ids.size
+    lr, eps, b1, b2, step = 2.0 ** -6, 1e-3, 0.875, 0.9375, 3
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    tab = _t(table).to(tdt)
+    S0 = _t(s0)
+    S1 = _t(s1) if s1 is not None else None
+    gu = torch.full((n, d), float("nan"), device=DEV)
+    ws = ctr.workspace(ctr.ctr_bwd_update_workspace_size(n, d))
+    nu = torch.tensor([dd["n_unique"]], dtype=torch.int64, device=DEV)
+    ro = torch.from_numpy(np.concatenate([dd["run_offsets"], np.zeros(n - dd["n_unique"], np.int32)])).to(DEV)
+    kind = {"adagrad": ctr.OPT_ADAGRAD, "rowwise_adagrad": ctr.OPT_ROWWISE_ADAGRAD, "adam": ctr.OPT_ADAM}[opt]
+    o = ctr.optimizer(kind, eps=eps, beta1=b1, beta2=b2, step=step, state0=S0, state1=S1)
+    ctr.ctr_embedding_bag_bwd_update_opt(_t(G), F * d, d, _t(offsets), F, B, ctr.POOL_SUM, _t(dd["unique_rows"]), nu,
+                                         ro, _t(dd["sorted_bag"]), n, lr, tab, d, gu, ctr.BWD_ALL, o, ws)
+    assert ctr.ctr_check_status(ws) == 0
+    rows_t = dd["unique_rows"]
+    _, g_ref, _ = O.embedding_bag_bwd_update(G, ids, offsets, F, B, b2t, rb, d, lr, rows_t, table=table)
+    np.testing.assert_array_equal(_np(gu)[:dd["n_unique"]], g_ref.astype(np.float32))   # exact gradients
+    w_new, s0_new, s1_new = O.optimizer_step(opt, table[rows_t].astype(np.float64), g_ref, lr, state0=s0[rows_t],
+                                             state1=None if s1 is None else s1[rows_t], eps=eps, beta1=b1, beta2=b2,
+                                             step=step, dtype=dtype)
+    got = _np(tab)[rows_t]
+    if dtype == "f32":
+        step_ref = np.abs(table[rows_t].astype(np.float64) - w_new.astype(np.float64))
+        err = np.abs(got.astype(np.float64) - w_new.astype(np.float64))
+        tol = 2 * U32 * np.abs(w_new.astype(np.float64)) + 12 * U32 * step_ref + 1e-30
+        assert np.all(err <= tol), (opt, float((err - tol).max()))
+    else:
+        # bf16 rows: at most one bf16 rounding step apart (the rounding boundary may fall between fp32 and fp64)
+        a = W.bf16_bits_to_f32(got).astype(np.float64)
+        r = W.bf16_bits_to_f32(w_new).astype(np.float64)
+        assert np.all(np.abs(a - r) <= np.abs(r) * 2.0 ** -7 + 1e-30)
+    S0n = _np(S0)
+    if opt == "rowwise_adagrad":
+        np.testing.assert_allclose(S0n[rows_t], s0_new, rtol=4 * U32)
+    else:
+        np.testing.assert_allclose(S0n[rows_t], s0_new, rtol=4 * U32, atol=1e-30)
+    if s1 is not None:
+        np.testing.assert_allclose(_np(S1)[rows_t], s1_new, rtol=4 * U32, atol=1e-30)
+    # rows and states the batch does not touch are unchanged
+    untouched = np.setdiff1d(np.arange(sum(rows)), rows_t)
+    np.testing.assert_array_equal(S0n[untouched], s0[untouched])
+    if dtype == "f32":
+        np.testing.assert_array_equal(_np(tab)[untouched], table[untouched])
+
+
+def test_bwd_update_optimizer_validation():
+    n, d = 8, 16
+    ws = ctr.workspace(ctr.ctr_bwd_update_workspace_size(n, d))
+    z = torch.zeros(64, device=DEV)
+    i64 = torch.zeros(8, dtype=torch.int64, device=DEV)
+    i32 = torch.zeros(9, dtype=torch.int32, device=DEV)
+    tab = torch.zeros((4, 16), device=DEV)
+    for o in (ctr.optimizer(ctr.OPT_ADAGRAD, state0=None),                          # state missing
+              ctr.optimizer(ctr.OPT_ADAM, state0=tab, state1=tab, step=0),           # step must be >= 1
+              ctr.optimizer(ctr.OPT_ADAGRAD, eps=0.0, state0=tab),                   # eps must be > 0
+              ctr.optimizer(7)):
+        with pytest.raises(ctr.CtrError):
+            ctr.ctr_embedding_bag_bwd_update_opt(z, d, d, i64, 1, 2, ctr.POOL_SUM, i64, i64, i32, i32, n, 0.1, tab, d,
+                                                 None, ctr.BWD_ALL, o, ws)
