@@ -60,6 +60,10 @@
  *                                kept only for the rows the batch touches
  *                                (the pages name no rule; the Baidu page's
  *                                k-step Adam merge is multi-worker).
+ *   oracle_bf16_stochastic_round the stochastic rounding of updated bf16 rows
+ *                                ("DHEN" notes, section 6.4: low-precision
+ *                                embeddings with stochastic rounding), its
+ *                                random bits drawn from splitmix64.
  *   oracle_table_rows            the counter-based table generator
  *                                (splitmix64, Steele/Lea/Flood 2014); input
  *                                generation, not the method.
@@ -405,10 +409,11 @@ int oracle_bag_fm(const void* table, int dtype, int gen_kind, uint64_t gen_seed,
  *                            w -= lr (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps)
  * s0 is the Adagrad state or Adam's m ([n][d]; [n] for row-wise), s1 Adam's v.
  * New values are computed in fp64 and rounded once (w to the table dtype,
- * state to fp32). */
+ * state to fp32); x_out (may be NULL) receives the unrounded new values, for
+ * stochastic rounding. */
 int oracle_optimizer_step(int opt, double lr, double eps, double beta1, double beta2, int64_t step, int32_t d,
                           int64_t n, const double* w_old, const double* g, const float* s0_in, const float* s1_in,
-                          void* w_new, int dtype, float* s0_out, float* s1_out) {
+                          void* w_new, int dtype, float* s0_out, float* s1_out, double* x_out) {
   if (opt < 0 || opt > 3 || d <= 0 || n < 0 || !w_old || !g || !w_new) return OR_ERR_ARG;
   if (opt != 0 && (!s0_in || !s0_out)) return OR_ERR_ARG;
   if (opt == 3 && (!s1_in || !s1_out || step < 1)) return OR_ERR_ARG;
@@ -444,6 +449,48 @@ int oracle_optimizer_step(int opt, double lr, double eps, double beta1, double b
         upd = lr * (m / bc1) / (sqrt(v / bc2) + eps);
       }
       store_value(w_new, dtype, e, w_old[e] - upd);
+      if (x_out) x_out[e] = w_old[e] - upd;
+    }
+  }
+  return OR_OK;
+}
+
+/* Stochastic rounding of values x (fp64) at elements (rows[r], c) of a table
+ * with d columns to bf16.  With lo and hi the bf16 neighbours of x below and
+ * above in magnitude (lo = x when x is a bf16 value) and f = (|x| - |lo|) /
+ * (|hi| - |lo|) in [0, 1), x rounds to hi when f + u / 2^16 >= 1, u the 16
+ * random bits of the element: the 4 values of column chunk q = c / 4 of a row
+ * take bits 16 j .. 16 j + 15 (j = c mod 4) of splitmix64(seed ^ (row d / 4 +
+ * q)); d must be a multiple of 4.  So P(hi) = f: the rounding is unbiased.
+ * Values outside the finite bf16 range round to nearest (not exercised).
+ * out: uint16 bf16 bits [n][d]. */
+int oracle_bf16_stochastic_round(const double* x, const int64_t* rows, int64_t n, int32_t d, uint64_t seed,
+                                 uint16_t* out) {
+  if (!x || !rows || !out || d <= 0 || d % 4 != 0) return OR_ERR_ARG;
+  for (int64_t r = 0; r < n; ++r) {
+    for (int32_t c = 0; c < d; ++c) {
+      double v = x[r * d + c];
+      uint64_t h = oracle_splitmix64(seed ^ (uint64_t)(rows[r] * (d / 4) + c / 4));
+      uint32_t u = (uint32_t)((h >> (16 * (c % 4))) & 0xFFFFu);
+      double a = fabs(v);
+      if (!(a < 0x1.fep127) || a == 0.0) {  /* zero, huge, inf, nan: nearest */
+        out[r * d + c] = round_bf16(v);
+        continue;
+      }
+      /* lo: |v| with its fp32 mantissa cut to bf16's 7 bits (toward zero) */
+      int e;
+      double m = frexp(a, &e);                    /* a = m 2^e, 0.5 <= m < 1 */
+      double lo, ulp;
+      if (e - 1 < -126) {                         /* below the normal range: spacing 2^-133 */
+        ulp = 0x1p-133;
+        lo = floor(a / ulp) * ulp;
+      } else {
+        ulp = ldexp(1.0, e - 8);                  /* bf16 keeps 8 significant bits */
+        lo = floor(m * 256.0) / 256.0 * ldexp(1.0, e);
+      }
+      double f = (a - lo) / ulp;                  /* exact: a - lo < ulp */
+      double mag = (f + (double)u / 65536.0 >= 1.0) ? lo + ulp : lo;
+      out[r * d + c] = round_bf16(v < 0 ? -mag : mag);
     }
   }
   return OR_OK;

@@ -47,9 +47,11 @@ def lib():
         L.oracle_dot_interaction.argtypes = [_p, C.c_int, C.c_int32, C.c_int32, C.c_int32, _p, C.c_int64, _p, _p]
         L.oracle_dot_interaction_bwd.restype = C.c_int
         L.oracle_dot_interaction_bwd.argtypes = [_p, _p, C.c_int32, C.c_int32, C.c_int32, _p, C.c_int64, _p, _p]
+        L.oracle_bf16_stochastic_round.restype = C.c_int
+        L.oracle_bf16_stochastic_round.argtypes = [_p, _p, C.c_int64, C.c_int32, C.c_uint64, _p]
         L.oracle_optimizer_step.restype = C.c_int
         L.oracle_optimizer_step.argtypes = [C.c_int, C.c_double, C.c_double, C.c_double, C.c_double, C.c_int64,
-                                            C.c_int32, C.c_int64, _p, _p, _p, _p, _p, C.c_int, _p, _p]
+                                            C.c_int32, C.c_int64, _p, _p, _p, _p, _p, C.c_int, _p, _p, _p]
         L.oracle_bag_fm.restype = C.c_int
         L.oracle_bag_fm.argtypes = [_p, C.c_int, C.c_int, C.c_uint64, C.c_float, C.c_int32, _p, _p, C.c_int32,
                                     C.c_int32, _p, _p, C.c_int32, _p, C.c_int64, _p, _p]
@@ -264,11 +266,12 @@ OPTIMIZERS = {"sgd": 0, "adagrad": 1, "rowwise_adagrad": 2, "adam": 3}
 
 
 def optimizer_step(opt, w_old, g, lr, state0=None, state1=None, eps=1e-8, beta1=0.9, beta2=0.999, step=1,
-                   dtype="f32"):
+                   dtype="f32", sr_seed=None, rows=None):
     """One optimizer step on rows w_old [n, d] (fp64 values) with exact gradients g [n, d] (fp64).
 
     Returns (w_new in the table dtype, state0_new, state1_new) with fp32 states:
-    Adagrad's sum of squares [n, d] (row-wise: [n]) or Adam's m [n, d]; Adam's v [n, d]."""
+    Adagrad's sum of squares [n, d] (row-wise: [n]) or Adam's m [n, d]; Adam's v [n, d].
+    With sr_seed (bf16 tables) the new rows are stochastically rounded at table rows `rows`."""
     o = OPTIMIZERS[opt]
     w_old = _c(w_old, np.float64)
     g = _c(g, np.float64)
@@ -278,11 +281,26 @@ def optimizer_step(opt, w_old, g, lr, state0=None, state1=None, eps=1e-8, beta1=
     w_new = np.zeros((n, d), dtype=np.float32 if dtype == "f32" else np.uint16)
     s0o = None if s0 is None else np.zeros_like(s0)
     s1o = None if s1 is None else np.zeros_like(s1)
+    x = np.zeros((n, d), dtype=np.float64)
     st = lib().oracle_optimizer_step(o, float(lr), float(eps), float(beta1), float(beta2), int(step), int(d), int(n),
                                      _ptr(w_old), _ptr(g), _ptr(s0), _ptr(s1), _ptr(w_new), _DT[dtype], _ptr(s0o),
-                                     _ptr(s1o))
+                                     _ptr(s1o), _ptr(x))
     _check(st, "oracle_optimizer_step")
+    if sr_seed is not None:
+        assert dtype == "bf16" and rows is not None
+        w_new = bf16_stochastic_round(x, rows, sr_seed)
     return w_new, s0o, s1o
+
+
+def bf16_stochastic_round(x, rows, seed):
+    """Stochastically rounded bf16 bits of values x [n, d] (fp64) at table rows `rows` [n]."""
+    x = _c(x, np.float64)
+    rows = _c(rows, np.int64)
+    n, d = x.shape
+    out = np.zeros((n, d), dtype=np.uint16)
+    _check(lib().oracle_bf16_stochastic_round(_ptr(x), _ptr(rows), n, d, C.c_uint64(seed & (2 ** 64 - 1)), _ptr(out)),
+           "oracle_bf16_stochastic_round")
+    return out
 
 
 def embedding_bag_bwd_update(G, ids, offsets, num_fields, batch, bag_to_table, row_base, d, lr, target_rows,

@@ -438,6 +438,69 @@ def test_optimizer_adam_matches_torch(oracle, step):
 
 
 # ---------------------------------------------------------------------------
+# stochastic rounding of updated bf16 rows
+# ---------------------------------------------------------------------------
+def _bf16_neighbours(x):
+    """bf16 values just below and above |x| (toward zero first), as float64."""
+    f = np.asarray(x, dtype=np.float32)
+    bits = f.view(np.uint32) & np.uint32(0x7FFFFFFF)
+    lo = ((bits >> np.uint32(16)) << np.uint32(16)).view(np.float32).astype(np.float64)
+    hi = (((bits >> np.uint32(16)) + np.uint32(1)) << np.uint32(16)).view(np.float32).astype(np.float64)
+    return lo, hi
+
+
+def test_stochastic_round_keeps_bf16_values(oracle):
+    rng = np.random.default_rng(50)
+    x = W.bf16_bits_to_f32(W.f32_to_bf16_bits(rng.standard_normal((5, 8)).astype(np.float32))).astype(np.float64)
+    for seed in range(4):
+        out = oracle.bf16_stochastic_round(x, np.arange(5), seed)
+        np.testing.assert_array_equal(W.bf16_bits_to_f32(out).astype(np.float64), x)
+
+
+def test_stochastic_round_picks_a_neighbour_unbiased(oracle):
+    # one value per element, 4000 seeds: the result is always lo or hi, and the
+    # fraction rounded up matches (|x| - lo) / (hi - lo) within a binomial bound
+    rng = np.random.default_rng(51)
+    x32 = (rng.standard_normal((1, 16)) * 3).astype(np.float32)
+    x = x32.astype(np.float64)
+    lo, hi = _bf16_neighbours(x32)
+    frac = (np.abs(x) - lo) / (hi - lo)
+    seeds = 4000
+    ups = np.zeros(x.shape)
+    for seed in range(seeds):
+        got = np.abs(W.bf16_bits_to_f32(oracle.bf16_stochastic_round(x, [7], seed)).astype(np.float64))
+        assert np.all((got == lo) | (got == hi))
+        ups += got == hi
+    p = ups / seeds
+    assert np.all(np.abs(p - frac) <= 4.5 * np.sqrt(frac * (1 - frac) / seeds) + 1e-3)
+
+
+def test_stochastic_round_matches_the_carry_formulation(oracle):
+    # the same rounding written as fp32 bits: add the 16 random bits to the low
+    # half and truncate (the carry reaches the bf16 bits exactly when f + u/2^16 >= 1)
+    rng = np.random.default_rng(52)
+    x32 = (rng.standard_normal((6, 12)) * 2.0 ** rng.integers(-20, 20, size=(6, 1))).astype(np.float32)
+    rows = np.array([3, 0, 11, 5, 1 << 33, 17], dtype=np.int64)
+    seed = 0x1234ABCD
+    got = oracle.bf16_stochastic_round(x32.astype(np.float64), rows, seed)
+    d = x32.shape[1]
+    mask = (1 << 64) - 1
+
+    def splitmix(z):
+        z = (z + 0x9E3779B97F4A7C15) & mask
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & mask
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & mask
+        return z ^ (z >> 31)
+    bits = x32.view(np.uint32)
+    for r in range(x32.shape[0]):
+        for c in range(d):
+            u = (splitmix(seed ^ (int(rows[r]) * (d // 4) + c // 4)) >> (16 * (c % 4))) & 0xFFFF
+            b = int(bits[r, c])
+            expect = ((b & 0x80000000) | ((b & 0x7FFFFFFF) + u)) >> 16
+            assert int(got[r, c]) == expect, (r, c)
+
+
+# ---------------------------------------------------------------------------
 # interaction variants: products with the diagonal, the full Gram matrix
 # ---------------------------------------------------------------------------
 def test_interaction_cross_mode_is_the_default_interaction(oracle):
