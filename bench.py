@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller cases for profiling)")
     ap.add_argument("--rows", type=int, default=0, help="override rows per table (smaller cases for profiling)")
     ap.add_argument("--fm", action="store_true", help="the gather also writes each bag's FM second-order term")
+    ap.add_argument("--dtype", default="", choices=["", "f32", "bf16"], help="override the table dtype")
+    ap.add_argument("--stochastic-rounding", action="store_true",
+                    help="bf16 tables: round the updated rows stochastically")
     ap.add_argument("--optimizer", default="sgd", choices=["sgd", "adagrad", "rowwise_adagrad", "adam"],
                     help="row update rule (state kept for the batch's rows)")
     ap.add_argument("--interaction-mode", default="", choices=["", "cross", "with_self", "full"],
@@ -68,6 +71,10 @@ def workload_cfg(args):
             rows = 1 << bits
             kw["ids"] = (cfg.ids[0], cfg.ids[1], cfg.ids[2], bits)
         kw["rows_per_table"] = tuple([rows] * cfg.num_tables)
+    if getattr(args, "dtype", "") and args.dtype != cfg.dtype:
+        # each table dtype has its own generator: uniform for fp32, the 4-sum normal for bf16
+        kw["dtype"] = args.dtype
+        kw["table_init"] = ("normal4", cfg.table_init[1]) if args.dtype == "bf16" else ("uniform", cfg.table_init[1])
     if getattr(args, "interaction_mode", ""):
         kw["interaction_mode"] = args.interaction_mode
     return cfg.shrink(**kw) if kw else cfg
@@ -295,7 +302,7 @@ def run_ours(args, rank, world):
     cfg = workload_cfg(args)
     w = W.make_workload(cfg)
     n_ids = int(w["ids"].size)
-    path = CtrPath(cfg, n_ids, fm=args.fm, optimizer=args.optimizer)
+    path = CtrPath(cfg, n_ids, fm=args.fm, optimizer=args.optimizer, stochastic_rounding=args.stochastic_rounding)
     path.upload(w)
     torch.cuda.synchronize()
     path.reset_status()
@@ -425,6 +432,7 @@ def run_ours(args, rank, world):
         "config": {"workload": cfg.name, "batch": cfg.batch, "fields": cfg.num_fields, "tables": cfg.num_tables,
                    "interaction": cfg.interaction_mode if cfg.interaction else None, "fm_term": bool(args.fm),
                    "optimizer": args.optimizer if cfg.backward != "none" else None,
+                   "stochastic_rounding": bool(path.stochastic_rounding and cfg.backward != "none"),
                    "rows_per_table": cfg.rows_per_table[0], "d": cfg.d, "bag_len": list(cfg.bag_len),
                    "ids": list(cfg.ids), "n_ids": n_ids, "n_unique": n_unique, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (tables %.1f GB, ids %.2f GB)" % (

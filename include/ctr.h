@@ -331,7 +331,17 @@ int ctr_embedding_bag_bwd_update_phases(const float* grad_pooled, int64_t g_stri
  * 16-byte aligned, and only the batch's rows are read and written.  t = step
  * (>= 1) is this update's step number for Adam's bias correction; eps > 0.
  * phases as in ctr_embedding_bag_bwd_update_phases.  The optimizer
- * arithmetic is fp32. */
+ * arithmetic is fp32.
+ *
+ * Stochastic rounding ("DHEN" notes, section 6.4: low-precision embeddings
+ * with stochastic rounding; applied here to bf16 tables, with any kind): the
+ * new value x (fp32) of element (row, c) becomes the bf16 neighbour above it
+ * in magnitude with probability f = (|x| - lo) / (hi - lo), lo and hi its bf16
+ * neighbours, else lo: with u the element's 16 random bits, x rounds up when
+ * f + u / 2^16 >= 1, i.e. u is added to the 16 bits bf16 drops and the carry
+ * kept.  The 4 values of column chunk q = c / 4 take bits 16 (c mod 4) ..
+ * 16 (c mod 4) + 15 of splitmix64(sr_seed ^ (row d / 4 + q)).  Values at or
+ * beyond the largest finite bf16 round to nearest.  fp32 tables ignore it. */
 typedef enum { CTR_OPT_SGD = 0, CTR_OPT_ADAGRAD = 1, CTR_OPT_ROWWISE_ADAGRAD = 2, CTR_OPT_ADAM = 3 } ctr_opt_kind;
 typedef struct {
   int kind;       /* ctr_opt_kind */
@@ -341,6 +351,8 @@ typedef struct {
   int64_t step;   /* Adam: t >= 1 */
   float* state0;  /* Adagrad sum of squares, or Adam m */
   float* state1;  /* Adam v */
+  int32_t stochastic_rounding;  /* bf16 tables: round the new rows stochastically (below) */
+  uint64_t sr_seed;             /* its random bits; use a new seed every step */
 } ctr_optimizer;
 int ctr_embedding_bag_bwd_update_opt(const float* grad_pooled, int64_t g_stride_b, int64_t g_stride_f,
                                      const int64_t* offsets, int32_t num_fields, int32_t batch, ctr_pool pool,

@@ -44,12 +44,6 @@ void timing_mark(int kernel, bool before, cudaStream_t s) {
 
 namespace {
 
-__device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
-  uint64_t z = x + 0x9E3779B97F4A7C15ull;
-  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-  return z ^ (z >> 31);
-}
 
 __global__ void fill_uniform_f32(float* __restrict__ t, int64_t count, uint64_t idx0, uint64_t seed, float scale) {
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < count; e += (int64_t)gridDim.x * blockDim.x) {

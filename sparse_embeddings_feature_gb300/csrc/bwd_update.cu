@@ -69,6 +69,8 @@ struct BwdArgs {
   float eps, beta1, beta2, bc1, bc2;
   float* s0;
   float* s1;
+  int sr;              // bf16 tables: stochastic rounding of the new rows
+  uint64_t sr_seed;
   int64_t n_cap;       // occurrences (sorted_bag length)
   int64_t nbags;       // F * B
   int TU;              // uniques per tile
@@ -176,9 +178,37 @@ __device__ __forceinline__ float rowwise_inv(const BwdArgs& a, int64_t row, floa
 
 __device__ __forceinline__ float sumsq4(float4 g) { return fmaf(g.w, g.w, fmaf(g.z, g.z, fmaf(g.y, g.y, g.x * g.x))); }
 
+// Stochastic rounding of x to bf16 bits with 16 random bits u: u is added to
+// the 16 bits bf16 drops, and the carry kept (rounds up in magnitude with
+// probability equal to the dropped fraction).  Non-finite values and values at
+// or beyond the largest finite bf16 round to nearest.
+__device__ __forceinline__ uint32_t bf16_sr(float x, uint32_t u) {
+  const uint32_t b = __float_as_uint(x);
+  const uint32_t mag = b & 0x7fffffffu;
+  if (mag >= 0x7f7f0000u) {
+    const __nv_bfloat16 r = __float2bfloat16_rn(x);
+    return (uint32_t)*(const uint16_t*)&r;
+  }
+  return ((b & 0x80000000u) | (mag + u)) >> 16;
+}
+
+// Store one 4-value chunk of a bf16 row with stochastic rounding: the chunk's
+// 64 random bits are splitmix64(seed ^ (row d/4 + chunk)), 16 per value.  Out
+// of line: the hash inlined into the unrolled tile loops bloats them.
+__device__ __noinline__ void store_bf16_sr(const BwdArgs& a, int64_t row, int ch, float x0, float x1, float x2,
+                                           float x3) {
+  const uint64_t h = splitmix64(a.sr_seed ^ (uint64_t)(row * (a.d / 4) + ch));
+  uint2 out;
+  out.x = bf16_sr(x0, (uint32_t)h & 0xffffu) | (bf16_sr(x1, (uint32_t)(h >> 16) & 0xffffu) << 16);
+  out.y = bf16_sr(x2, (uint32_t)(h >> 32) & 0xffffu) | (bf16_sr(x3, (uint32_t)(h >> 48) & 0xffffu) << 16);
+  *(uint2*)((__nv_bfloat16*)a.table + row * a.d + ch * 4) = out;
+}
+
 // Update one 4-value chunk of a row: w -= step, the elementwise states given
-// (st, sv: their previous values) written back.
-template <int OPT>
+// (st, sv: their previous values) written back.  SR: the build that honours
+// stochastic rounding (bf16 tables with a.sr set); without it the store has no
+// out-of-line call and the tile loops keep their registers.
+template <int OPT, bool SR = false>
 __device__ __forceinline__ void store_row_chunk_s(const BwdArgs& a, int64_t row, int64_t u, int ch, float4 g,
                                                   float4 w, uint2 wb, uint64_t pol, float row_inv, float4 st,
                                                   float4 sv) {
@@ -201,20 +231,26 @@ __device__ __forceinline__ void store_row_chunk_s(const BwdArgs& a, int64_t row,
   } else {
     const float w0 = __uint_as_float(wb.x << 16), w1 = __uint_as_float(wb.x & 0xffff0000u);
     const float w2 = __uint_as_float(wb.y << 16), w3 = __uint_as_float(wb.y & 0xffff0000u);
-    __nv_bfloat162 p0 = __floats2bfloat162_rn(fmaf(k, step.x, w0), fmaf(k, step.y, w1));
-    __nv_bfloat162 p1 = __floats2bfloat162_rn(fmaf(k, step.z, w2), fmaf(k, step.w, w3));
-    *(uint2*)((__nv_bfloat16*)a.table + row * a.d + ch * 4) = make_uint2(*(uint32_t*)&p0, *(uint32_t*)&p1);
+    const float x0 = fmaf(k, step.x, w0), x1 = fmaf(k, step.y, w1);
+    const float x2 = fmaf(k, step.z, w2), x3 = fmaf(k, step.w, w3);
+    if (SR && a.sr) {
+      store_bf16_sr(a, row, ch, x0, x1, x2, x3);
+    } else {
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(x0, x1);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(x2, x3);
+      *(uint2*)((__nv_bfloat16*)a.table + row * a.d + ch * 4) = make_uint2(*(uint32_t*)&p0, *(uint32_t*)&p1);
+    }
   }
 }
 
 // store_row_chunk_s as one out-of-line copy: the tile kernel's occurrence loop
 // is unrolled 32 times, and an inlined optimizer update in each copy overflows
 // the instruction cache.
-template <int OPT>
+template <int OPT, bool SR>
 __device__ __noinline__ void store_row_chunk_call(const BwdArgs& a, int64_t row, int64_t u, int ch, float4 g,
                                                   float4 w, uint2 wb, uint64_t pol, float row_inv, float4 st,
                                                   float4 sv) {
-  store_row_chunk_s<OPT>(a, row, u, ch, g, w, wb, pol, row_inv, st, sv);
+  store_row_chunk_s<OPT, SR>(a, row, u, ch, g, w, wb, pol, row_inv, st, sv);
 }
 
 // The same, reading the elementwise states from global memory.
@@ -225,10 +261,11 @@ __device__ __forceinline__ void store_row_chunk_t(const BwdArgs& a, int64_t row,
   const int64_t e = row * a.d + ch * 4;
   if constexpr (kElemStates<OPT> >= 1) st = *(const float4*)(a.s0 + e);
   if constexpr (kElemStates<OPT> >= 2) sv = *(const float4*)(a.s1 + e);
-  store_row_chunk_s<OPT>(a, row, u, ch, g, w, wb, pol, row_inv, st, sv);
+  store_row_chunk_s<OPT, true>(a, row, u, ch, g, w, wb, pol, row_inv, st, sv);
 }
 
-// The same with the optimizer chosen at run time (for the kernels off the hot path).
+// The same with the optimizer and the rounding chosen at run time (for the
+// kernels off the hot path).
 __device__ __forceinline__ void store_row_chunk(const BwdArgs& a, int64_t row, int64_t u, int ch, float4 g,
                                                 float4 w, uint2 wb, uint64_t pol = 0, float row_inv = 0.f) {
   switch (a.opt) {
@@ -671,7 +708,7 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 #define CTR_TILE_OPT_MINB 2
 #endif
 constexpr int kOptStageBytes = 12288;  // staged bytes per warp (rows and states) with an optimizer
-template <int OPT>
+template <int OPT, bool SR>
 __global__ void __launch_bounds__(kTileThreads, OPT == CTR_OPT_SGD ? CTR_TILE_ASYNC_MINB : CTR_TILE_OPT_MINB)
     bwd_tiles_async_kernel(const BwdArgs a) {
   extern __shared__ __align__(16) unsigned char wsm_raw[];
@@ -789,9 +826,9 @@ __global__ void __launch_bounds__(kTileThreads, OPT == CTR_OPT_SGD ? CTR_TILE_AS
               if constexpr (NS >= 2) sv = *(const float4*)(ssm + (TU + sg) * state_bytes + lane * 16);
               // the elementwise optimizers' updates (a divide and a square root per value) out of line
               if constexpr (OPT == CTR_OPT_ADAGRAD || OPT == CTR_OPT_ADAM)
-                store_row_chunk_call<OPT>(a, rs, tile * TU + sg, lane, acc, w, wb, pol_stream, rinv, st, sv);
+                store_row_chunk_call<OPT, SR>(a, rs, tile * TU + sg, lane, acc, w, wb, pol_stream, rinv, st, sv);
               else
-                store_row_chunk_s<OPT>(a, rs, tile * TU + sg, lane, acc, w, wb, pol_stream, rinv, st, sv);
+                store_row_chunk_s<OPT, SR>(a, rs, tile * TU + sg, lane, acc, w, wb, pol_stream, rinv, st, sv);
             }
             acc = make_float4(0.f, 0.f, 0.f, 0.f);
           }
@@ -912,10 +949,14 @@ int launch_short(const BwdArgs& a, cudaStream_t s, int64_t n) {
   const int chunks = a.d / 4;
   const size_t acc_smem = (size_t)kTileWarps * a.TU * chunks * sizeof(float4);
   const bool use_async = CPL == 1 && a.g4_ok;
-  auto async_k = a.opt == CTR_OPT_ADAGRAD           ? bwd_tiles_async_kernel<CTR_OPT_ADAGRAD>
-                 : a.opt == CTR_OPT_ROWWISE_ADAGRAD ? bwd_tiles_async_kernel<CTR_OPT_ROWWISE_ADAGRAD>
-                 : a.opt == CTR_OPT_ADAM            ? bwd_tiles_async_kernel<CTR_OPT_ADAM>
-                                                    : bwd_tiles_async_kernel<CTR_OPT_SGD>;
+  auto async_k = a.sr ? (a.opt == CTR_OPT_ADAGRAD           ? bwd_tiles_async_kernel<CTR_OPT_ADAGRAD, true>
+                         : a.opt == CTR_OPT_ROWWISE_ADAGRAD ? bwd_tiles_async_kernel<CTR_OPT_ROWWISE_ADAGRAD, true>
+                         : a.opt == CTR_OPT_ADAM            ? bwd_tiles_async_kernel<CTR_OPT_ADAM, true>
+                                                            : bwd_tiles_async_kernel<CTR_OPT_SGD, true>)
+                      : (a.opt == CTR_OPT_ADAGRAD           ? bwd_tiles_async_kernel<CTR_OPT_ADAGRAD, false>
+                         : a.opt == CTR_OPT_ROWWISE_ADAGRAD ? bwd_tiles_async_kernel<CTR_OPT_ROWWISE_ADAGRAD, false>
+                         : a.opt == CTR_OPT_ADAM            ? bwd_tiles_async_kernel<CTR_OPT_ADAM, false>
+                                                            : bwd_tiles_async_kernel<CTR_OPT_SGD, false>);
   auto tk = use_async ? async_k : bwd_tiles_kernel<CPL>;
   const int ns = a.opt == CTR_OPT_ADAGRAD ? 1 : (a.opt == CTR_OPT_ADAM ? 2 : 0);
   const size_t tile_smem =
@@ -1052,6 +1093,8 @@ int bwd_update_phases(const float* grad_pooled, int64_t g_stride_b, int64_t g_st
   a.bc2 = kind == CTR_OPT_ADAM ? (float)(1.0 - std::pow((double)opt->beta2, (double)opt->step)) : 1.f;
   a.s0 = kind != CTR_OPT_SGD ? opt->state0 : nullptr;
   a.s1 = kind == CTR_OPT_ADAM ? opt->state1 : nullptr;
+  a.sr = (opt && opt->stochastic_rounding && dtype == CTR_BF16) ? 1 : 0;
+  a.sr_seed = opt ? opt->sr_seed : 0;
   a.n_cap = n_ids;
   a.nbags = (int64_t)num_fields * batch;
   {

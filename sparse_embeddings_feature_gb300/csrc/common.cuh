@@ -143,6 +143,15 @@ __device__ __forceinline__ void stg_f4_policy(float* p, float4 v, uint64_t pol) 
                : "memory");
 }
 
+// splitmix64 output function (Steele, Lea and Flood, OOPSLA 2014): a
+// counter-based source of 64 random bits per index.
+__device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
+  uint64_t z = x + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
 // Four-lane accumulation with packed fp32 pairs (f32x2, sm_100+): two
 // instructions instead of four; each half is the same IEEE operation as the
 // scalar form, so the results are bit-identical.

@@ -290,13 +290,16 @@ OPT_SGD, OPT_ADAGRAD, OPT_ROWWISE_ADAGRAD, OPT_ADAM = 0, 1, 2, 3
 class CtrOptimizer(C.Structure):
     """ctr_optimizer of ctr.h."""
     _fields_ = [("kind", C.c_int), ("eps", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float),
-                ("step", C.c_int64), ("state0", C.c_void_p), ("state1", C.c_void_p)]
+                ("step", C.c_int64), ("state0", C.c_void_p), ("state1", C.c_void_p),
+                ("stochastic_rounding", C.c_int32), ("sr_seed", C.c_uint64)]
 
 
 def optimizer(kind: int, eps: float = 1e-8, beta1: float = 0.9, beta2: float = 0.999, step: int = 1,
-              state0: Optional[torch.Tensor] = None, state1: Optional[torch.Tensor] = None) -> CtrOptimizer:
+              state0: Optional[torch.Tensor] = None, state1: Optional[torch.Tensor] = None,
+              stochastic_rounding: bool = False, sr_seed: int = 0) -> CtrOptimizer:
     return CtrOptimizer(int(kind), float(eps), float(beta1), float(beta2), int(step),
-                        None if state0 is None else _ptr(state0), None if state1 is None else _ptr(state1))
+                        None if state0 is None else _ptr(state0), None if state1 is None else _ptr(state1),
+                        1 if stochastic_rounding else 0, int(sr_seed) & ((1 << 64) - 1))
 
 
 def ctr_embedding_bag_bwd_update_opt(grad_pooled: torch.Tensor, g_stride_b: int, g_stride_f: int,

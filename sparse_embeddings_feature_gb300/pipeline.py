@@ -28,7 +28,7 @@ _MODES = {"cross": ctr.INTERACT_CROSS, "with_self": ctr.INTERACT_WITH_SELF, "ful
 class CtrPath:
     def __init__(self, cfg: Config, n_ids: int, device="cuda", fill: bool = True, table_chunk_rows: int = 1 << 24,
                  keep_sorted_pos: bool = False, fm: bool = False, optimizer: str = "sgd", eps: float = 1e-8,
-                 betas=(0.9, 0.999)):
+                 betas=(0.9, 0.999), stochastic_rounding: bool = False, sr_seed: int = 0x5EED):
         self.cfg = cfg
         self.dev = torch.device(device)
         self.n_ids = int(n_ids)
@@ -68,6 +68,9 @@ class CtrPath:
         self.opt_kind = {"sgd": ctr.OPT_SGD, "adagrad": ctr.OPT_ADAGRAD, "rowwise_adagrad": ctr.OPT_ROWWISE_ADAGRAD,
                          "adam": ctr.OPT_ADAM}[optimizer]
         self.eps, self.betas, self.opt_step = eps, betas, 0
+        # bf16 tables: stochastic rounding of the updated rows, a fresh seed per update
+        self.stochastic_rounding = bool(stochastic_rounding) and cfg.dtype == "bf16"
+        self.sr_seed, self.updates = int(sr_seed), 0
         R = cfg.total_rows
         self.state0 = None if optimizer == "sgd" else torch.zeros(
             (R,) if optimizer == "rowwise_adagrad" else (R, d), dtype=torch.float32, device=self.dev)
@@ -164,10 +167,14 @@ class CtrPath:
             G, sb, sf = self.grad_pooled, F * d, d
         args = (G, sb, sf, self.offsets, F, B, pool, self.unique_rows, self.n_unique, self.run_offsets, self.sorted_bag,
                 max(self.n_ids, 1), cfg.lr, self.table, d, grad_unique_out)
-        if self.opt_kind != ctr.OPT_SGD:
-            self.opt_step += 1
+        self.updates += 1
+        if self.opt_kind != ctr.OPT_SGD or self.stochastic_rounding:
+            if self.opt_kind != ctr.OPT_SGD:
+                self.opt_step += 1
             opt = ctr.optimizer(self.opt_kind, eps=self.eps, beta1=self.betas[0], beta2=self.betas[1],
-                                step=self.opt_step, state0=self.state0, state1=self.state1)
+                                step=max(self.opt_step, 1), state0=self.state0, state1=self.state1,
+                                stochastic_rounding=self.stochastic_rounding,
+                                sr_seed=self.sr_seed * 0x9E3779B97F4A7C15 + self.updates)
             ctr.ctr_embedding_bag_bwd_update_opt(*args, ctr.BWD_ALL, opt, self.ws_bwd)
             return
         if not overlap:

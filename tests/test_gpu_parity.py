@@ -836,3 +836,82 @@ def test_bwd_update_optimizer_validation():
         with pytest.raises(ctr.CtrError):
             ctr.ctr_embedding_bag_bwd_update_opt(z, d, d, i64, 1, 2, ctr.POOL_SUM, i64, i64, i32, i32, n, 0.1, tab, d,
                                                  None, ctr.BWD_ALL, o, ws)
+
+
+# ---------------------------------------------------------------------------
+# stochastic rounding of the updated bf16 rows
+# ---------------------------------------------------------------------------
+def _bf16_ulp(v):
+    """Spacing of bf16 values at |v| (8 significant bits; subnormal spacing 2^-133)."""
+    a = np.maximum(np.abs(v), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
+@pytest.mark.parametrize("opt", ["sgd", "adagrad", "rowwise_adagrad", "adam"])
+@pytest.mark.parametrize("d", [32, 64, 256])
+def test_bwd_update_stochastic_rounding(opt, d):
+    F, B, rows, ids, offsets, table, G, rb, s0, s1 = _opt_case(3 * d + len(opt), d, "bf16",
+                                                               "adagrad" if opt == "sgd" else opt)
+    b2t = np.arange(F, dtype=np.int32)
+    st, dd = gpu_dedup(ids, offsets, F, B, b2t, rb)
+    assert st == 0
+    n = ids.size
+    lr, eps, b1, b2, step = 2.0 ** -6, 1e-3, 0.875, 0.9375, 2
+    seed = 0x5EED0000 + 977 * d + len(opt)
+    tab = _t(table).to(torch.bfloat16)
+    S0 = None if opt == "sgd" else _t(s0)
+    S1 = _t(s1) if (opt == "adam") else None
+    ws = ctr.workspace(ctr.ctr_bwd_update_workspace_size(n, d))
+    nu = torch.tensor([dd["n_unique"]], dtype=torch.int64, device=DEV)
+    ro = torch.from_numpy(np.concatenate([dd["run_offsets"], np.zeros(n - dd["n_unique"], np.int32)])).to(DEV)
+    kind = {"sgd": ctr.OPT_SGD, "adagrad": ctr.OPT_ADAGRAD, "rowwise_adagrad": ctr.OPT_ROWWISE_ADAGRAD,
+            "adam": ctr.OPT_ADAM}[opt]
+    o = ctr.optimizer(kind, eps=eps, beta1=b1, beta2=b2, step=step, state0=S0, state1=S1,
+                      stochastic_rounding=True, sr_seed=seed)
+    ctr.ctr_embedding_bag_bwd_update_opt(_t(G), F * d, d, _t(offsets), F, B, ctr.POOL_SUM, _t(dd["unique_rows"]), nu,
+                                         ro, _t(dd["sorted_bag"]), n, lr, tab, d, None, ctr.BWD_ALL, o, ws)
+    assert ctr.ctr_check_status(ws) == 0
+    rows_t = dd["unique_rows"]
+    _, g_ref, _ = O.embedding_bag_bwd_update(G, ids, offsets, F, B, b2t, rb, d, lr, rows_t, table=table)
+    w_old = table[rows_t].astype(np.float64)
+    kw = dict(state0=None if opt == "sgd" else s0[rows_t], state1=s1[rows_t] if opt == "adam" else None,
+              eps=eps, beta1=b1, beta2=b2, step=step, dtype="bf16")
+    w_sr, _, _ = O.optimizer_step(opt, w_old, g_ref, lr, sr_seed=seed, rows=rows_t, **kw)
+    w_rn, _, _ = O.optimizer_step(opt, w_old, g_ref, lr, **kw)
+    got = _np(tab).view(np.uint16)[rows_t]
+    if opt == "sgd":
+        # dyadic inputs: w - lr g is exact in fp32 and fp64, so the same random bits give the same bits
+        np.testing.assert_array_equal(got, w_sr)
+    else:
+        # the fp32 and fp64 values may straddle a rounding boundary: one bf16 step apart at most, rarely
+        a = W.bf16_bits_to_f32(got).astype(np.float64)
+        r = W.bf16_bits_to_f32(w_sr).astype(np.float64)
+        assert np.all(np.abs(a - r) <= _bf16_ulp(np.maximum(np.abs(a), np.abs(r))) + 1e-300)
+        assert np.mean(got != w_sr) < 0.01
+    # stochastic, not nearest: a good share of the values that were not representable round the other way
+    inexact = W.bf16_bits_to_f32(w_rn).astype(np.float64) != W.bf16_bits_to_f32(w_sr).astype(np.float64)
+    assert inexact.mean() > 0.05 and np.mean(got != w_rn) > 0.05
+    # rows the batch does not touch are unchanged
+    untouched = np.setdiff1d(np.arange(sum(rows)), rows_t)
+    np.testing.assert_array_equal(_np(tab).view(np.uint16)[untouched], W.f32_to_bf16_bits(table[untouched]))
+
+
+def test_bwd_update_stochastic_rounding_ignored_for_f32():
+    d = 64
+    F, B, rows, ids, offsets, table, G, rb, s0, s1 = _opt_case(11, d, "f32", "adagrad")
+    b2t = np.arange(F, dtype=np.int32)
+    st, dd = gpu_dedup(ids, offsets, F, B, b2t, rb)
+    n = ids.size
+    nu = torch.tensor([dd["n_unique"]], dtype=torch.int64, device=DEV)
+    ro = torch.from_numpy(np.concatenate([dd["run_offsets"], np.zeros(n - dd["n_unique"], np.int32)])).to(DEV)
+    outs = []
+    for sr in (False, True):
+        tab = _t(table)
+        ws = ctr.workspace(ctr.ctr_bwd_update_workspace_size(n, d))
+        o = ctr.optimizer(ctr.OPT_SGD, stochastic_rounding=sr, sr_seed=12345)
+        ctr.ctr_embedding_bag_bwd_update_opt(_t(G), F * d, d, _t(offsets), F, B, ctr.POOL_SUM,
+                                             _t(dd["unique_rows"]), nu, ro, _t(dd["sorted_bag"]), n, 2.0 ** -6, tab,
+                                             d, None, ctr.BWD_ALL, o, ws)
+        assert ctr.ctr_check_status(ws) == 0
+        outs.append(_np(tab))
+    np.testing.assert_array_equal(outs[0], outs[1])
