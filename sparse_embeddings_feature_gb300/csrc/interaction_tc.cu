@@ -12,14 +12,15 @@
 // the tile's Gram matrix, whose S diagonal n x n blocks are the samples' own.
 // A and B are the same shared-memory tile (both K-major, 128-byte swizzle),
 // loaded by TMA straight from X viewed as [B*n, d].  The accumulator lives in
-// TMEM (fp32, double-buffered); the epilogue reads it with tcgen05.ld, keeps
-// the products its mode emits from each diagonal block (the strict lower
-// triangle; or with the diagonal, "DHEN" notes section 3.1; or the whole
-// block, the Gram matrix of "DHEN" notes section 3.3, Eq. (7)), rounds to
-// bf16, adds the dense pass-through (first two modes) and writes the samples'
-// output rows with coalesced stores through a shared-memory staging buffer.
+// TMEM (fp32, double-buffered); the epilogue reads the columns of each warp's
+// diagonal blocks with tcgen05.ld, rounds them to bf16 into a shared-memory
+// copy of the tile's Gram matrix, and writes the samples' output rows from it
+// in output order with coalesced stores: the dense pass-through first (first
+// two modes), then the products the mode emits from each diagonal block (the
+// strict lower triangle; or with the diagonal, "DHEN" notes section 3.1; or the
+// whole block, the Gram matrix of "DHEN" notes section 3.3, Eq. (7)).
 //
-// Roles (persistent CTA, one per SM): warp 0 issues TMA loads, warp 1 owns
+// Roles (persistent CTAs, two per SM where shared memory allows): warp 0 issues TMA loads, warp 1 owns
 // TMEM and issues the MMAs, warps 2..5 run the epilogue.  Every mbarrier wait
 // is bounded by a wall-clock limit; on expiry the kernel records
 // CTR_ERR_TIMEOUT, waits (bounded) for its own copies and MMAs, frees TMEM and
@@ -38,10 +39,14 @@ namespace {
 constexpr int kTcThreads = 192;
 constexpr int kTcEpiWarps = 4;
 constexpr uint32_t kTmemCols = 256;
+// Shared memory asked for per CTA, at least: more than a third of the SM's
+// 228 KB, so no more than two CTAs (2 x 256 TMEM columns) are ever resident.
+constexpr int kTcSmemFloor = 80 * 1024;
+constexpr int kDensePre = 2;  // dense-vector pieces per epilogue thread loaded early
 
 struct TcParams {
-  int32_t batch, n, d, S, rows, N, kb, stages, W, mode;
-  uint32_t stage_bytes, tx_bytes, staging_bytes;
+  int32_t batch, n, d, S, rows, N, kb, stages, W, mode, GS;
+  uint32_t stage_bytes, tx_bytes, epi_bytes;
   const __nv_bfloat16* X;
   __nv_bfloat16* out;
   int* err;
@@ -79,11 +84,15 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+// 32 consecutive accumulator columns of this warp's 32 lanes, then the wait.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -113,7 +122,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzled tiles need 1024-byte alignment
   uint8_t* base_ptr = smem_raw + (base - raw);
-  __nv_bfloat16* staging = (__nv_bfloat16*)(base_ptr + (size_t)p.stages * p.stage_bytes);
   const uint32_t full0 = smem_u32(&bars[0]);
   const uint32_t empty0 = smem_u32(&bars[8]);
   const uint32_t tfull0 = smem_u32(&bars[16]);
@@ -206,62 +214,123 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
+    // Phase A: each thread (one tile row = one TMEM lane) converts the
+    // accumulator columns of its warp's diagonal blocks to bf16 and stores them
+    // into the shared Gram tile; the tile's dense vectors go to shared memory.
+    // Phase B: the 128 threads write the tile's output rows in output order,
+    // each product read from the Gram tile through the mode's source table.
     const int q = warp & 3;              // TMEM lane quarter this warp may read
     const int row = q * 32 + lane;       // tile row = TMEM lane
-    const int k = row / p.n;             // sample within the tile
-    const int r = row - k * p.n;         // vector index within the sample
-    // this row's products: columns j < jend of its sample's block, written from slot base
-    //   mode 0: j < r at d + r(r-1)/2;  mode 1: j <= r at d + r(r+1)/2;  mode 2: all j at r n
-    const int jend = p.mode == 0 ? r : (p.mode == 1 ? r + 1 : p.n);
-    const int base = p.mode == 0 ? p.d + r * (r - 1) / 2 : (p.mode == 1 ? p.d + r * (r + 1) / 2 : r * p.n);
+    const int tid = threadIdx.x - 64;
+    // the accumulator columns this warp's rows need: the diagonal blocks of the
+    // samples its 32 rows belong to, read 32 columns at a time (columns past N
+    // lie inside the accumulator's 128 and are never read back)
+    const int c_lo = ((q * 32) / p.n * p.n) & ~31;
+    const int c_hi = min(p.N, ((q * 32 + 31) / p.n + 1) * p.n);
+    const int dd = p.mode != 2 ? p.d : 0;  // dense pass-through width of an output row
+    const int dchunks = dd / 8;            // its 16-byte pieces
+    uint16_t* gram = (uint16_t*)(base_ptr + (size_t)p.stages * p.stage_bytes);
+    uint16_t* dsm = gram + (size_t)128 * p.GS;
+    int16_t* ptab = (int16_t*)(dsm + (size_t)p.S * dd);
+    // source of product slot u of a sample, relative to its block's corner:
+    //   mode 0: pair (r, j), j < r, at u = r(r-1)/2 + j;  mode 1: j <= r at
+    //   u = r(r+1)/2 + j;  mode 2: (u / n, u mod n)
+    for (int u = tid; u < p.W - dd; u += 128) {
+      int r = 0, j = 0;
+      if (p.mode == 2) {
+        r = u / p.n;
+        j = u - r * p.n;
+      } else {
+        const int sh = p.mode == 0 ? -1 : 1;  // row r starts at r(r + sh)/2
+        while ((r + 1) * (r + 1 + sh) / 2 <= u) ++r;
+        j = u - r * (r + sh) / 2;
+      }
+      ptab[u] = (int16_t)(r * p.GS + j);
+    }
     int64_t it = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
       const int acc = (int)(it & 1);
       const uint32_t aph = (uint32_t)((it >> 1) & 1);
+      const int nvalid = (int)imin64(p.S, p.batch - t * p.S);
+      // the tile's dense vectors: the first kDensePre pieces per thread are
+      // loaded before the wait for the accumulator, so their latency overlaps it
+      const int dense_n = nvalid * dchunks;
+      uint4 dpre[kDensePre];
+#pragma unroll
+      for (int m = 0; m < kDensePre; ++m) {
+        const int idx = tid + m * 128;
+        if (idx < dense_n) {
+          const int ks = idx / dchunks, c = idx - ks * dchunks;
+          dpre[m] = *(const uint4*)(p.X + ((t * p.S + ks) * (int64_t)p.n) * p.d + c * 8);
+        }
+      }
       const bool ok = mbar_wait(tfull0 + 8 * acc, aph);
       if (!ok) {
         set_error(p.err, CTR_ERR_TIMEOUT);
         atomicExch(&abort_flag, 1);
       }
-      // one decision for all 128 epilogue threads (also: the staging buffer is free again)
+      // one decision for all 128 epilogue threads (also: the Gram tile and the
+      // dense vectors of the previous tile have been written out)
       if (epi_any(!ok || *(volatile int*)&abort_flag)) break;
       fence_after();
-      const int64_t b = t * p.S + k;
-      const bool valid = k < p.S && b < p.batch;
-      __nv_bfloat16* st = staging + (size_t)k * p.W;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * 128u;
-      for (int c0 = 0; c0 < p.N; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(tbase + (uint32_t)c0, v);
+      uint16_t* grow = gram + (size_t)row * p.GS;
+      for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tbase + (uint32_t)c0, v);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int j = c0 + e - k * p.n;
-          if (valid && j >= 0 && j < jend) st[base + j] = __float2bfloat16_rn(__uint_as_float(v[e]));
+        for (int g = 0; g < 4; ++g) {
+          uint32_t w[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[g * 8 + 2 * h]),
+                                                      __uint_as_float(v[g * 8 + 2 * h + 1]));
+            w[h] = *(uint32_t*)&b2;
+          }
+          *(uint4*)(grow + c0 + g * 8) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-      if (valid && p.mode != 2) {
-        const __nv_bfloat16* xd = p.X + b * (int64_t)p.n * p.d;  // dense vector of sample b
-        for (int c = r; c < p.d / 8; c += p.n) {
-          uint4 w = *(const uint4*)(xd + c * 8);
-          const __nv_bfloat16* h = (const __nv_bfloat16*)&w;
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);  // the accumulator is free for the MMA two tiles on
+      for (int idx = tid; idx < dense_n; idx += 128) {
+        const int m = idx / 128;
+        const int ks = idx / dchunks, c = idx - ks * dchunks;
+        uint4 w;
+        if (m < kDensePre) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) st[c * 8 + e] = h[e];
+          for (int mm = 0; mm < kDensePre; ++mm)
+            if (mm == m) w = dpre[mm];
+        } else {
+          w = *(const uint4*)(p.X + ((t * p.S + ks) * (int64_t)p.n) * p.d + c * 8);
         }
+        *(uint4*)(dsm + (size_t)ks * dd + c * 8) = w;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");  // staging complete
-      const int64_t nvalid = imin64(p.S, p.batch - t * p.S);
-      const int64_t elems = nvalid * p.W;
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // Gram tile and dense vectors complete
+      // Phase B: output element e of the tile is slot e mod W of sample e / W
+      const int elems = nvalid * p.W;
       __nv_bfloat16* dst = p.out + t * p.S * (int64_t)p.W;
-      const int tid = threadIdx.x - 64;
+      const int blk = p.n * (p.GS + 1);  // offset between consecutive samples' block corners
       if (((uintptr_t)dst % 8) == 0 && (elems % 4) == 0) {
-        const uint2* src2 = (const uint2*)staging;
-        uint2* dst2 = (uint2*)dst;
-        for (int64_t e = tid; e < elems / 4; e += 128) dst2[e] = src2[e];
+        for (int e = 4 * tid; e < elems; e += 4 * 128) {
+          int ks = e / p.W, u = e - ks * p.W;
+          uint32_t h[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            h[x] = u < dd ? dsm[ks * dd + u] : gram[ks * blk + ptab[u - dd]];
+            if (++u == p.W) {
+              u = 0;
+              ++ks;
+            }
+          }
+          *(uint2*)(dst + e) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+        }
       } else {
-        for (int64_t e = tid; e < elems; e += 128) dst[e] = staging[e];
+        uint16_t* dst16 = (uint16_t*)dst;
+        for (int e = tid; e < elems; e += 128) {
+          const int ks = e / p.W, u = e - ks * p.W;
+          dst16[e] = u < dd ? dsm[ks * dd + u] : gram[ks * blk + ptab[u - dd]];
+        }
       }
     }
   }
@@ -294,7 +363,12 @@ int interaction_bf16_tc(const void* X, int32_t batch, int32_t n, int32_t d, int 
   p.stages = std::max(2, std::min(4, (int)((160 * 1024) / p.stage_bytes)));
   p.mode = mode;
   p.W = mode == 0 ? d + n * (n - 1) / 2 : (mode == 1 ? d + n * (n + 1) / 2 : n * n);
-  p.staging_bytes = (uint32_t)align_up((size_t)p.S * p.W * 2, 16);
+  // epilogue shared memory: the Gram tile (128 rows of GS bf16: every 32-column
+  // window that is read back, plus 8 columns against bank conflicts), the
+  // dense vectors, the product source table
+  p.GS = (p.N + 31) / 32 * 32 + 8;
+  const int dd = mode != 2 ? d : 0;
+  p.epi_bytes = (uint32_t)((size_t)128 * p.GS * 2 + (size_t)p.S * dd * 2 + align_up((size_t)(p.W - dd) * 2, 16));
   p.X = (const __nv_bfloat16*)X;
   p.out = (__nv_bfloat16*)out;
   p.err = err;
@@ -308,12 +382,35 @@ int interaction_bf16_tc(const void* X, int32_t batch, int32_t n, int32_t d, int 
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return CTR_ERR_CUDA;
-  const size_t smem = 1024 + (size_t)p.stages * p.stage_bytes + p.staging_bytes;
+  // Two CTAs per SM where they fit: each holds kTmemCols of the SM's 512 TMEM
+  // columns, and the shared memory asked for keeps a third off the SM (its
+  // allocation would wait for one of the two to exit).
+  const size_t need = 1024 + (size_t)p.stages * p.stage_bytes + p.epi_bytes;
+  const size_t smem = std::max(need, (size_t)kTcSmemFloor);
   auto kern = interaction_bf16_tc_kernel;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     return CTR_ERR_CUDA;
+  // resident CTAs per SM from the SM's shared memory and registers (the
+  // occupancy query reports one for this kernel where both allow two)
+  int per_sm = 1;
+  {
+    int dev = 0, smem_sm = 0, reserved = 0, regs_sm = 0;
+    cudaFuncAttributes fa;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, kern) != cudaSuccess)
+      return CTR_ERR_CUDA;
+    const size_t per_cta_smem = smem + fa.sharedSizeBytes + (size_t)reserved;
+    const int regs_cta = kTcThreads * ((fa.numRegs + 7) / 8 * 8);
+    per_sm = (int)std::min<size_t>(smem_sm / per_cta_smem, (size_t)(regs_sm / std::max(regs_cta, 1)));
+    per_sm = std::max(1, std::min(per_sm, (int)(512 / kTmemCols)));
+  }
   const int64_t ntiles = ceil_div(batch, p.S);
-  const int grid = (int)std::max<int64_t>(1, imin64(ntiles, num_sms()));
+  const int grid = (int)std::max<int64_t>(1, imin64(ntiles, (int64_t)per_sm * num_sms()));
   kern<<<grid, kTcThreads, smem, s>>>(p, map); count_launch();
   return launch_status();
 }
