@@ -261,12 +261,18 @@ def algorithmic_bytes(cfg, path, n_ids, n_unique):
     return out
 
 
-def profile_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if its source is unchanged."""
+def profile_traffic(kernel, args):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary: only for the workload and
+    options it was captured on (the full step as configured, SGD, fp32) and while its source is unchanged."""
     p = os.path.join(ROOT, "profiles", "full_step_kernel_traffic.json")
+    if (args.batch or args.rows or getattr(args, "dtype", "") not in ("", "f32") or args.optimizer != "sgd"
+            or args.fm or args.stochastic_rounding or getattr(args, "interaction_mode", "") not in ("", "cross")):
+        return None
     try:
         with open(p) as f:
             j = json.load(f)
+        if j.get("workload") != args.workload:
+            return None
         entry = j["kernels"][kernel]
         src = os.path.join(ROOT, "sparse_embeddings_feature_gb300", "csrc", entry["source"])
         with open(src, "rb") as f:
@@ -421,7 +427,7 @@ def run_ours(args, rank, world):
             gbs = algo[name] / (ms_k / 1e3) / 1e9
             kern[name] = {"ms": ms_k, "algorithmic_bytes": algo[name], "achieved_GBs": gbs, "frac": gbs / hbm}
     dominant = max(kern, key=lambda k: kern[k]["ms"])
-    traffic = profile_traffic(dominant)
+    traffic = profile_traffic(dominant, args)
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": kern[dominant]["achieved_GBs"], "peak": hbm,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": kern[dominant]["frac"], "traffic": traffic,
                 "algorithmic_bytes_per_launch": algo[dominant], "launch_ms": kern[dominant]["ms"]}

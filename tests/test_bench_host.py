@@ -71,3 +71,24 @@ def test_reference_arm_prints_on_rank_zero_only(tmp_path):
     assert r.returncode == 0, r.stderr
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def _bench_args(*argv):
+    old = sys.argv
+    sys.argv = ["bench.py", *argv]
+    try:
+        return bench.parse()
+    finally:
+        sys.argv = old
+
+
+def test_profiled_traffic_only_for_the_captured_workload():
+    # the committed DRAM counts belong to the full step as configured: any other
+    # workload or option reports no traffic rather than another kernel's bytes
+    j = json.load(open(os.path.join(ROOT, "profiles", "full_step_kernel_traffic.json")))
+    assert j["workload"] == "full_step"
+    got = bench.profile_traffic("bwd_tiles", _bench_args())
+    assert got is None or got == float(j["kernels"]["bwd_tiles"]["dram_bytes_per_launch"])
+    for argv in (["--workload", "tensornet"], ["--optimizer", "adam"], ["--batch", "1024"], ["--rows", "1000"],
+                 ["--dtype", "bf16"], ["--fm"], ["--stochastic-rounding"], ["--interaction-mode", "full"]):
+        assert bench.profile_traffic("bwd_tiles", _bench_args(*argv)) is None, argv
