@@ -71,6 +71,7 @@ class CtrPath:
         # bf16 tables: stochastic rounding of the updated rows, a fresh seed per update
         self.stochastic_rounding = bool(stochastic_rounding) and cfg.dtype == "bf16"
         self.sr_seed, self.updates = int(sr_seed), 0
+        self.last_sr_seed = None  # the seed of the latest update's rounding
         R = cfg.total_rows
         self.state0 = None if optimizer == "sgd" else torch.zeros(
             (R,) if optimizer == "rowwise_adagrad" else (R, d), dtype=torch.float32, device=self.dev)
@@ -171,10 +172,10 @@ class CtrPath:
         if self.opt_kind != ctr.OPT_SGD or self.stochastic_rounding:
             if self.opt_kind != ctr.OPT_SGD:
                 self.opt_step += 1
+            self.last_sr_seed = (self.sr_seed * 0x9E3779B97F4A7C15 + self.updates) & ((1 << 64) - 1)
             opt = ctr.optimizer(self.opt_kind, eps=self.eps, beta1=self.betas[0], beta2=self.betas[1],
                                 step=max(self.opt_step, 1), state0=self.state0, state1=self.state1,
-                                stochastic_rounding=self.stochastic_rounding,
-                                sr_seed=self.sr_seed * 0x9E3779B97F4A7C15 + self.updates)
+                                stochastic_rounding=self.stochastic_rounding, sr_seed=self.last_sr_seed)
             ctr.ctr_embedding_bag_bwd_update_opt(*args, ctr.BWD_ALL, opt, self.ws_bwd)
             return
         if not overlap:
