@@ -195,23 +195,29 @@ __device__ __forceinline__ uint32_t bf16_sr(float x, uint32_t u) {
 // Store one 4-value chunk of a bf16 row with stochastic rounding: the chunk's
 // 64 random bits are splitmix64(seed ^ (row d/4 + chunk)), 16 per value.  Out
 // of line: the hash inlined into the unrolled tile loops bloats them.
-__device__ __noinline__ void store_bf16_sr(const BwdArgs& a, int64_t row, int ch, float x0, float x1, float x2,
-                                           float x3) {
+__device__ __forceinline__ void store_bf16_sr_inl(const BwdArgs& a, int64_t row, int ch, float x0, float x1,
+                                                  float x2, float x3) {
   const uint64_t h = splitmix64(a.sr_seed ^ (uint64_t)(row * (a.d / 4) + ch));
   uint2 out;
   out.x = bf16_sr(x0, (uint32_t)h & 0xffffu) | (bf16_sr(x1, (uint32_t)(h >> 16) & 0xffffu) << 16);
   out.y = bf16_sr(x2, (uint32_t)(h >> 32) & 0xffffu) | (bf16_sr(x3, (uint32_t)(h >> 48) & 0xffffu) << 16);
   *(uint2*)((__nv_bfloat16*)a.table + row * a.d + ch * 4) = out;
 }
+__device__ __noinline__ void store_bf16_sr(const BwdArgs& a, int64_t row, int ch, float x0, float x1, float x2,
+                                           float x3) {
+  store_bf16_sr_inl(a, row, ch, x0, x1, x2, x3);
+}
 
 // Update one 4-value chunk of a row: w -= step, the elementwise states given
 // (st, sv: their previous values) written back.  SR: the build that honours
 // stochastic rounding (bf16 tables with a.sr set); without it the store has no
-// out-of-line call and the tile loops keep their registers.
+// out-of-line call and the tile loops keep their registers.  xdefer (SR
+// builds): the new fp32 values go there, for the caller to round and store
+// after its loop, instead of to the table.
 template <int OPT, bool SR = false>
 __device__ __forceinline__ void store_row_chunk_s(const BwdArgs& a, int64_t row, int64_t u, int ch, float4 g,
                                                   float4 w, uint2 wb, uint64_t pol, float row_inv, float4 st,
-                                                  float4 sv) {
+                                                  float4 sv, float* xdefer = nullptr) {
   if (a.grad_out) *(float4*)(a.grad_out + u * a.d + ch * 4) = g;
   // SGD keeps its single fused multiply-add per value
   float4 step = g;
@@ -233,7 +239,9 @@ __device__ __forceinline__ void store_row_chunk_s(const BwdArgs& a, int64_t row,
     const float w2 = __uint_as_float(wb.y << 16), w3 = __uint_as_float(wb.y & 0xffff0000u);
     const float x0 = fmaf(k, step.x, w0), x1 = fmaf(k, step.y, w1);
     const float x2 = fmaf(k, step.z, w2), x3 = fmaf(k, step.w, w3);
-    if (SR && a.sr) {
+    if (SR && a.sr && xdefer) {
+      *(float4*)xdefer = make_float4(x0, x1, x2, x3);
+    } else if (SR && a.sr) {
       store_bf16_sr(a, row, ch, x0, x1, x2, x3);
     } else {
       __nv_bfloat162 p0 = __floats2bfloat162_rn(x0, x1);
@@ -249,8 +257,8 @@ __device__ __forceinline__ void store_row_chunk_s(const BwdArgs& a, int64_t row,
 template <int OPT, bool SR>
 __device__ __noinline__ void store_row_chunk_call(const BwdArgs& a, int64_t row, int64_t u, int ch, float4 g,
                                                   float4 w, uint2 wb, uint64_t pol, float row_inv, float4 st,
-                                                  float4 sv) {
-  store_row_chunk_s<OPT, SR>(a, row, u, ch, g, w, wb, pol, row_inv, st, sv);
+                                                  float4 sv, float* xdefer) {
+  store_row_chunk_s<OPT, SR>(a, row, u, ch, g, w, wb, pol, row_inv, st, sv, xdefer);
 }
 
 // The same, reading the elementwise states from global memory.
@@ -702,6 +710,17 @@ __device__ __forceinline__ void cp_async_chunk(uint32_t dst, const void* src, in
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+// Shared memory of one warp of the async tile kernel: the tile's TU table rows,
+// then (from a 16-byte boundary) the elementwise optimizer states [ns][TU][d]
+// fp32, then with stochastic rounding the rows' new values [TU][d] fp32.
+__host__ __device__ constexpr size_t tile_rows_bytes(int TU, int d, int esz) {
+  return ((size_t)TU * d * esz + 15) / 16 * 16;
+}
+__host__ __device__ constexpr size_t tile_warp_bytes(int TU, int d, int esz, int ns, int xs) {
+  return tile_rows_bytes(TU, d, esz) + (size_t)(ns + xs) * TU * d * 4;
+}
+constexpr int kSrDeferBytes = 4096;  // stochastic rounding: new values held per warp (caps TU)
+
 // Optimizers with state run at 2 blocks per SM: the state arithmetic needs the
 // registers, and the staged states the shared memory.
 #ifndef CTR_TILE_OPT_MINB
@@ -720,10 +739,12 @@ __global__ void __launch_bounds__(kTileThreads, OPT == CTR_OPT_SGD ? CTR_TILE_AS
   const int chunk = 4 * esz;  // this lane's 4 elements
   // per warp: the tile's table rows, then its elementwise optimizer states (fp32)
   constexpr int NS = kElemStates<OPT>;
+  constexpr int XS = SR ? 1 : 0;
   const int state_bytes = a.d * 4;
-  unsigned char* wsm = wsm_raw + (size_t)warp * TU * (row_bytes + NS * state_bytes);
+  unsigned char* wsm = wsm_raw + (size_t)warp * tile_warp_bytes(TU, a.d, esz, NS, XS);
   const uint32_t wsm_s = (uint32_t)__cvta_generic_to_shared(wsm);
-  unsigned char* ssm = wsm + (size_t)TU * row_bytes;  // state s of unique j: ssm + (s * TU + j) * state_bytes
+  unsigned char* ssm = wsm + tile_rows_bytes(TU, a.d, esz);  // state s of unique j: ssm + (s * TU + j) * state_bytes
+  float* xsm = (float*)(ssm + (size_t)NS * TU * state_bytes);  // new values of unique j: xsm + j * d
   const uint32_t ssm_s = (uint32_t)__cvta_generic_to_shared(ssm);
   const float* Gl = a.G + lane * 4;
   // pooled-gradient rows are re-read by every unique of their bags: keep them
@@ -826,9 +847,11 @@ __global__ void __launch_bounds__(kTileThreads, OPT == CTR_OPT_SGD ? CTR_TILE_AS
               if constexpr (NS >= 2) sv = *(const float4*)(ssm + (TU + sg) * state_bytes + lane * 16);
               // the elementwise optimizers' updates (a divide and a square root per value) out of line
               if constexpr (OPT == CTR_OPT_ADAGRAD || OPT == CTR_OPT_ADAM)
-                store_row_chunk_call<OPT, SR>(a, rs, tile * TU + sg, lane, acc, w, wb, pol_stream, rinv, st, sv);
+                store_row_chunk_call<OPT, SR>(a, rs, tile * TU + sg, lane, acc, w, wb, pol_stream, rinv, st, sv,
+                                              SR ? xsm + sg * a.d + lane * 4 : nullptr);
               else
-                store_row_chunk_s<OPT, SR>(a, rs, tile * TU + sg, lane, acc, w, wb, pol_stream, rinv, st, sv);
+                store_row_chunk_s<OPT, SR>(a, rs, tile * TU + sg, lane, acc, w, wb, pol_stream, rinv, st, sv,
+                                           SR ? xsm + sg * a.d + lane * 4 : nullptr);
             }
             acc = make_float4(0.f, 0.f, 0.f, 0.f);
           }
@@ -838,6 +861,22 @@ __global__ void __launch_bounds__(kTileThreads, OPT == CTR_OPT_SGD ? CTR_TILE_AS
       pend = ahead;
       gcur = gnxt;
       sc_cur = sc_nxt;
+    }
+    if constexpr (SR) {
+      // the tile's new rows, rounded and stored outside the unrolled loop, with
+      // every lane busy: 32 / (d/4) rows per round, one column chunk per lane
+      __syncwarp();  // the chunks written above by other lanes
+      const int chunks = a.d >> 2;
+      const int rpi = 32 / chunks;
+      const int jl = lane / chunks, ch = lane - jl * chunks;
+      for (int j0 = 0; j0 < TU; j0 += rpi) {
+        const int j = j0 + jl;
+        const int64_t rj = __shfl_sync(kFull, row, j < 32 ? j : 0);
+        if (jl < rpi && j < TU && rj >= 0) {
+          const float4 x = *(const float4*)(xsm + j * a.d + ch * 4);
+          store_bf16_sr_inl(a, rj, ch, x.x, x.y, x.z, x.w);
+        }
+      }
     }
     cp_async_wait_all();  // nothing may land in the buffer after the next tile reuses it
     __syncwarp();
@@ -960,7 +999,7 @@ int launch_short(const BwdArgs& a, cudaStream_t s, int64_t n) {
   auto tk = use_async ? async_k : bwd_tiles_kernel<CPL>;
   const int ns = a.opt == CTR_OPT_ADAGRAD ? 1 : (a.opt == CTR_OPT_ADAM ? 2 : 0);
   const size_t tile_smem =
-      use_async ? (size_t)kTileWarps * a.TU * ((size_t)a.d * (a.bf16 ? 2 : 4) + (size_t)ns * a.d * 4) : acc_smem;
+      use_async ? (size_t)kTileWarps * tile_warp_bytes(a.TU, a.d, a.bf16 ? 2 : 4, ns, a.sr ? 1 : 0) : acc_smem;
   if (tile_smem > 48 * 1024 &&
       cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tile_smem) != cudaSuccess)
     return CTR_ERR_CUDA;
@@ -1104,6 +1143,7 @@ int bwd_update_phases(const float* grad_pooled, int64_t g_stride_b, int64_t g_st
     const int staged = d * (dtype == CTR_BF16 ? 2 : 4) + ns * d * 4;
     const int budget = kind == CTR_OPT_SGD ? kAccFloats * 4 : kOptStageBytes;
     a.TU = std::max(1, std::min({32, kAccFloats / d, budget / staged}));
+    if (a.sr) a.TU = std::max(1, std::min(a.TU, kSrDeferBytes / (d * 4)));
   }
   {
     const int64_t max_off = (int64_t)(batch - 1) * g_stride_b + (int64_t)(num_fields - 1) * g_stride_f + d;

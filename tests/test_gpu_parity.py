@@ -770,7 +770,8 @@ def _opt_case(seed, d, dtype, opt):
 
 
 @pytest.mark.parametrize("opt", ["adagrad", "rowwise_adagrad", "adam"])
-@pytest.mark.parametrize("d,dtype", [(32, "f32"), (128, "f32"), (256, "f32"), (64, "bf16")])
+@pytest.mark.parametrize("d,dtype", [(32, "f32"), (128, "f32"), (256, "f32"), (64, "bf16"),
+                                     (44, "bf16"), (116, "bf16")])   # odd uniques per tile x odd d/4
 def test_bwd_update_optimizers_exact_gradients(opt, d, dtype):
     F, B, rows, ids, offsets, table, G, rb, s0, s1 = _opt_case(d + len(opt), d, dtype, opt)
     b2t = np.arange(F, dtype=np.int32)
@@ -848,7 +849,7 @@ def _bf16_ulp(v):
 
 
 @pytest.mark.parametrize("opt", ["sgd", "adagrad", "rowwise_adagrad", "adam"])
-@pytest.mark.parametrize("d", [32, 64, 256])
+@pytest.mark.parametrize("d", [32, 44, 64, 256])
 def test_bwd_update_stochastic_rounding(opt, d):
     F, B, rows, ids, offsets, table, G, rb, s0, s1 = _opt_case(3 * d + len(opt), d, "bf16",
                                                                "adagrad" if opt == "sgd" else opt)
