@@ -711,13 +711,12 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // Shared memory of one warp of the async tile kernel: the tile's TU table rows,
-// then (from a 16-byte boundary) the elementwise optimizer states [ns][TU][d]
-// fp32, then with stochastic rounding the rows' new values [TU][d] fp32.
-__host__ __device__ constexpr size_t tile_rows_bytes(int TU, int d, int esz) {
-  return ((size_t)TU * d * esz + 15) / 16 * 16;
-}
-__host__ __device__ constexpr size_t tile_warp_bytes(int TU, int d, int esz, int ns, int xs) {
-  return tile_rows_bytes(TU, d, esz) + (size_t)(ns + xs) * TU * d * 4;
+// then the elementwise optimizer states [ns][TU][d] fp32, then with stochastic
+// rounding the rows' new values [TU][d] fp32; TU * row bytes is a multiple of
+// 16 (the host keeps TU even for bf16 rows of d = 4 mod 8), so every section
+// starts on a 16-byte boundary.
+constexpr size_t tile_warp_bytes(int TU, int d, int esz, int ns, int xs) {
+  return (size_t)TU * d * esz + (size_t)(ns + xs) * TU * d * 4;
 }
 constexpr int kSrDeferBytes = 4096;  // stochastic rounding: new values held per warp (caps TU)
 
@@ -739,12 +738,12 @@ __global__ void __launch_bounds__(kTileThreads, OPT == CTR_OPT_SGD ? CTR_TILE_AS
   const int chunk = 4 * esz;  // this lane's 4 elements
   // per warp: the tile's table rows, then its elementwise optimizer states (fp32)
   constexpr int NS = kElemStates<OPT>;
-  constexpr int XS = SR ? 1 : 0;
   const int state_bytes = a.d * 4;
-  unsigned char* wsm = wsm_raw + (size_t)warp * tile_warp_bytes(TU, a.d, esz, NS, XS);
+  constexpr int XS = SR ? 1 : 0;
+  unsigned char* wsm = wsm_raw + (size_t)warp * TU * (row_bytes + (NS + XS) * state_bytes);
   const uint32_t wsm_s = (uint32_t)__cvta_generic_to_shared(wsm);
-  unsigned char* ssm = wsm + tile_rows_bytes(TU, a.d, esz);  // state s of unique j: ssm + (s * TU + j) * state_bytes
-  float* xsm = (float*)(ssm + (size_t)NS * TU * state_bytes);  // new values of unique j: xsm + j * d
+  unsigned char* ssm = wsm + (size_t)TU * row_bytes;  // state s of unique j: ssm + (s * TU + j) * state_bytes
+  float* xsm = (float*)(ssm + NS * TU * state_bytes);  // new values of unique j: xsm + j * d
   const uint32_t ssm_s = (uint32_t)__cvta_generic_to_shared(ssm);
   const float* Gl = a.G + lane * 4;
   // pooled-gradient rows are re-read by every unique of their bags: keep them
@@ -998,6 +997,7 @@ int launch_short(const BwdArgs& a, cudaStream_t s, int64_t n) {
                                                             : bwd_tiles_async_kernel<CTR_OPT_SGD, false>);
   auto tk = use_async ? async_k : bwd_tiles_kernel<CPL>;
   const int ns = a.opt == CTR_OPT_ADAGRAD ? 1 : (a.opt == CTR_OPT_ADAM ? 2 : 0);
+  if (use_async && ((size_t)a.TU * a.d * (a.bf16 ? 2 : 4)) % 16 != 0) return CTR_ERR_UNSUPPORTED;  // layout rule
   const size_t tile_smem =
       use_async ? (size_t)kTileWarps * tile_warp_bytes(a.TU, a.d, a.bf16 ? 2 : 4, ns, a.sr ? 1 : 0) : acc_smem;
   if (tile_smem > 48 * 1024 &&
@@ -1144,6 +1144,9 @@ int bwd_update_phases(const float* grad_pooled, int64_t g_stride_b, int64_t g_st
     const int budget = kind == CTR_OPT_SGD ? kAccFloats * 4 : kOptStageBytes;
     a.TU = std::max(1, std::min({32, kAccFloats / d, budget / staged}));
     if (a.sr) a.TU = std::max(1, std::min(a.TU, kSrDeferBytes / (d * 4)));
+    // the async tile kernel's per-warp sections start on 16-byte boundaries:
+    // TU rows of bf16 with d = 4 (mod 8) take an even TU
+    if (dtype == CTR_BF16 && d % 8 != 0 && a.TU > 1) a.TU &= ~1;
   }
   {
     const int64_t max_off = (int64_t)(batch - 1) * g_stride_b + (int64_t)(num_fields - 1) * g_stride_f + d;

@@ -823,7 +823,13 @@ int dedup_bitmap(const int64_t* ids, const int64_t* offsets, int32_t F, int32_t 
   // ranks go straight into the caller's inverse map, which the first pass reads
   uint32_t* ranks = inverse ? (uint32_t*)inverse : keys[0];
   {
-    const int64_t blocks = std::max<int64_t>(1, imin64(ceil_div(n_ids, 256 * kRankPer), (int64_t)sms * 6));
+    // one full wave: the grid-stride rounds split evenly over the resident blocks
+    // (a grid of more than the resident blocks ran a second, partly empty wave)
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bitmap_rank_kernel, 256, 0) != cudaSuccess)
+      return CTR_ERR_CUDA;
+    const int64_t blocks =
+        std::max<int64_t>(1, imin64(ceil_div(n_ids, 256 * kRankPer), (int64_t)std::max(per_sm, 1) * sms));
     const int vec = ((uintptr_t)ranks % 16) == 0;
     bitmap_rank_kernel<<<(unsigned)blocks, 256, 0, s>>>(keys[1], n_ids, total_rows, pk, dplan, ranks, vec, g_hist,
                                                         err);
