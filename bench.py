@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller cases for profiling)")
     ap.add_argument("--rows", type=int, default=0, help="override rows per table (smaller cases for profiling)")
     ap.add_argument("--fm", action="store_true", help="the gather also writes each bag's FM second-order term")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every kernel of every step from the host instead of replaying captured steps")
     ap.add_argument("--dtype", default="", choices=["", "f32", "bf16"], help="override the table dtype")
     ap.add_argument("--stochastic-rounding", action="store_true",
                     help="bf16 tables: round the updated rows stochastically")
@@ -354,6 +356,21 @@ def run_ours(args, rank, world):
         return e
 
     kev = [{k: (new_event(), new_event()) for k in kernels} for _ in range(args.steps)]
+    # captured steps: one CUDA graph per timed step, each holding its own timing events
+    # (a step's host-side values must not change between steps: Adam and stochastic
+    # rounding run eagerly)
+    use_graph = not args.eager and args.optimizer != "adam" and not path.stochastic_rounding
+    graphs = None
+    if use_graph:
+        graphs = []
+        for k in range(args.steps):
+            for name, kid in kernels.items():
+                ctr.ctr_set_timing_events(kid, *kev[k][name])
+            graphs.append(path.capture())
+        for kid in kernels.values():
+            ctr.ctr_set_timing_events(kid, None, None)
+        for g in graphs:  # each graph's first launch (its upload) outside the timed region
+            g.replay()
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
@@ -365,11 +382,16 @@ def run_ours(args, rank, world):
         t_start.record(stream)
         launches0 = ctr.ctr_launch_count()
         for k in range(args.steps):
-            for name, kid in kernels.items():
-                ctr.ctr_set_timing_events(kid, *kev[k][name])
-            path.step()
+            if graphs is not None:
+                graphs[k].replay()
+            else:
+                for name, kid in kernels.items():
+                    ctr.ctr_set_timing_events(kid, *kev[k][name])
+                path.step()
         t_end.record(stream)
         launches = ctr.ctr_launch_count() - launches0
+        if graphs is not None:
+            launches = sum(g.launches for g in graphs)
         torch.cuda.synchronize()
         time.sleep(0.25)
         mark1 = clk.mark()
@@ -400,7 +422,7 @@ def run_ours(args, rank, world):
         if cfg.dtype == "bf16":
             host["dense"] = host["dense"].view(torch.int16).view(torch.bfloat16)
         from sparse_embeddings_feature_gb300.pipeline import HostPipeline
-        pipe = HostPipeline(path)
+        pipe = HostPipeline(path, graphs=use_graph)
         result = path.out if path.out is not None else path.pooled
         outs = [torch.empty(result.shape, dtype=result.dtype).pin_memory() for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -441,6 +463,7 @@ def run_ours(args, rank, world):
                    "stochastic_rounding": bool(path.stochastic_rounding and cfg.backward != "none"),
                    "rows_per_table": cfg.rows_per_table[0], "d": cfg.d, "bag_len": list(cfg.bag_len),
                    "ids": list(cfg.ids), "n_ids": n_ids, "n_unique": n_unique, "parallelism": f"replicas{world}",
+                   "launch": "cuda_graph" if use_graph else "eager",
                    "l2": "inputs larger than L2 (tables %.1f GB, ids %.2f GB)" % (
                        cfg.total_rows * cfg.d * 4 / 1e9, n_ids * 8 / 1e9)},
         "interaction_samples_per_s": cfg.batch * world / (ms / 1e3),

@@ -39,7 +39,14 @@ void timing_mark(int kernel, bool before, cudaStream_t s) {
     std::lock_guard<std::mutex> lock(g_timing_mu);
     e = g_timing[kernel][before ? 0 : 1];
   }
-  if (e) cudaEventRecord(e, s);
+  if (!e) return;
+  // inside a stream capture a plain record is only a dependency edge; an
+  // external record becomes a node that records the event at every replay
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
 }
 
 namespace {

@@ -235,15 +235,44 @@ class CtrPath:
             self.bwd_update(overlap=self.overlap_backward)
 
 
+    def capture(self) -> "StepGraph":
+        """One step captured as a CUDA graph (the same kernels, streams and buffers), replayed
+        with `.replay()` on the current stream: one launch per step instead of one per kernel.
+
+        A graph fixes the host-side values of the step it captured: the ID count, and Adam's
+        step number and the stochastic-rounding seed, which change every step, so those two
+        are refused here (SGD and both Adagrads are step-independent)."""
+        if self.opt_kind == ctr.OPT_ADAM or self.stochastic_rounding:
+            raise ValueError("a captured step would repeat Adam's step number or the rounding seed")
+        g = torch.cuda.CUDAGraph()
+        n0 = ctr.ctr_launch_count()
+        with torch.cuda.graph(g):
+            self.step()
+        return StepGraph(g, ctr.ctr_launch_count() - n0, self.n_ids)
+
+
+class StepGraph:
+    """A captured CtrPath step: `replay()` runs it on the current stream; `launches` is the
+    number of library kernels it holds, `n_ids` the ID count it was captured for."""
+
+    def __init__(self, graph, launches: int, n_ids: int):
+        self.graph, self.launches, self.n_ids = graph, int(launches), int(n_ids)
+
+    def replay(self) -> None:
+        self.graph.replay()
+
+
 class HostPipeline:
     """Runs CtrPath steps over batches held in pinned host memory, with the copies overlapped.
 
-    Two device buffer sets hold the per-batch inputs (IDs, offsets, dense
+    `depth` device buffer sets hold the per-batch inputs (IDs, offsets, dense
     vectors, upstream gradient) and the step's output.  While step k runs on
-    the compute stream, the inputs of step k+1 are copied in on one copy stream
-    and the output of step k-1 is copied out on another, so the host<->device
-    transfers hide behind the kernels.  Every batch's inputs and every step's
-    output still cross the host boundary, in full, once per step.
+    the compute stream, the inputs of step k + depth - 1 are copied in on one
+    copy stream and the output of step k-1 is copied out on another, so the
+    host<->device transfers hide behind the kernels; a copy may take up to
+    depth - 1 steps (host-to-device copies on the GB300 machine occasionally stall
+    for tens of milliseconds).  Every batch's inputs and every step's output
+    still cross the host boundary, in full, once per step.
 
     A batch is a dict with pinned CPU tensors "ids" (int64), "offsets" (int64,
     [F*B+1]), "dense" ([B, d], the table dtype), and "dout" ([B, width] fp32) or
@@ -252,13 +281,16 @@ class HostPipeline:
     the pooled vectors for workloads without one).
     """
 
-    def __init__(self, path: CtrPath):
+    def __init__(self, path: CtrPath, graphs: bool = False, depth: int = 4):
+        if depth < 2:
+            raise ValueError("the pipeline needs at least two buffer sets")
         self.path = path
+        self.depth = D = int(depth)
         cfg = path.cfg
         self.result_name = "out" if path.out is not None else "pooled"
         names = ["ids", "offsets"] + [k for k in ("dout", "grad_pooled") if getattr(path, k) is not None]
         self.sets = []
-        for s in range(2):
+        for s in range(D):
             bufs = {k: (getattr(path, k) if s == 0 else torch.empty_like(getattr(path, k))) for k in names}
             bufs["dense"] = torch.empty((cfg.batch, cfg.d), dtype=path.X.dtype, device=path.dev)
             res = getattr(path, self.result_name)
@@ -268,12 +300,26 @@ class HostPipeline:
         self.compute = torch.cuda.current_stream(path.dev)
         self.h2d = torch.cuda.Stream(path.dev)
         self.d2h = torch.cuda.Stream(path.dev)
-        self.ev_in = [torch.cuda.Event() for _ in range(2)]
-        self.ev_done = [torch.cuda.Event() for _ in range(2)]
-        self.ev_out = [torch.cuda.Event() for _ in range(2)]
-        for s in range(2):   # create the events in a completed state
+        self.ev_in = [torch.cuda.Event() for _ in range(D)]
+        self.ev_done = [torch.cuda.Event() for _ in range(D)]
+        self.ev_out = [torch.cuda.Event() for _ in range(D)]
+        for s in range(D):   # create the events in a completed state
             self.ev_done[s].record(self.compute)
             self.ev_out[s].record(self.compute)
+        # with graphs: one captured step per buffer set (batches must keep the ID count)
+        self.graphs = None
+        if graphs:
+            self.graphs = []
+            for s in range(D):
+                self._bind(s)
+                self.graphs.append(path.capture())
+            self._bind(0)
+
+    def _bind(self, s):
+        bufs = self.sets[s]
+        for name in self.names:
+            setattr(self.path, name, bufs[name])
+        setattr(self.path, self.result_name, bufs["result"])
 
     def _copy_in(self, batch, s):
         bufs = self.sets[s]
@@ -302,28 +348,33 @@ class HostPipeline:
             return
         if start_event is not None:
             start_event.record(self.compute)
+        D = self.depth
         self.h2d.wait_stream(self.compute)
-        self._copy_in(batches[0], 0)
+        for j in range(min(D - 1, K)):
+            self._copy_in(batches[j], j)
         for k in range(K):
-            s = k & 1
+            s = k % D
             bufs = self.sets[s]
             n = batches[k]["ids"].numel()
             if n > path.ids.numel():
                 raise ValueError(f"batch {k} has {n} IDs, more than the path's capacity {path.ids.numel()}")
             self.compute.wait_event(self.ev_in[s])
             self.compute.wait_event(self.ev_out[s])         # the previous output in this set has been copied out
-            path.n_ids = n
-            for name in self.names:
-                setattr(path, name, bufs[name])
-            setattr(path, self.result_name, bufs["result"])
             path.X[:, 0, :].copy_(bufs["dense"], non_blocking=True)
-            path.step()
+            if self.graphs is not None:
+                if n != self.graphs[s].n_ids:
+                    raise ValueError(f"batch {k} has {n} IDs; the captured steps were for {self.graphs[s].n_ids}")
+                self.graphs[s].replay()
+            else:
+                path.n_ids = n
+                self._bind(s)
+                path.step()
             self.ev_done[s].record(self.compute)
-            if k + 1 < K:
-                self._copy_in(batches[k + 1], (k + 1) & 1)
+            if k + D - 1 < K:
+                self._copy_in(batches[k + D - 1], (k + D - 1) % D)
             with torch.cuda.stream(self.d2h):
                 self.d2h.wait_event(self.ev_done[s])
                 outputs[k].copy_(bufs["result"], non_blocking=True)
                 self.ev_out[s].record(self.d2h)
-        self.compute.wait_event(self.ev_out[(K - 1) & 1])
-        self.compute.wait_event(self.ev_out[K & 1])
+        for s in range(D):
+            self.compute.wait_event(self.ev_out[s])

@@ -12,7 +12,7 @@ import torch
 from oracle import oracle as O
 from sparse_embeddings_feature_gb300 import ctr
 from sparse_embeddings_feature_gb300 import workload as W
-from sparse_embeddings_feature_gb300.pipeline import CtrPath
+from sparse_embeddings_feature_gb300.pipeline import CtrPath, HostPipeline
 
 from _tol import bf16_close, f32_close
 
@@ -916,3 +916,77 @@ def test_bwd_update_stochastic_rounding_ignored_for_f32():
         assert ctr.ctr_check_status(ws) == 0
         outs.append(_np(tab))
     np.testing.assert_array_equal(outs[0], outs[1])
+
+
+# ---------------------------------------------------------------------------
+# captured steps (CUDA graphs)
+# ---------------------------------------------------------------------------
+def _small_path(name, **kw):
+    cfg = W.CONFIGS[name]
+    if name == "full_step":
+        cfg = cfg.shrink(batch=512, rows_per_table=tuple([20000] * 26))
+    elif name == "tensornet":
+        cfg = cfg.shrink(batch=1024, rows_per_table=(1 << 20,), ids=cfg.ids[:3] + (20,))
+    w = W.make_workload(cfg)
+    path = CtrPath(cfg, w["ids"].size, **kw)
+    path.upload(w)
+    return cfg, w, path
+
+
+@pytest.mark.parametrize("name,opt", [("full_step", "sgd"), ("tensornet", "sgd"), ("full_step", "rowwise_adagrad")])
+def test_captured_step_equals_eager_steps(name, opt):
+    # two identical paths: one steps eagerly, the other replays a captured step;
+    # after three steps every output, the table and the optimizer state agree bit for bit
+    _, _, pe = _small_path(name, optimizer=opt)
+    _, _, pg = _small_path(name, optimizer=opt)
+    g = pg.capture()
+    assert g.launches > 0
+    for _ in range(3):
+        pe.step()
+        g.replay()
+    torch.cuda.synchronize()
+    assert pe.check_status() == pg.check_status() == {k: 0 for k in pe.check_status()}
+    nu = int(pe.n_unique.item())
+    assert nu == int(pg.n_unique.item())
+    n = pe.n_ids
+    defined = {"unique_rows": nu, "run_offsets": nu + 1, "inverse": n, "sorted_bag": n}  # capacity-sized buffers
+    for attr in ("unique_rows", "inverse", "sorted_bag", "run_offsets", "X", "out", "pooled", "dX", "table", "state0"):
+        a, b = getattr(pe, attr, None), getattr(pg, attr, None)
+        if a is None:
+            continue
+        if attr in defined:
+            a, b = a[:defined[attr]], b[:defined[attr]]
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b), attr
+
+
+def test_capture_refuses_step_dependent_values():
+    _, _, p = _small_path("tensornet", optimizer="adam")
+    with pytest.raises(ValueError):
+        p.capture()
+    base = W.CONFIGS["tensornet"]
+    cfg = base.shrink(batch=256, dtype="bf16", table_init=("normal4", 0.01), rows_per_table=(1 << 20,),
+                      ids=base.ids[:3] + (20,))
+    w = W.make_workload(cfg)
+    p = CtrPath(cfg, w["ids"].size, stochastic_rounding=True)
+    with pytest.raises(ValueError):
+        p.capture()
+
+
+def test_host_pipeline_with_captured_steps_equals_eager():
+    cfg = W.CONFIGS["full_step"].shrink(batch=512, rows_per_table=tuple([20000] * 26))
+    w = W.make_workload(cfg)
+    host = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in w.items()
+            if k in ("ids", "offsets", "dense", "dout")}
+    outs = {}
+    for graphs in (False, True):
+        path = CtrPath(cfg, w["ids"].size)
+        path.upload(w)
+        pipe = HostPipeline(path, graphs=graphs)
+        res = [torch.empty(path.out.shape, dtype=path.out.dtype).pin_memory() for _ in range(4)]
+        pipe.run([host] * 4, res)
+        torch.cuda.synchronize()
+        outs[graphs] = ([r.clone() for r in res], path.table.cpu())
+    for a, b in zip(outs[False][0], outs[True][0]):
+        assert torch.equal(a, b)
+    assert torch.equal(outs[False][1], outs[True][1])
