@@ -105,6 +105,13 @@ int ctr_set_timing_events(int kernel, void* before_event, void* after_event);
  * never fails. */
 uint64_t ctr_launch_count(void);
 
+/* Gather variant of ctr_embedding_bag_fwd for fp32 tables with d = 128 and no
+ * FM output: on != 0 selects the TMA row gather (cp.async.bulk.tensor with
+ * tile::gather4 into a shared-memory ring), 0 (the default) the register-window
+ * gather, which measured faster on GB300.  Both sum each bag in index order.
+ * Process-wide; returns the previous setting. */
+int ctr_set_tma_gather(int on);
+
 /* ------------------------------------------------------------------------ */
 /* Input generation (not part of the method)                                 */
 /* ------------------------------------------------------------------------ */

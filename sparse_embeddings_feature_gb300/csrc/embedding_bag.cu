@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "common.cuh"
@@ -223,10 +224,9 @@ __global__ void __launch_bounds__(kBagThreads) bag_fwd_kernel(const BagArgs a, c
 // one 16-byte load per lane and four adds.  Each bag is summed in the order of
 // its indices; at its last occurrence the warp stores the row.
 constexpr int kWinF = 8;
-#ifndef CTR_TMA_GATHER
-#define CTR_TMA_GATHER 0  // measured slower than the register window on GB300; kept selectable
-#endif
-constexpr bool kUseTmaGather = CTR_TMA_GATHER != 0;
+// The TMA gather variant is off unless selected (ctr_set_tma_gather): measured
+// slower than the register window on GB300.
+std::atomic<int> g_tma_gather{0};
 constexpr uint32_t kNoRow = 0xffffffffu;
 #ifndef CTR_FLAT_MINB
 #define CTR_FLAT_MINB 3  // resident blocks per SM the register budget is sized for
@@ -596,7 +596,7 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
   }
   const int chunks = a.d / V;
   CUtensorMap map;
-  if (std::is_same<TT, float>::value && a.d == 128 && kUseTmaGather && !a.fm_out && make_row_map(a, &map)) {
+  if (std::is_same<TT, float>::value && a.d == 128 && g_tma_gather.load(std::memory_order_relaxed) && !a.fm_out && make_row_map(a, &map)) {
     auto k = bag_fwd_tma_kernel<IT>;
     const size_t smem = 1024 + (size_t)kTmaWarps * kTmaStages * kTmaStageBytes;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -670,6 +670,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const char* __restrict
 using namespace ctr;
 
 extern "C" size_t ctr_embedding_bag_workspace_size(void) { return kWsHeader; }
+
+extern "C" int ctr_set_tma_gather(int on) { return g_tma_gather.exchange(on ? 1 : 0); }
 
 namespace {
 

@@ -33,6 +33,7 @@ _SIGS = {
     "ctr_version": (C.c_int, []),
     "ctr_set_timing_events": (C.c_int, [C.c_int, _p, _p]),
     "ctr_launch_count": (C.c_uint64, []),
+    "ctr_set_tma_gather": (C.c_int, [C.c_int]),
     "ctr_status_reset": (C.c_int, [_p, _p]),
     "ctr_check_status": (C.c_int, [_p, _p]),
     "ctr_fill_table": (C.c_int, [_p, C.c_int, _i64, _i32, _i64, C.c_int, _u64, _f32, _p]),
@@ -138,6 +139,11 @@ def ctr_set_timing_events(kernel: int, before=None, after=None) -> None:
 def ctr_launch_count() -> int:
     """Kernel launches the library has issued in this process so far."""
     return int(lib().ctr_launch_count())
+
+
+def ctr_set_tma_gather(on: bool) -> bool:
+    """Select the TMA row-gather variant of the fp32 d=128 pooled gather; returns the previous setting."""
+    return bool(lib().ctr_set_tma_gather(1 if on else 0))
 
 
 # ---------------------------------------------------------------------------

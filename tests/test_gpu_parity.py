@@ -990,3 +990,22 @@ def test_host_pipeline_with_captured_steps_equals_eager():
     for a, b in zip(outs[False][0], outs[True][0]):
         assert torch.equal(a, b)
     assert torch.equal(outs[False][1], outs[True][1])
+
+
+@pytest.mark.parametrize("name", ["dlrm_fp32", "full_step_b128"])
+def test_embedding_bag_fwd_tma_gather_variant(name):
+    # the TMA row-gather variant (fp32, d = 128), off by default: same bags, same
+    # summation order as the default gather, so the same bits; and the oracle's values
+    cfg = FWD_CASES[name]
+    w = W.make_workload(cfg, with_grads=False)
+    plain = _fwd_case(cfg, w)
+    prev = ctr.ctr_set_tma_gather(True)
+    try:
+        got = _fwd_case(cfg, w)
+    finally:
+        ctr.ctr_set_tma_gather(prev)
+    ref, mag = O.embedding_bag_fwd(w["ids"], w["offsets"], cfg.num_fields, cfg.batch, w["bag_to_table"],
+                                   w["row_base"], cfg.d, pool=cfg.pool, dtype=cfg.dtype, gen=_gen(cfg),
+                                   with_mag=True)
+    f32_close(got, ref, mag, int(np.diff(w["offsets"]).max()) + 1, what=f"TMA gather {name}")
+    np.testing.assert_array_equal(got, plain)
