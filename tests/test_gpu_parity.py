@@ -1009,3 +1009,24 @@ def test_embedding_bag_fwd_tma_gather_variant(name):
                                    with_mag=True)
     f32_close(got, ref, mag, int(np.diff(w["offsets"]).max()) + 1, what=f"TMA gather {name}")
     np.testing.assert_array_equal(got, plain)
+
+
+def test_full_path_with_every_bag_empty():
+    # zero IDs: the dedup finds no rows, the pooled vectors are zero, the
+    # interaction sees only the dense vector, and no table row changes
+    cfg = W.CONFIGS["full_step"].shrink(batch=64, rows_per_table=tuple([1000] * 26), bag_len=("fixed", 0))
+    w = W.make_workload(cfg)
+    assert w["ids"].size == 0
+    path = CtrPath(cfg, 0)
+    before = path.table.clone()
+    path.upload(w)
+    path.reset_status()
+    path.step()
+    torch.cuda.synchronize()
+    assert all(v == 0 for v in path.check_status().values())
+    assert int(path.n_unique.item()) == 0
+    n, d = cfg.n_vectors, cfg.d
+    X = np.concatenate([w["dense"][:, None, :], np.zeros((cfg.batch, n - 1, d), np.float32)], axis=1)
+    ref, mag = O.dot_interaction(X, n, d, with_mag=True)
+    f32_close(_np(path.out), ref, mag, d + 64, what="interaction of empty bags")
+    assert torch.equal(path.table, before)
