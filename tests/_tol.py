@@ -1,6 +1,6 @@
 """Tolerances used by the GPU-vs-oracle parity tests.
 
-fp32 outputs (spec tolerance): |gpu - ref| <= atol + rtol |ref| with
+fp32 outputs (the path's stated tolerance): |gpu - ref| <= atol + rtol |ref| with
 rtol = 1e-5, atol = 1e-6.  Every fp32 output of the path is a sum, and a sum
 whose terms cancel has no relative accuracy in any summation order, so the
 bound adds the standard a-priori forward-error term of recursive summation,
@@ -8,12 +8,12 @@ gamma_k * sum|terms| with gamma_k = k u / (1 - k u), u = 2^-24 and k the
 longest chain of dependent fp32 additions the kernel performs for that output
 (its reduction depth).  The oracle reports sum|terms| (the "magnitude") next
 to every value.  For outputs whose terms do not cancel the extra term is below
-the spec one, and the exact-arithmetic tests (dyadic inputs, where every
+the stated one, and the exact-arithmetic tests (dyadic inputs, where every
 sum is exact) compare bit for bit, so a dropped or doubled term cannot hide in
 the tolerance.
 
 bf16 outputs: |gpu - ref| <= rtol |ref| + atol + gamma_k sum|terms| with
-rtol = 1e-2 (the benchmark spec), the fp32 accumulation term as above, and atol = 1e-5
+rtol = 1e-2 (the stated bf16 tolerance), the fp32 accumulation term as above, and atol = 1e-5
 for pooled bf16 values (atol 0 for interaction outputs).
 
 `mrel` adds mrel * sum|terms| to the bound.  It is used where a sum's inputs
