@@ -234,7 +234,6 @@ class CtrPath:
         if cfg.backward != "none":
             self.bwd_update(overlap=self.overlap_backward)
 
-
     def capture(self) -> "StepGraph":
         """One step captured as a CUDA graph (the same kernels, streams and buffers), replayed
         with `.replay()` on the current stream: one launch per step instead of one per kernel.
