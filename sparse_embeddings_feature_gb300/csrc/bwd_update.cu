@@ -570,7 +570,7 @@ __device__ __forceinline__ uint64_t g_policy() {
 __device__ __forceinline__ uint64_t row_policy() { return CTR_BWD_ROW_STREAM ? l2_evict_first() : l2_evict_normal(); }
 
 #ifndef CTR_BWD_MINB
-#define CTR_BWD_MINB 3  // resident blocks per SM the register budget is sized for
+#define CTR_BWD_MINB 8  // piece kernel: resident blocks per SM (full occupancy, 32 registers)
 #endif
 
 // Rows wider than 512 bytes: one warp per piece, kU / CPL rows in flight.
@@ -619,6 +619,15 @@ __device__ __forceinline__ uint32_t bag_g4(const BwdArgs& a, int32_t bag, float&
   return (uint32_t)(((int64_t)b * a.sb + (int64_t)f * a.sf) >> 2);
 }
 
+// Gradient-row loads in flight per lane in the piece kernel.  The kernel is
+// latency-bound (ncu: L2 at half its throughput, 37% of warps active at 3
+// blocks per SM with 8 loads each); 2 loads per lane at 8 blocks per SM keep
+// more rows in flight per SM and cut it by 29% (4 at 4: 7%; 16 at 2: slower).
+#ifndef CTR_PIECE_WIN
+#define CTR_PIECE_WIN 2
+#endif
+constexpr int kPieceWin = CTR_PIECE_WIN;
+static_assert(32 % kPieceWin == 0, "the load window must divide the chunk");
 __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(const BwdArgs a) {
   const int lane = threadIdx.x & 31;
   const bool col = lane * 4 < a.d;  // this lane's 16-byte column exists
@@ -637,9 +646,9 @@ __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(c
     int32_t bag_b = (32 + lane < n) ? sb[32 + lane] : -1;
     float sc_cur;
     uint32_t cur = bag_g4(a, (lane < n) ? sb[lane] : -1, sc_cur);
-    float4 buf[kWin];
+    float4 buf[kPieceWin];
 #pragma unroll
-    for (int u = 0; u < kWin; ++u) {
+    for (int u = 0; u < kPieceWin; ++u) {
       const uint32_t r = __shfl_sync(kFull, cur, u);
       buf[u] = (r != kNoG && col) ? ldg_f4_policy(Gl + (uint64_t)r * 4, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -648,12 +657,12 @@ __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(c
       const int32_t bag_c = (c0 + 64 + lane < n) ? sb[c0 + 64 + lane] : -1;
       float sc_nxt;
       const uint32_t nxt = bag_g4(a, bag_b, sc_nxt);
-      for (int g = 0; g < 32; g += kWin) {
+      for (int g = 0; g < 32; g += kPieceWin) {
 #pragma unroll
-        for (int j = 0; j < kWin; ++j) {
+        for (int j = 0; j < kPieceWin; ++j) {
           const int t = g + j;
           const float4 x = buf[j];
-          const int tn = t + kWin;
+          const int tn = t + kPieceWin;
           const uint32_t r = __shfl_sync(kFull, tn < 32 ? cur : nxt, tn & 31);
           buf[j] = (r != kNoG && col) ? ldg_f4_policy(Gl + (uint64_t)r * 4, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
           if (a.mean) acc = fma4(x, __shfl_sync(kFull, sc_cur, t), acc);

@@ -231,7 +231,10 @@ __global__ void __launch_bounds__(kBagThreads, CPL == 1 ? CTR_BAG_MINB : 1) bag_
 // drains the pipeline.  Per occurrence the warp spends one shuffle (the row),
 // one 16-byte load per lane and four adds.  Each bag is summed in the order of
 // its indices; at its last occurrence the warp stores the row.
-constexpr int kWinF = 8;
+#ifndef CTR_FLAT_WIN
+#define CTR_FLAT_WIN 8
+#endif
+constexpr int kWinF = CTR_FLAT_WIN;  // table-row loads in flight per lane in the flat gather
 // The TMA gather variant is off unless selected (ctr_set_tma_gather): measured
 // slower than the register window on GB300.
 std::atomic<int> g_tma_gather{0};
