@@ -375,10 +375,13 @@ int ctr_embedding_bag_bwd_update_opt(const float* grad_pooled, int64_t g_stride_
  * plugin inside a runtime that owns every device allocation, a server whose
  * memory budget is fixed at start-up, or a latency-critical loop where an
  * allocation could stall the device.  Same inputs and outputs as ctr_dedup,
- * but the scratch space is a fixed array inside the library (about 24 MB per
- * GPU that loads the library, held until exit) instead of a caller workspace.
- *   n_ids            at most 1048576 (2^20); larger calls return
- *                    CTR_ERR_UNSUPPORTED and launch nothing.
+ * but the scratch space is a fixed array inside the library (48 MB per GPU
+ * that loads the library, held until exit) instead of a caller workspace.
+ *   n_ids            at most 1048576 (2^20), for any total row count (the
+ *                    array covers the largest scratch ctr_dedup_workspace_size
+ *                    gives at 2^20 IDs, 46 MB at total rows = 64 x 2^20);
+ *                    larger calls return CTR_ERR_UNSUPPORTED and launch
+ *                    nothing.
  *   device_status    optional device int32: receives this call's device-side
  *                    error code (0, CTR_ERR_INDEX_OUT_OF_RANGE or
  *                    CTR_ERR_BAD_OFFSETS) once the call's work has run.
@@ -386,7 +389,9 @@ int ctr_embedding_bag_bwd_update_opt(const float* grad_pooled, int64_t g_stride_
  * error word is cleared at the start of every call.  Calls that overlap on
  * the GPU race on the array: order them (one stream, or explicit events).
  * The first call on a device looks up the array's address with that device
- * current and caches it; make that first call before any stream capture.
+ * current and caches it; make that first call before any stream capture, and
+ * do not call this entry point on a device again after cudaDeviceReset in the
+ * same process (the cached address belongs to the old context).
  * Nothing here calls cudaMalloc, cudaFree or any other allocator. */
 int ctr_dedup_static(const int64_t* ids, const int64_t* offsets, int32_t num_fields, int32_t batch,
                      const int32_t* bag_to_table, const int64_t* row_base, int32_t num_tables, int64_t n_ids,

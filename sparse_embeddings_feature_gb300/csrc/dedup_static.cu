@@ -10,9 +10,13 @@
 // outputs.
 //
 // Limits and sharing:
-//   * The array is sized for at most kStaticMaxIds IDs per call (about 24 MB,
-//     held on every GPU that loads the library until the process exits);
-//     larger calls return CTR_ERR_UNSUPPORTED and launch nothing.
+//   * The array holds the scratch of a call of up to kStaticMaxIds (2^20) IDs
+//     whatever the tables' total row count: 48 MB, held on every GPU that
+//     loads the library until the process exits.  The dedup's scratch depends
+//     on the IDs and the row count; it peaks where the presence-bitmap path
+//     meets its largest bitmap (total rows = 64 x IDs: 46 MB at 2^20 IDs), and
+//     the sorted-key path needs 22 MB.  Larger calls return
+//     CTR_ERR_UNSUPPORTED and launch nothing.
 //   * Every call uses the same array, and the array keeps the previous call's
 //     contents.  The error word at its head is cleared at the start of each
 //     call; the sort's scratch is fully rewritten before it is read.  Two calls
@@ -20,7 +24,9 @@
 //     without ordering) race on the array and must not be issued.
 //   * The first call on each device looks up the array's device address
 //     (cudaGetSymbolAddress, with that device current) and caches it; make that
-//     first call before any stream capture begins.
+//     first call before any stream capture begins.  The cached address belongs
+//     to the device's current context: do not call this entry point again on a
+//     device after cudaDeviceReset in the same process.
 #include <mutex>
 
 #include "common.cuh"
@@ -29,7 +35,7 @@ namespace ctr {
 namespace {
 
 constexpr int64_t kStaticMaxIds = 1 << 20;
-constexpr size_t kStaticScratchBytes = (size_t)24 << 20;
+constexpr size_t kStaticScratchBytes = (size_t)48 << 20;
 
 static __device__ __align__(256) unsigned char g_dedup_scratch[kStaticScratchBytes];
 

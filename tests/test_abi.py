@@ -108,3 +108,21 @@ def test_product_code_never_imports_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert not pat.search(text), f
+
+
+def test_static_dedup_array_covers_every_row_count_at_its_id_limit(lib):
+    # the allocation-free dedup keeps its scratch in a 48 MB array and accepts up to
+    # 2^20 IDs: the dedup's workspace at 2^20 IDs must fit for any total row count
+    # (it peaks on the presence-bitmap path at total rows = 64 x IDs)
+    from sparse_embeddings_feature_gb300 import ctr
+    n = 1 << 20
+    static_bytes = 48 << 20
+    counts = {1, 2, 1000, 64 * n - 1, 64 * n, 64 * n + 1, 1 << 32}
+    counts |= {int(x) for x in __import__("numpy").geomspace(2, 1 << 32, 2000)}
+    sizes = {t: ctr.ctr_dedup_workspace_size(n, 26, 131072, t) for t in counts}
+    worst = max(sizes, key=sizes.get)
+    assert sizes[worst] <= static_bytes, (worst, sizes[worst])
+    assert worst == 64 * n
+    st = lib.ctr_dedup_static(C.c_void_p(256), C.c_void_p(256), 1, 1, (C.c_int32 * 1)(0), (C.c_int64 * 2)(0, 10), 1,
+                              C.c_int64(n + 1), None, None, None, None, None, None, None, None, None)
+    assert st == -2                                     # beyond 2^20 IDs: refused before any CUDA call

@@ -8,11 +8,15 @@ gather -> interaction -> interaction backward -> SGD row update).
   distinct keys, unique_rows[inverse] = key, the bags in the order of a stable
   host sort of the keys, run bounds, per-table offsets), all vectorised over
   the 86.9M IDs;
-* pooled rows, interaction outputs and interaction gradients: on sampled bags
-  and samples, recomputed by the oracle from the generator's table values;
-* row updates: on sampled rows the batch touches only a few times, whose
-  gradient the oracle can rebuild from the few samples that contain them; and
-  on sampled rows the batch does not touch (unchanged bits).
+* pooled rows: on sampled samples, recomputed by the oracle from the
+  generator's table values;
+* interaction outputs and gradients: the oracle applied to the GPU's own
+  interaction input (checked just before), so each step is checked on its
+  real input with the bound of its own reduction depth;
+* row updates: on the 20 hottest rows (the Zipf head) and 2000 random unique
+  rows, with the oracle summing the GPU's own pooled gradient over every
+  occurrence of the batch; and on sampled rows the batch does not touch
+  (unchanged bits).
 """
 import numpy as np
 import pytest
@@ -22,7 +26,7 @@ from oracle import oracle as O
 from sparse_embeddings_feature_gb300 import workload as W
 from sparse_embeddings_feature_gb300.pipeline import CtrPath
 
-from _tol import f32_close
+from _tol import bwd_depth, f32_close
 
 pytestmark = pytest.mark.gpu
 
@@ -73,14 +77,16 @@ def test_full_size_dedup_properties(full_step):
     np.testing.assert_array_equal(uo, np.searchsorted(uq, cfg.row_base, side="left"))
 
 
-def _oracle_X(cfg, w, samples):
-    """Oracle interaction input [len(samples), 27, 128] for the listed samples."""
+def _oracle_pooled(cfg, w, samples):
+    """Oracle pooled rows [len(samples), F, d], their magnitude sums and bag lengths."""
     F, B, d = cfg.num_fields, cfg.batch, cfg.d
     gen = (cfg.fill_kind, cfg.fill_seed, cfg.fill_scale)
     bags = (np.arange(F)[None, :] * B + np.asarray(samples)[:, None]).ravel()
-    pooled = O.embedding_bag_fwd(w["ids"], w["offsets"], F, B, w["bag_to_table"], w["row_base"], d, gen=gen,
-                                 bag_list=bags)
-    return np.concatenate([w["dense"][samples][:, None, :], pooled.reshape(len(samples), F, d)], axis=1)
+    pooled, mag = O.embedding_bag_fwd(w["ids"], w["offsets"], F, B, w["bag_to_table"], w["row_base"], d, gen=gen,
+                                      bag_list=bags, with_mag=True)
+    lens = np.diff(w["offsets"])[bags]
+    shape = (len(samples), F, d)
+    return pooled.reshape(shape), mag.reshape(shape), lens.reshape(len(samples), F, 1)
 
 
 def test_full_size_forward_interaction_and_backward_on_samples(full_step):
@@ -89,41 +95,46 @@ def test_full_size_forward_interaction_and_backward_on_samples(full_step):
     rng = np.random.default_rng(77)
     samples = np.sort(rng.choice(B, size=300, replace=False))
     samples[-1] = B - 1                                              # include the ragged end
-    X = _oracle_X(cfg, w, samples)
+    pooled, pmag, lens = _oracle_pooled(cfg, w, samples)
     sel = torch.from_numpy(samples).cuda()
-    f32_close(_np(path.X[sel]), X, None, 0, atol=2e-6, what="pooled rows")
-    out_ref, out_mag = O.dot_interaction(X, n, d, with_mag=True)
-    f32_close(_np(path.out[sel]), out_ref, out_mag, d + 64, what="interaction")
-    dX_ref, dX_mag = O.dot_interaction_bwd(w["dout"][samples], X, n, d, with_mag=True)
-    f32_close(_np(path.dX[sel]), dX_ref, dX_mag, n + 64, what="interaction bwd")
+    Xg = _np(path.X[sel])
+    np.testing.assert_array_equal(Xg[:, 0, :], w["dense"][samples])  # slot 0: the dense vector, copied
+    # a bag of L rows is a sum of L terms: depth L in any summation order
+    f32_close(Xg[:, 1:, :], pooled, pmag, lens, what="pooled rows")
+    # each later step is checked on its real input, the GPU's own X (checked just above)
+    out_ref, out_mag = O.dot_interaction(Xg, n, d, with_mag=True)
+    np.testing.assert_array_equal(_np(path.out[sel])[:, :d], w["dense"][samples])
+    f32_close(_np(path.out[sel]), out_ref, out_mag, d, what="interaction")  # a d-term dot product
+    dX_ref, dX_mag = O.dot_interaction_bwd(w["dout"][samples], Xg, n, d, with_mag=True)
+    # dx_i: n - 1 products, plus the pass-through gradient added to the dense slot
+    f32_close(_np(path.dX[sel]), dX_ref, dX_mag, n, what="interaction bwd")
 
 
-def test_full_size_row_updates_on_sampled_rows(full_step):
+def test_full_size_row_updates_on_hot_and_sampled_rows(full_step):
+    """The row update at the real skew: the 20 longest runs (the Zipf head, about
+    0.29 M occurrences each, summed by the long-run pieces and the combine) and
+    2000 random unique rows, from the GPU's own pooled gradient dX[:, 1:, :]
+    (the interaction backward is checked on its own above)."""
     cfg, w, path = full_step
     F, B, d, n = cfg.num_fields, cfg.batch, cfg.d, cfg.n_vectors
     nu = int(path.n_unique.item())
     ro = _np(path.run_offsets[:nu + 1]).astype(np.int64)
     run_len = np.diff(ro)
     rng = np.random.default_rng(5)
-    cold = np.nonzero(run_len <= 3)[0]
-    picks = np.sort(rng.choice(cold, size=40, replace=False))
+    hot = np.argsort(run_len, kind="stable")[-20:]
+    picks = np.unique(np.concatenate([hot, rng.choice(nu, size=2000, replace=False)]))
+    assert run_len[hot].min() > 100_000                              # the long-run path, many pieces
     uq = _np(path.unique_rows[:nu])
     rows = uq[picks]
-    sbag = _np(path.sorted_bag)
-    # the samples whose bags hold the picked rows (the dedup is checked above)
-    occ_bags = np.concatenate([sbag[ro[u]:ro[u + 1]] for u in picks]).astype(np.int64)
-    samples = np.unique(occ_bags % B)
-    X = _oracle_X(cfg, w, samples)
-    dX = O.dot_interaction_bwd(w["dout"][samples], X, n, d)
-    # gradient of the pooled outputs, scattered back to a [B, F, d] view over the needed samples only
-    G = np.zeros((B, F, d), dtype=np.float32)
-    G[samples] = dX[:, 1:, :]
+    G = _np(path.dX[:, 1:, :])                                       # [B, F, d], as the update reads it
     gen = (cfg.fill_kind, cfg.fill_seed, cfg.fill_scale)
     new_ref, _, mag = O.embedding_bag_bwd_update(G, w["ids"], w["offsets"], F, B, w["bag_to_table"], w["row_base"],
                                                  d, cfg.lr, rows, gen=gen)
+    del G
     got = _np(path.table[torch.from_numpy(rows).cuda()])
     old = O.table_rows(gen[0], gen[1], gen[2], d, rows)
-    f32_close(got, new_ref, cfg.lr * mag + np.abs(old), 200, what="updated cold rows")
+    depth = bwd_depth(run_len[picks])[:, None] + 2                   # + the product lr * g and the subtraction
+    f32_close(got, new_ref, cfg.lr * mag + np.abs(old), depth, what="updated rows (hot and sampled)")
     # rows no bag touches keep their bits
     probe = rng.integers(0, cfg.total_rows, size=4000)
     probe = np.setdiff1d(probe, uq)
