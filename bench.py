@@ -6,7 +6,10 @@ uniform 1..50, Zipf(1.05) IDs): dedup -> pooled gather into the interaction
 input -> dot interaction -> interaction backward -> per-unique-row gradient
 reduce + SGD row update.  Inputs are resident in HBM when the timed region
 starts; the tables (106.5 GB) and the ID array (0.7 GB) are far larger than
-L2, so no flush is needed between steps.
+L2, so no flush is needed between steps.  Consecutive steps take different
+batches (--batches of them, drawn from the workload's distribution with new
+IDs, dense vectors and gradients, rotated), so no step finds the previous
+step's batch in L2 or in the dedup's state.
 
 Prints one JSON line (rank 0).  With --impl reference the CPU oracle runs the
 same path on a bounded sample of the batch instead.
@@ -54,6 +57,13 @@ def parse():
                     help="samples of the batch the oracle runs for cpu_baseline (about 10 s of CPU work)")
     ap.add_argument("--ref-sample", type=int, default=2048,
                     help="samples of the batch per step of the reference arm (the oracle)")
+    ap.add_argument("--batches", type=int, default=4,
+                    help="distinct batches rotated over the steps (same bag lengths, new IDs, dense vectors and "
+                         "gradients)")
+    ap.add_argument("--uniform-ids", action="store_true",
+                    help="draw IDs uniformly over each table instead of the workload's Zipf: with full-size tables "
+                         "no row repeats (the gather's random-row rate from HBM); with --rows small enough for "
+                         "the tables to sit in L2, its random-row rate from L2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -79,6 +89,10 @@ def workload_cfg(args):
         kw["table_init"] = ("normal4", cfg.table_init[1]) if args.dtype == "bf16" else ("uniform", cfg.table_init[1])
     if getattr(args, "interaction_mode", ""):
         kw["interaction_mode"] = args.interaction_mode
+    if getattr(args, "uniform_ids", False):
+        if cfg.ids[0] != "zipf":
+            raise SystemExit("--uniform-ids applies to the workloads with per-table Zipf IDs")
+        kw["ids"] = ("uniform",)
     return cfg.shrink(**kw) if kw else cfg
 
 
@@ -231,6 +245,8 @@ def algorithmic_bytes(cfg, path, n_ids, n_unique):
     idx_bytes = 4 if cfg.dedup_gather else 8          # int32 inverse into U, or int64 IDs
     out = {"gather": n_unique * row + n_ids * idx_bytes + (nbags + 1) * 8 + nbags * row
            + (nbags * 4 if path.fm is not None else 0)}
+    # every lookup reading its whole row (the bytes through L2 when no row is reused in L1)
+    out["gather_logical"] = out["gather"] - n_unique * row + n_ids * row
     if cfg.backward != "none" or cfg.dedup_gather:
         # radix passes of 8 bits over the sort keys: ranks of the distinct rows when
         # the tables are at most 64x the batch (presence bitmap), else the rows
@@ -304,14 +320,17 @@ def run_ours(args, rank, world):
     import torch
     from sparse_embeddings_feature_gb300 import ctr
     from sparse_embeddings_feature_gb300 import workload as W
-    from sparse_embeddings_feature_gb300.pipeline import CtrPath
+    from sparse_embeddings_feature_gb300.pipeline import CtrPath, DeviceBatches
 
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     cfg = workload_cfg(args)
-    w = W.make_workload(cfg)
+    nb = max(1, args.batches)
+    ws_host = [W.make_workload(cfg, batch_index=j) for j in range(nb)]
+    w = ws_host[0]
     n_ids = int(w["ids"].size)
     path = CtrPath(cfg, n_ids, fm=args.fm, optimizer=args.optimizer, stochastic_rounding=args.stochastic_rounding)
     path.upload(w)
+    batches = DeviceBatches(path, ws_host)
     torch.cuda.synchronize()
     path.reset_status()
     stream = torch.cuda.current_stream()
@@ -320,23 +339,34 @@ def run_ours(args, rank, world):
         if world > 1:
             torch.distributed.barrier()
 
-    for _ in range(args.warmup):
+    for i in range(args.warmup):
+        batches.bind(i)
         path.step()
     torch.cuda.synchronize()
     status = path.check_status()
     if any(v != 0 for v in status.values()):
         raise RuntimeError(f"device error during warm-up: {status}")
-    n_unique = int(path.n_unique.item())
 
+    # distinct rows and compulsory bytes of each batch (outside the timed region), averaged
     has_dedup = cfg.backward != "none" or cfg.dedup_gather
-    if not has_dedup:
-        # distinct rows of the batch, for the gather's compulsory bytes (outside the timed region)
-        lens = torch.from_numpy(np.diff(w["offsets"])).cuda()
-        bag_table = torch.from_numpy(np.asarray(cfg.field_to_table, dtype=np.int64)).cuda().repeat_interleave(cfg.batch)
-        base = torch.from_numpy(np.asarray(cfg.row_base, dtype=np.int64)).cuda()[bag_table]
-        keys = base.repeat_interleave(lens) + path.ids[:n_ids]
-        n_unique = int(torch.unique(keys).numel())
-        del lens, bag_table, base, keys
+    uniques, algos = [], []
+    for j in range(nb):
+        batches.bind(j)
+        if has_dedup:
+            path.dedup()
+            uniques.append(int(path.n_unique.item()))
+            algos.append(algorithmic_bytes(cfg, path, n_ids, uniques[-1]))
+        else:
+            lens = torch.from_numpy(np.diff(w["offsets"])).cuda()
+            bag_table = torch.from_numpy(np.asarray(cfg.field_to_table, dtype=np.int64)).cuda().repeat_interleave(
+                cfg.batch)
+            base = torch.from_numpy(np.asarray(cfg.row_base, dtype=np.int64)).cuda()[bag_table]
+            keys = base.repeat_interleave(lens) + path.ids[:n_ids]
+            uniques.append(int(torch.unique(keys).numel()))
+            algos.append(algorithmic_bytes(cfg, path, n_ids, uniques[-1]))
+            del lens, bag_table, base, keys
+    n_unique = int(round(sum(uniques) / len(uniques)))
+    algo = {k: sum(a[k] for a in algos) / len(algos) for k in algos[0]}
     kernels = {"gather": ctr.KERNEL_GATHER}
     if has_dedup:
         kernels["sort"] = ctr.KERNEL_SORT
@@ -366,6 +396,7 @@ def run_ours(args, rank, world):
         for k in range(args.steps):
             for name, kid in kernels.items():
                 ctr.ctr_set_timing_events(kid, *kev[k][name])
+            batches.bind(k)
             graphs.append(path.capture())
         for kid in kernels.values():
             ctr.ctr_set_timing_events(kid, None, None)
@@ -387,6 +418,7 @@ def run_ours(args, rank, world):
             else:
                 for name, kid in kernels.items():
                     ctr.ctr_set_timing_events(kid, *kev[k][name])
+                batches.bind(k)
                 path.step()
         t_end.record(stream)
         launches = ctr.ctr_launch_count() - launches0
@@ -417,22 +449,25 @@ def run_ours(args, rank, world):
     # neighbouring steps' kernels
     e2e = None
     if not args.no_e2e:
-        host = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in w.items()
-                if k in ("ids", "offsets", "dense", "dout", "grad_pooled")}
-        if cfg.dtype == "bf16":
-            host["dense"] = host["dense"].view(torch.int16).view(torch.bfloat16)
+        hosts = []
+        for wj in ws_host:
+            host = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in wj.items()
+                    if k in ("ids", "offsets", "dense", "dout", "grad_pooled")}
+            if cfg.dtype == "bf16":
+                host["dense"] = host["dense"].view(torch.int16).view(torch.bfloat16)
+            hosts.append(host)
         from sparse_embeddings_feature_gb300.pipeline import HostPipeline
         pipe = HostPipeline(path, graphs=use_graph)
         result = path.out if path.out is not None else path.pooled
         outs = [torch.empty(result.shape, dtype=result.dtype).pin_memory() for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = outs[0].numel() * outs[0].element_size()
-        pipe.run([host] * 2, outs)
+        pipe.run(hosts[:2], outs)
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         barrier()
-        pipe.run([host] * args.steps, [outs[k & 1] for k in range(args.steps)], start_event=a)
+        pipe.run([hosts[k % nb] for k in range(args.steps)], [outs[k & 1] for k in range(args.steps)], start_event=a)
         b.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -442,12 +477,13 @@ def run_ours(args, rank, world):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     hbm, peak_kind = peaks()
-    algo = algorithmic_bytes(cfg, path, n_ids, n_unique)
     kern = {}
     for name, ms_k in kernel_ms.items():
         if name in algo:
             gbs = algo[name] / (ms_k / 1e3) / 1e9
             kern[name] = {"ms": ms_k, "algorithmic_bytes": algo[name], "achieved_GBs": gbs, "frac": gbs / hbm}
+            if name + "_logical" in algo:
+                kern[name]["logical_GBs"] = algo[name + "_logical"] / (ms_k / 1e3) / 1e9
     dominant = max(kern, key=lambda k: kern[k]["ms"])
     traffic = profile_traffic(dominant, args)
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": kern[dominant]["achieved_GBs"], "peak": hbm,
@@ -464,6 +500,8 @@ def run_ours(args, rank, world):
                    "rows_per_table": cfg.rows_per_table[0], "d": cfg.d, "bag_len": list(cfg.bag_len),
                    "ids": list(cfg.ids), "n_ids": n_ids, "n_unique": n_unique, "parallelism": f"replicas{world}",
                    "launch": "cuda_graph" if use_graph else "eager",
+                   "batches": f"{nb} distinct batches rotated over the steps (same bag lengths; new IDs, dense "
+                              f"vectors and gradients)",
                    "l2": "inputs larger than L2 (tables %.1f GB, ids %.2f GB)" % (
                        cfg.total_rows * cfg.d * 4 / 1e9, n_ids * 8 / 1e9)},
         "interaction_samples_per_s": cfg.batch * world / (ms / 1e3),

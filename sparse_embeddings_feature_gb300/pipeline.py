@@ -84,6 +84,8 @@ class CtrPath:
         self.b2t = np.asarray(cfg.field_to_table, dtype=np.int32)
         self.row_base = cfg.row_base
         self._side = None          # side stream of the overlapped dedup and long runs (created on first use)
+        # when set (DeviceBatches), every step first copies these dense vectors into slot 0 of X
+        self.dense_src = None
         # the long-run and short-run phases of the backward are persistent grids that each
         # fill the GPU, so overlapping them was measured slower: off by default
         self.overlap_backward = False
@@ -214,6 +216,8 @@ class CtrPath:
         cfg = self.cfg
         needs_dedup = cfg.backward != "none" or cfg.dedup_gather
         overlap = needs_dedup and not cfg.dedup_gather and cfg.backward != "none"
+        if self.dense_src is not None:
+            self.X[:, 0, :].copy_(self.dense_src, non_blocking=True)
         if overlap:
             main = torch.cuda.current_stream(self.dev)
             side = self._side_stream()
@@ -261,6 +265,45 @@ class StepGraph:
         self.graph.replay()
 
 
+class DeviceBatches:
+    """Several batches of one workload held on the device at once, each in its own input
+    buffers (IDs, offsets, upstream gradient, dense vectors).  `bind(k)` points the path
+    at batch k mod the count; the path's steps then read that batch, starting with a copy
+    of its dense vectors into slot 0 of X (inside a captured step too).  The batches must
+    share the ID count (a captured step fixes it)."""
+
+    def __init__(self, path: CtrPath, batches):
+        self.path = path
+        cfg = path.cfg
+        self.names = ["ids", "offsets"] + [k for k in ("dout", "grad_pooled") if getattr(path, k) is not None]
+        self.sets = []
+        for j, w in enumerate(batches):
+            if w["ids"].size != path.n_ids:
+                raise ValueError(f"batch {j} has {w['ids'].size} IDs; the path holds {path.n_ids}")
+            bufs = {k: (getattr(path, k) if j == 0 else torch.empty_like(getattr(path, k))) for k in self.names}
+            n = w["ids"].size
+            if n:
+                bufs["ids"][:n].copy_(torch.from_numpy(w["ids"]))
+            bufs["offsets"].copy_(torch.from_numpy(w["offsets"]))
+            for k in ("dout", "grad_pooled"):
+                if k in bufs:
+                    bufs[k].copy_(torch.from_numpy(w[k]))
+            dense = w["dense"]
+            dt = torch.from_numpy(dense.view(np.int16)).view(torch.bfloat16) if cfg.dtype == "bf16" \
+                else torch.from_numpy(dense)
+            bufs["dense"] = dt.to(path.dev)
+            self.sets.append(bufs)
+
+    def __len__(self):
+        return len(self.sets)
+
+    def bind(self, k: int) -> None:
+        bufs = self.sets[k % len(self.sets)]
+        for name in self.names:
+            setattr(self.path, name, bufs[name])
+        self.path.dense_src = bufs["dense"]
+
+
 class HostPipeline:
     """Runs CtrPath steps over batches held in pinned host memory, with the copies overlapped.
 
@@ -286,6 +329,7 @@ class HostPipeline:
         self.path = path
         self.depth = D = int(depth)
         cfg = path.cfg
+        path.dense_src = None  # the pipeline copies each batch's dense vectors itself
         self.result_name = "out" if path.out is not None else "pooled"
         names = ["ids", "offsets"] + [k for k in ("dout", "grad_pooled") if getattr(path, k) is not None]
         self.sets = []

@@ -232,8 +232,16 @@ def bag_lengths(cfg: Config) -> np.ndarray:
     raise ValueError(kind)
 
 
-def draw_ids(cfg: Config, lengths: np.ndarray) -> np.ndarray:
-    """Table-local row IDs for every bag occurrence, field-major CSR order."""
+def _batch_stream(batch_index: int, *stream: int):
+    """Stream key of one array of batch `batch_index` (batch 0 keeps the original keys)."""
+    return (*stream, batch_index) if batch_index else stream
+
+
+def draw_ids(cfg: Config, lengths: np.ndarray, batch_index: int = 0) -> np.ndarray:
+    """Table-local row IDs for every bag occurrence, field-major CSR order.
+
+    Batches with another `batch_index` draw new IDs from the same distribution
+    (the same hot rows: the rank -> row map is a property of the table)."""
     B = cfg.batch
     per_field = lengths.reshape(cfg.num_fields, B).sum(axis=1)
     ids = np.empty(int(per_field.sum()), dtype=np.int64)
@@ -245,7 +253,7 @@ def draw_ids(cfg: Config, lengths: np.ndarray) -> np.ndarray:
         t = cfg.field_to_table[f]
         nrows = cfg.rows_per_table[t]
         m = int(per_field[f])
-        rng = _rng(cfg.seed, 2, f)
+        rng = _rng(cfg.seed, *_batch_stream(batch_index, 2, f))
         if kind == "uniform":
             v = rng.integers(0, nrows, size=m, dtype=np.int64)
         elif kind == "zipf":
@@ -263,22 +271,26 @@ def draw_ids(cfg: Config, lengths: np.ndarray) -> np.ndarray:
     return ids
 
 
-def make_workload(cfg: Config, with_grads: bool = True) -> Dict[str, np.ndarray]:
-    """All host-side inputs of one step for `cfg` (tables excluded)."""
+def make_workload(cfg: Config, with_grads: bool = True, batch_index: int = 0) -> Dict[str, np.ndarray]:
+    """All host-side inputs of one step for `cfg` (tables excluded).
+
+    `batch_index` > 0 gives another batch of the same workload: new IDs, dense
+    vectors and upstream gradients, with the same bag lengths (so every batch
+    has the same ID count, which a captured step fixes)."""
     lengths = bag_lengths(cfg)
     offsets = np.zeros(lengths.size + 1, dtype=np.int64)
     np.cumsum(lengths, out=offsets[1:])
     w = {
         "offsets": offsets,
-        "ids": draw_ids(cfg, lengths),
+        "ids": draw_ids(cfg, lengths, batch_index),
         "bag_to_table": np.asarray(cfg.field_to_table, dtype=np.int32),
         "row_base": cfg.row_base,
     }
-    drng = _rng(cfg.seed, 3)
+    drng = _rng(cfg.seed, *_batch_stream(batch_index, 3))
     dense = drng.standard_normal((cfg.batch, cfg.d)).astype(np.float32)
     w["dense"] = f32_to_bf16_bits(dense) if cfg.dtype == "bf16" else dense
     if with_grads:
-        grng = _rng(cfg.seed, 4)
+        grng = _rng(cfg.seed, *_batch_stream(batch_index, 4))
         if cfg.backward == "pooled_grad":
             w["grad_pooled"] = grng.standard_normal((cfg.batch, cfg.num_fields, cfg.d)).astype(np.float32)
         elif cfg.backward == "full":
