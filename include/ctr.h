@@ -112,6 +112,17 @@ uint64_t ctr_launch_count(void);
  * Process-wide; returns the previous setting. */
 int ctr_set_tma_gather(int on);
 
+/* Short-run pass of the row update for fp32 rows of d = 128 under plain SGD
+ * (no optimizer state, no stochastic rounding): mode 2 processes the short
+ * runs in two 64-column slices, two occurrences per warp step, so the pooled-
+ * gradient rows of one table take half the L2 space; mode 1 never slices; 0
+ * (the default) slices when one table's pooled-gradient rows (batch x 512
+ * bytes) exceed 32 MB.  Every mode gives a deterministic result within the
+ * same summation bound (each run's sum order is fixed; the sliced pass adds
+ * the run's even and odd positions separately, then the two partials).
+ * Process-wide; returns the previous mode (a mode outside 0..2 selects 0). */
+int ctr_set_tile_slices(int mode);
+
 /* ------------------------------------------------------------------------ */
 /* Input generation (not part of the method)                                 */
 /* ------------------------------------------------------------------------ */

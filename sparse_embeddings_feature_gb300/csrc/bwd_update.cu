@@ -30,6 +30,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "common.cuh"
@@ -59,7 +60,9 @@ struct BwdArgs {
   float lr;
   void* table;
   int bf16;
-  int32_t d;
+  int32_t d;           // columns this launch processes
+  int32_t ld;          // row stride (elements) of the table, the states and grad_out: d, or more when
+                       // the short runs are processed in column slices
   int64_t total_rows;
   float* grad_out;
   int* err;
@@ -201,7 +204,7 @@ __device__ __forceinline__ void store_bf16_sr_inl(const BwdArgs& a, int64_t row,
   uint2 out;
   out.x = bf16_sr(x0, (uint32_t)h & 0xffffu) | (bf16_sr(x1, (uint32_t)(h >> 16) & 0xffffu) << 16);
   out.y = bf16_sr(x2, (uint32_t)(h >> 32) & 0xffffu) | (bf16_sr(x3, (uint32_t)(h >> 48) & 0xffffu) << 16);
-  *(uint2*)((__nv_bfloat16*)a.table + row * a.d + ch * 4) = out;
+  *(uint2*)((__nv_bfloat16*)a.table + row * a.ld + ch * 4) = out;
 }
 __device__ __noinline__ void store_bf16_sr(const BwdArgs& a, int64_t row, int ch, float x0, float x1, float x2,
                                            float x3) {
@@ -218,20 +221,20 @@ template <int OPT, bool SR = false>
 __device__ __forceinline__ void store_row_chunk_s(const BwdArgs& a, int64_t row, int64_t u, int ch, float4 g,
                                                   float4 w, uint2 wb, uint64_t pol, float row_inv, float4 st,
                                                   float4 sv, float* xdefer = nullptr) {
-  if (a.grad_out) *(float4*)(a.grad_out + u * a.d + ch * 4) = g;
+  if (a.grad_out) *(float4*)(a.grad_out + u * a.ld + ch * 4) = g;
   // SGD keeps its single fused multiply-add per value
   float4 step = g;
   float k = -a.lr;
   if constexpr (OPT != CTR_OPT_SGD) {
     step = opt_step<OPT>(a, g, st, sv, row_inv);
     k = -1.f;
-    const int64_t e = row * a.d + ch * 4;
+    const int64_t e = row * a.ld + ch * 4;
     if constexpr (kElemStates<OPT> >= 1) *(float4*)(a.s0 + e) = st;
     if constexpr (kElemStates<OPT> >= 2) *(float4*)(a.s1 + e) = sv;
   }
   if (!a.bf16) {
     float4 x = make_float4(fmaf(k, step.x, w.x), fmaf(k, step.y, w.y), fmaf(k, step.z, w.z), fmaf(k, step.w, w.w));
-    float* dst = (float*)a.table + row * a.d + ch * 4;
+    float* dst = (float*)a.table + row * a.ld + ch * 4;
     if (pol) stg_f4_policy(dst, x, pol);
     else *(float4*)dst = x;
   } else {
@@ -246,7 +249,7 @@ __device__ __forceinline__ void store_row_chunk_s(const BwdArgs& a, int64_t row,
     } else {
       __nv_bfloat162 p0 = __floats2bfloat162_rn(x0, x1);
       __nv_bfloat162 p1 = __floats2bfloat162_rn(x2, x3);
-      *(uint2*)((__nv_bfloat16*)a.table + row * a.d + ch * 4) = make_uint2(*(uint32_t*)&p0, *(uint32_t*)&p1);
+      *(uint2*)((__nv_bfloat16*)a.table + row * a.ld + ch * 4) = make_uint2(*(uint32_t*)&p0, *(uint32_t*)&p1);
     }
   }
 }
@@ -266,7 +269,7 @@ template <int OPT>
 __device__ __forceinline__ void store_row_chunk_t(const BwdArgs& a, int64_t row, int64_t u, int ch, float4 g,
                                                   float4 w, uint2 wb, uint64_t pol, float row_inv) {
   float4 st = make_float4(0.f, 0.f, 0.f, 0.f), sv = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int64_t e = row * a.d + ch * 4;
+  const int64_t e = row * a.ld + ch * 4;
   if constexpr (kElemStates<OPT> >= 1) st = *(const float4*)(a.s0 + e);
   if constexpr (kElemStates<OPT> >= 2) sv = *(const float4*)(a.s1 + e);
   store_row_chunk_s<OPT, true>(a, row, u, ch, g, w, wb, pol, row_inv, st, sv);
@@ -287,8 +290,8 @@ __device__ __forceinline__ void store_row_chunk(const BwdArgs& a, int64_t row, i
 }
 
 __device__ __forceinline__ void load_row_chunk(const BwdArgs& a, int64_t row, int ch, float4& w, uint2& wb) {
-  if (!a.bf16) w = *(const float4*)((const float*)a.table + row * a.d + ch * 4);
-  else wb = *(const uint2*)((const __nv_bfloat16*)a.table + row * a.d + ch * 4);
+  if (!a.bf16) w = *(const float4*)((const float*)a.table + row * a.ld + ch * 4);
+  else wb = *(const uint2*)((const __nv_bfloat16*)a.table + row * a.ld + ch * 4);
 }
 
 // Walk occurrences [s0, s1) of one run, kU rows in flight, summing in order.
@@ -729,6 +732,168 @@ constexpr size_t tile_warp_bytes(int TU, int d, int esz, int ns, int xs) {
 }
 constexpr int kSrDeferBytes = 4096;  // stochastic rounding: new values held per warp (caps TU)
 
+// Short runs of fp32 rows under SGD, one column slice of every row per launch
+// (the host runs one launch per slice).  Why slices: the tile kernel keeps the
+// pooled-gradient rows of the table it is working on in L2 (they are re-read
+// by every unique of their bags); at the full step's batch one table's
+// gradient rows take 67 MB, more than the L2 holds next to the streamed table
+// rows, and ncu counted 3.7 GB of re-fetched gradient rows per step.  A slice
+// of half the columns halves that footprint.
+//
+// Each half-warp (16 lanes x 16 bytes = 64 columns) takes every other
+// occurrence of the tile's flattened run list: a warp step consumes a pair of
+// occurrences, so a slice costs no more instructions per byte than the whole
+// row does in the plain kernel.  When a run closes, the two halves' partial
+// sums are added (shuffle across the halves) and half 0 updates the row's
+// slice, staged in shared memory by cp.async when the tile started.  Each run
+// is summed in a fixed order (its even and odd positions in the flattened
+// list separately, then the two partials), so the results are deterministic.
+#ifndef CTR_PAIR_WIN
+#define CTR_PAIR_WIN 4
+#endif
+#ifndef CTR_PAIR_TU
+#define CTR_PAIR_TU 32
+#endif
+constexpr int kPairWin = CTR_PAIR_WIN;  // occurrence pairs in flight per warp
+constexpr int kPairTU = CTR_PAIR_TU;    // uniques per tile
+#ifndef CTR_TILE_PAIR_MINB
+#define CTR_TILE_PAIR_MINB 3
+#endif
+template <bool MEAN>
+__global__ void __launch_bounds__(kTileThreads, CTR_TILE_PAIR_MINB) bwd_tiles_pair_kernel(const BwdArgs a) {
+  extern __shared__ __align__(16) unsigned char wsm_raw[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int h = lane >> 4, sub = lane & 15;
+  const bool col = sub * 4 < a.d;  // a.d <= 64 columns in this slice
+  const int TU = a.TU;
+  const int row_bytes = a.d * 4;
+  unsigned char* wsm = wsm_raw + (size_t)warp * TU * row_bytes;
+  const uint32_t wsm_s = (uint32_t)__cvta_generic_to_shared(wsm);
+  const float* Gl = a.G + sub * 4;
+  const uint64_t pol_keep = g_policy(), pol_stream = row_policy();
+  const int64_t nu = n_uniques(a);
+  const int64_t ntiles = ceil_div(nu, TU);
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t tile = next_unit(a.work); tile < ntiles; tile = next_unit(a.work)) {
+    const int64_t u = tile * TU + lane;
+    const bool valid = lane < TU && u < nu;
+    int64_t r0 = 0, r1 = 0;
+    if (valid) run_bounds(a, u, r0, r1);
+    const int64_t len = r1 - r0;
+    const bool is_long = valid && len > kShort;
+    const bool is_short = valid && !is_long && len > 0;
+    int64_t row = -1;
+    if (is_short) {
+      row = a.unique_rows[u];
+      if (row < 0 || row >= a.total_rows) {
+        set_error(a.err, CTR_ERR_INDEX_OUT_OF_RANGE);
+        row = -1;
+      }
+    }
+    // stage the slices of the tile's rows: half h copies rows h, h + 2, ...
+    for (int j0 = 0; j0 < TU; j0 += 2) {
+      const int j = j0 + h;
+      const int64_t rj = __shfl_sync(kFull, row, j & 31);
+      if (j < TU && rj >= 0 && col)
+        cp_async_chunk(wsm_s + j * row_bytes + sub * 16, (const float*)a.table + rj * a.ld + sub * 4, 16,
+                       pol_stream);
+    }
+    cp_async_commit();
+    const int slen = is_short ? (int)len : 0;
+    int inc = slen;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const int e = inc - slen;
+    const int E = __shfl_sync(kFull, inc, 31);
+    const int r0i = (int)r0;
+
+    TileChunk cur = tile_chunk(a, lane, E, e, r0i, slen);
+    TileChunk pend = tile_chunk(a, 32 + lane, E, e, r0i, slen);
+    float sc_cur;
+    uint32_t gcur = bag_g4(a, cur.bag, sc_cur);
+    float4 buf[kPairWin];
+#pragma unroll
+    for (int q = 0; q < kPairWin; ++q) {
+      const uint32_t r = __shfl_sync(kFull, gcur, 2 * q + h);
+      buf[q] = (r != kNoG && col) ? ldg_f4_policy(Gl + (uint64_t)r * 4, pol_keep) : zero;
+    }
+    float4 acc = zero;
+    bool staged = false;
+    // close run `sg` with this half's partial `part`: the halves' partials are
+    // added, half 0 updates the slice of the row
+    auto finish = [&](int sg, float4 part) {
+      float4 tot;
+      tot.x = part.x + __shfl_xor_sync(kFull, part.x, 16);
+      tot.y = part.y + __shfl_xor_sync(kFull, part.y, 16);
+      tot.z = part.z + __shfl_xor_sync(kFull, part.z, 16);
+      tot.w = part.w + __shfl_xor_sync(kFull, part.w, 16);
+      const int64_t rs = __shfl_sync(kFull, row, sg);
+      if (!staged) {  // the slices were staged by both halves: wait for all of them
+        cp_async_wait_all();
+        __syncwarp();
+        staged = true;
+      }
+      if (h == 0 && rs >= 0 && col) {
+        if (a.grad_out) *(float4*)(a.grad_out + (tile * TU + sg) * a.ld + sub * 4) = tot;
+        const float4 w = *(const float4*)(wsm + sg * row_bytes + sub * 16);
+        const float k = -a.lr;
+        stg_f4_policy((float*)a.table + rs * a.ld + sub * 4,
+                      make_float4(fmaf(k, tot.x, w.x), fmaf(k, tot.y, w.y), fmaf(k, tot.z, w.z), fmaf(k, tot.w, w.w)),
+                      pol_stream);
+      }
+    };
+    for (int c0 = 0; c0 < E; c0 += 32) {
+      const TileChunk ahead = tile_chunk(a, c0 + 64 + lane, E, e, r0i, slen);
+      float sc_nxt;
+      const uint32_t gnxt = bag_g4(a, pend.bag, sc_nxt);
+      for (int g = 0; g < 16; g += kPairWin) {
+#pragma unroll
+        for (int j = 0; j < kPairWin; ++j) {
+          const int q = g + j;
+          const int t0 = 2 * q, t1 = 2 * q + 1;
+          const float4 x = buf[j];
+          const int tn = 2 * (q + kPairWin) + h;  // refill the slot with pair q + kPairWin
+          const uint32_t r = __shfl_sync(kFull, tn < 32 ? gcur : gnxt, tn & 31);
+          buf[j] = (r != kNoG && col) ? ldg_f4_policy(Gl + (uint64_t)r * 4, pol_keep) : zero;
+          const bool v0 = c0 + t0 < E, v1 = c0 + t1 < E;
+          if (!v0) continue;  // warp-uniform: the chunk's tail
+          const float sc = MEAN ? __shfl_sync(kFull, sc_cur, 2 * q + h) : 1.f;
+          const int seg0 = __shfl_sync(kFull, cur.seg, t0), seg1 = __shfl_sync(kFull, cur.seg, t1);
+          const bool last1 = v1 && ((cur.lastm >> t1) & 1u);
+          if (v1 && seg0 == seg1) {  // both occurrences belong to one run
+            acc = MEAN ? fma4(x, sc, acc) : make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
+            if (last1) {
+              finish(seg1, acc);
+              acc = zero;
+            }
+          } else {  // occurrence t0 closes its run; t1 (if any) starts the next one
+            float4 mine = acc;
+            if (h == 0) mine = MEAN ? fma4(x, sc, acc) : make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
+            finish(seg0, mine);
+            acc = zero;
+            if (v1) {
+              if (h == 1) acc = MEAN ? fma4(x, sc, zero) : x;
+              if (last1) {
+                finish(seg1, acc);
+                acc = zero;
+              }
+            }
+          }
+        }
+      }
+      cur = pend;
+      pend = ahead;
+      gcur = gnxt;
+      sc_cur = sc_nxt;
+    }
+    cp_async_wait_all();  // nothing may land in the buffer after the next tile reuses it
+    __syncwarp();
+  }
+}
+
 // Optimizers with state run at 2 blocks per SM: the state arithmetic needs the
 // registers, and the staged states the shared memory.
 #ifndef CTR_TILE_OPT_MINB
@@ -782,12 +947,12 @@ __global__ void __launch_bounds__(kTileThreads, OPT == CTR_OPT_SGD ? CTR_TILE_AS
     for (int j = 0; j < TU; ++j) {
       const int64_t rj = __shfl_sync(kFull, row, j);
       if (rj >= 0 && col) {
-        cp_async_chunk(wsm_s + j * row_bytes + lane * chunk, (const char*)a.table + rj * row_bytes + lane * chunk,
-                       chunk, pol_stream);
+        cp_async_chunk(wsm_s + j * row_bytes + lane * chunk,
+                       (const char*)a.table + (rj * a.ld) * esz + lane * chunk, chunk, pol_stream);
         if constexpr (NS >= 1)
-          cp_async_chunk(ssm_s + j * state_bytes + lane * 16, a.s0 + rj * a.d + lane * 4, 16, pol_stream);
+          cp_async_chunk(ssm_s + j * state_bytes + lane * 16, a.s0 + rj * a.ld + lane * 4, 16, pol_stream);
         if constexpr (NS >= 2)
-          cp_async_chunk(ssm_s + (TU + j) * state_bytes + lane * 16, a.s1 + rj * a.d + lane * 4, 16, pol_stream);
+          cp_async_chunk(ssm_s + (TU + j) * state_bytes + lane * 16, a.s1 + rj * a.ld + lane * 4, 16, pol_stream);
       }
     }
     cp_async_commit();
@@ -991,6 +1156,52 @@ int grid_of(K kernel, int threads, size_t smem, int64_t want) {
   return (int)std::max<int64_t>(1, imin64(want, (int64_t)std::max(per_sm, 1) * num_sms()));
 }
 
+// Short runs of fp32 rows under SGD in column slices (bwd_tiles_pair_kernel):
+// 0 = automatic (when one table's pooled-gradient rows, batch x 512 bytes at
+// d = 128, exceed 32 MB and would not stay in L2), 1 = never, 2 = always where
+// supported.  Process-wide (ctr_set_tile_slices).
+std::atomic<int> g_tile_slices{0};
+constexpr int64_t kSliceGradBytes = (int64_t)32 << 20;
+
+bool use_pair_slices(const BwdArgs& a) {
+  if (a.opt != CTR_OPT_SGD || a.sr || a.bf16 || !a.g4_ok || a.d != 128) return false;
+  const int mode = g_tile_slices.load();
+  if (mode == 1) return false;
+  if (mode == 2) return true;
+  return (int64_t)a.B * a.d * 4 > kSliceGradBytes;
+}
+
+// The short-run pass: the tile kernel once, or the pair kernel once per
+// 64-column slice.
+template <typename K>
+int launch_tiles(const BwdArgs& a, K tk, size_t tile_smem, cudaStream_t s, int64_t n) {
+  if (use_pair_slices(a)) {
+    auto pk = a.mean ? bwd_tiles_pair_kernel<true> : bwd_tiles_pair_kernel<false>;
+    for (int c0 = 0; c0 < a.d; c0 += 64) {
+      BwdArgs b = a;
+      b.d = 64;
+      b.ld = a.d;
+      b.table = (float*)a.table + c0;
+      b.G = a.G + c0;
+      if (a.grad_out) b.grad_out = a.grad_out + c0;
+      b.TU = kPairTU;
+      const size_t smem = (size_t)kTileWarps * b.TU * b.d * 4;
+      if (smem > 48 * 1024 &&
+          cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return CTR_ERR_CUDA;
+      if (cudaMemsetAsync(a.work, 0, sizeof(unsigned long long), s) != cudaSuccess) return CTR_ERR_CUDA;
+      pk<<<grid_of(pk, kTileThreads, smem, ceil_div(n, (int64_t)b.TU * kTileWarps)), kTileThreads, smem, s>>>(b);
+      count_launch();
+      if (int st = launch_status()) return st;
+    }
+    return CTR_OK;
+  }
+  if (cudaMemsetAsync(a.work, 0, sizeof(unsigned long long), s) != cudaSuccess) return CTR_ERR_CUDA;
+  tk<<<grid_of(tk, kTileThreads, tile_smem, ceil_div(n, (int64_t)a.TU * kTileWarps)), kTileThreads, tile_smem, s>>>(a);
+  count_launch();
+  return launch_status();
+}
+
 template <int CPL>
 int launch_short(const BwdArgs& a, cudaStream_t s, int64_t n) {
   const int chunks = a.d / 4;
@@ -1012,9 +1223,8 @@ int launch_short(const BwdArgs& a, cudaStream_t s, int64_t n) {
   if (tile_smem > 48 * 1024 &&
       cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tile_smem) != cudaSuccess)
     return CTR_ERR_CUDA;
-  if (cudaMemsetAsync(a.work, 0, sizeof(unsigned long long), s) != cudaSuccess) return CTR_ERR_CUDA;
   timing_mark(CTR_KERNEL_BWD_TILES, true, s);
-  tk<<<grid_of(tk, kTileThreads, tile_smem, ceil_div(n, (int64_t)a.TU * kTileWarps)), kTileThreads, tile_smem, s>>>(a); count_launch();
+  if (int st = launch_tiles(a, tk, tile_smem, s, n)) return st;
   timing_mark(CTR_KERNEL_BWD_TILES, false, s);
   return launch_status();
 }
@@ -1074,6 +1284,8 @@ int launch_finish(const BwdArgs& a, cudaStream_t s) {
 
 using namespace ctr;
 
+extern "C" int ctr_set_tile_slices(int mode) { return g_tile_slices.exchange(mode < 0 || mode > 2 ? 0 : mode); }
+
 extern "C" size_t ctr_bwd_update_workspace_size(int64_t n_ids, int32_t d) {
   WsSizer s;
   bwd_layout(s, n_ids > 0 ? n_ids : 1, d > 0 ? d : 1);
@@ -1130,6 +1342,7 @@ int bwd_update_phases(const float* grad_pooled, int64_t g_stride_b, int64_t g_st
   a.table = table;
   a.bf16 = dtype == CTR_BF16;
   a.d = d;
+  a.ld = d;
   a.total_rows = total_rows;
   a.grad_out = grad_unique_out;
   a.err = (int*)ws;

@@ -248,6 +248,37 @@ constexpr uint32_t kNoRow = 0xffffffffu;
 #define CTR_FLAT_MINB 8
 #endif
 
+// Cache handling of the flat gather's loads (a build-time choice):
+//   0  IDs and table rows with the default policy;
+//   1  IDs streamed (L1 no-allocate, L2 evict-first), table rows evict-last
+//      (the default: the IDs are read once, and keeping them out of L2 leaves
+//      it to the rows that repeat; the gather 1.7% faster in the full step,
+//      measured twice: 3.30 -> 3.24 ms);
+//   2  IDs streamed, table rows with the default policy (3.28 ms).
+#ifndef CTR_FLAT_POLICY
+#define CTR_FLAT_POLICY 1
+#endif
+template <typename IT>
+__device__ __forceinline__ IT ld_id(const IT* p, uint64_t pol) {
+  if constexpr (CTR_FLAT_POLICY == 0) {
+    (void)pol;
+    return *p;
+  } else if constexpr (sizeof(IT) == 8) {
+    unsigned long long v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u64 %0, [%1], %2;" : "=l"(v) : "l"(p), "l"(pol));
+    return (IT)v;
+  } else {
+    unsigned v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
+    return (IT)v;
+  }
+}
+__device__ __forceinline__ float4 ld_row16(const float* p, uint64_t pol) {
+  if constexpr (CTR_FLAT_POLICY == 1) return ldg_f4_policy(p, pol);
+  (void)pol;
+  return *(const float4*)p;
+}
+
 struct FlatChunk {
   uint32_t row;    // global row of this lane's occurrence, kNoRow if none
   uint32_t lastm;  // ballot: occurrence t closes its bag
@@ -294,6 +325,7 @@ __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kerne
   const float* table = (const float*)a.table + lane * 4;
   const int64_t end_all = a.offsets[nbags];
   const uint64_t pol_stream = l2_evict_first();  // pooled outputs are written once
+  const uint64_t pol_rows = l2_evict_last();
   unsigned long long* counter = (unsigned long long*)((char*)a.err + kWsCounterOffset);
   (void)nwarps;
   for (int64_t blk = next_unit(counter); blk < nblk; blk = next_unit(counter)) {
@@ -327,18 +359,18 @@ __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kerne
     const int total = (int)(S1 - S0);
 
     const IT* ib = idx + S0;
-    IT id_b = (32 + lane < total) ? ib[32 + lane] : IT(0);
-    FlatChunk cur = flat_chunk(a, lane, (lane < total) ? ib[lane] : IT(0), rel0, rel1, base, nrows);
+    IT id_b = (32 + lane < total) ? ld_id(ib + 32 + lane, pol_stream) : IT(0);
+    FlatChunk cur = flat_chunk(a, lane, (lane < total) ? ld_id(ib + lane, pol_stream) : IT(0), rel0, rel1, base, nrows);
     float4 buf[kWinF];
 #pragma unroll
     for (int u = 0; u < kWinF; ++u) {
       const uint32_t r = __shfl_sync(kFull, cur.row, u);
-      buf[u] = (r != kNoRow) ? *(const float4*)(table + (uint64_t)r * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+      buf[u] = (r != kNoRow) ? ld_row16(table + (uint64_t)r * 128, pol_rows) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float sq = 0.f;
     for (int c0 = 0; c0 < total; c0 += 32) {
-      const IT id_c = (c0 + 64 + lane < total) ? ib[c0 + 64 + lane] : IT(0);
+      const IT id_c = (c0 + 64 + lane < total) ? ld_id(ib + c0 + 64 + lane, pol_stream) : IT(0);
       const FlatChunk nxt = flat_chunk(a, c0 + 32 + lane, id_b, rel0, rel1, base, nrows);
       for (int g = 0; g < 32; g += kWinF) {
 #pragma unroll
@@ -347,7 +379,7 @@ __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kerne
           const float4 x = buf[j];
           const int tn = t + kWinF;  // refill the slot with occurrence tn
           const uint32_t r = __shfl_sync(kFull, tn < 32 ? cur.row : nxt.row, tn & 31);
-          buf[j] = (r != kNoRow) ? *(const float4*)(table + (uint64_t)r * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+          buf[j] = (r != kNoRow) ? ld_row16(table + (uint64_t)r * 128, pol_rows) : make_float4(0.f, 0.f, 0.f, 0.f);
           acc = add4_packed(acc, x);
           if (FM) sq = fmaf(x.w, x.w, fmaf(x.z, x.z, fmaf(x.y, x.y, fmaf(x.x, x.x, sq))));
           if ((cur.lastm >> t) & 1u) {

@@ -34,6 +34,7 @@ _SIGS = {
     "ctr_set_timing_events": (C.c_int, [C.c_int, _p, _p]),
     "ctr_launch_count": (C.c_uint64, []),
     "ctr_set_tma_gather": (C.c_int, [C.c_int]),
+    "ctr_set_tile_slices": (C.c_int, [C.c_int]),
     "ctr_status_reset": (C.c_int, [_p, _p]),
     "ctr_check_status": (C.c_int, [_p, _p]),
     "ctr_fill_table": (C.c_int, [_p, C.c_int, _i64, _i32, _i64, C.c_int, _u64, _f32, _p]),
@@ -144,6 +145,12 @@ def ctr_launch_count() -> int:
 def ctr_set_tma_gather(on: bool) -> bool:
     """Select the TMA row-gather variant of the fp32 d=128 pooled gather; returns the previous setting."""
     return bool(lib().ctr_set_tma_gather(1 if on else 0))
+
+
+def ctr_set_tile_slices(mode: int) -> int:
+    """Short-run pass of the fp32 d=128 SGD row update: 0 automatic, 1 never sliced, 2 always in
+    64-column slices; returns the previous mode."""
+    return int(lib().ctr_set_tile_slices(int(mode)))
 
 
 # ---------------------------------------------------------------------------

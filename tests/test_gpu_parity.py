@@ -460,6 +460,72 @@ def test_bwd_update_exact_arithmetic_with_long_runs():
     np.testing.assert_array_equal(new_tab[untouched], table[untouched])
 
 
+@pytest.fixture
+def tile_slices():
+    """Sets the short-run pass's column-slice mode for one test, restoring it after."""
+    prev = []
+
+    def set_mode(mode):
+        prev.append(ctr.ctr_set_tile_slices(mode))
+
+    yield set_mode
+    if prev:
+        ctr.ctr_set_tile_slices(prev[0])
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_bwd_update_exact_arithmetic_d128_sliced_and_plain(mode, tile_slices):
+    # fp32 d = 128 under SGD: mode 2 forces the pair kernel (two 64-column slices, two
+    # occurrences per warp step), mode 1 the plain tile kernel; dyadic inputs make every
+    # sum exact, so both must equal the oracle bit for bit, long runs and ragged tiles included
+    tile_slices(mode)
+    rng = np.random.default_rng(12 + mode)
+    F, B, d = 3, 901, 128
+    rows = [37, 5, 4000]
+    lens = rng.integers(0, 9, size=F * B)
+    lens[B:B + 30] = 300                               # long runs in field 1
+    ids, offsets = _csr(lens, rng, rows, B)
+    cfg = W.CONFIGS["tiny"].shrink(batch=B, num_fields=F, field_to_table=(0, 1, 2), rows_per_table=tuple(rows),
+                                   d=d, lr=2.0 ** -6)
+    table = (rng.integers(-256, 256, size=(sum(rows), d)) / 256).astype(np.float32)
+    G = (rng.integers(-16, 17, size=(B, F, d)) / 16).astype(np.float32)
+    w = {"ids": ids, "offsets": offsets, "bag_to_table": np.arange(F, dtype=np.int32),
+         "row_base": cfg.row_base, "grad_pooled": G}
+    new_tab, g, dd = gpu_bwd(cfg, w, table_np=table)
+    run_len = np.diff(dd["run_offsets"])
+    assert (run_len <= 128).sum() > 1000 and (run_len > 128).any()
+    rows_t = dd["unique_rows"]
+    ref_new, ref_g, _ = O.embedding_bag_bwd_update(G, ids, offsets, F, B, w["bag_to_table"], cfg.row_base, d,
+                                                   cfg.lr, rows_t, table=table)
+    np.testing.assert_array_equal(g, ref_g.astype(np.float32))
+    np.testing.assert_array_equal(new_tab[rows_t], ref_new)
+    untouched = np.setdiff1d(np.arange(sum(rows)), rows_t)
+    np.testing.assert_array_equal(new_tab[untouched], table[untouched])
+
+
+@pytest.mark.parametrize("pool", ["sum", "mean"])
+def test_bwd_update_sliced_pass_against_oracle_and_deterministic(pool, tile_slices):
+    # the pair kernel on the full step's row shape (d = 128, Zipf IDs, 26 tables), forced on
+    # at a small batch: the oracle within each run's depth, and the same bits twice
+    tile_slices(2)
+    cfg = W.CONFIGS["full_step"].shrink(batch=700, rows_per_table=tuple([40_000] * 26), backward="pooled_grad",
+                                        pool=pool)
+    w = W.make_workload(cfg)
+    F, B, d = cfg.num_fields, cfg.batch, cfg.d
+    new_tab, g, dd = gpu_bwd(cfg, w)
+    new_tab2, g2, _ = gpu_bwd(cfg, w)
+    np.testing.assert_array_equal(g, g2)
+    np.testing.assert_array_equal(new_tab, new_tab2)
+    rows_t = dd["unique_rows"]
+    ref_new, ref_g, mag = O.embedding_bag_bwd_update(w["grad_pooled"], w["ids"], w["offsets"], F, B,
+                                                     w["bag_to_table"], w["row_base"], d, cfg.lr, rows_t,
+                                                     pool=pool, gen=_gen(cfg))
+    depth = bwd_depth(np.diff(dd["run_offsets"]))[:, None]
+    f32_close(g, ref_g, mag, depth, what=f"sliced grad ({pool})")
+    old = O.table_rows(cfg.fill_kind, cfg.fill_seed, cfg.fill_scale, d, rows_t)
+    f32_close(new_tab[rows_t], ref_new, cfg.lr * mag + np.abs(old), depth + 2, what=f"sliced rows ({pool})")
+
+
 BWD_CASES = {
     "tiny": W.CONFIGS["tiny"],
     "tensornet_b512": W.CONFIGS["tensornet"].shrink(batch=512),
