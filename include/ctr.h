@@ -112,6 +112,14 @@ uint64_t ctr_launch_count(void);
  * Process-wide; returns the previous setting. */
 int ctr_set_tma_gather(int on);
 
+/* Diagnostics: the wall-clock limit (nanoseconds, default 1e9) of each wait of
+ * a ctr_dedup radix pass on a predecessor tile's counts.  A wait that runs out
+ * records CTR_ERR_TIMEOUT in the workspace (read by ctr_check_status), the
+ * pass keeps every write inside its buffers, and the call's outputs are then
+ * meaningless.  A short limit makes ordinary waits run out: it exists to test
+ * that path.  Process-wide, read at each launch; returns the previous limit. */
+uint64_t ctr_set_wait_limit_ns(uint64_t ns);
+
 /* Short-run pass of the row update for fp32 rows of d = 128 under plain SGD
  * (no optimizer state, no stochastic rounding): mode 2 processes the short
  * runs in two 64-column slices, two occurrences per warp step, so the pooled-

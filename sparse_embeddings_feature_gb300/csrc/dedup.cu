@@ -28,6 +28,7 @@
 //              (gather of the bag of each sorted position), unique_offsets.
 // Each radix pass is one kernel (Onesweep-style decoupled look-back, below).
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 #include "scan.cuh"
@@ -119,7 +120,10 @@ static __device__ __forceinline__ uint64_t now_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-constexpr uint64_t kLookbackLimitNs = 1000000000ull;  // 1 s
+// Wall-clock limit of one look-back wait: 1 s, or what ctr_set_wait_limit_ns
+// set (a diagnostic: a short limit makes ordinary waits run out, which tests
+// the timeout path without faulting or hanging anything).
+std::atomic<uint64_t> g_lookback_limit_ns{1000000000ull};
 
 // One radix pass in one kernel (single-pass, after Adinets and Merrill's
 // Onesweep): a block takes the next tile in launch order, ranks its keys
@@ -137,7 +141,7 @@ __global__ void __launch_bounds__(kRsThreads) onesweep_kernel(
     const uint32_t* __restrict__ keys_in, const int32_t* __restrict__ vals_in, uint32_t* __restrict__ keys_out,
     int32_t* __restrict__ vals_out, int64_t n, int shift, int nbits, const PassPlan* __restrict__ dplan, int pass,
     int32_t* __restrict__ vals_final, const uint32_t* __restrict__ g_hist, uint64_t* __restrict__ lookback,
-    uint32_t* __restrict__ tile_counter, int* err) {
+    uint32_t* __restrict__ tile_counter, int* err, uint64_t limit_ns) {
   if (dplan) {  // digit plan decided on the device (rank keys): passes beyond it do nothing
     if (pass >= dplan->passes) return;
     shift = dplan->shift[pass];
@@ -234,7 +238,7 @@ __global__ void __launch_bounds__(kRsThreads) onesweep_kernel(
       if (stalled) {
         const uint64_t t = now_ns();
         if (t0 == 0) t0 = t;
-        else if (t - t0 > kLookbackLimitNs) {
+        else if (t - t0 > limit_ns) {
           timed_out = true;
           break;
         }
@@ -844,7 +848,8 @@ int dedup_bitmap(const int64_t* ids, const int64_t* offsets, int32_t F, int32_t 
                                                            vals[(p + 1) & 1], n_ids, 0, 0, dplan, p, vals_final,
                                                            g_hist + p * kMaxDigits,
                                                            lookback + (int64_t)p * tiles * kMaxDigits,
-                                                           tile_counter + p, err); count_launch();
+                                                           tile_counter + p, err, g_lookback_limit_ns.load());
+    count_launch();
     if (int st = launch_status()) return st;
   }
   timing_mark(CTR_KERNEL_SORT, false, s);
@@ -860,6 +865,8 @@ int dedup_bitmap(const int64_t* ids, const int64_t* offsets, int32_t F, int32_t 
 }  // namespace ctr
 
 using namespace ctr;
+
+extern "C" uint64_t ctr_set_wait_limit_ns(uint64_t ns) { return g_lookback_limit_ns.exchange(ns); }
 
 extern "C" size_t ctr_dedup_workspace_size(int64_t n_ids, int32_t num_fields, int32_t batch, int64_t total_rows) {
   (void)num_fields;
@@ -951,7 +958,8 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
                                                            plan.shift[p], plan.bits[p], nullptr, p, nullptr,
                                                            g_hist + p * kMaxDigits,
                                                            lookback + (int64_t)p * tiles * kMaxDigits,
-                                                           tile_counter + p, err); count_launch();
+                                                           tile_counter + p, err, g_lookback_limit_ns.load());
+    count_launch();
     if (int st = launch_status()) return st;
     vin = vout;
   }

@@ -248,15 +248,18 @@ constexpr uint32_t kNoRow = 0xffffffffu;
 #define CTR_FLAT_MINB 8
 #endif
 
-// Cache handling of the flat gather's loads (a build-time choice):
-//   0  IDs and table rows with the default policy;
-//   1  IDs streamed (L1 no-allocate, L2 evict-first), table rows evict-last
-//      (the default: the IDs are read once, and keeping them out of L2 leaves
-//      it to the rows that repeat; the gather 1.7% faster in the full step,
-//      measured twice: 3.30 -> 3.24 ms);
-//   2  IDs streamed, table rows with the default policy (3.28 ms).
+// Cache handling of the flat gather's loads (a build-time choice; full-step
+// gather times in the same sessions):
+//   0  IDs and table rows with the default policy (3.30 ms);
+//   1  IDs streamed (L1 no-allocate, L2 evict-first), table rows L2
+//      evict-last (3.24 ms, twice);
+//   2  IDs streamed, table rows with the default policy (3.28 ms);
+//   3  as 1, and table rows not allocated in L1 (the default: 3.21 ms against
+//      3.25 for 1): the Zipf head's L1 hits save nothing, so keeping hot rows
+//      on chip (L1 or shared memory) does not pay for this gather;
+//   4  as 1, with table rows L1 evict-last (3.27 ms).
 #ifndef CTR_FLAT_POLICY
-#define CTR_FLAT_POLICY 1
+#define CTR_FLAT_POLICY 3
 #endif
 template <typename IT>
 __device__ __forceinline__ IT ld_id(const IT* p, uint64_t pol) {
@@ -274,7 +277,24 @@ __device__ __forceinline__ IT ld_id(const IT* p, uint64_t pol) {
   }
 }
 __device__ __forceinline__ float4 ld_row16(const float* p, uint64_t pol) {
-  if constexpr (CTR_FLAT_POLICY == 1) return ldg_f4_policy(p, pol);
+  if constexpr (CTR_FLAT_POLICY == 1 || CTR_FLAT_POLICY == 2) {
+    if constexpr (CTR_FLAT_POLICY == 1) return ldg_f4_policy(p, pol);
+    return *(const float4*)p;
+  }
+  if constexpr (CTR_FLAT_POLICY == 3) {  // rows not kept in L1
+    float4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(p), "l"(pol));
+    return r;
+  }
+  if constexpr (CTR_FLAT_POLICY == 4) {  // rows kept in L1 as long as possible
+    float4 r;
+    asm volatile("ld.global.nc.L1::evict_last.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(p), "l"(pol));
+    return r;
+  }
   (void)pol;
   return *(const float4*)p;
 }

@@ -21,6 +21,9 @@ from . import build as _build
 F32, BF16 = 0, 1
 POOL_SUM, POOL_MEAN = 0, 1
 DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
+# status codes (ctr_status in include/ctr.h)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE = 0, -1, -2, -3
+ERR_INDEX_OUT_OF_RANGE, ERR_CUDA, ERR_TIMEOUT, ERR_NOT_IMPLEMENTED, ERR_BAD_OFFSETS = -4, -5, -6, -7, -8
 
 _lock = threading.Lock()
 _lib = None
@@ -35,6 +38,7 @@ _SIGS = {
     "ctr_launch_count": (C.c_uint64, []),
     "ctr_set_tma_gather": (C.c_int, [C.c_int]),
     "ctr_set_tile_slices": (C.c_int, [C.c_int]),
+    "ctr_set_wait_limit_ns": (C.c_uint64, [C.c_uint64]),
     "ctr_status_reset": (C.c_int, [_p, _p]),
     "ctr_check_status": (C.c_int, [_p, _p]),
     "ctr_fill_table": (C.c_int, [_p, C.c_int, _i64, _i32, _i64, C.c_int, _u64, _f32, _p]),
@@ -145,6 +149,11 @@ def ctr_launch_count() -> int:
 def ctr_set_tma_gather(on: bool) -> bool:
     """Select the TMA row-gather variant of the fp32 d=128 pooled gather; returns the previous setting."""
     return bool(lib().ctr_set_tma_gather(1 if on else 0))
+
+
+def ctr_set_wait_limit_ns(ns: int) -> int:
+    """Wall-clock limit of each radix-pass look-back wait of ctr_dedup (diagnostics); returns the previous."""
+    return int(lib().ctr_set_wait_limit_ns(int(ns)))
 
 
 def ctr_set_tile_slices(mode: int) -> int:
