@@ -64,6 +64,10 @@ def parse():
                     help="draw IDs uniformly over each table instead of the workload's Zipf: with full-size tables "
                          "no row repeats (the gather's random-row rate from HBM); with --rows small enough for "
                          "the tables to sit in L2, its random-row rate from L2")
+    ap.add_argument("--gather-order", action="store_true",
+                    help="instead of the step: time the pooled gather of one batch with its bags in field-major "
+                         "order (the path's order) and in sample-major order (the order a gather fused with the "
+                         "per-sample interaction would need), same lookups, same kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -542,8 +546,61 @@ def run_reference(args):
             "e2e": {"value": v, "unit": "lookups/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_gather_order(args):
+    """The gather of one batch in two bag orders, through the unmapped entry point (global rows
+    as indices, one field), so the kernel, the lookups and the bytes are the same: only the
+    order in which the bags (and so the tables) are visited differs."""
+    import torch
+    from sparse_embeddings_feature_gb300 import ctr
+    from sparse_embeddings_feature_gb300 import workload as W
+    from sparse_embeddings_feature_gb300.pipeline import CtrPath
+
+    cfg = workload_cfg(args)
+    w = W.make_workload(cfg, with_grads=False)
+    F, B, d = cfg.num_fields, cfg.batch, cfg.d
+    n = int(w["ids"].size)
+    path = CtrPath(cfg, n)
+    lens = np.diff(w["offsets"])
+    field_of = np.repeat(np.arange(F * B) // B, lens)
+    rows = (np.asarray(cfg.row_base)[np.asarray(cfg.field_to_table)[field_of]] + w["ids"]).astype(np.int64)
+    # sample-major: bag (b, f) at position b * F + f
+    perm_bags = (np.arange(F)[None, :] * B + np.arange(B)[:, None]).ravel()
+    starts = w["offsets"][:-1][perm_bags]
+    sm_lens = lens[perm_bags]
+    sm_offsets = np.concatenate([[0], np.cumsum(sm_lens)]).astype(np.int64)
+    idx = np.repeat(starts - sm_offsets[:-1], sm_lens) + np.arange(n)
+    sm_rows = rows[idx]
+    out = torch.empty((F * B, d), dtype=path.table.dtype, device="cuda")
+    ws = ctr.workspace(ctr.ctr_embedding_bag_workspace_size())
+    pool = ctr.POOL_MEAN if cfg.pool == "mean" else ctr.POOL_SUM
+    res = {}
+    for name, r, o in (("field_major", rows, w["offsets"]), ("sample_major", sm_rows, sm_offsets)):
+        rd = torch.from_numpy(r).cuda()
+        od = torch.from_numpy(o).cuda()
+
+        def call():
+            ctr.ctr_embedding_bag_fwd(path.table, d, rd, od, 1, F * B, None, None, pool, out, d, 0, ws, n_indices=n)
+        for _ in range(max(args.warmup, 3)):
+            call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            call()
+        b.record()
+        torch.cuda.synchronize()
+        assert ctr.ctr_check_status(ws) == 0
+        res[name] = a.elapsed_time(b) / args.steps
+        del rd, od
+    return {"workload": cfg.name, "gather_ms": res, "n_ids": n,
+            "x_reread_bytes_saved_by_fusion": int(B * cfg.n_vectors * d * (4 if cfg.dtype == "f32" else 2))}
+
+
 def main():
     args = parse()
+    if args.gather_order:
+        print(json.dumps(run_gather_order(args)), flush=True)
+        return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     if args.impl == "reference":

@@ -95,6 +95,7 @@ __device__ __forceinline__ void store_out(void* out, int64_t off, const float* v
 struct BagArgs {
   const void* table;
   int32_t d;
+  int32_t ld;      // row stride of the table in elements (d, or more for a column slice)
   int64_t total_rows;
   const void* idx;
   int64_t n_idx;
@@ -436,6 +437,193 @@ __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kerne
   }
 }
 
+// Narrow rows (2 to 16 chunks of 16 bytes: bf16 d = 16..128, fp32 d = 8..64):
+// the flattened walk of bag_fwd_flat_kernel with several rows per warp step.
+// A lane group of G = chunks lanes holds one row; the NG = 32 / G groups of a
+// warp take NG consecutive occurrences of the block's flattened list per step,
+// with a window of kNarrowWin steps of row loads in flight that continues
+// across bag and chunk boundaries (so a bag end never drains the pipeline, and
+// short bags cost no more than long ones).  Each group sums the occurrences it
+// takes of the open bag; when the bag closes, the groups' partials are added
+// by a fixed butterfly and group 0 stores the row.  Every bag's summation
+// order depends only on the bag lengths, so results are deterministic.  With
+// FM, each lane also sums the squares of its columns of the rows it takes; at
+// a bag's close both sums are reduced the same way and lane 0 stores
+// 1/2 (|sum v|^2 - sum |v|^2) (exactly 0 for a one-ID bag: both terms then
+// round identically).
+// Repeated IDs (a build-time option, off): within each chunk of 32
+// occurrences, the occurrences of one bag that name the same row can be merged
+// (match.any on bag and row; the first loads the row and adds it times the
+// count, the others load nothing).  Under Zipf IDs a bag often repeats its
+// hottest rows (about 28% of the lookups of the bf16 workload's bags of ~30
+// IDs at alpha = 1.2), but those are L1/L2 hits, and the match costs more than
+// they do: bf16 workload 1.26 -> 1.34 ms, TensorNet pooling 0.258 -> 0.301 ms.
+#ifndef CTR_NARROW_WIN
+#define CTR_NARROW_WIN 4
+#endif
+#ifndef CTR_NARROW_MINB
+#define CTR_NARROW_MINB 4
+#endif
+constexpr int kNarrowWin = CTR_NARROW_WIN;
+#ifndef CTR_USE_NARROW
+#define CTR_USE_NARROW 1
+#endif
+#ifndef CTR_NARROW_MERGE
+#define CTR_NARROW_MERGE 0
+#endif
+
+// Merge the repeats of (bag, row) among a chunk's occurrences: returns this
+// occurrence's weight (the group's size for its first occurrence, 0 for the
+// others, whose row becomes kNoRow so they load nothing).
+__device__ __forceinline__ float merge_repeats(FlatChunk& m) {
+  if (!CTR_NARROW_MERGE) return 1.f;
+  const unsigned long long key =
+      m.row == kNoRow ? ~0ull : (((unsigned long long)(unsigned)m.seg << 32) | (unsigned long long)m.row);
+  const unsigned peers = __match_any_sync(kFull, key);
+  const int lane = threadIdx.x & 31;
+  if (m.row == kNoRow) return 0.f;
+  if (__ffs(peers) - 1 != lane) {
+    m.row = kNoRow;
+    return 0.f;
+  }
+  return (float)__popc(peers);
+}
+
+template <typename TT, int G, typename IT, bool FM>
+__global__ void __launch_bounds__(kBagThreads, CTR_NARROW_MINB) bag_fwd_narrow_kernel(
+    const BagArgs a, const __grid_constant__ FieldMap fm) {
+  constexpr int V = Vec<TT>::kN;  // elements per 16-byte chunk
+  constexpr int NG = 32 / G;      // rows per warp step
+  constexpr int STEPS = 32 / NG;  // steps per chunk of 32 occurrences
+  const int lane = threadIdx.x & 31;
+  const int grp = lane / G, sub = lane % G;
+  const int64_t nbags = (int64_t)a.F * a.B;
+  const int64_t nblk = ceil_div(nbags, 32);
+  const IT* idx = (const IT*)a.idx;
+  const TT* table = (const TT*)a.table + sub * V;
+  const int64_t end_all = a.offsets[nbags];
+  const uint64_t pol_stream = l2_evict_first();
+  const uint64_t pol_rows = l2_evict_last();
+  unsigned long long* counter = (unsigned long long*)((char*)a.err + kWsCounterOffset);
+  for (int64_t blk = next_unit(counter); blk < nblk; blk = next_unit(counter)) {
+    const int64_t bag = blk * 32 + lane;
+    const bool bvalid = bag < nbags;
+    int64_t o0 = bvalid ? a.offsets[bag] : end_all;
+    int64_t o1 = bvalid ? a.offsets[bag + 1] : end_all;
+    const bool bad = o0 < 0 || o1 < o0 || o1 > a.n_idx;
+    const int f = bvalid ? (int)(bag / a.B) : 0;
+    const int b = bvalid ? (int)(bag - (int64_t)f * a.B) : 0;
+    const int64_t ooff = (int64_t)b * a.sb + (int64_t)f * a.sf;  // this lane's bag's output row
+    const float lenf = (float)(o1 - o0);
+    const int64_t S0 = __shfl_sync(kFull, o0, 0);
+    const int64_t S1 = __shfl_sync(kFull, o1, 31);
+    if (__any_sync(kFull, bad) || S1 - S0 >= ((int64_t)1 << 30)) {
+      if (lane == 0) set_error(a.err, CTR_ERR_BAD_OFFSETS);
+      o0 = o1 = S0;  // write this block as zeros
+    }
+    unsigned empty = __ballot_sync(kFull, bvalid && o1 == o0);  // empty bags produce zero rows
+    while (empty) {
+      const int j = __ffs(empty) - 1;
+      empty &= empty - 1;
+      const float z[V] = {};
+      const int64_t oj = __shfl_sync(kFull, ooff, j);
+      if (lane < G) store_out(a.out, oj + (int64_t)lane * V, z, V, a.out_bf16, a.vec_out);
+    }
+    if (FM && bvalid && o1 == o0) a.fm_out[bag] = 0.f;
+    if (__all_sync(kFull, o1 == o0)) continue;
+    const int rel0 = (int)(o0 - S0), rel1 = (int)(o1 - S0);
+    const uint32_t base = a.mapped ? (uint32_t)fm.base[f] : 0u;
+    const uint32_t nrows = a.mapped ? (uint32_t)fm.rows[f] : (uint32_t)a.total_rows;
+    const int total = (int)(S1 - S0);
+
+    const IT* ib = idx + S0;
+    IT id_b = (32 + lane < total) ? ld_id(ib + 32 + lane, pol_stream) : IT(0);
+    FlatChunk cur = flat_chunk(a, lane, (lane < total) ? ld_id(ib + lane, pol_stream) : IT(0), rel0, rel1, base, nrows);
+    float cur_w = merge_repeats(cur);
+    float sq = 0.f;  // FM: this lane's sum of squares of the open bag's rows
+    uint4 buf[kNarrowWin];
+#pragma unroll
+    for (int u = 0; u < kNarrowWin; ++u) {
+      const int t = u * NG + grp;  // the first steps stay inside the first chunk (kNarrowWin * NG <= 32)
+      const uint32_t r = __shfl_sync(kFull, cur.row, t);
+      buf[u] = (r != kNoRow) ? ldg16(table + (uint64_t)r * a.ld) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float acc[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] = 0.f;
+    for (int c0 = 0; c0 < total; c0 += 32) {
+      const IT id_c = (c0 + 64 + lane < total) ? ld_id(ib + c0 + 64 + lane, pol_stream) : IT(0);
+      FlatChunk nxt = flat_chunk(a, c0 + 32 + lane, id_b, rel0, rel1, base, nrows);
+      const float nxt_w = merge_repeats(nxt);
+      for (int q0 = 0; q0 < STEPS; q0 += kNarrowWin) {
+#pragma unroll
+        for (int j = 0; j < kNarrowWin; ++j) {
+          const int q = q0 + j;
+          const int t = q * NG + grp;  // this group's occurrence in this step
+          float x[V];
+          unpack(buf[j], x, TT());
+          const int tn = t + kNarrowWin * NG;  // refill the slot (tn < 32 is the same for every group)
+          const uint32_t r = __shfl_sync(kFull, tn < 32 ? cur.row : nxt.row, tn & 31);
+          buf[j] = (r != kNoRow) ? ldg16(table + (uint64_t)r * a.ld) : make_uint4(0u, 0u, 0u, 0u);
+          if (c0 + q * NG >= total) continue;  // warp-uniform: past the block's last occurrence
+          const bool valid = c0 + t < total;
+          const int sg = __shfl_sync(kFull, cur.seg, t);
+          const float wt = __shfl_sync(kFull, cur_w, t);  // 0 for a merged repeat (its row loaded nothing)
+          const bool last = valid && ((cur.lastm >> t) & 1u);
+          // the open bag is group 0's (occurrences are in bag order); close every bag that
+          // ends in this step, in order, then keep the one that continues
+          int open = __shfl_sync(kFull, cur.seg, q * NG);
+          while (true) {
+            if (valid && sg == open) {
+#pragma unroll
+              for (int v = 0; v < V; ++v) acc[v] = fmaf(x[v], wt, acc[v]);
+              if (FM) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) sq = fmaf(x[v], x[v] * wt, sq);
+              }
+            }
+            if (!__any_sync(kFull, valid && sg == open && last)) break;  // the open bag continues
+#pragma unroll
+            for (int o = G; o < 32; o <<= 1) {
+#pragma unroll
+              for (int v = 0; v < V; ++v) acc[v] += __shfl_xor_sync(kFull, acc[v], o);
+              if (FM) sq += __shfl_xor_sync(kFull, sq, o);
+            }
+            if (FM) {  // every group now holds the bag's sums; reduce over the G lanes of a row
+              float s2 = acc[0] * acc[0];
+#pragma unroll
+              for (int v = 1; v < V; ++v) s2 = fmaf(acc[v], acc[v], s2);
+#pragma unroll
+              for (int o = 1; o < G; o <<= 1) {
+                s2 += __shfl_xor_sync(kFull, s2, o);
+                sq += __shfl_xor_sync(kFull, sq, o);
+              }
+              if (lane == 0) a.fm_out[blk * 32 + open] = 0.5f * (s2 - sq);
+              sq = 0.f;
+            }
+            const float lj = __shfl_sync(kFull, lenf, open);
+            const int64_t oj = __shfl_sync(kFull, ooff, open);
+            if (grp == 0) {  // a closed bag is never empty
+              float out[V];
+#pragma unroll
+              for (int v = 0; v < V; ++v) out[v] = a.mean ? acc[v] / lj : acc[v];
+              store_out(a.out, oj + (int64_t)sub * V, out, V, a.out_bf16, a.vec_out);
+            }
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[v] = 0.f;
+            const unsigned later = __ballot_sync(kFull, valid && sg > open);
+            if (!later) break;  // the bag closed at this step's last occurrence
+            open = __shfl_sync(kFull, sg, __ffs(later) - 1);
+          }
+        }
+      }
+      cur = nxt;
+      cur_w = nxt_w;
+      id_b = id_c;
+    }
+  }
+}
+
 // The same flattened walk as bag_fwd_flat_kernel, with the rows staged by TMA
 // instead of loaded into registers: for every four occurrences one lane issues
 // a tile::gather4 (four 512-byte rows by row index, one mbarrier) into a ring
@@ -676,6 +864,26 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
     k<<<grid, kTmaWarps * 32, smem, s>>>(a, fm, map); count_launch();
     return launch_status();
   }
+#ifndef CTR_GATHER_SLICES
+#define CTR_GATHER_SLICES 1
+#endif
+  if (CTR_GATHER_SLICES > 1 && std::is_same<TT, float>::value && a.d == 128 && !a.fm_out &&
+      a.total_rows < 0xffffffffll) {
+    // column slices of 64 through the narrow walk: each slice's rows take half the L2
+    for (int c0 = 0; c0 < 128; c0 += 64) {
+      BagArgs b = a;
+      b.d = 64;
+      b.table = (const float*)a.table + c0;
+      b.out = a.out_bf16 ? (void*)((__nv_bfloat16*)a.out + c0) : (void*)((float*)a.out + c0);
+      if (cudaMemsetAsync((char*)a.err + kWsCounterOffset, 0, sizeof(unsigned long long), s) != cudaSuccess)
+        return CTR_ERR_CUDA;
+      auto k = bag_fwd_narrow_kernel<TT, 16, IT, false>;
+      k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(b, fm);
+      count_launch();
+      if (int st = launch_status()) return st;
+    }
+    return CTR_OK;
+  }
   if (std::is_same<TT, float>::value && a.d == 128 && a.total_rows < 0xffffffffll) {
     if (cudaMemsetAsync((char*)a.err + kWsCounterOffset, 0, sizeof(unsigned long long), s) != cudaSuccess)
       return CTR_ERR_CUDA;
@@ -687,6 +895,23 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
       k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm); count_launch();
     }
     return launch_status();
+  }
+  // narrow rows: the flattened walk with several rows per warp step (CTR_USE_NARROW=0 builds the
+  // one-bag-per-warp kernel below instead, for comparison)
+  if (CTR_USE_NARROW && (chunks == 4 || chunks == 8 || chunks == 16) && a.total_rows < 0xffffffffll) {
+    if (cudaMemsetAsync((char*)a.err + kWsCounterOffset, 0, sizeof(unsigned long long), s) != cudaSuccess)
+      return CTR_ERR_CUDA;
+#define CTR_NARROW(G)                                                                       \
+  {                                                                                         \
+    auto k = a.fm_out ? bag_fwd_narrow_kernel<TT, G, IT, true> : bag_fwd_narrow_kernel<TT, G, IT, false>; \
+    k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm);                      \
+    count_launch();                                                                         \
+    return launch_status();                                                                 \
+  }
+    if (chunks == 4) CTR_NARROW(4)
+    if (chunks == 8) CTR_NARROW(8)
+    CTR_NARROW(16)
+#undef CTR_NARROW
   }
 #define CTR_LAUNCH(LPR, CPL)                                 \
   {                                                          \
@@ -768,6 +993,7 @@ int embedding_bag_fwd(const void* table, ctr_dtype dtype, int32_t d, int64_t tot
   BagArgs a;
   a.table = table;
   a.d = d;
+  a.ld = d;
   a.total_rows = total_rows;
   a.idx = indices;
   a.n_idx = n_indices;
