@@ -864,26 +864,6 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
     k<<<grid, kTmaWarps * 32, smem, s>>>(a, fm, map); count_launch();
     return launch_status();
   }
-#ifndef CTR_GATHER_SLICES
-#define CTR_GATHER_SLICES 1
-#endif
-  if (CTR_GATHER_SLICES > 1 && std::is_same<TT, float>::value && a.d == 128 && !a.fm_out &&
-      a.total_rows < 0xffffffffll) {
-    // column slices of 64 through the narrow walk: each slice's rows take half the L2
-    for (int c0 = 0; c0 < 128; c0 += 64) {
-      BagArgs b = a;
-      b.d = 64;
-      b.table = (const float*)a.table + c0;
-      b.out = a.out_bf16 ? (void*)((__nv_bfloat16*)a.out + c0) : (void*)((float*)a.out + c0);
-      if (cudaMemsetAsync((char*)a.err + kWsCounterOffset, 0, sizeof(unsigned long long), s) != cudaSuccess)
-        return CTR_ERR_CUDA;
-      auto k = bag_fwd_narrow_kernel<TT, 16, IT, false>;
-      k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(b, fm);
-      count_launch();
-      if (int st = launch_status()) return st;
-    }
-    return CTR_OK;
-  }
   if (std::is_same<TT, float>::value && a.d == 128 && a.total_rows < 0xffffffffll) {
     if (cudaMemsetAsync((char*)a.err + kWsCounterOffset, 0, sizeof(unsigned long long), s) != cudaSuccess)
       return CTR_ERR_CUDA;

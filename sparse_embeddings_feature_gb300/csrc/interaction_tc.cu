@@ -13,15 +13,20 @@
 // A and B are the same shared-memory tile (both K-major, 128-byte swizzle),
 // loaded by TMA straight from X viewed as [B*n, d].  The accumulator lives in
 // TMEM (fp32, double-buffered); the epilogue reads the columns of each warp's
-// diagonal blocks with tcgen05.ld, rounds them to bf16 into a shared-memory
-// copy of the tile's Gram matrix, and writes the samples' output rows from it
-// in output order with coalesced stores: the dense pass-through first (first
-// two modes), then the products the mode emits from each diagonal block (the
-// strict lower triangle; or with the diagonal, "DHEN" notes section 3.1; or the
-// whole block, the Gram matrix of "DHEN" notes section 3.3, Eq. (7)).
+// diagonal blocks with tcgen05.ld, rounds the samples' own n x n blocks to
+// bf16 into shared memory (only the diagonal blocks: S n x n values), and
+// writes the samples' output rows from them in output order with coalesced
+// stores: the dense pass-through first (first two modes), then the products
+// the mode emits from each diagonal block (the strict lower triangle; or with
+// the diagonal, "DHEN" notes section 3.1; or the whole block, the Gram matrix
+// of "DHEN" notes section 3.3, Eq. (7)).
 //
-// Roles (persistent CTAs, two per SM where shared memory allows): warp 0 issues TMA loads, warp 1 owns
-// TMEM and issues the MMAs, warps 2..5 run the epilogue.  Every mbarrier wait
+// Roles (persistent CTAs, two per SM where shared memory allows): warp 0
+// issues TMA loads, warp 1 owns TMEM and issues the MMAs, and two epilogue
+// groups of four warps (warps 2..5 and 6..9) take alternate tiles, each with
+// its own TMEM accumulator and shared-memory blocks, so one group's output
+// writes overlap the other's accumulator read-back (with one group the
+// epilogue, about 1.7 us per tile, bounded the kernel).  Every mbarrier wait
 // is bounded by a wall-clock limit; on expiry the kernel records
 // CTR_ERR_TIMEOUT, waits (bounded) for its own copies and MMAs, frees TMEM and
 // returns.
@@ -36,8 +41,9 @@
 namespace ctr {
 namespace {
 
-constexpr int kTcThreads = 192;
-constexpr int kTcEpiWarps = 4;
+constexpr int kTcEpiWarps = 4;                        // warps per epilogue group
+constexpr int kTcEpiGroups = 2;                       // groups, one per TMEM accumulator
+constexpr int kTcThreads = 64 + 32 * kTcEpiWarps * kTcEpiGroups;
 constexpr uint32_t kTmemCols = 256;
 // Shared memory asked for per CTA, at least: more than a third of the SM's
 // 228 KB, so no more than two CTAs (2 x 256 TMEM columns) are ever resident.
@@ -98,17 +104,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 // Named barrier 1 over the 128 epilogue threads, returning the OR of `pred`.
-__device__ __forceinline__ bool epi_any(bool pred) {
+// Named barrier `id` over one epilogue group's 128 threads, returning the OR of `pred`.
+__device__ __forceinline__ bool epi_any(uint32_t id, bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.or.pred p, 1, 128, q;\n\t"
+      "bar.red.or.pred p, %2, 128, q;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)pred)
+      : "r"((uint32_t)pred), "r"(id)
       : "memory");
   return r != 0;
+}
+__device__ __forceinline__ void epi_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(const TcParams p,
@@ -213,15 +223,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (two groups of warps 2..5 and 6..9) ----------------
     // Phase A: each thread (one tile row = one TMEM lane) converts the
-    // accumulator columns of its warp's diagonal blocks to bf16 and stores them
-    // into the shared Gram tile; the tile's dense vectors go to shared memory.
-    // Phase B: the 128 threads write the tile's output rows in output order,
-    // each product read from the Gram tile through the mode's source table.
-    const int q = warp & 3;              // TMEM lane quarter this warp may read
-    const int row = q * 32 + lane;       // tile row = TMEM lane
-    const int tid = threadIdx.x - 64;
+    // accumulator columns of its own sample's diagonal block to bf16 into the
+    // group's shared blocks; the tile's dense vectors go to shared memory.
+    // Phase B: the group's 128 threads write the tile's output rows in output
+    // order, each product read from the blocks through the mode's source table.
+    const int g = (warp - 2) / kTcEpiWarps;  // epilogue group: tiles it = g, g + 2, ...
+    const uint32_t gbar = 1u + (uint32_t)g;  // the group's named barrier
+    const int q = warp & 3;                  // TMEM lane quarter this warp may read
+    const int row = q * 32 + lane;           // tile row = TMEM lane
+    const int tid = threadIdx.x - 64 - g * 32 * kTcEpiWarps;  // 0..127 within the group
     // the accumulator columns this warp's rows need: the diagonal blocks of the
     // samples its 32 rows belong to, read 32 columns at a time (columns past N
     // lie inside the accumulator's 128 and are never read back)
@@ -229,13 +241,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
     const int c_hi = min(p.N, ((q * 32 + 31) / p.n + 1) * p.n);
     const int dd = p.mode != 2 ? p.d : 0;  // dense pass-through width of an output row
     const int dchunks = dd / 8;            // its 16-byte pieces
-    uint16_t* gram = (uint16_t*)(base_ptr + (size_t)p.stages * p.stage_bytes);
-    uint16_t* dsm = gram + (size_t)128 * p.GS;
-    int16_t* ptab = (int16_t*)(dsm + (size_t)p.S * dd);
-    // source of product slot u of a sample, relative to its block's corner:
+    const int nn = p.n * p.n;
+    int16_t* ptab = (int16_t*)(base_ptr + (size_t)p.stages * p.stage_bytes);
+    uint8_t* gsm = base_ptr + (size_t)p.stages * p.stage_bytes + align_up((size_t)(p.W - dd) * 2, 16) +
+                   (size_t)g * p.epi_bytes;
+    uint16_t* blocks = (uint16_t*)gsm;                      // [S][n][n] bf16: sample s, row i, column j
+    uint16_t* dsm = blocks + align_up((size_t)p.S * nn, 8);  // [S][dd] bf16
+    // source of product slot u of a sample, relative to its block:
     //   mode 0: pair (r, j), j < r, at u = r(r-1)/2 + j;  mode 1: j <= r at
     //   u = r(r+1)/2 + j;  mode 2: (u / n, u mod n)
-    for (int u = tid; u < p.W - dd; u += 128) {
+    for (int u = threadIdx.x - 64; u < p.W - dd; u += 32 * kTcEpiWarps * kTcEpiGroups) {
       int r = 0, j = 0;
       if (p.mode == 2) {
         r = u / p.n;
@@ -245,11 +260,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
         while ((r + 1) * (r + 1 + sh) / 2 <= u) ++r;
         j = u - r * (r + sh) / 2;
       }
-      ptab[u] = (int16_t)(r * p.GS + j);
+      ptab[u] = (int16_t)(r * p.n + j);
     }
-    int64_t it = 0;
-    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-      const int acc = (int)(it & 1);
+    epi_sync(3, 32 * kTcEpiWarps * kTcEpiGroups);  // the table is complete for both groups
+    // this thread's sample and row within it (rows past S n hold no sample)
+    const int my_s = row / p.n, my_i = row - my_s * p.n;
+    const bool my_row = row < p.S * p.n;
+    for (int64_t it = g;; it += kTcEpiGroups) {
+      const int64_t t = blockIdx.x + it * (int64_t)gridDim.x;
+      if (t >= ntiles) break;
+      const int acc = (int)(it & 1);  // = g: each group owns one accumulator
       const uint32_t aph = (uint32_t)((it >> 1) & 1);
       const int nvalid = (int)imin64(p.S, p.batch - t * p.S);
       // the tile's dense vectors: the first kDensePre pieces per thread are
@@ -269,25 +289,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
         set_error(p.err, CTR_ERR_TIMEOUT);
         atomicExch(&abort_flag, 1);
       }
-      // one decision for all 128 epilogue threads (also: the Gram tile and the
-      // dense vectors of the previous tile have been written out)
-      if (epi_any(!ok || *(volatile int*)&abort_flag)) break;
+      // one decision for the group's 128 threads (also: the blocks and the
+      // dense vectors of its previous tile have been written out)
+      if (epi_any(gbar, !ok || *(volatile int*)&abort_flag)) break;
       fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * 128u;
-      uint16_t* grow = gram + (size_t)row * p.GS;
+      uint16_t* brow = blocks + (size_t)my_s * nn + (size_t)my_i * p.n;  // this row of its sample's block
+      const int b0 = my_s * p.n;                                       // the block's first column
       for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tbase + (uint32_t)c0, v);
+        if (my_row) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t w[4];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[g * 8 + 2 * h]),
-                                                      __uint_as_float(v[g * 8 + 2 * h + 1]));
-            w[h] = *(uint32_t*)&b2;
+          for (int cc = 0; cc < 32; ++cc) {
+            const int j = c0 + cc - b0;
+            if (j >= 0 && j < p.n) {
+              const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[cc]));
+              brow[j] = *(const uint16_t*)&h;
+            }
           }
-          *(uint4*)(grow + c0 + g * 8) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       fence_before();
@@ -306,18 +326,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
         }
         *(uint4*)(dsm + (size_t)ks * dd + c * 8) = w;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");  // Gram tile and dense vectors complete
+      epi_sync(gbar, 128);  // the blocks and the dense vectors are complete
       // Phase B: output element e of the tile is slot e mod W of sample e / W
       const int elems = nvalid * p.W;
       __nv_bfloat16* dst = p.out + t * p.S * (int64_t)p.W;
-      const int blk = p.n * (p.GS + 1);  // offset between consecutive samples' block corners
       if (((uintptr_t)dst % 8) == 0 && (elems % 4) == 0) {
         for (int e = 4 * tid; e < elems; e += 4 * 128) {
           int ks = e / p.W, u = e - ks * p.W;
           uint32_t h[4];
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
-            h[x] = u < dd ? dsm[ks * dd + u] : gram[ks * blk + ptab[u - dd]];
+            h[x] = u < dd ? dsm[ks * dd + u] : blocks[ks * nn + ptab[u - dd]];
             if (++u == p.W) {
               u = 0;
               ++ks;
@@ -329,7 +348,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
         uint16_t* dst16 = (uint16_t*)dst;
         for (int e = tid; e < elems; e += 128) {
           const int ks = e / p.W, u = e - ks * p.W;
-          dst16[e] = u < dd ? dsm[ks * dd + u] : gram[ks * blk + ptab[u - dd]];
+          dst16[e] = u < dd ? dsm[ks * dd + u] : blocks[ks * nn + ptab[u - dd]];
         }
       }
     }
@@ -363,12 +382,11 @@ int interaction_bf16_tc(const void* X, int32_t batch, int32_t n, int32_t d, int 
   p.stages = std::max(2, std::min(4, (int)((160 * 1024) / p.stage_bytes)));
   p.mode = mode;
   p.W = mode == 0 ? d + n * (n - 1) / 2 : (mode == 1 ? d + n * (n + 1) / 2 : n * n);
-  // epilogue shared memory: the Gram tile (128 rows of GS bf16: every 32-column
-  // window that is read back, plus 8 columns against bank conflicts), the
-  // dense vectors, the product source table
-  p.GS = (p.N + 31) / 32 * 32 + 8;
+  // epilogue shared memory: the product source table (shared), then per group
+  // the samples' diagonal blocks (S n x n bf16) and dense vectors (S x d bf16)
+  p.GS = n;
   const int dd = mode != 2 ? d : 0;
-  p.epi_bytes = (uint32_t)((size_t)128 * p.GS * 2 + (size_t)p.S * dd * 2 + align_up((size_t)(p.W - dd) * 2, 16));
+  p.epi_bytes = (uint32_t)align_up((align_up((size_t)p.S * n * n, 8) + (size_t)p.S * dd) * 2, 16);
   p.X = (const __nv_bfloat16*)X;
   p.out = (__nv_bfloat16*)out;
   p.err = err;
@@ -385,7 +403,8 @@ int interaction_bf16_tc(const void* X, int32_t batch, int32_t n, int32_t d, int 
   // Two CTAs per SM where they fit: each holds kTmemCols of the SM's 512 TMEM
   // columns, and the shared memory asked for keeps a third off the SM (its
   // allocation would wait for one of the two to exit).
-  const size_t need = 1024 + (size_t)p.stages * p.stage_bytes + p.epi_bytes;
+  const size_t need = 1024 + (size_t)p.stages * p.stage_bytes + align_up((size_t)(p.W - dd) * 2, 16) +
+                      (size_t)kTcEpiGroups * p.epi_bytes;
   const size_t smem = std::max(need, (size_t)kTcSmemFloor);
   auto kern = interaction_bf16_tc_kernel;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
