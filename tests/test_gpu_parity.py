@@ -145,6 +145,42 @@ def test_dedup_bitmap_path(name):
         assert_dedup_equal(got, ref)
 
 
+def test_dedup_permuted_tables_and_empty_fields():
+    # fields read tables in another order (the outputs follow table order), one field
+    # has only empty bags, and one field's IDs span many sort tiles with a ragged tail
+    rng = np.random.default_rng(21)
+    F, B = 5, 3000
+    rows = [4000, 90, 1, 70_000, 600]
+    b2t = np.array([3, 0, 4, 1, 2], dtype=np.int32)
+    rb = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    lens = rng.integers(0, 9, size=F * B)
+    lens[2 * B:3 * B] = 0                              # field 2 (table 4) has no IDs
+    ids, offsets = _csr(lens, rng, [rows[t] for t in b2t], B)
+    assert sum(rows) <= 64 * ids.size
+    ref = O.dedup(ids, offsets, F, B, b2t, rb)
+    for with_pos in (True, False):
+        st, got = gpu_dedup(ids, offsets, F, B, b2t, rb, with_pos=with_pos)
+        assert st == 0, ctr.status_string(st)
+        assert_dedup_equal(got, ref)
+
+
+def test_dedup_table_with_more_than_2_20_distinct_rows():
+    # one table with about 2.1M distinct rows in the batch (22-bit ranks within the table)
+    rng = np.random.default_rng(22)
+    F, B, rows = 2, 1_500_000, [1 << 22, 1000]
+    lens = np.concatenate([np.full(B, 2), rng.integers(0, 3, size=B)]).astype(np.int64)
+    offsets = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    ids = np.concatenate([rng.integers(0, rows[0], size=2 * B), rng.integers(0, rows[1], size=int(lens[B:].sum()))])
+    b2t = np.array([0, 1], dtype=np.int32)
+    rb = np.array([0, rows[0], rows[0] + rows[1]], dtype=np.int64)
+    assert sum(rows) <= 64 * ids.size
+    ref = O.dedup(ids, offsets, F, B, b2t, rb)
+    assert ref["unique_offsets"][1] - ref["unique_offsets"][0] > (1 << 20)
+    st, got = gpu_dedup(ids, offsets, F, B, b2t, rb, with_pos=False)
+    assert st == 0, ctr.status_string(st)
+    assert_dedup_equal(got, ref)
+
+
 def test_dedup_edge_cases():
     rng = np.random.default_rng(0)
     # (F, B, rows per table, bag lengths builder)
