@@ -1056,8 +1056,57 @@ __global__ void __launch_bounds__(kTileThreads, OPT == CTR_OPT_SGD ? CTR_TILE_AS
   }
 }
 
-// One CTA per long run: warps sum fixed contiguous segments of its partials,
-// then a fixed pairwise tree over the warps, then the row update.
+// Long runs of at most kCombWarpPieces pieces (most of them: a run of up to
+// 4096 occurrences) are finished by one warp each, summing the run's partials
+// in order with several loads in flight, then updating the row; no block
+// barrier.  Longer runs (the Zipf head) take a CTA each (combine_long_kernel).
+constexpr int kCombWarpPieces = 32;
+__global__ void __launch_bounds__(256) combine_short_kernel(const BwdArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int chunks = a.d / 4;
+  const int64_t nl = imin64(*a.long_count, a.max_long);
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < nl; i += nwarps) {
+    const int64_t u = a.long_list[i];
+    int64_t r0, r1;
+    run_bounds(a, u, r0, r1);
+    const int64_t pcs = ceil_div(r1 - r0, kPiece);
+    if (pcs > kCombWarpPieces) continue;  // warp-uniform: a CTA finishes it
+    const int64_t p0 = a.long_pstart[i];
+    const int64_t row = a.unique_rows[u];
+    if (row < 0 || row >= a.total_rows) {
+      if (lane == 0) set_error(a.err, CTR_ERR_INDEX_OUT_OF_RANGE);
+      continue;
+    }
+    for (int ch = lane; ch < chunks; ch += 32) {
+      float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      int64_t q = 0;
+      for (; q + 4 <= pcs; q += 4) {  // four loads in flight, summed in order
+        const float4 x0 = ldg_f4(a.partial + (p0 + q) * a.d + ch * 4);
+        const float4 x1 = ldg_f4(a.partial + (p0 + q + 1) * a.d + ch * 4);
+        const float4 x2 = ldg_f4(a.partial + (p0 + q + 2) * a.d + ch * 4);
+        const float4 x3 = ldg_f4(a.partial + (p0 + q + 3) * a.d + ch * 4);
+        s4 = fma4(x0, 1.f, s4);
+        s4 = fma4(x1, 1.f, s4);
+        s4 = fma4(x2, 1.f, s4);
+        s4 = fma4(x3, 1.f, s4);
+      }
+      for (; q < pcs; ++q) s4 = fma4(ldg_f4(a.partial + (p0 + q) * a.d + ch * 4), 1.f, s4);
+      float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+      uint2 wb = make_uint2(0u, 0u);
+      if (a.opt != CTR_OPT_ROWWISE_ADAGRAD) {
+        load_row_chunk(a, row, ch, w, wb);
+        store_row_chunk(a, row, u, ch, s4, w, wb, 0, 0.f);
+      }
+    }
+  }
+}
+
+// One CTA per long run of more than kCombWarpPieces pieces (all long runs for
+// row-wise Adagrad, whose row state needs the whole row): its 8 warps sum
+// fixed contiguous segments of its partials, then a fixed pairwise tree over
+// the warps (3 levels), then the row update.  (CTAs of 32 warps shorten the
+// longest runs' chains but fit one per SM: 0.28 against 0.13 ms.)
 __global__ void __launch_bounds__(kCombThreads) combine_long_kernel(const BwdArgs a) {
   constexpr int W = kCombThreads / 32;
   extern __shared__ float sm[];  // [W][d]
@@ -1069,6 +1118,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_long_kernel(const BwdArg
     int64_t r0, r1;
     run_bounds(a, u, r0, r1);
     const int64_t pcs = ceil_div(r1 - r0, kPiece);
+    if (pcs <= kCombWarpPieces && a.opt != CTR_OPT_ROWWISE_ADAGRAD) continue;  // block-uniform: a warp finished it
     const int64_t p0 = a.long_pstart[i];
     const int64_t seg = ceil_div(pcs, W);
     const int64_t q0 = imin64(pcs, warp * seg), q1 = imin64(pcs, q0 + seg);
@@ -1270,11 +1320,23 @@ int launch_long(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
 
 int launch_finish(const BwdArgs& a, cudaStream_t s) {
   const size_t csmem = (size_t)(kCombThreads / 32) * a.d * sizeof(float);
+  if (csmem > 48 * 1024 &&
+      cudaFuncSetAttribute(combine_long_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem) != cudaSuccess)
+    return CTR_ERR_CUDA;
   // one CTA per long run in flight, as many as fit (each run is a short latency chain)
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_long_kernel, kCombThreads, csmem) != cudaSuccess)
     per_sm = 2;
   const int64_t cgrid = imin64(std::max<int64_t>(a.max_long, 1), (int64_t)std::max(per_sm, 1) * num_sms());
+  if (a.opt != CTR_OPT_ROWWISE_ADAGRAD) {
+    int per_sm_w = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_w, combine_short_kernel, 256, 0) != cudaSuccess)
+      per_sm_w = 4;
+    const int64_t wgrid = imin64(std::max<int64_t>(ceil_div(a.max_long, (int64_t)8), 1),
+                                 (int64_t)std::max(per_sm_w, 1) * num_sms());
+    combine_short_kernel<<<(unsigned)wgrid, 256, 0, s>>>(a); count_launch();
+    if (int st = launch_status()) return st;
+  }
   combine_long_kernel<<<(unsigned)cgrid, kCombThreads, csmem, s>>>(a); count_launch();
   return launch_status();
 }

@@ -88,17 +88,18 @@ def bf16_close(got_bits, ref_bits, mag=None, depth=0, rtol=1e-2, atol=0.0, what=
 
 # Reduction depth of the row-update kernels for a run of L occurrences: runs
 # of at most 128 are summed by one warp (L terms, any order: depth L); longer
-# runs are cut into pieces of 128 summed in order, each of the 8 warps of the
-# combine sums ceil(pieces / 8) consecutive partials in order, and a pairwise
-# tree joins the 8 warps (3 levels).
-SHORT_RUN, PIECE, COMBINE_WARPS = 128, 128, 8
+# runs are cut into pieces of 128 summed in order; a run of at most 32 pieces
+# is finished by one warp summing its partials in order (depth 128 + pieces);
+# a longer one by 8 warps each summing ceil(pieces / 8) consecutive partials
+# in order, joined by a pairwise tree (3 levels).
+SHORT_RUN, PIECE, COMBINE_WARPS, WARP_PIECES = 128, 128, 8, 32
 
 
 def bwd_depth(run_len):
     L = np.asarray(run_len, dtype=np.int64)
     pieces = -(-L // PIECE)
-    long_depth = PIECE + (-(-pieces // COMBINE_WARPS)) + int(np.log2(COMBINE_WARPS))
-    return np.where(L <= SHORT_RUN, L, long_depth)
+    cta_depth = PIECE + (-(-pieces // COMBINE_WARPS)) + int(np.log2(COMBINE_WARPS))
+    return np.where(L <= SHORT_RUN, L, np.where(pieces <= WARP_PIECES, PIECE + pieces, cta_depth))
 
 
 def pool_depth(offsets, num_fields, batch):
