@@ -66,6 +66,8 @@ __device__ __forceinline__ void store_out(void* out, int64_t off, const float* v
     float* o = (float*)out + off;
     if (vec_ok && n == 4) {
       *(float4*)o = make_float4(v[0], v[1], v[2], v[3]);
+    } else if (vec_ok && n == 2) {
+      *(float2*)o = make_float2(v[0], v[1]);
     } else if (vec_ok && n == 8) {
       ((float4*)o)[0] = make_float4(v[0], v[1], v[2], v[3]);
       ((float4*)o)[1] = make_float4(v[4], v[5], v[6], v[7]);
@@ -86,6 +88,8 @@ __device__ __forceinline__ void store_out(void* out, int64_t off, const float* v
       __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]);
       __nv_bfloat162 p1 = __floats2bfloat162_rn(v[2], v[3]);
       *(uint2*)o = make_uint2(*(uint32_t*)&p0, *(uint32_t*)&p1);
+    } else if (vec_ok && n == 2) {
+      *(__nv_bfloat162*)o = __floats2bfloat162_rn(v[0], v[1]);
     } else {
       for (int i = 0; i < n; ++i) o[i] = __float2bfloat16_rn(v[i]);
     }
@@ -445,8 +449,13 @@ __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kerne
 // across bag and chunk boundaries (so a bag end never drains the pipeline, and
 // short bags cost no more than long ones).  Each group sums the occurrences it
 // takes of the open bag; when the bag closes, the groups' partials are added
-// by a fixed butterfly and group 0 stores the row.  Every bag's summation
-// order depends only on the bag lengths, so results are deterministic.  With
+// in a fixed tree: a reduce-scatter where each lane's V columns split evenly
+// over the groups (each group then divides, for a mean, and stores its share
+// of the row: fewer shuffles, adds and divisions than a butterfly), else a
+// butterfly after which group 0 stores the row.  A step in which no bag closes
+// (told by the chunk's bag-end mask, the same for the whole warp) only adds
+// its rows.  Every bag's summation order depends only on the bag lengths, so
+// results are deterministic.  With
 // FM, each lane also sums the squares of its columns of the rows it takes; at
 // a bag's close both sums are reduced the same way and lane 0 stores
 // 1/2 (|sum v|^2 - sum |v|^2) (exactly 0 for a one-ID bag: both terms then
@@ -471,6 +480,13 @@ constexpr int kNarrowWin = CTR_NARROW_WIN;
 #ifndef CTR_NARROW_MERGE
 #define CTR_NARROW_MERGE 0
 #endif
+#ifndef CTR_NARROW_FAST
+#define CTR_NARROW_FAST 1
+#endif
+#ifndef CTR_NARROW_SCATTER
+#define CTR_NARROW_SCATTER 1
+#endif
+constexpr bool kNarrowFast = CTR_NARROW_FAST;
 
 // Merge the repeats of (bag, row) among a chunk's occurrences: returns this
 // occurrence's weight (the group's size for its first occurrence, 0 for the
@@ -495,6 +511,13 @@ __global__ void __launch_bounds__(kBagThreads, CTR_NARROW_MINB) bag_fwd_narrow_k
   constexpr int V = Vec<TT>::kN;  // elements per 16-byte chunk
   constexpr int NG = 32 / G;      // rows per warp step
   constexpr int STEPS = 32 / NG;  // steps per chunk of 32 occurrences
+  constexpr unsigned kStepMask = (1u << NG) - 1u;  // a step's occurrences in a chunk's masks
+  static_assert(STEPS % kNarrowWin == 0, "the load window must divide a chunk's steps");
+  // without FM, a closing bag's sums are reduce-scattered over the groups (each group divides and
+  // stores V / NG of each lane's columns) where the columns split evenly; else summed by a
+  // butterfly into every group and stored by group 0
+  constexpr bool kScatter = !FM && (V % NG == 0) && CTR_NARROW_SCATTER;
+  constexpr int VG = kScatter ? V / NG : V;
   const int lane = threadIdx.x & 31;
   const int grp = lane / G, sub = lane % G;
   const int64_t nbags = (int64_t)a.F * a.B;
@@ -566,9 +589,19 @@ __global__ void __launch_bounds__(kBagThreads, CTR_NARROW_MINB) bag_fwd_narrow_k
           const uint32_t r = __shfl_sync(kFull, tn < 32 ? cur.row : nxt.row, tn & 31);
           buf[j] = (r != kNoRow) ? ldg16(table + (uint64_t)r * a.ld) : make_uint4(0u, 0u, 0u, 0u);
           if (c0 + q * NG >= total) continue;  // warp-uniform: past the block's last occurrence
+          const float wt = CTR_NARROW_MERGE ? __shfl_sync(kFull, cur_w, t) : 1.f;  // 0: a merged repeat
+          if (kNarrowFast && ((cur.lastm >> (q * NG)) & kStepMask) == 0 && c0 + (q + 1) * NG <= total) {
+            // no bag closes in this step and all its occurrences exist: they all belong to the open bag
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[v] = CTR_NARROW_MERGE ? fmaf(x[v], wt, acc[v]) : acc[v] + x[v];
+            if (FM) {
+#pragma unroll
+              for (int v = 0; v < V; ++v) sq = fmaf(x[v], x[v] * wt, sq);
+            }
+            continue;
+          }
           const bool valid = c0 + t < total;
           const int sg = __shfl_sync(kFull, cur.seg, t);
-          const float wt = __shfl_sync(kFull, cur_w, t);  // 0 for a merged repeat (its row loaded nothing)
           const bool last = valid && ((cur.lastm >> t) & 1u);
           // the open bag is group 0's (occurrences are in bag order); close every bag that
           // ends in this step, in order, then keep the one that continues
@@ -576,13 +609,44 @@ __global__ void __launch_bounds__(kBagThreads, CTR_NARROW_MINB) bag_fwd_narrow_k
           while (true) {
             if (valid && sg == open) {
 #pragma unroll
-              for (int v = 0; v < V; ++v) acc[v] = fmaf(x[v], wt, acc[v]);
+              for (int v = 0; v < V; ++v) acc[v] = CTR_NARROW_MERGE ? fmaf(x[v], wt, acc[v]) : acc[v] + x[v];
               if (FM) {
 #pragma unroll
                 for (int v = 0; v < V; ++v) sq = fmaf(x[v], x[v] * wt, sq);
               }
             }
             if (!__any_sync(kFull, valid && sg == open && last)) break;  // the open bag continues
+            const float lj = __shfl_sync(kFull, lenf, open);
+            const int64_t oj = __shfl_sync(kFull, ooff, open);
+            if constexpr (kScatter) {
+              // reduce-scatter over the groups, lowest group bit first (the pairs the
+              // butterfly below adds, in the same order, so both give the same bits): at each
+              // level a lane sends the half of its live columns that its partner keeps and
+              // adds the partner's copy of the half it keeps; each group ends with VG of each
+              // lane's V columns, starting at column `coff`
+              int coff = 0;
+#pragma unroll
+              for (int o = G, h = V / 2; o < 32; o <<= 1, h >>= 1) {
+                const bool hi = (grp & (o / G)) != 0;
+#pragma unroll
+                for (int i = 0; i < h; ++i) {
+                  const float send = hi ? acc[i] : acc[h + i];
+                  const float keep = hi ? acc[h + i] : acc[i];
+                  acc[i] = keep + __shfl_xor_sync(kFull, send, o);
+                }
+                if (hi) coff += h;
+              }
+              float out[VG];
+#pragma unroll
+              for (int v = 0; v < VG; ++v) out[v] = a.mean ? acc[v] / lj : acc[v];
+              store_out(a.out, oj + (int64_t)sub * V + coff, out, VG, a.out_bf16, a.vec_out);
+#pragma unroll
+              for (int v = 0; v < V; ++v) acc[v] = 0.f;
+              const unsigned later = __ballot_sync(kFull, valid && sg > open);
+              if (!later) break;  // the bag closed at this step's last occurrence
+              open = __shfl_sync(kFull, sg, __ffs(later) - 1);
+              continue;
+            }
 #pragma unroll
             for (int o = G; o < 32; o <<= 1) {
 #pragma unroll
@@ -601,8 +665,6 @@ __global__ void __launch_bounds__(kBagThreads, CTR_NARROW_MINB) bag_fwd_narrow_k
               if (lane == 0) a.fm_out[blk * 32 + open] = 0.5f * (s2 - sq);
               sq = 0.f;
             }
-            const float lj = __shfl_sync(kFull, lenf, open);
-            const int64_t oj = __shfl_sync(kFull, ooff, open);
             if (grp == 0) {  // a closed bag is never empty
               float out[V];
 #pragma unroll

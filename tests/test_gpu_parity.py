@@ -303,7 +303,8 @@ def test_embedding_bag_fwd_configs(name):
 @pytest.mark.parametrize("d,dtype,pool", [(12, "f32", "sum"), (20, "f32", "mean"), (32, "f32", "sum"),
                                           (64, "f32", "mean"), (256, "f32", "sum"), (512, "f32", "sum"),
                                           (8, "bf16", "sum"), (16, "bf16", "mean"), (128, "bf16", "sum"),
-                                          (36, "bf16", "mean")])
+                                          (36, "bf16", "mean"), (16, "f32", "mean"), (32, "bf16", "mean"),
+                                          (64, "bf16", "sum")])
 def test_embedding_bag_fwd_shapes(d, dtype, pool):
     cfg = W.CONFIGS["dlrm_fp32"].shrink(batch=97, num_fields=5, field_to_table=(0, 1, 2, 3, 4),
                                         rows_per_table=(1000, 1, 50, 70_000, 9), d=d, dtype=dtype, pool=pool,
@@ -314,6 +315,44 @@ def test_embedding_bag_fwd_shapes(d, dtype, pool):
     ref, mag = O.embedding_bag_fwd(w["ids"], w["offsets"], cfg.num_fields, cfg.batch, w["bag_to_table"],
                                    w["row_base"], d, pool=pool, dtype=dtype, gen=_gen(cfg), with_mag=True)
     depth = pool_depth(w["offsets"], cfg.num_fields, cfg.batch)
+    if dtype == "f32":
+        f32_close(got, ref, mag, depth, what=f"d={d}")
+    else:
+        bf16_close(got, ref, mag, depth, atol=1e-5, what=f"d={d}")
+
+
+@pytest.mark.parametrize("d,dtype,pool", [(16, "f32", "mean"), (32, "f32", "mean"), (64, "f32", "sum"),
+                                          (32, "bf16", "mean"), (64, "bf16", "sum"), (128, "bf16", "mean")])
+def test_embedding_bag_fwd_narrow_rows_unaligned_output(d, dtype, pool):
+    """Rows of 4, 8 and 16 chunks of 16 bytes (several rows per warp step) written
+    through an output whose row stride is odd, so no 16-byte vector store applies:
+    the same bits as the aligned output, and the oracle's values."""
+    cfg = W.CONFIGS["dlrm_fp32"].shrink(batch=131, num_fields=6, field_to_table=(0, 1, 2, 3, 4, 2),
+                                        rows_per_table=(3000, 1, 70_000, 17, 500), d=d, dtype=dtype, pool=pool,
+                                        table_init=("uniform", 0.5) if dtype == "f32" else ("normal4", 0.1),
+                                        bag_len=("uniform", 0, 70))
+    w = W.make_workload(cfg, with_grads=False)
+    F, B = cfg.num_fields, cfg.batch
+    aligned = _fwd_case(cfg, w)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    tab = torch.empty((cfg.total_rows, d), dtype=tdt, device=DEV)
+    ctr.ctr_fill_table(tab, d, 0, cfg.fill_kind, cfg.fill_seed, cfg.fill_scale)
+    sb = F * d + 1
+    out = torch.full((B * sb,), float("nan"), dtype=tdt, device=DEV)
+    ws = ctr.workspace(ctr.ctr_embedding_bag_workspace_size())
+    cpool = ctr.POOL_MEAN if pool == "mean" else ctr.POOL_SUM
+    ctr.ctr_embedding_bag_fwd(tab, d, _t(w["ids"]), _t(w["offsets"]), F, B, w["bag_to_table"], w["row_base"], cpool,
+                              out, sb, d, ws)
+    assert ctr.ctr_check_status(ws) == 0
+    got = _np(out).reshape(B, sb)
+    untouched = _np(torch.full((B,), float("nan"), dtype=tdt))
+    np.testing.assert_array_equal(got[:, -1].view(np.uint32 if dtype == "f32" else np.uint16),
+                                  untouched.view(np.uint32 if dtype == "f32" else np.uint16))  # the gap column
+    got = got[:, :F * d].reshape(B, F, d)
+    np.testing.assert_array_equal(got, aligned)
+    ref, mag = O.embedding_bag_fwd(w["ids"], w["offsets"], F, B, w["bag_to_table"], w["row_base"], d, pool=pool,
+                                   dtype=dtype, gen=_gen(cfg), with_mag=True)
+    depth = pool_depth(w["offsets"], F, B)
     if dtype == "f32":
         f32_close(got, ref, mag, depth, what=f"d={d}")
     else:
