@@ -52,6 +52,7 @@ constexpr int kDensePre = 2;  // dense-vector pieces per epilogue thread loaded 
 
 struct TcParams {
   int32_t batch, n, d, S, rows, N, kb, stages, W, mode, GS;
+  int32_t aligned;  // 1: every sample at a 32-row boundary of the tile (17 <= n <= 32)
   uint32_t stage_bytes, tx_bytes, epi_bytes;
   const __nv_bfloat16* X;
   __nv_bfloat16* out;
@@ -177,7 +178,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
         mbar_expect_tx(full0 + 8 * s, p.tx_bytes);
         const uint32_t dst = base + (uint32_t)s * p.stage_bytes;
         const int32_t row0 = (int32_t)(t * p.S * p.n);
-        for (int kb = 0; kb < p.kb; ++kb) tma_load_2d(dst + kb * 16384u, &map, kb * 64, row0, full0 + 8 * s);
+        for (int kb = 0; kb < p.kb; ++kb) {
+          if (p.aligned) {  // one 32-row box per sample (rows past the sample's n are never read back)
+            for (int q = 0; q < 4; ++q)
+              tma_load_2d(dst + kb * 16384u + q * 4096u, &map, kb * 64, row0 + q * p.n, full0 + 8 * s);
+          } else {
+            tma_load_2d(dst + kb * 16384u, &map, kb * 64, row0, full0 + 8 * s);
+          }
+        }
       }
       // drain: every issued load must have landed before the CTA can exit
       const int64_t issued = it;
@@ -241,11 +249,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
     const int c_hi = min(p.N, ((q * 32 + 31) / p.n + 1) * p.n);
     const int dd = p.mode != 2 ? p.d : 0;  // dense pass-through width of an output row
     const int dchunks = dd / 8;            // its 16-byte pieces
-    const int nn = p.n * p.n;
+    const int nn = p.aligned ? 32 * 32 : p.n * p.n;  // a sample's block in shared memory
     int16_t* ptab = (int16_t*)(base_ptr + (size_t)p.stages * p.stage_bytes);
     uint8_t* gsm = base_ptr + (size_t)p.stages * p.stage_bytes + align_up((size_t)(p.W - dd) * 2, 16) +
                    (size_t)g * p.epi_bytes;
-    uint16_t* blocks = (uint16_t*)gsm;                      // [S][n][n] bf16: sample s, row i, column j
+    // [S][n][n] bf16 (sample s, row i, column j); aligned: [S][32][32], the
+    // 16-byte pieces of row i rotated by (i / 2) mod 4 so the rows' vector
+    // stores spread over the banks
+    uint16_t* blocks = (uint16_t*)gsm;
     uint16_t* dsm = blocks + align_up((size_t)p.S * nn, 8);  // [S][dd] bf16
     // source of product slot u of a sample, relative to its block:
     //   mode 0: pair (r, j), j < r, at u = r(r-1)/2 + j;  mode 1: j <= r at
@@ -260,7 +271,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
         while ((r + 1) * (r + 1 + sh) / 2 <= u) ++r;
         j = u - r * (r + sh) / 2;
       }
-      ptab[u] = (int16_t)(r * p.n + j);
+      ptab[u] = (int16_t)(p.aligned ? r * 32 + ((((j >> 3) ^ (r >> 1)) & 3) << 3) + (j & 7) : r * p.n + j);
     }
     epi_sync(3, 32 * kTcEpiWarps * kTcEpiGroups);  // the table is complete for both groups
     // this thread's sample and row within it (rows past S n hold no sample)
@@ -294,9 +305,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) interaction_bf16_tc_kernel(cons
       if (epi_any(gbar, !ok || *(volatile int*)&abort_flag)) break;
       fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * 128u;
+      if (p.aligned) {
+        // warp q holds sample q's rows, and its block is accumulator columns 32q .. 32q + 31:
+        // one read, then the row as four 16-byte stores
+        uint32_t v[32];
+        tmem_ld32(tbase + (uint32_t)(q * 32), v);
+        if (q < nvalid && lane < p.n) {
+          uint4* brow4 = (uint4*)(blocks + (size_t)q * nn + (size_t)lane * 32);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const __nv_bfloat162 h2 =
+                  __floats2bfloat162_rn(__uint_as_float(v[8 * c + 2 * k]), __uint_as_float(v[8 * c + 2 * k + 1]));
+              w[k] = *(const uint32_t*)&h2;
+            }
+            brow4[c ^ ((lane >> 1) & 3)] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
       uint16_t* brow = blocks + (size_t)my_s * nn + (size_t)my_i * p.n;  // this row of its sample's block
       const int b0 = my_s * p.n;                                       // the block's first column
-      for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+      for (int c0 = c_lo; c0 < (p.aligned ? c_lo : c_hi); c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tbase + (uint32_t)c0, v);
         if (my_row) {
@@ -373,8 +404,12 @@ int interaction_bf16_tc(const void* X, int32_t batch, int32_t n, int32_t d, int 
   p.batch = batch;
   p.n = n;
   p.d = d;
-  p.S = 128 / n;
-  p.rows = p.S * n;
+  // 17 <= n <= 32: four samples per tile, each at a 32-row boundary, so each
+  // epilogue warp's TMEM lanes are one sample and its block one aligned
+  // 32-column read; else S = floor(128 / n) samples packed back to back
+  p.aligned = n >= 17 ? 1 : 0;
+  p.S = p.aligned ? 4 : 128 / n;
+  p.rows = p.aligned ? 128 : p.S * n;
   p.N = (p.rows + 15) / 16 * 16;
   p.kb = d / 64;
   p.stage_bytes = 16384u * p.kb;
@@ -386,7 +421,8 @@ int interaction_bf16_tc(const void* X, int32_t batch, int32_t n, int32_t d, int 
   // the samples' diagonal blocks (S n x n bf16) and dense vectors (S x d bf16)
   p.GS = n;
   const int dd = mode != 2 ? d : 0;
-  p.epi_bytes = (uint32_t)align_up((align_up((size_t)p.S * n * n, 8) + (size_t)p.S * dd) * 2, 16);
+  const size_t block_elems = p.aligned ? (size_t)32 * 32 : (size_t)n * n;
+  p.epi_bytes = (uint32_t)align_up((align_up((size_t)p.S * block_elems, 8) + (size_t)p.S * dd) * 2, 16);
   p.X = (const __nv_bfloat16*)X;
   p.out = (__nv_bfloat16*)out;
   p.err = err;
@@ -394,7 +430,7 @@ int interaction_bf16_tc(const void* X, int32_t batch, int32_t n, int32_t d, int 
   CUtensorMap map;
   cuuint64_t gdim[2] = {(cuuint64_t)d, (cuuint64_t)batch * n};
   cuuint64_t gstride[1] = {(cuuint64_t)d * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)p.rows};
+  cuuint32_t box[2] = {64, (cuuint32_t)(p.aligned ? 32 : p.rows)};
   cuuint32_t estride[2] = {1, 1};
   if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), gdim, gstride, box, estride,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -427,7 +427,7 @@ def _rand_X(B, n, d, dtype, seed):
 @pytest.mark.parametrize("B,n,d,dtype", [(1001, 27, 128, "f32"), (64, 5, 16, "f32"), (33, 9, 40, "f32"),
                                          (1001, 27, 64, "bf16"), (257, 5, 64, "bf16"), (130, 32, 128, "bf16"),
                                          (77, 2, 256, "bf16"), (40, 16, 192, "bf16"), (50, 27, 48, "bf16"),
-                                         (3, 27, 64, "bf16")])
+                                         (3, 27, 64, "bf16"), (515, 17, 256, "bf16"), (129, 20, 64, "bf16")])
 def test_dot_interaction(B, n, d, dtype):
     X = _rand_X(B, n, d, dtype, seed=B + n + d)
     Xd = _t(X.view(np.int16) if dtype == "bf16" else X)
@@ -792,7 +792,8 @@ MODES = {"cross": ctr.INTERACT_CROSS, "with_self": ctr.INTERACT_WITH_SELF, "full
 
 @pytest.mark.parametrize("mode", list(MODES))
 @pytest.mark.parametrize("B,n,d,dtype", [(1001, 27, 128, "f32"), (33, 9, 40, "f32"), (1001, 27, 64, "bf16"),
-                                         (130, 32, 128, "bf16"), (77, 2, 256, "bf16"), (50, 27, 48, "bf16")])
+                                         (130, 32, 128, "bf16"), (77, 2, 256, "bf16"), (50, 27, 48, "bf16"),
+                                         (129, 20, 64, "bf16"), (6, 17, 192, "bf16")])
 def test_dot_interaction_modes(mode, B, n, d, dtype):
     X = _rand_X(B, n, d, dtype, seed=B + n + d + 7)
     Xd = _t(X.view(np.int16) if dtype == "bf16" else X)
