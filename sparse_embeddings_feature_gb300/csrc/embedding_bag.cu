@@ -999,6 +999,44 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const char* __restrict
   }
 }
 
+// Rows of G 16-byte chunks (G = 1..32, a power of two): a group of G lanes
+// copies one row and the 32 / G groups of a warp take consecutive uniques, with
+// kRowSteps such steps in flight per warp (their row indices, then their rows,
+// are loaded before any is stored), so short rows keep every lane and many
+// loads busy instead of one row per warp at a time.
+constexpr int kRowSteps = 4;
+template <int G>
+__global__ void __launch_bounds__(256) gather_rows_grouped_kernel(const char* __restrict__ table, int64_t row_bytes,
+                                                                  int64_t total_rows,
+                                                                  const int64_t* __restrict__ unique_rows,
+                                                                  const int64_t* __restrict__ n_unique,
+                                                                  int64_t capacity, char* __restrict__ U, int* err) {
+  constexpr int RPW = 32 / G;  // rows per warp step
+  const int lane = threadIdx.x & 31, grp = lane / G, sub = lane % G;
+  const int64_t n = imin64(*n_unique, capacity);
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  for (int64_t u0 = w0 * (RPW * kRowSteps); u0 < n; u0 += nwarps * (RPW * kRowSteps)) {
+    int64_t r[kRowSteps];
+#pragma unroll
+    for (int k = 0; k < kRowSteps; ++k) {
+      const int64_t u = u0 + k * RPW + grp;
+      r[k] = u < n ? unique_rows[u] : -1;
+      if (u < n && (r[k] < 0 || r[k] >= total_rows)) {
+        set_error(err, CTR_ERR_INDEX_OUT_OF_RANGE);
+        r[k] = -1;
+      }
+    }
+    uint4 v[kRowSteps];
+#pragma unroll
+    for (int k = 0; k < kRowSteps; ++k)
+      v[k] = r[k] >= 0 ? ldg16(table + r[k] * row_bytes + sub * 16) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int k = 0; k < kRowSteps; ++k)
+      if (r[k] >= 0) *(uint4*)(U + (u0 + k * RPW + grp) * row_bytes + sub * 16) = v[k];
+  }
+}
+
 }  // namespace
 }  // namespace ctr
 
@@ -1101,10 +1139,27 @@ extern "C" int ctr_gather_rows(const void* table, ctr_dtype dtype, int32_t d, in
   if (capacity == 0) return CTR_OK;
   const int64_t row_bytes = (int64_t)d * (dtype == CTR_F32 ? 4 : 2);
   if (row_bytes % 16 == 0 && (((uintptr_t)table | (uintptr_t)U) % 16) != 0) return CTR_ERR_INVALID_ARG;
-  int64_t blocks = imin64(ceil_div(capacity, 8), (int64_t)num_sms() * 16);
+  const int64_t chunks = row_bytes / 16;
+  const bool grouped = row_bytes % 16 == 0 && chunks <= 32 && (chunks & (chunks - 1)) == 0;
   timing_mark(CTR_KERNEL_GATHER_ROWS, true, (cudaStream_t)stream);
-  gather_rows_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
-      (const char*)table, row_bytes, total_rows, unique_rows, n_unique, capacity, (char*)U, (int*)ws); count_launch();
+  if (grouped) {
+    // a full wave of 8 blocks per SM; each warp step covers 32 / chunks uniques
+    const int64_t per_block = (int64_t)8 * (32 / chunks) * kRowSteps;
+    const int64_t blocks = std::max<int64_t>(1, imin64(ceil_div(capacity, per_block), (int64_t)num_sms() * 8));
+    auto k = chunks == 1    ? gather_rows_grouped_kernel<1>
+             : chunks == 2  ? gather_rows_grouped_kernel<2>
+             : chunks == 4  ? gather_rows_grouped_kernel<4>
+             : chunks == 8  ? gather_rows_grouped_kernel<8>
+             : chunks == 16 ? gather_rows_grouped_kernel<16>
+                            : gather_rows_grouped_kernel<32>;
+    k<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>((const char*)table, row_bytes, total_rows, unique_rows,
+                                                         n_unique, capacity, (char*)U, (int*)ws);
+  } else {
+    const int64_t blocks = imin64(ceil_div(capacity, 8), (int64_t)num_sms() * 16);
+    gather_rows_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
+        (const char*)table, row_bytes, total_rows, unique_rows, n_unique, capacity, (char*)U, (int*)ws);
+  }
+  count_launch();
   timing_mark(CTR_KERNEL_GATHER_ROWS, false, (cudaStream_t)stream);
   return launch_status();
 }

@@ -386,6 +386,29 @@ def test_embedding_bag_fwd_exact_and_int32_unique_path():
     np.testing.assert_array_equal(_np(out), ref)
 
 
+@pytest.mark.parametrize("d,dtype", [(8, "bf16"), (16, "f32"), (32, "f32"), (64, "f32"), (128, "f32"),
+                                     (256, "bf16"), (24, "bf16"), (3, "f32"), (160, "f32")])
+def test_gather_rows_copies_the_unique_rows(d, dtype):
+    """The batch-sized matrix of the unique rows: row k of U is table row
+    unique_rows[k] for k < n_unique, bit for bit, and the rows past n_unique are
+    not written (rows of 1 to 32 chunks of 16 bytes, and other widths)."""
+    rng = np.random.default_rng(d)
+    rows = 5000
+    table = rng.standard_normal((rows, d)).astype(np.float32)
+    tab = _t(table) if dtype == "f32" else _t(table).to(torch.bfloat16)
+    cap = 1300
+    nu = 1237                                                        # ragged against every warp step
+    uq = np.sort(rng.choice(rows, size=cap, replace=False)).astype(np.int64)
+    U = torch.full((cap, d), float("nan"), dtype=tab.dtype, device=DEV)
+    ws = ctr.workspace(256)
+    ctr.ctr_gather_rows(tab, d, _t(uq), torch.tensor([nu], dtype=torch.int64, device=DEV), U, ws)
+    assert ctr.ctr_check_status(ws) == 0
+    got, want = _np(U), _np(tab)
+    np.testing.assert_array_equal(got[:nu], want[uq[:nu]])
+    nan_bits = _np(torch.full((cap - nu, d), float("nan"), dtype=tab.dtype))
+    np.testing.assert_array_equal(got[nu:].view(nan_bits.dtype), nan_bits)
+
+
 def test_embedding_bag_fwd_strided_into_interaction_slots():
     cfg = FWD_CASES["full_step_b128"]
     w = W.make_workload(cfg, with_grads=False)
