@@ -120,15 +120,18 @@ int ctr_set_tma_gather(int on);
  * that path.  Process-wide, read at each launch; returns the previous limit. */
 uint64_t ctr_set_wait_limit_ns(uint64_t ns);
 
-/* Short-run pass of the row update for fp32 rows of d = 128 under plain SGD
- * (no optimizer state, no stochastic rounding): mode 2 processes the short
- * runs in two 64-column slices, two occurrences per warp step, so the pooled-
- * gradient rows of one table take half the L2 space; mode 1 never slices; 0
- * (the default) slices when one table's pooled-gradient rows (batch x 512
- * bytes) exceed 32 MB.  Every mode gives a deterministic result within the
- * same summation bound (each run's sum order is fixed; the sliced pass adds
- * the run's even and odd positions separately, then the two partials).
- * Process-wide; returns the previous mode (a mode outside 0..2 selects 0). */
+/* Short-run pass of the row update for fp32 rows under plain SGD (no
+ * optimizer state, no stochastic rounding) of d = 128, or of d <= 64 with d a
+ * multiple of 4: mode 2 processes the short runs in slices of at most 64
+ * columns (two for d = 128, one for d <= 64), two occurrences per warp step,
+ * so the pooled-gradient rows of one table take half the L2 space at d = 128
+ * and narrow rows keep twice the lanes busy; mode 1 never does; 0 (the
+ * default) does for d <= 64 always, and for d = 128 when one table's
+ * pooled-gradient rows (batch x 512 bytes) exceed 32 MB.  Every mode gives a
+ * deterministic result within the same summation bound (each run's sum order
+ * is fixed; the sliced pass adds the run's even and odd positions separately,
+ * then the two partials).  Process-wide; returns the previous mode (a mode
+ * outside 0..2 selects 0). */
 int ctr_set_tile_slices(int mode);
 
 /* ------------------------------------------------------------------------ */

@@ -631,6 +631,12 @@ __device__ __forceinline__ uint32_t bag_g4(const BwdArgs& a, int32_t bag, float&
 #endif
 constexpr int kPieceWin = CTR_PIECE_WIN;
 static_assert(32 % kPieceWin == 0, "the load window must divide the chunk");
+#ifndef CTR_PIECE_L1
+#define CTR_PIECE_L1 0  // 1: gradient rows of the pieces not allocated in L1
+#endif
+__device__ __forceinline__ float4 ld_piece_g(const float* p, uint64_t pol) {
+  return CTR_PIECE_L1 ? ldg_f4_policy_na(p, pol) : ldg_f4_policy(p, pol);
+}
 __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(const BwdArgs a) {
   const int lane = threadIdx.x & 31;
   const bool col = lane * 4 < a.d;  // this lane's 16-byte column exists
@@ -653,7 +659,7 @@ __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(c
 #pragma unroll
     for (int u = 0; u < kPieceWin; ++u) {
       const uint32_t r = __shfl_sync(kFull, cur, u);
-      buf[u] = (r != kNoG && col) ? ldg_f4_policy(Gl + (uint64_t)r * 4, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+      buf[u] = (r != kNoG && col) ? ld_piece_g(Gl + (uint64_t)r * 4, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c0 = 0; c0 < n; c0 += 32) {
@@ -667,7 +673,7 @@ __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(c
           const float4 x = buf[j];
           const int tn = t + kPieceWin;
           const uint32_t r = __shfl_sync(kFull, tn < 32 ? cur : nxt, tn & 31);
-          buf[j] = (r != kNoG && col) ? ldg_f4_policy(Gl + (uint64_t)r * 4, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+          buf[j] = (r != kNoG && col) ? ld_piece_g(Gl + (uint64_t)r * 4, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
           if (a.mean) acc = fma4(x, __shfl_sync(kFull, sc_cur, t), acc);
           else acc = make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
         }
@@ -677,6 +683,70 @@ __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(c
       bag_b = bag_c;
     }
     if (col) *(float4*)(a.partial + p * a.d + lane * 4) = acc;
+  }
+}
+
+// The same pieces for rows of at most 64 columns: a group of G lanes (one per
+// 16-byte column, G = 4, 8 or 16) takes every (32 / G)-th occurrence of the
+// piece, so narrow rows keep every lane and more loads busy; each group sums
+// its occurrences in order and the groups' partials are added by a fixed
+// butterfly (depth at most 128 / (32 / G) + log2(32 / G)).
+template <int G>
+__global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_grouped_kernel(const BwdArgs a) {
+  constexpr int NG = 32 / G;     // occurrences per warp step
+  constexpr int STEPS = 32 / NG;  // steps per chunk of 32 occurrences
+  static_assert(STEPS % kPieceWin == 0, "the load window must divide a chunk's steps");
+  const int lane = threadIdx.x & 31, grp = lane / G, sub = lane % G;
+  const bool col = sub * 4 < a.d;
+  const float* Gl = a.G + sub * 4;
+  const uint64_t pol_keep = g_policy();
+  const int64_t np = *a.pieces_total;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t p = next_unit(a.work + 1); p < np; p = next_unit(a.work + 1)) {
+    const int64_t i = a.piece_owner[p];
+    int64_t r0, r1;
+    run_bounds(a, a.long_list[i], r0, r1);
+    const int64_t k = p - (int64_t)a.long_pstart[i];
+    const int32_t* sb = a.sorted_bag + r0 + k * kPiece;
+    const int n = (int)imin64(kPiece, r1 - (r0 + k * kPiece));
+    int32_t bag_b = (32 + lane < n) ? sb[32 + lane] : -1;
+    float sc_cur;
+    uint32_t cur = bag_g4(a, (lane < n) ? sb[lane] : -1, sc_cur);
+    float4 buf[kPieceWin];
+#pragma unroll
+    for (int u = 0; u < kPieceWin; ++u) {
+      const uint32_t r = __shfl_sync(kFull, cur, u * NG + grp);
+      buf[u] = (r != kNoG && col) ? ldg_f4_policy(Gl + (uint64_t)r * 4, pol_keep) : zero;
+    }
+    float4 acc = zero;
+    for (int c0 = 0; c0 < n; c0 += 32) {
+      const int32_t bag_c = (c0 + 64 + lane < n) ? sb[c0 + 64 + lane] : -1;
+      float sc_nxt;
+      const uint32_t nxt = bag_g4(a, bag_b, sc_nxt);
+      for (int g = 0; g < STEPS; g += kPieceWin) {
+#pragma unroll
+        for (int j = 0; j < kPieceWin; ++j) {
+          const int t = (g + j) * NG + grp;  // this group's occurrence in the chunk
+          const float4 x = buf[j];
+          const int tn = t + kPieceWin * NG;
+          const uint32_t r = __shfl_sync(kFull, tn < 32 ? cur : nxt, tn & 31);
+          buf[j] = (r != kNoG && col) ? ldg_f4_policy(Gl + (uint64_t)r * 4, pol_keep) : zero;
+          if (a.mean) acc = fma4(x, __shfl_sync(kFull, sc_cur, t), acc);
+          else acc = make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
+        }
+      }
+      cur = nxt;
+      sc_cur = sc_nxt;
+      bag_b = bag_c;
+    }
+#pragma unroll
+    for (int o = G; o < 32; o <<= 1) {
+      acc.x += __shfl_xor_sync(kFull, acc.x, o);
+      acc.y += __shfl_xor_sync(kFull, acc.y, o);
+      acc.z += __shfl_xor_sync(kFull, acc.z, o);
+      acc.w += __shfl_xor_sync(kFull, acc.w, o);
+    }
+    if (grp == 0 && col) *(float4*)(a.partial + p * a.d + sub * 4) = acc;
   }
 }
 
@@ -1207,18 +1277,22 @@ int grid_of(K kernel, int threads, size_t smem, int64_t want) {
 }
 
 // Short runs of fp32 rows under SGD in column slices (bwd_tiles_pair_kernel):
-// 0 = automatic (when one table's pooled-gradient rows, batch x 512 bytes at
-// d = 128, exceed 32 MB and would not stay in L2), 1 = never, 2 = always where
-// supported.  Process-wide (ctr_set_tile_slices).
+// 0 = automatic (rows of at most 64 columns always; d = 128 when one table's
+// pooled-gradient rows, batch x 512 bytes, exceed 32 MB and would not stay in
+// L2), 1 = never, 2 = always where supported.  Process-wide
+// (ctr_set_tile_slices).
 std::atomic<int> g_tile_slices{0};
 constexpr int64_t kSliceGradBytes = (int64_t)32 << 20;
 
 bool use_pair_slices(const BwdArgs& a) {
-  if (a.opt != CTR_OPT_SGD || a.sr || a.bf16 || !a.g4_ok || a.d != 128) return false;
+  if (a.opt != CTR_OPT_SGD || a.sr || a.bf16 || !a.g4_ok) return false;
+  if (a.d != 128 && !(a.d <= 64 && a.d % 4 == 0)) return false;
   const int mode = g_tile_slices.load();
   if (mode == 1) return false;
   if (mode == 2) return true;
-  return (int64_t)a.B * a.d * 4 > kSliceGradBytes;
+  // rows of at most 64 columns are one slice: two occurrences per warp step
+  // keep twice the lanes of the plain kernel busy
+  return a.d <= 64 || (int64_t)a.B * a.d * 4 > kSliceGradBytes;
 }
 
 // The short-run pass: the tile kernel once, or the pair kernel once per
@@ -1229,7 +1303,7 @@ int launch_tiles(const BwdArgs& a, K tk, size_t tile_smem, cudaStream_t s, int64
     auto pk = a.mean ? bwd_tiles_pair_kernel<true> : bwd_tiles_pair_kernel<false>;
     for (int c0 = 0; c0 < a.d; c0 += 64) {
       BwdArgs b = a;
-      b.d = 64;
+      b.d = std::min(64, a.d - c0);
       b.ld = a.d;
       b.table = (float*)a.table + c0;
       b.G = a.G + c0;
@@ -1307,7 +1381,11 @@ int launch_long(const BwdArgs& a, WsCarver& c, cudaStream_t s, int64_t n) {
   expand_long_kernel<<<std::max(1, num_sms() * 2), 256, 0, s>>>(a); count_launch();
   if (int st = launch_status()) return st;
   timing_mark(CTR_KERNEL_BWD_PIECES, true, s);
-  if (CPL == 1 && a.g4_ok) {
+  if (CPL == 1 && a.g4_ok && a.d <= 64) {
+    auto pk = a.d <= 16 ? long_pieces_grouped_kernel<4>
+              : a.d <= 32 ? long_pieces_grouped_kernel<8> : long_pieces_grouped_kernel<16>;
+    pk<<<grid_of(pk, 256, 0, ceil_div(sizes(n).max_pieces, 8)), 256, 0, s>>>(a); count_launch();
+  } else if (CPL == 1 && a.g4_ok) {
     auto pk = long_pieces_stream_kernel;
     pk<<<grid_of(pk, 256, 0, ceil_div(sizes(n).max_pieces, 8)), 256, 0, s>>>(a); count_launch();
   } else {

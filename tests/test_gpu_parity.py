@@ -572,13 +572,14 @@ def tile_slices():
 
 
 @pytest.mark.parametrize("mode", [1, 2])
-def test_bwd_update_exact_arithmetic_d128_sliced_and_plain(mode, tile_slices):
-    # fp32 d = 128 under SGD: mode 2 forces the pair kernel (two 64-column slices, two
+@pytest.mark.parametrize("d", [128, 64, 32, 20, 4])
+def test_bwd_update_exact_arithmetic_sliced_and_plain(mode, d, tile_slices):
+    # fp32 rows under SGD: mode 2 forces the pair kernel (slices of at most 64 columns, two
     # occurrences per warp step), mode 1 the plain tile kernel; dyadic inputs make every
     # sum exact, so both must equal the oracle bit for bit, long runs and ragged tiles included
     tile_slices(mode)
-    rng = np.random.default_rng(12 + mode)
-    F, B, d = 3, 901, 128
+    rng = np.random.default_rng(12 + mode + d)
+    F, B = 3, 901
     rows = [37, 5, 4000]
     lens = rng.integers(0, 9, size=F * B)
     lens[B:B + 30] = 300                               # long runs in field 1
