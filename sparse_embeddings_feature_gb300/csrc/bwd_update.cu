@@ -631,12 +631,7 @@ __device__ __forceinline__ uint32_t bag_g4(const BwdArgs& a, int32_t bag, float&
 #endif
 constexpr int kPieceWin = CTR_PIECE_WIN;
 static_assert(32 % kPieceWin == 0, "the load window must divide the chunk");
-#ifndef CTR_PIECE_L1
-#define CTR_PIECE_L1 0  // 1: gradient rows of the pieces not allocated in L1
-#endif
-__device__ __forceinline__ float4 ld_piece_g(const float* p, uint64_t pol) {
-  return CTR_PIECE_L1 ? ldg_f4_policy_na(p, pol) : ldg_f4_policy(p, pol);
-}
+
 __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(const BwdArgs a) {
   const int lane = threadIdx.x & 31;
   const bool col = lane * 4 < a.d;  // this lane's 16-byte column exists
@@ -659,7 +654,7 @@ __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(c
 #pragma unroll
     for (int u = 0; u < kPieceWin; ++u) {
       const uint32_t r = __shfl_sync(kFull, cur, u);
-      buf[u] = (r != kNoG && col) ? ld_piece_g(Gl + (uint64_t)r * 4, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+      buf[u] = (r != kNoG && col) ? ldg_f4_policy(Gl + (uint64_t)r * 4, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c0 = 0; c0 < n; c0 += 32) {
@@ -673,7 +668,7 @@ __global__ void __launch_bounds__(256, CTR_BWD_MINB) long_pieces_stream_kernel(c
           const float4 x = buf[j];
           const int tn = t + kPieceWin;
           const uint32_t r = __shfl_sync(kFull, tn < 32 ? cur : nxt, tn & 31);
-          buf[j] = (r != kNoG && col) ? ld_piece_g(Gl + (uint64_t)r * 4, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
+          buf[j] = (r != kNoG && col) ? ldg_f4_policy(Gl + (uint64_t)r * 4, pol_keep) : make_float4(0.f, 0.f, 0.f, 0.f);
           if (a.mean) acc = fma4(x, __shfl_sync(kFull, sc_cur, t), acc);
           else acc = make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
         }

@@ -137,14 +137,6 @@ __device__ __forceinline__ float4 ldg_f4_policy(const float* p, uint64_t pol) {
                : "l"(p), "l"(pol));
   return r;
 }
-// The same load, not allocated in L1 (for rows no other warp of the SM reads soon).
-__device__ __forceinline__ float4 ldg_f4_policy_na(const float* p, uint64_t pol) {
-  float4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
-               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
-               : "l"(p), "l"(pol));
-  return r;
-}
 __device__ __forceinline__ void stg_f4_policy(float* p, float4 v, uint64_t pol) {
   asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
                "f"(v.w), "l"(pol)

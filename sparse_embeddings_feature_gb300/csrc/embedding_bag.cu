@@ -240,7 +240,12 @@ __global__ void __launch_bounds__(kBagThreads, CPL == 1 ? CTR_BAG_MINB : 1) bag_
 // budget is sized for: 2 loads at 8 blocks per SM (32 registers).  Alone the
 // kernel is within 2% of 8 loads at 4 blocks, and in the full training step,
 // where the dedup runs beside it on a side stream, the step is 0.9% faster
-// (measured twice); 8 loads at 3 blocks was 10% slower alone.
+// (measured twice); 8 loads at 3 blocks was 10% slower alone.  A small batch
+// gives too few 32-bag blocks to fill the GPU (DLRM's 2048 samples: 1664
+// warps): there each warp's chain of row loads is the bound, and 8 loads at 2
+// blocks per SM gathered 0.140 -> 0.097 ms (4 at 4: 0.116 ms).
+constexpr int kWinSmall = 8, kMinbSmall = 2;
+constexpr int64_t kSmallGridBlocks = 64;  // 32-bag blocks per SM below which the deeper window is used
 #ifndef CTR_FLAT_WIN
 #define CTR_FLAT_WIN 2
 #endif
@@ -338,10 +343,10 @@ __device__ __forceinline__ FlatChunk flat_chunk(const BagArgs& a, int kr, IT id,
 // With FM, each lane also sums the squares of its columns of the rows, and at a
 // bag's last occurrence the warp reduces |sum v|^2 and sum |v|^2 of the bag
 // and stores 1/2 (|sum v|^2 - sum |v|^2).
-template <typename IT, bool FM>
-__global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kernel(const BagArgs a,
+template <typename IT, bool FM, int WIN = kWinF, int MINB = CTR_FLAT_MINB>
+__global__ void __launch_bounds__(kBagThreads, MINB) bag_fwd_flat_kernel(const BagArgs a,
                                                                       const __grid_constant__ FieldMap fm) {
-  static_assert(32 % kWinF == 0, "the load window must divide the chunk");
+  static_assert(32 % WIN == 0, "the load window must divide the chunk");
   const int lane = threadIdx.x & 31;
   const int64_t nbags = (int64_t)a.F * a.B;
   const int64_t nblk = ceil_div(nbags, 32);
@@ -386,9 +391,9 @@ __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kerne
     const IT* ib = idx + S0;
     IT id_b = (32 + lane < total) ? ld_id(ib + 32 + lane, pol_stream) : IT(0);
     FlatChunk cur = flat_chunk(a, lane, (lane < total) ? ld_id(ib + lane, pol_stream) : IT(0), rel0, rel1, base, nrows);
-    float4 buf[kWinF];
+    float4 buf[WIN];
 #pragma unroll
-    for (int u = 0; u < kWinF; ++u) {
+    for (int u = 0; u < WIN; ++u) {
       const uint32_t r = __shfl_sync(kFull, cur.row, u);
       buf[u] = (r != kNoRow) ? ld_row16(table + (uint64_t)r * 128, pol_rows) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -397,12 +402,12 @@ __global__ void __launch_bounds__(kBagThreads, CTR_FLAT_MINB) bag_fwd_flat_kerne
     for (int c0 = 0; c0 < total; c0 += 32) {
       const IT id_c = (c0 + 64 + lane < total) ? ld_id(ib + c0 + 64 + lane, pol_stream) : IT(0);
       const FlatChunk nxt = flat_chunk(a, c0 + 32 + lane, id_b, rel0, rel1, base, nrows);
-      for (int g = 0; g < 32; g += kWinF) {
+      for (int g = 0; g < 32; g += WIN) {
 #pragma unroll
-        for (int j = 0; j < kWinF; ++j) {
+        for (int j = 0; j < WIN; ++j) {
           const int t = g + j;
           const float4 x = buf[j];
-          const int tn = t + kWinF;  // refill the slot with occurrence tn
+          const int tn = t + WIN;  // refill the slot with occurrence tn
           const uint32_t r = __shfl_sync(kFull, tn < 32 ? cur.row : nxt.row, tn & 31);
           buf[j] = (r != kNoRow) ? ld_row16(table + (uint64_t)r * 128, pol_rows) : make_float4(0.f, 0.f, 0.f, 0.f);
           acc = add4_packed(acc, x);
@@ -929,13 +934,10 @@ int launch_bag_fwd(const BagArgs& a, const FieldMap& fm, cudaStream_t s) {
   if (std::is_same<TT, float>::value && a.d == 128 && a.total_rows < 0xffffffffll) {
     if (cudaMemsetAsync((char*)a.err + kWsCounterOffset, 0, sizeof(unsigned long long), s) != cudaSuccess)
       return CTR_ERR_CUDA;
-    if (a.fm_out) {
-      auto k = bag_fwd_flat_kernel<IT, true>;
-      k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm); count_launch();
-    } else {
-      auto k = bag_fwd_flat_kernel<IT, false>;
-      k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm); count_launch();
-    }
+    const bool small = ceil_div(nbags, 32) < kSmallGridBlocks * num_sms();
+    auto k = a.fm_out ? (small ? bag_fwd_flat_kernel<IT, true, kWinSmall, kMinbSmall> : bag_fwd_flat_kernel<IT, true>)
+                      : (small ? bag_fwd_flat_kernel<IT, false, kWinSmall, kMinbSmall> : bag_fwd_flat_kernel<IT, false>);
+    k<<<grid_for(k, ceil_div(nbags, 32)), kBagThreads, 0, s>>>(a, fm); count_launch();
     return launch_status();
   }
   // narrow rows: the flattened walk with several rows per warp step (CTR_USE_NARROW=0 builds the
