@@ -191,6 +191,26 @@ int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num_fields, in
               int64_t* unique_rows, int64_t* n_unique, int32_t* inverse, int32_t* sorted_pos, int32_t* sorted_bag,
               int32_t* run_offsets, int64_t* unique_offsets, void* ws, size_t ws_bytes, ctr_stream_t stream);
 
+/* The same dedup in two parts, so a caller can schedule the other work of a
+ * step between them.  CTR_DEDUP_PREPARE launches everything before the radix
+ * passes (the keys, and on the presence-bitmap path the bitmap, unique_rows,
+ * n_unique, unique_offsets and inverse); CTR_DEDUP_SORT launches the radix
+ * passes and what follows them (sorted_pos, sorted_bag, run_offsets, and on
+ * the path that sorts the rows themselves the unique outputs too).
+ * CTR_DEDUP_ALL = both = ctr_dedup.  A SORT call must follow the PREPARE call
+ * in stream order (or behind an event), with the same arguments and the same
+ * workspace, which carries the state between them; outputs a part does not
+ * write are undefined until the other part has run.  Errors as ctr_dedup;
+ * CTR_ERR_INVALID_ARG for a phase mask outside 1..3. */
+#define CTR_DEDUP_PREPARE 1
+#define CTR_DEDUP_SORT 2
+#define CTR_DEDUP_ALL 3
+int ctr_dedup_phases(const int64_t* ids, const int64_t* offsets, int32_t num_fields, int32_t batch,
+                     const int32_t* bag_to_table, const int64_t* row_base, int32_t num_tables, int64_t n_ids,
+                     int64_t* unique_rows, int64_t* n_unique, int32_t* inverse, int32_t* sorted_pos,
+                     int32_t* sorted_bag, int32_t* run_offsets, int64_t* unique_offsets, int32_t phases, void* ws,
+                     size_t ws_bytes, ctr_stream_t stream);
+
 /* TensorNet's batch-sized matrix (same passage): U[u] = table[unique_rows[u]]
  * for u < *n_unique.  capacity (host) bounds n_unique; rows of U at or beyond
  * n_unique are left untouched.  U is [capacity, d] of the table's dtype. */

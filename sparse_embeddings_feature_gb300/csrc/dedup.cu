@@ -38,7 +38,13 @@ namespace {
 
 constexpr int kRsThreads = 256;
 constexpr int kRsWarps = kRsThreads / 32;
-constexpr int kRsItems = 16;                      // keys per lane per tile
+#ifndef CTR_RS_ITEMS
+#define CTR_RS_ITEMS 16
+#endif
+#ifndef CTR_RS_MINB
+#define CTR_RS_MINB 1
+#endif
+constexpr int kRsItems = CTR_RS_ITEMS;            // keys per lane per tile
 constexpr int kRsTile = kRsThreads * kRsItems;    // 4096 keys
 constexpr int kRsWarpKeys = 32 * kRsItems;        // 512 keys per warp
 constexpr int kMaxBits = 8;                       // digit width limit (256 buckets)
@@ -137,16 +143,19 @@ std::atomic<uint64_t> g_lookback_limit_ns{1000000000ull};
 // wall-clock limit, after which the block records CTR_ERR_TIMEOUT and keeps
 // its writes inside the output.  vals_in == nullptr means the values are
 // the positions 0..n-1 (first pass).
-__global__ void __launch_bounds__(kRsThreads) onesweep_kernel(
+__global__ void __launch_bounds__(kRsThreads, CTR_RS_MINB) onesweep_kernel(
     const uint32_t* __restrict__ keys_in, const int32_t* __restrict__ vals_in, uint32_t* __restrict__ keys_out,
     int32_t* __restrict__ vals_out, int64_t n, int shift, int nbits, const PassPlan* __restrict__ dplan, int pass,
     int32_t* __restrict__ vals_final, const uint32_t* __restrict__ g_hist, uint64_t* __restrict__ lookback,
-    uint32_t* __restrict__ tile_counter, int* err, uint64_t limit_ns) {
+    uint32_t* __restrict__ tile_counter, int* err, uint64_t limit_ns, int32_t* __restrict__ run_offsets,
+    const int64_t* __restrict__ n_unique) {
+  bool runs = false;  // this pass also writes the run starts (and not the sorted keys)
   if (dplan) {  // digit plan decided on the device (rank keys): passes beyond it do nothing
     if (pass >= dplan->passes) return;
     shift = dplan->shift[pass];
     nbits = dplan->bits[pass];
     if (pass == dplan->passes - 1 && vals_final) vals_out = vals_final;
+    runs = run_offsets != nullptr && pass == dplan->passes - 1;
   }
   __shared__ uint32_t wcnt[kRsWarps][kMaxDigits];
   __shared__ uint32_t tile_start[kMaxDigits];
@@ -265,13 +274,28 @@ __global__ void __launch_bounds__(kRsThreads) onesweep_kernel(
   }
   __syncthreads();
   const int count = min(kRsTile, n32 - tile_base);
+  const int64_t nu = runs ? *n_unique : 0;
   for (int i = threadIdx.x; i < count; i += kRsThreads) {
     const uint32_t k = skeys[i];
     const uint32_t d = digit_of(k, shift, mask);
     const uint32_t dest = glob_start[d] + (uint32_t)i - tile_start[d];
     if (dest < (uint32_t)n32) {  // always true unless a look-back timed out
-      keys_out[dest] = k;
       vals_out[dest] = svals[i];
+      if (!runs) {
+        keys_out[dest] = k;
+      } else if ((int64_t)k >= nu) {  // only after an error that left key slots unwritten
+        set_error(err, CTR_ERR_BAD_OFFSETS);
+      } else if (i > (int)tile_start[d]) {
+        // the element before it in the output is the one before it in this tile's
+        // digit group: a run starts here iff the keys differ
+        if (skeys[i - 1] != k) run_offsets[k] = (int32_t)dest;
+      } else {
+        // first of its digit group in this tile: the element before it was written by
+        // an earlier tile, so every such candidate is offered and the smallest kept (the
+        // starts were set to 0xffffffff when the ranks were assigned)
+        atomicMin((unsigned int*)(run_offsets + k), dest);
+      }
+      if (runs && dest == (uint32_t)n32 - 1) run_offsets[nu] = n32;
     }
   }
 }
@@ -529,7 +553,8 @@ __global__ void __launch_bounds__(256) bitmap_count_kernel(const uint32_t* __res
 // the set bits in order.
 __global__ void __launch_bounds__(256) bitmap_pack_kernel(const uint32_t* __restrict__ bitmap, int64_t W,
                                                           const uint32_t* __restrict__ bscan,
-                                                          uint2* __restrict__ pk, int64_t* __restrict__ unique_rows) {
+                                                          uint2* __restrict__ pk, int64_t* __restrict__ unique_rows,
+                                                          int32_t* __restrict__ run_starts) {
   __shared__ uint32_t warp_tot[8];
   constexpr int kPer = kBmWords / 256;
   const int64_t w0 = (int64_t)blockIdx.x * kBmWords + threadIdx.x * kPer;
@@ -547,7 +572,10 @@ __global__ void __launch_bounds__(256) bitmap_pack_kernel(const uint32_t* __rest
     if (w >= W) break;
     uint32_t r = base + v[j];
     pk[w] = make_uint2(b[j], r);
-    for (uint32_t bits = b[j]; bits; bits &= bits - 1) unique_rows[r++] = w * 32 + (__ffs(bits) - 1);
+    for (uint32_t bits = b[j]; bits; bits &= bits - 1) {
+      if (run_starts) run_starts[r] = -1;  // the last radix pass keeps the smallest start offered
+      unique_rows[r++] = w * 32 + (__ffs(bits) - 1);
+    }
   }
 }
 
@@ -781,7 +809,7 @@ void clear_words(uint64_t* p, int64_t words, cudaStream_t s) {
 int dedup_bitmap(const int64_t* ids, const int64_t* offsets, int32_t F, int32_t B, const FieldMap& fm,
                  const TableBases& tb, int64_t total_rows, int64_t n_ids, int64_t* unique_rows, int64_t* n_unique,
                  int32_t* inverse, int32_t* sorted_pos, int32_t* sorted_bag, int32_t* run_offsets,
-                 int64_t* unique_offsets, void* ws, size_t ws_bytes, cudaStream_t s) {
+                 int64_t* unique_offsets, int phases, void* ws, size_t ws_bytes, cudaStream_t s) {
   int* err = (int*)ws;
   WsCarver c(ws, ws_bytes);
   const int64_t tiles = ceil_div(n_ids, kRsTile);
@@ -808,6 +836,9 @@ int dedup_bitmap(const int64_t* ids, const int64_t* offsets, int32_t F, int32_t 
   // the sort carries positions only when the caller asks for them; otherwise
   // it carries bags, and its last pass writes the grouped bags in place
   const bool pos = sorted_pos != nullptr;
+  // without positions to carry, the last radix pass writes the run starts itself
+  const bool fused_runs = run_offsets != nullptr && !pos;
+  if (phases & CTR_DEDUP_PREPARE) {
   clear_words(state, sw + ceil_div(W, (int64_t)2), s);
   if (int st = launch_status()) return st;
   bitmap_keys_kernel<<<(unsigned)key_blocks, 256, 0, s>>>(ids, offsets, F, B, n_ids, fm, keys[1], vals[0],
@@ -820,7 +851,8 @@ int dedup_bitmap(const int64_t* ids, const int64_t* offsets, int32_t F, int32_t 
     WsCarver scan_ws = c;
     if (int st = scan_exclusive<uint32_t>(bsum, bsum, nblk, nullptr, total, scan_ws, s)) return st;
   }
-  bitmap_pack_kernel<<<(unsigned)nblk, 256, 0, s>>>(bitmap, W, bsum, pk, unique_rows); count_launch();
+  bitmap_pack_kernel<<<(unsigned)nblk, 256, 0, s>>>(bitmap, W, bsum, pk, unique_rows,
+                                                    fused_runs ? run_offsets : nullptr); count_launch();
   if (int st = launch_status()) return st;
   bitmap_plan_kernel<<<1, 256, 0, s>>>(total, n_unique, tb, total_rows, pk, unique_offsets, dplan); count_launch();
   if (int st = launch_status()) return st;
@@ -840,6 +872,9 @@ int dedup_bitmap(const int64_t* ids, const int64_t* offsets, int32_t F, int32_t 
     count_launch();
     if (int st = launch_status()) return st;
   }
+  }  // prepare
+  if (!(phases & CTR_DEDUP_SORT)) return CTR_OK;
+  uint32_t* ranks = inverse ? (uint32_t*)inverse : keys[0];
   int32_t* vals_final = pos ? sorted_pos : sorted_bag;
   const int max_passes = (key_bits(imin64(n_ids, total_rows)) + kMaxBits - 1) / kMaxBits;
   timing_mark(CTR_KERNEL_SORT, true, s);
@@ -848,12 +883,13 @@ int dedup_bitmap(const int64_t* ids, const int64_t* offsets, int32_t F, int32_t 
                                                            vals[(p + 1) & 1], n_ids, 0, 0, dplan, p, vals_final,
                                                            g_hist + p * kMaxDigits,
                                                            lookback + (int64_t)p * tiles * kMaxDigits,
-                                                           tile_counter + p, err, g_lookback_limit_ns.load());
+                                                           tile_counter + p, err, g_lookback_limit_ns.load(),
+                                                           fused_runs ? run_offsets : nullptr, n_unique);
     count_launch();
     if (int st = launch_status()) return st;
   }
   timing_mark(CTR_KERNEL_SORT, false, s);
-  if (run_offsets || (pos && sorted_bag)) {
+  if ((run_offsets && !fused_runs) || (pos && sorted_bag)) {
     const int64_t blocks = std::max<int64_t>(1, imin64(ceil_div(n_ids, 1024), (int64_t)sms * 8));
     runs_kernel<<<(unsigned)blocks, 256, 0, s>>>(keys[0], keys[1], dplan, n_ids, n_unique, run_offsets, sorted_pos,
                                                  bag_of, pos ? sorted_bag : nullptr, err); count_launch();
@@ -881,7 +917,19 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
                          int64_t* unique_rows, int64_t* n_unique, int32_t* inverse, int32_t* sorted_pos,
                          int32_t* sorted_bag, int32_t* run_offsets, int64_t* unique_offsets, void* ws,
                          size_t ws_bytes, ctr_stream_t stream) {
+  return ctr_dedup_phases(ids, offsets, num_fields, batch, bag_to_table, row_base, num_tables, n_ids, unique_rows,
+                          n_unique, inverse, sorted_pos, sorted_bag, run_offsets, unique_offsets, CTR_DEDUP_ALL, ws,
+                          ws_bytes, stream);
+}
+
+extern "C" int ctr_dedup_phases(const int64_t* ids, const int64_t* offsets, int32_t num_fields, int32_t batch,
+                                const int32_t* bag_to_table, const int64_t* row_base, int32_t num_tables,
+                                int64_t n_ids, int64_t* unique_rows, int64_t* n_unique, int32_t* inverse,
+                                int32_t* sorted_pos, int32_t* sorted_bag, int32_t* run_offsets,
+                                int64_t* unique_offsets, int32_t phases, void* ws, size_t ws_bytes,
+                                ctr_stream_t stream) {
   cudaStream_t s = (cudaStream_t)stream;
+  if (phases < CTR_DEDUP_PREPARE || phases > CTR_DEDUP_ALL) return CTR_ERR_INVALID_ARG;
   if (!offsets || !bag_to_table || !row_base || !unique_rows || !n_unique) return CTR_ERR_INVALID_ARG;
   if (num_fields <= 0 || batch <= 0 || num_tables <= 0) return CTR_ERR_INVALID_ARG;
   if (num_fields > CTR_MAX_FIELDS || num_tables > CTR_MAX_TABLES) return CTR_ERR_UNSUPPORTED;
@@ -907,13 +955,15 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
   for (int t = 0; t <= num_tables; ++t) tb.row_base[t] = row_base[t];
 
   if (n_ids == 0) {
-    dedup_empty_kernel<<<1, 1, 0, s>>>(n_unique, run_offsets, unique_offsets, num_tables); count_launch();
+    if (phases & CTR_DEDUP_PREPARE) {
+      dedup_empty_kernel<<<1, 1, 0, s>>>(n_unique, run_offsets, unique_offsets, num_tables); count_launch();
+    }
     return launch_status();
   }
 
   if (use_bitmap(n_ids, total_rows))
     return dedup_bitmap(ids, offsets, num_fields, batch, fm, tb, total_rows, n_ids, unique_rows, n_unique, inverse,
-                        sorted_pos, sorted_bag, run_offsets, unique_offsets, ws, ws_bytes, s);
+                        sorted_pos, sorted_bag, run_offsets, unique_offsets, phases, ws, ws_bytes, s);
 
   WsCarver c(ws, ws_bytes);
   const int64_t tiles = ceil_div(n_ids, kRsTile);
@@ -941,15 +991,16 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
     sh += pb;
   }
   const int sms = num_sms();
-  clear_words(state, state_words(tiles), s);
-  if (int st = launch_status()) return st;
-  const int64_t nbags = (int64_t)num_fields * batch;
-  {
+  if (phases & CTR_DEDUP_PREPARE) {
+    clear_words(state, state_words(tiles), s);
+    if (int st = launch_status()) return st;
+    const int64_t nbags = (int64_t)num_fields * batch;
     int64_t blocks = imin64(ceil_div(nbags, 8), (int64_t)sms * 16);
     keygen_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, s>>>(ids, offsets, num_fields, batch, n_ids, fm,
                                                                         keys[0], bag_of, plan, g_hist, err); count_launch();
     if (int st = launch_status()) return st;
   }
+  if (!(phases & CTR_DEDUP_SORT)) return CTR_OK;
   const int32_t* vin = nullptr;
   timing_mark(CTR_KERNEL_SORT, true, s);
   for (int p = 0; p < passes; ++p) {
@@ -958,7 +1009,8 @@ extern "C" int ctr_dedup(const int64_t* ids, const int64_t* offsets, int32_t num
                                                            plan.shift[p], plan.bits[p], nullptr, p, nullptr,
                                                            g_hist + p * kMaxDigits,
                                                            lookback + (int64_t)p * tiles * kMaxDigits,
-                                                           tile_counter + p, err, g_lookback_limit_ns.load());
+                                                           tile_counter + p, err, g_lookback_limit_ns.load(),
+                                                           nullptr, nullptr);
     count_launch();
     if (int st = launch_status()) return st;
     vin = vout;

@@ -44,6 +44,8 @@ _SIGS = {
     "ctr_fill_table": (C.c_int, [_p, C.c_int, _i64, _i32, _i64, C.c_int, _u64, _f32, _p]),
     "ctr_dedup_workspace_size": (_sz, [_i64, _i32, _i32, _i64]),
     "ctr_dedup": (C.c_int, [_p, _p, _i32, _i32, _p, _p, _i32, _i64, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "ctr_dedup_phases": (C.c_int, [_p, _p, _i32, _i32, _p, _p, _i32, _i64, _p, _p, _p, _p, _p, _p, _p, _i32, _p, _sz,
+                                   _p]),
     "ctr_gather_rows": (C.c_int, [_p, C.c_int, _i32, _i64, _p, _p, _i64, _p, _p, _sz, _p]),
     "ctr_embedding_bag_workspace_size": (_sz, []),
     "ctr_embedding_bag_fwd": (C.c_int, [_p, C.c_int, _i32, _i64, _p, C.c_int, _i64, _p, _i32, _i32, _p, _p, _i32, C.c_int,
@@ -217,6 +219,24 @@ def ctr_dedup(ids: torch.Tensor, offsets: torch.Tensor, num_fields: int, batch: 
                          _ptr(sorted_bag), _ptr(run_offsets), _ptr(unique_offsets), _ptr(ws), ws.numel(),
                          _stream(stream))
     _ok("ctr_dedup", st)
+
+
+DEDUP_PREPARE, DEDUP_SORT, DEDUP_ALL = 1, 2, 3
+
+
+def ctr_dedup_phases(ids: torch.Tensor, offsets: torch.Tensor, num_fields: int, batch: int,
+                     bag_to_table: Sequence[int], row_base: Sequence[int], unique_rows: torch.Tensor,
+                     n_unique: torch.Tensor, inverse: Optional[torch.Tensor], sorted_pos: Optional[torch.Tensor],
+                     sorted_bag: Optional[torch.Tensor], run_offsets: Optional[torch.Tensor],
+                     unique_offsets: Optional[torch.Tensor], phases: int, ws: torch.Tensor,
+                     n_ids: Optional[int] = None, stream=None) -> None:
+    n = int(ids.numel()) if n_ids is None else int(n_ids)
+    rb = np.asarray(row_base, dtype=np.int64)
+    st = lib().ctr_dedup_phases(_ptr(ids), _ptr(offsets), num_fields, batch, _host_i32(bag_to_table),
+                                _host_i64(rb), rb.size - 1, n, _ptr(unique_rows), _ptr(n_unique), _ptr(inverse),
+                                _ptr(sorted_pos), _ptr(sorted_bag), _ptr(run_offsets), _ptr(unique_offsets),
+                                int(phases), _ptr(ws), ws.numel(), _stream(stream))
+    _ok("ctr_dedup_phases", st)
 
 
 def ctr_gather_rows(table: torch.Tensor, d: int, unique_rows: torch.Tensor, n_unique: torch.Tensor, U: torch.Tensor,

@@ -123,11 +123,11 @@ class CtrPath:
                 (("dedup", self.ws_dedup), ("bag", self.ws_bag), ("interaction", self.ws_int), ("bwd", self.ws_bwd))}
 
     # -- steps ------------------------------------------------------------
-    def dedup(self) -> None:
+    def dedup(self, phases: int = ctr.DEDUP_ALL) -> None:
         cfg = self.cfg
-        ctr.ctr_dedup(self.ids, self.offsets, cfg.num_fields, cfg.batch, self.b2t, self.row_base, self.unique_rows,
-                      self.n_unique, self.inverse, self.sorted_pos, self.sorted_bag, self.run_offsets,
-                      self.unique_offsets, self.ws_dedup, n_ids=self.n_ids)
+        ctr.ctr_dedup_phases(self.ids, self.offsets, cfg.num_fields, cfg.batch, self.b2t, self.row_base,
+                             self.unique_rows, self.n_unique, self.inverse, self.sorted_pos, self.sorted_bag,
+                             self.run_offsets, self.unique_offsets, phases, self.ws_dedup, n_ids=self.n_ids)
 
     def forward(self) -> None:
         cfg = self.cfg
@@ -212,6 +212,8 @@ class CtrPath:
         bound), and the backward waits for it.  The side stream first waits for
         everything queued before the step, and the step's end (on the current
         stream) comes after the dedup, so the step orders like a sequential one.
+        (Running the radix passes after the interaction backward instead, with
+        only the dedup's first part beside the gather, was slower.)
         """
         cfg = self.cfg
         needs_dedup = cfg.backward != "none" or cfg.dedup_gather

@@ -85,6 +85,10 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert st == -2                                     # n_ids beyond int32 positions
     st = lib.ctr_dedup(dummy, dummy, 1, 1, b2t, rb, 1, 5, dummy, dummy, null, null, null, null, null, dummy, 16, null)
     assert st == -3                                     # workspace too small
+    for phases in (0, 4):
+        st = lib.ctr_dedup_phases(dummy, dummy, 1, 1, b2t, rb, 1, 5, dummy, dummy, null, null, null, null, null,
+                                  phases, dummy, 1 << 20, null)
+        assert st == -1                                 # no such part of the dedup
     st = lib.ctr_embedding_bag_fwd(dummy, 7, 16, 10, dummy, 0, 4, dummy, 1, 1, b2t, rb, 1, 0, dummy, 0, 16, 16,
                                    dummy, 256, null)
     assert st == -1                                     # bad dtype

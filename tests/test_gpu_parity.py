@@ -145,6 +145,44 @@ def test_dedup_bitmap_path(name):
         assert_dedup_equal(got, ref)
 
 
+@pytest.mark.parametrize("name", ["full_step_b256", "bitmap"])
+def test_dedup_in_two_parts_equals_one_call(name):
+    """ctr_dedup_phases: the prepare part, then (on another stream, behind an
+    event) the sort part, give the one-call dedup's outputs, on both paths."""
+    cfg = DEDUP_CASES["full_step_b256"] if name != "bitmap" else BITMAP_CASES["tensornet_b4096"]
+    w = W.make_workload(cfg, with_grads=False)
+    args = (w["ids"], w["offsets"], cfg.num_fields, cfg.batch, w["bag_to_table"], w["row_base"])
+    ref = O.dedup(*args)
+    n = int(w["offsets"][-1])
+    F, B, T = cfg.num_fields, cfg.batch, len(w["row_base"]) - 1
+    for with_pos in (True, False):
+        out = {k: torch.full((n,), -7, dtype=torch.int32, device=DEV) for k in ("inverse", "sorted_pos", "sorted_bag")}
+        if not with_pos:
+            out["sorted_pos"] = None
+        uq = torch.full((n,), -7, dtype=torch.int64, device=DEV)
+        nu = torch.full((1,), -7, dtype=torch.int64, device=DEV)
+        ro = torch.full((n + 1,), -7, dtype=torch.int32, device=DEV)
+        uo = torch.full((T + 1,), -7, dtype=torch.int64, device=DEV)
+        ws = ctr.workspace(ctr.ctr_dedup_workspace_size(n, F, B, int(w["row_base"][-1])))
+        ids, offs = _t(w["ids"]), _t(w["offsets"])
+        call = (ids, offs, F, B, w["bag_to_table"], w["row_base"], uq, nu, out["inverse"], out["sorted_pos"],
+                out["sorted_bag"], ro, uo)
+        side = torch.cuda.Stream()
+        ev = torch.cuda.Event()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            ctr.ctr_dedup_phases(*call, ctr.DEDUP_PREPARE, ws)
+            ev.record(side)
+        torch.cuda.current_stream().wait_event(ev)
+        ctr.ctr_dedup_phases(*call, ctr.DEDUP_SORT, ws)
+        assert ctr.ctr_check_status(ws) == 0
+        k = int(_np(nu)[0])
+        got = {"unique_rows": _np(uq)[:k], "n_unique": k, "inverse": _np(out["inverse"]),
+               "sorted_pos": _np(out["sorted_pos"]) if with_pos else None, "sorted_bag": _np(out["sorted_bag"]),
+               "run_offsets": _np(ro)[:k + 1], "unique_offsets": _np(uo)}
+        assert_dedup_equal(got, ref)
+
+
 def test_dedup_permuted_tables_and_empty_fields():
     # fields read tables in another order (the outputs follow table order), one field
     # has only empty bags, and one field's IDs span many sort tiles with a ragged tail
@@ -205,10 +243,11 @@ def test_dedup_edge_cases():
             ids[::2] = np.array(rows)[np.repeat(np.arange(F), [offsets[(f + 1) * B] - offsets[f * B]
                                                                 for f in range(F)])][::2] - 1
             ids[1::3] = 0
-        st, got = gpu_dedup(ids, offsets, F, B, b2t, rb)
-        assert st == 0
         ref = O.dedup(ids, offsets, F, B, b2t, rb)
-        assert_dedup_equal(got, ref)
+        for with_pos in (True, False):
+            st, got = gpu_dedup(ids, offsets, F, B, b2t, rb, with_pos=with_pos)
+            assert st == 0
+            assert_dedup_equal(got, ref)
 
 
 def test_dedup_tables_sharing_and_empty_tables():
