@@ -38,15 +38,19 @@ namespace {
 
 constexpr int kRsThreads = 256;
 constexpr int kRsWarps = kRsThreads / 32;
+// Keys per lane per tile, and resident blocks per SM the registers are capped
+// for: 12 keys at 4 blocks (64 registers, 3072-key tiles) against 16 at 3 (80
+// registers): the full step 13.61 -> 13.44 ms in one session (20 keys at 2
+// blocks: 13.45; 8 at 5: slower).
 #ifndef CTR_RS_ITEMS
-#define CTR_RS_ITEMS 16
+#define CTR_RS_ITEMS 12
 #endif
 #ifndef CTR_RS_MINB
-#define CTR_RS_MINB 1
+#define CTR_RS_MINB 4
 #endif
 constexpr int kRsItems = CTR_RS_ITEMS;            // keys per lane per tile
-constexpr int kRsTile = kRsThreads * kRsItems;    // 4096 keys
-constexpr int kRsWarpKeys = 32 * kRsItems;        // 512 keys per warp
+constexpr int kRsTile = kRsThreads * kRsItems;    // 3072 keys
+constexpr int kRsWarpKeys = 32 * kRsItems;        // 384 keys per warp
 constexpr int kMaxBits = 8;                       // digit width limit (256 buckets)
 constexpr int kMaxDigits = 1 << kMaxBits;
 constexpr int kMaxPasses = 4;                     // 32-bit keys
@@ -338,17 +342,17 @@ __device__ __forceinline__ int table_of(const int64_t* rb, int T, int64_t k) {
   return lo;
 }
 
-// Ranks and outputs of one tile of sorted keys.  The tile's 4096 slots are read
-// as 16 coalesced rows of 256 (slot = row * 256 + thread): head flags come from
-// one ballot per warp and row, and a scan of the 16 x 8 per-warp head counts
-// gives every slot its rank.
+// Ranks and outputs of one tile of sorted keys.  The tile's slots are read as
+// kRsItems coalesced rows of 256 (slot = row * 256 + thread): head flags come
+// from one ballot per warp and row, and a scan of the kRsItems x 8 per-warp
+// head counts gives every slot its rank.
 __global__ void __launch_bounds__(kRsThreads) unique_write_kernel(
     const uint32_t* __restrict__ skeys, const int32_t* __restrict__ spos, int64_t n,
     const uint32_t* __restrict__ tile_base_scan, const __grid_constant__ TableBases tb,
     const int32_t* __restrict__ bag_of, int64_t* __restrict__ unique_rows, int64_t* __restrict__ n_unique,
     int32_t* __restrict__ inverse, int32_t* __restrict__ sorted_bag, int32_t* __restrict__ run_offsets,
     int64_t* __restrict__ unique_offsets) {
-  constexpr int kRows = kRsTile / kRsThreads;  // 16
+  constexpr int kRows = kRsTile / kRsThreads;  // keys per thread
   __shared__ uint32_t cnt[kRows * kRsWarps];     // heads per (row, warp), then exclusive offsets
   __shared__ int64_t rb[CTR_MAX_TABLES + 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
