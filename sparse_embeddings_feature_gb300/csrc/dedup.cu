@@ -372,11 +372,14 @@ __global__ void __launch_bounds__(kRsThreads) unique_write_kernel(
     if (lane == 0) cnt[r * kRsWarps + warp] = __popc(mask[r]);
   }
   __syncthreads();
-  if (warp == 0) {  // exclusive scan of the 128 counts, 4 per lane, in slot order
-    uint32_t v[4], sum = 0;
+  if (warp == 0) {  // exclusive scan of the kRows x kRsWarps counts, kPer per lane, in slot order
+    constexpr int kCounts = kRows * kRsWarps;
+    constexpr int kPer = (kCounts + 31) / 32;
+    uint32_t v[kPer], sum = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      v[q] = cnt[lane * 4 + q];
+    for (int q = 0; q < kPer; ++q) {
+      const int i = lane * kPer + q;
+      v[q] = i < kCounts ? cnt[i] : 0u;
       sum += v[q];
     }
     uint32_t inc = sum;
@@ -387,8 +390,9 @@ __global__ void __launch_bounds__(kRsThreads) unique_write_kernel(
     }
     uint32_t run = inc - sum;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      cnt[lane * 4 + q] = run;
+    for (int q = 0; q < kPer; ++q) {
+      const int i = lane * kPer + q;
+      if (i < kCounts) cnt[i] = run;
       run += v[q];
     }
   }
