@@ -257,9 +257,13 @@ def algorithmic_bytes(cfg, path, n_ids, n_unique):
     if cfg.backward != "none" or cfg.dedup_gather:
         # radix passes of 8 bits over the sort keys: ranks of the distinct rows when
         # the tables are at most 64x the batch (presence bitmap), else the rows
-        span = n_unique if cfg.total_rows <= 64 * n_ids else cfg.total_rows
+        bitmap = cfg.total_rows <= 64 * n_ids
+        span = n_unique if bitmap else cfg.total_rows
         bits = max(1, int(span - 1).bit_length())
         out["sort"] = -(-bits // 8) * n_ids * 16
+        if bitmap and path.sorted_pos is None:
+            # the last pass writes the run starts (4 B per distinct row) instead of the sorted keys
+            out["sort"] += n_unique * 4 - n_ids * 4
     if cfg.dedup_gather:
         out["gather_rows"] = n_unique * (2 * row + 8)
     if cfg.interaction:

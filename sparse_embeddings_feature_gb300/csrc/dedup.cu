@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kRsThreads, CTR_RS_MINB) onesweep_kernel(
       } else {
         // first of its digit group in this tile: the element before it was written by
         // an earlier tile, so every such candidate is offered and the smallest kept (the
-        // starts were set to 0xffffffff when the ranks were assigned)
+        // starts were set to 0xffffffff before the passes)
         atomicMin((unsigned int*)(run_offsets + k), dest);
       }
       if (runs && dest == (uint32_t)n32 - 1) run_offsets[nu] = n32;
@@ -561,8 +561,7 @@ __global__ void __launch_bounds__(256) bitmap_count_kernel(const uint32_t* __res
 // the set bits in order.
 __global__ void __launch_bounds__(256) bitmap_pack_kernel(const uint32_t* __restrict__ bitmap, int64_t W,
                                                           const uint32_t* __restrict__ bscan,
-                                                          uint2* __restrict__ pk, int64_t* __restrict__ unique_rows,
-                                                          int32_t* __restrict__ run_starts) {
+                                                          uint2* __restrict__ pk, int64_t* __restrict__ unique_rows) {
   __shared__ uint32_t warp_tot[8];
   constexpr int kPer = kBmWords / 256;
   const int64_t w0 = (int64_t)blockIdx.x * kBmWords + threadIdx.x * kPer;
@@ -580,10 +579,7 @@ __global__ void __launch_bounds__(256) bitmap_pack_kernel(const uint32_t* __rest
     if (w >= W) break;
     uint32_t r = base + v[j];
     pk[w] = make_uint2(b[j], r);
-    for (uint32_t bits = b[j]; bits; bits &= bits - 1) {
-      if (run_starts) run_starts[r] = -1;  // the last radix pass keeps the smallest start offered
-      unique_rows[r++] = w * 32 + (__ffs(bits) - 1);
-    }
+    for (uint32_t bits = b[j]; bits; bits &= bits - 1) unique_rows[r++] = w * 32 + (__ffs(bits) - 1);
   }
 }
 
@@ -621,6 +617,13 @@ __global__ void bitmap_plan_kernel(const uint32_t* __restrict__ total, int64_t* 
       const int64_t k = tb.row_base[t];
       unique_offsets[t] = k >= total_rows ? (int64_t)nu : (int64_t)bitmap_rank(pk, (uint32_t)k);
     }
+}
+
+// Run starts of the n_unique ranks set to all ones (coalesced, n_unique read on the device).
+__global__ void fill_starts_kernel(int32_t* __restrict__ run_offsets, const int64_t* __restrict__ n_unique) {
+  const int64_t nu = *n_unique;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nu; i += (int64_t)gridDim.x * blockDim.x)
+    run_offsets[i] = -1;
 }
 
 // Rank of every key among the distinct keys (the inverse map, which is also
@@ -859,11 +862,15 @@ int dedup_bitmap(const int64_t* ids, const int64_t* offsets, int32_t F, int32_t 
     WsCarver scan_ws = c;
     if (int st = scan_exclusive<uint32_t>(bsum, bsum, nblk, nullptr, total, scan_ws, s)) return st;
   }
-  bitmap_pack_kernel<<<(unsigned)nblk, 256, 0, s>>>(bitmap, W, bsum, pk, unique_rows,
-                                                    fused_runs ? run_offsets : nullptr); count_launch();
+  bitmap_pack_kernel<<<(unsigned)nblk, 256, 0, s>>>(bitmap, W, bsum, pk, unique_rows); count_launch();
   if (int st = launch_status()) return st;
   bitmap_plan_kernel<<<1, 256, 0, s>>>(total, n_unique, tb, total_rows, pk, unique_offsets, dplan); count_launch();
   if (int st = launch_status()) return st;
+  if (fused_runs) {  // the last radix pass keeps the smallest start offered for each rank
+    fill_starts_kernel<<<(unsigned)std::max<int64_t>(1, imin64(ceil_div(n_ids, 1024), (int64_t)sms * 4)), 256, 0, s>>>(
+        run_offsets, n_unique); count_launch();
+    if (int st = launch_status()) return st;
+  }
   // ranks go straight into the caller's inverse map, which the first pass reads
   uint32_t* ranks = inverse ? (uint32_t*)inverse : keys[0];
   {
