@@ -435,7 +435,8 @@ __global__ void __launch_bounds__(kRsThreads) unique_write_kernel(
 // bitmap over all table rows, so the inverse map and the unique rows come from
 // the bitmap directly; the radix sort only groups the occurrences by rank
 // (ceil(bits(n_unique) / 8) passes instead of ceil(bits(total_rows) / 8)) and
-// carries each occurrence's bag, so the grouped bags come out of its last pass.
+// carries each occurrence's bag, so the grouped bags, and the run starts, come
+// out of its last pass.
 // ---------------------------------------------------------------------------
 constexpr int64_t kBitmapRowsPerId = 64;  // bitmap path iff total_rows <= 64 * n_ids
 constexpr int kBmWords = 1024;            // bitmap words per prefix block (4 per thread)
