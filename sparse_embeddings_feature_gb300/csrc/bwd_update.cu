@@ -824,6 +824,9 @@ constexpr int kPairTU = CTR_PAIR_TU;    // uniques per tile
 #ifndef CTR_TILE_PAIR_MINB
 #define CTR_TILE_PAIR_MINB 3
 #endif
+#ifndef CTR_PAIR_FAST
+#define CTR_PAIR_FAST 1  // a step in which neither occurrence closes its run only adds
+#endif
 template <bool MEAN>
 __global__ void __launch_bounds__(kTileThreads, CTR_TILE_PAIR_MINB) bwd_tiles_pair_kernel(const BwdArgs a) {
   extern __shared__ __align__(16) unsigned char wsm_raw[];
@@ -926,6 +929,11 @@ __global__ void __launch_bounds__(kTileThreads, CTR_TILE_PAIR_MINB) bwd_tiles_pa
           const bool v0 = c0 + t0 < E, v1 = c0 + t1 < E;
           if (!v0) continue;  // warp-uniform: the chunk's tail
           const float sc = MEAN ? __shfl_sync(kFull, sc_cur, 2 * q + h) : 1.f;
+          if (CTR_PAIR_FAST && v1 && ((cur.lastm >> t0) & 3u) == 0u) {
+            // neither occurrence closes its run, so both belong to the open one
+            acc = MEAN ? fma4(x, sc, acc) : make_float4(acc.x + x.x, acc.y + x.y, acc.z + x.z, acc.w + x.w);
+            continue;
+          }
           const int seg0 = __shfl_sync(kFull, cur.seg, t0), seg1 = __shfl_sync(kFull, cur.seg, t1);
           const bool last1 = v1 && ((cur.lastm >> t1) & 1u);
           if (v1 && seg0 == seg1) {  // both occurrences belong to one run
