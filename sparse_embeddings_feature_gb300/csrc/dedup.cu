@@ -639,12 +639,18 @@ __device__ __forceinline__ uint32_t rank_or_flag(const uint2* __restrict__ pk, u
   return 0u;
 }
 
-constexpr int kRankVec = 4;                 // uint4 loads per thread and round
+// 8 keys per thread and round: in the full step, beside the gather and the
+// interaction, the sort took 2.86 ms live against 2.92 with 16 and 3.03 with 32
+// (and 4 keys: 3.14), one session.
+#ifndef CTR_RANK_VEC
+#define CTR_RANK_VEC 2
+#endif
+constexpr int kRankVec = CTR_RANK_VEC;      // uint4 loads per thread and round
 constexpr int kRankPer = 4 * kRankVec;      // keys per thread and round
 
 // kRankPer consecutive keys per thread and round: their bitmap lookups are
-// independent, so 16 are in flight per thread.  `vec` says both arrays are
-// 16-byte aligned.
+// independent, so kRankPer are in flight per thread.  `vec` says both arrays
+// are 16-byte aligned.
 __global__ void __launch_bounds__(256) bitmap_rank_kernel(const uint32_t* __restrict__ keys, int64_t n,
                                                           int64_t total_rows, const uint2* __restrict__ pk,
                                                           const PassPlan* __restrict__ dplan,
